@@ -1,0 +1,172 @@
+/*
+ * lora_layer.h -- C ABI of the mixed-adapter LoRA linear layer on GB300 (sm_103a).
+ *
+ * The layer computes, for every token row i of a batch,
+ *
+ *     y[i,:] = x[i,:] W  +  [slot_i != -1] * (alpha_s / r_s) * (x[i,:] A_s) B_s,   s = slot_i
+ *
+ * where W [K,N] is the shared base weight, A_s [K,r_s] and B_s [r_s,N] are the adapter
+ * held in slot s, and slot_i = -1 means "base only".
+ *   - "Serving multiple LoRAs: segmented matrix multiplies and adapter scheduling",
+ *     section "Not merging the weights, computing in batches": y = xW + s(xA)B with
+ *     A in R^{d x r}, B in R^{r x d'}; the base product is one multiply for the whole
+ *     batch; BGMV gathers each token's A and B (decode), SGMV groups same-adapter tokens
+ *     into segments (prefill); real kernels shrink to rank r, then expand and add.
+ *   - "LoRAX, in depth", section "Computing a batch that mixes adapters": s = alpha / r;
+ *     segment boundaries of length n_segments + 1 with an owner per segment; an owner of
+ *     "None" means base only.
+ *   - "Serving LoRA adapters: from the model name to the wrapped layer" (vLLM), Step 3
+ *     (activation copies A and B into a fixed number of stacked slot buffers sized for
+ *     the maximum rank; more adapters than slots or a rank above the maximum is an
+ *     error) and Step 5 (a token without an adapter gets slot -1).
+ *
+ * Conventions for every call:
+ *   - All matrices are dense and row-major (C order).  Element type is the layer's
+ *     dtype: LORA_BF16 (bfloat16, computed with fp32 accumulation; y is rounded to
+ *     bf16 once, round-to-nearest-even) or LORA_F32 (fp32 throughout).
+ *   - "stream" arguments are cudaStream_t values passed as void* (NULL = legacy
+ *     default stream).  Calls enqueue work and return without synchronising, except
+ *     where a call says it synchronises.
+ *   - Return value: LORA_OK or a negative lora_status.  Host-detectable errors are
+ *     returned at once and enqueue nothing.  Device-detectable errors (a token id outside
+ *     [-1, num_slots), a token naming a slot that holds no adapter) never trap: the
+ *     row is treated as base only and a device flag is set; lora_get_status reports it.
+ *   - A layer object is not thread-safe: calls on one layer come from one host thread.
+ */
+#ifndef LORA_LAYER_H
+#define LORA_LAYER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct lora_layer lora_layer_t; /* opaque */
+
+enum lora_dtype { LORA_F32 = 0, LORA_BF16 = 1 };
+
+enum lora_status {
+    LORA_OK = 0,
+    LORA_EINVAL = -1,   /* bad argument: null pointer, size, dtype, T above max_tokens ... */
+    LORA_ESLOT = -2,    /* slot index outside [0, num_slots) */
+    LORA_ERANK = -3,    /* adapter rank outside [1, max_rank] */
+    LORA_EID = -4,      /* (device) a token id outside [-1, num_slots) or naming an empty slot */
+    LORA_ECUDA = -5,    /* a CUDA runtime call failed; lora_last_error has the message */
+    LORA_ENOMEM = -6,   /* device or host allocation failed */
+    LORA_ESTATE = -7,   /* call out of order: lora_forward without matching set_batch_segments */
+    LORA_ETIMEOUT = -8  /* (device) a pipeline wait inside a kernel gave up; results invalid */
+};
+
+/*
+ * Create a layer for a K -> N projection with a table of num_slots adapter slots, each
+ * max_rank wide, for batches of at most max_tokens rows.
+ *   W_dev      [K,N] base weight in device memory, read during this call only: the layer
+ *              keeps its own packed copy (bf16: transposed to [N,K] for the tensor-core
+ *              operand layout; f32: [K,N]).
+ *   stream     stream on which the packing copy runs; the call synchronises it.
+ * Limits: K, N >= 1; for LORA_BF16, K and N are multiples of 8 (16-byte rows for TMA).
+ * 1 <= num_slots <= 4096; 1 <= max_rank <= 128; 1 <= max_tokens <= 1<<20.
+ * All slots start empty.  The layer owns every buffer it allocates (slot table, batch
+ * scratch, staging for host-buffer calls) and frees them in lora_layer_destroy.
+ * Errors: LORA_EINVAL, LORA_ENOMEM, LORA_ECUDA (then *out is NULL).
+ */
+int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
+                      int max_tokens, int dtype, const void* W_dev, void* stream);
+
+/*
+ * Copy one adapter into slot `slot` ("activation" in vLLM's Step 3).
+ *   A_src      [K,r] row-major, B_src [r,N] row-major, the layer's dtype.  Host (pinned
+ *              for a truly asynchronous copy) or device memory; it must stay valid and
+ *              unchanged until side_stream has executed the copy.
+ *   r          the adapter's true rank, 1 <= r <= max_rank; the slot is zero-padded to
+ *              max_rank and kernels read only its first r rank columns.
+ *   alpha      LoRA alpha; the slot's scale is alpha / r, computed in fp32 and applied in
+ *              fp32 to the rank-r intermediate (it is not folded into B).
+ * Ordering: the copy waits for the most recent lora_forward of this layer, so an adapter
+ * is never overwritten under a kernel still reading the slot; the next lora_forward waits
+ * for the copy.  Loading into an occupied slot replaces its adapter.
+ * Errors: LORA_ESLOT, LORA_ERANK, LORA_EINVAL (null), LORA_ECUDA.
+ */
+int load_adapter_slot(lora_layer_t* layer, int slot, const void* A_src, const void* B_src,
+                      int r, float alpha, void* side_stream);
+
+/*
+ * Mark slot `slot` empty (rows naming it are then flagged and computed base only).
+ * Ordered after the most recent lora_forward, like a load.  Errors: LORA_ESLOT, LORA_ECUDA.
+ */
+int unload_adapter_slot(lora_layer_t* layer, int slot, void* side_stream);
+
+/*
+ * Build the segment layout of a batch on the device.
+ *   token_slot_dev  [T] int32 in device memory: each row's slot, -1 = base only.
+ *   T               0 <= T <= max_tokens (T = 0 is an empty batch).
+ * Enqueues one kernel on `stream` that stably sorts the adapted rows by slot
+ * (ascending slot, original row order within a slot; base-only rows excluded; slots with
+ * no rows get no segment) into a row permutation, segment offsets (n_seg + 1) and each
+ * segment's slot, in layer-owned device memory.  The next lora_forward on the same
+ * stream uses this layout; token_slot_dev must stay valid until that forward has run.
+ * Errors: LORA_EINVAL, LORA_ECUDA.
+ */
+int set_batch_segments(lora_layer_t* layer, const int32_t* token_slot_dev, int T, void* stream);
+
+/*
+ * y = x W + per-row LoRA delta, for the batch described by the last set_batch_segments.
+ *   x_dev   [T,K] device, y_dev [T,N] device (overwritten; must not overlap x_dev).
+ *   T       must equal the T of the last set_batch_segments (else LORA_ESTATE).
+ * Enqueues the shrink kernel (v = x A_slot into an fp32 rank-wide buffer, SGMV over the
+ * segments) and the base GEMM, whose epilogue adds scale * v B_slot and writes y once.
+ * No host synchronisation; no allocation.
+ * Errors: LORA_EINVAL, LORA_ESTATE, LORA_ECUDA.
+ */
+int lora_forward(lora_layer_t* layer, const void* x_dev, void* y_dev, int T, void* stream);
+
+/*
+ * The whole layer for callers holding host buffers: copies x_host [T,K] and
+ * token_slot_host [T] to layer-owned device staging, runs set_batch_segments and
+ * lora_forward, and copies y back to y_host [T,N].  All on `stream`, asynchronously:
+ * host buffers (pinned for overlap) must stay valid until the stream has completed.
+ * Errors: as set_batch_segments and lora_forward.
+ */
+int lora_forward_host(lora_layer_t* layer, const void* x_host, const int32_t* token_slot_host,
+                      void* y_host, int T, void* stream);
+
+/*
+ * Synchronise `stream`, read and clear the layer's device error flags.
+ * Returns LORA_OK, LORA_EID (bad or empty-slot token ids since the last call) or
+ * LORA_ETIMEOUT (a kernel pipeline wait gave up), or LORA_ECUDA.
+ */
+int lora_get_status(lora_layer_t* layer, void* stream);
+
+/*
+ * Copy the current segment layout to host memory (synchronises `stream`).
+ *   perm [max_tokens], seg_offsets [num_slots + 1], seg_slot [num_slots]: caller-owned
+ *   host arrays; *n_seg and *n_adapted receive the segment count and the number of
+ *   adapted rows (perm[0..n_adapted) and seg_offsets[0..n_seg] are meaningful).
+ * Errors: LORA_EINVAL, LORA_ESTATE (no batch set), LORA_ECUDA.
+ */
+int lora_get_segments(lora_layer_t* layer, int32_t* perm, int32_t* seg_offsets,
+                      int32_t* seg_slot, int32_t* n_seg, int32_t* n_adapted, void* stream);
+
+/*
+ * Optional tracing of the layer's kernel launches (for timing on the launch stream).
+ *   events   NULL to stop tracing, or an array of 6 cudaEvent_t (as void*) owned by the
+ *            caller; afterwards every set_batch_segments records events[0] before and
+ *            events[1] after the segment-builder launch, and every lora_forward records
+ *            events[2] / events[3] around the shrink launch and events[4] / events[5]
+ *            around the base-GEMM launch, each on the call's stream.
+ * Tracing adds event records only; it changes no result.  Errors: LORA_EINVAL.
+ */
+int lora_set_trace_events(lora_layer_t* layer, void* const* events);
+
+/* Text of the last error raised on this layer ("" if none).  Owned by the layer. */
+const char* lora_last_error(const lora_layer_t* layer);
+
+/* Synchronise the layer's device, then free everything the layer owns.  NULL is a no-op. */
+void lora_layer_destroy(lora_layer_t* layer);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_LAYER_H */

@@ -1,0 +1,479 @@
+// lora_layer.cu -- the C ABI of include/lora_layer.h: layer state, slot loading, batch
+// segmentation and the forward pass (argument checks, buffer ownership, stream ordering).
+//
+// Every step of the computation runs in this library's kernels:
+//   set_batch_segments -> segment_builder_kernel            (builder.cu)
+//   lora_forward       -> shrink_kernel (SGMV/BGMV shrink)  (shrink.cu)
+//                      -> gemm_tc_kernel (bf16, tcgen05)    (gemm_tc.cu)  or
+//                         gemm_simt_f32_kernel (fp32)       (gemm_simt.cu)
+//   load_adapter_slot  -> copy + transpose_pad_kernel + slot_meta_kernel (slots.cu)
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/lora_layer.h"
+#include "lora_common.cuh"
+#include "lora_kernels.h"
+
+using namespace lora;
+
+namespace {
+
+constexpr int kMaxSlots = 4096;
+constexpr int kMaxRank = 128;
+constexpr int kMaxTokens = 1 << 20;
+constexpr int kShrinkRowsPerTile = 16;
+constexpr int kMaxKSplit = 8;
+
+}  // namespace
+
+struct lora_layer {
+  int K = 0, N = 0, S = 0, R = 0, T_max = 0, dtype = 0, device = 0, num_sms = 0;
+  size_t esize = 0;
+  void* Wp = nullptr;      // packed base weight: bf16 [N][K], f32 [K][N]
+  void* A_pool = nullptr;  // [S][R][K]
+  void* B_pool = nullptr;  // [S][R][N]
+  void* A_stage = nullptr; // [K][R] staging for the transposition of a loaded A
+  float* scale = nullptr;  // [S]
+  int32_t* rank = nullptr;    // [S]
+  int32_t* loaded = nullptr;  // [S]
+  // batch layout (segment builder outputs)
+  int32_t* row_slot = nullptr;   // [T_max]
+  int32_t* perm = nullptr;       // [T_max]
+  int32_t* seg_offsets = nullptr;// [S+1]
+  int32_t* seg_slot = nullptr;   // [S]
+  int32_t* tile_seg = nullptr;   // [max_tiles]
+  int32_t* tile_row0 = nullptr;  // [max_tiles]
+  int32_t* meta = nullptr;       // [4]
+  int32_t* err = nullptr;        // [1]
+  float* vpart = nullptr;        // [kMaxKSplit][T_max][R]
+  int max_tiles = 0;
+  int T_batch = -1;              // T of the last set_batch_segments, -1 = none
+  // staging for lora_forward_host
+  void* x_stage = nullptr;
+  int32_t* ids_stage = nullptr;
+  void* y_stage = nullptr;
+  // ordering
+  cudaEvent_t stage_free = nullptr;    // recorded after a load's transposition
+  cudaEvent_t last_forward = nullptr;  // recorded after each forward (when not capturing)
+  bool have_forward = false;
+  std::vector<cudaEvent_t> pending;    // loads not yet waited on by a forward
+  std::vector<cudaEvent_t> spare;
+  CUtensorMap tmap_w[3];
+  cudaEvent_t trace[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  bool tracing = false;
+  char last_error[512] = {0};
+};
+
+namespace {
+
+int fail(lora_layer* L, int code, const char* fmt, ...) {
+  if (L) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(L->last_error, sizeof(L->last_error), fmt, ap);
+    va_end(ap);
+  }
+  return code;
+}
+
+int cuda_fail(lora_layer* L, cudaError_t e, const char* what) {
+  return fail(L, LORA_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define LORA_CUDA(L, expr)                                   \
+  do {                                                       \
+    cudaError_t e_ = (expr);                                 \
+    if (e_ != cudaSuccess) return cuda_fail((L), e_, #expr); \
+  } while (0)
+
+template <typename T>
+cudaError_t dmalloc(T** p, size_t count) {
+  return cudaMalloc(reinterpret_cast<void**>(p), std::max<size_t>(count, 1) * sizeof(T));
+}
+
+void free_all(lora_layer* L) {
+  void* ptrs[] = {L->Wp, L->A_pool, L->B_pool, L->A_stage, L->scale, L->rank, L->loaded,
+                  L->row_slot, L->perm, L->seg_offsets, L->seg_slot, L->tile_seg,
+                  L->tile_row0, L->meta, L->err, L->vpart, L->x_stage, L->ids_stage,
+                  L->y_stage};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  if (L->stage_free) cudaEventDestroy(L->stage_free);
+  if (L->last_forward) cudaEventDestroy(L->last_forward);
+  for (cudaEvent_t e : L->pending) cudaEventDestroy(e);
+  for (cudaEvent_t e : L->spare) cudaEventDestroy(e);
+}
+
+cudaError_t trace_mark(const lora_layer* L, int idx, cudaStream_t s) {
+  return L->tracing ? cudaEventRecord(L->trace[idx], s) : cudaSuccess;
+}
+
+bool is_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) != cudaSuccess) return false;
+  return st != cudaStreamCaptureStatusNone;
+}
+
+// Split K into chunks so that (expected tiles) x (chunks) covers the SMs a few times over.
+void choose_ksplit(const lora_layer* L, int T, int* ksplit, int* kchunk) {
+  const int vec = 256;  // a warp's 32 lanes x 8 bf16
+  const int est_tiles = std::max(1, std::min(T, L->S) + T / kShrinkRowsPerTile);
+  int ks = (4 * L->num_sms + est_tiles - 1) / est_tiles;
+  ks = std::max(1, std::min(ks, kMaxKSplit));
+  ks = std::min(ks, std::max(1, L->K / vec));
+  int kc = (L->K + ks - 1) / ks;
+  kc = ((kc + vec - 1) / vec) * vec;
+  ks = (L->K + kc - 1) / kc;
+  *ksplit = ks;
+  *kchunk = kc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
+                      int max_tokens, int dtype, const void* W_dev, void* stream_) {
+  if (!out) return LORA_EINVAL;
+  *out = nullptr;
+  if (K < 1 || N < 1 || num_slots < 1 || num_slots > kMaxSlots || max_rank < 1 ||
+      max_rank > kMaxRank || max_tokens < 1 || max_tokens > kMaxTokens || !W_dev)
+    return LORA_EINVAL;
+  if (dtype != LORA_F32 && dtype != LORA_BF16) return LORA_EINVAL;
+  if (dtype == LORA_BF16 && (K % 8 != 0 || N % 8 != 0)) return LORA_EINVAL;
+
+  lora_layer* L = new (std::nothrow) lora_layer();
+  if (!L) return LORA_ENOMEM;
+  L->K = K;
+  L->N = N;
+  L->S = num_slots;
+  L->R = max_rank;
+  L->T_max = max_tokens;
+  L->dtype = dtype;
+  L->esize = dtype == LORA_BF16 ? 2 : 4;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+  auto bail = [&](int code) {
+    free_all(L);
+    delete L;
+    return code;
+  };
+  cudaError_t e = cudaGetDevice(&L->device);
+  if (e != cudaSuccess) return bail(LORA_ECUDA);
+  e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
+  if (e != cudaSuccess) return bail(LORA_ECUDA);
+
+  const size_t es = L->esize;
+  const size_t S = num_slots, R = max_rank;
+  L->max_tiles = (max_tokens + kShrinkRowsPerTile - 1) / kShrinkRowsPerTile + num_slots;
+  bool ok = cudaMalloc(&L->Wp, (size_t)K * N * es) == cudaSuccess &&
+            cudaMalloc(&L->A_pool, S * R * K * es) == cudaSuccess &&
+            cudaMalloc(&L->B_pool, S * R * N * es) == cudaSuccess &&
+            cudaMalloc(&L->A_stage, (size_t)K * R * es) == cudaSuccess &&
+            dmalloc(&L->scale, S) == cudaSuccess && dmalloc(&L->rank, S) == cudaSuccess &&
+            dmalloc(&L->loaded, S) == cudaSuccess &&
+            dmalloc(&L->row_slot, max_tokens) == cudaSuccess &&
+            dmalloc(&L->perm, max_tokens) == cudaSuccess &&
+            dmalloc(&L->seg_offsets, S + 1) == cudaSuccess &&
+            dmalloc(&L->seg_slot, S) == cudaSuccess &&
+            dmalloc(&L->tile_seg, L->max_tiles) == cudaSuccess &&
+            dmalloc(&L->tile_row0, L->max_tiles) == cudaSuccess &&
+            dmalloc(&L->meta, 4) == cudaSuccess && dmalloc(&L->err, 1) == cudaSuccess &&
+            dmalloc(&L->vpart, (size_t)kMaxKSplit * max_tokens * R) == cudaSuccess &&
+            cudaMalloc(&L->x_stage, (size_t)max_tokens * K * es) == cudaSuccess &&
+            dmalloc(&L->ids_stage, max_tokens) == cudaSuccess &&
+            cudaMalloc(&L->y_stage, (size_t)max_tokens * N * es) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return bail(LORA_ENOMEM);
+  }
+  ok = cudaEventCreateWithFlags(&L->stage_free, cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&L->last_forward, cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) return bail(LORA_ECUDA);
+
+  ok = cudaMemsetAsync(L->A_pool, 0, S * R * K * es, stream) == cudaSuccess &&
+       cudaMemsetAsync(L->B_pool, 0, S * R * N * es, stream) == cudaSuccess &&
+       cudaMemsetAsync(L->scale, 0, S * 4, stream) == cudaSuccess &&
+       cudaMemsetAsync(L->rank, 0, S * 4, stream) == cudaSuccess &&
+       cudaMemsetAsync(L->loaded, 0, S * 4, stream) == cudaSuccess &&
+       cudaMemsetAsync(L->meta, 0, 16, stream) == cudaSuccess &&
+       cudaMemsetAsync(L->err, 0, 4, stream) == cudaSuccess &&
+       cudaMemsetAsync(L->vpart, 0, (size_t)kMaxKSplit * max_tokens * R * 4, stream) ==
+           cudaSuccess;
+  if (!ok) return bail(LORA_ECUDA);
+
+  if (dtype == LORA_BF16) {
+    if (launch_pack_w_bf16(W_dev, L->Wp, K, N, stream) != cudaSuccess) return bail(LORA_ECUDA);
+    for (int i = 0; i < 3; ++i)
+      if (encode_tmap_bf16(&L->tmap_w[i], L->Wp, N, K, kTcTileN[i]) != cudaSuccess)
+        return bail(LORA_ECUDA);
+  } else {
+    if (cudaMemcpyAsync(L->Wp, W_dev, (size_t)K * N * es, cudaMemcpyDefault, stream) !=
+        cudaSuccess)
+      return bail(LORA_ECUDA);
+  }
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return bail(LORA_ECUDA);
+  *out = L;
+  return LORA_OK;
+}
+
+static cudaEvent_t take_event(lora_layer* L) {
+  if (!L->spare.empty()) {
+    cudaEvent_t e = L->spare.back();
+    L->spare.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+  return e;
+}
+
+int load_adapter_slot(lora_layer_t* L, int slot, const void* A_src, const void* B_src, int r,
+                      float alpha, void* side_) {
+  if (!L) return LORA_EINVAL;
+  if (slot < 0 || slot >= L->S) return fail(L, LORA_ESLOT, "slot %d outside [0, %d)", slot, L->S);
+  if (r < 1 || r > L->R) return fail(L, LORA_ERANK, "rank %d outside [1, %d]", r, L->R);
+  if (!A_src || !B_src) return fail(L, LORA_EINVAL, "null adapter pointer");
+  cudaStream_t side = static_cast<cudaStream_t>(side_);
+  const size_t es = L->esize;
+  const size_t K = L->K, N = L->N, R = L->R;
+
+  // never overwrite a slot under a forward still in flight, nor the staging buffer under
+  // the previous load's transposition
+  if (L->have_forward) LORA_CUDA(L, cudaStreamWaitEvent(side, L->last_forward, 0));
+  LORA_CUDA(L, cudaStreamWaitEvent(side, L->stage_free, 0));
+
+  LORA_CUDA(L, cudaMemcpyAsync(L->A_stage, A_src, K * r * es, cudaMemcpyDefault, side));
+  char* At = static_cast<char*>(L->A_pool) + (size_t)slot * R * K * es;
+  LORA_CUDA(L, launch_transpose_pad(L->A_stage, At, (int)K, r, (int)R, L->dtype == LORA_BF16,
+                                    side));
+  LORA_CUDA(L, cudaEventRecord(L->stage_free, side));
+  char* Bs = static_cast<char*>(L->B_pool) + (size_t)slot * R * N * es;
+  LORA_CUDA(L, cudaMemcpyAsync(Bs, B_src, (size_t)r * N * es, cudaMemcpyDefault, side));
+  if ((size_t)r < R)
+    LORA_CUDA(L, cudaMemsetAsync(Bs + (size_t)r * N * es, 0, (R - r) * N * es, side));
+  LORA_CUDA(L, launch_slot_meta(L->scale, L->rank, L->loaded, slot, alpha / (float)r, r, 1,
+                                side));
+  cudaEvent_t ev = take_event(L);
+  if (!ev) return fail(L, LORA_ECUDA, "cudaEventCreate failed");
+  LORA_CUDA(L, cudaEventRecord(ev, side));
+  L->pending.push_back(ev);
+  return LORA_OK;
+}
+
+int unload_adapter_slot(lora_layer_t* L, int slot, void* side_) {
+  if (!L) return LORA_EINVAL;
+  if (slot < 0 || slot >= L->S) return fail(L, LORA_ESLOT, "slot %d outside [0, %d)", slot, L->S);
+  cudaStream_t side = static_cast<cudaStream_t>(side_);
+  if (L->have_forward) LORA_CUDA(L, cudaStreamWaitEvent(side, L->last_forward, 0));
+  LORA_CUDA(L, launch_slot_meta(L->scale, L->rank, L->loaded, slot, 0.f, 0, 0, side));
+  cudaEvent_t ev = take_event(L);
+  if (!ev) return fail(L, LORA_ECUDA, "cudaEventCreate failed");
+  LORA_CUDA(L, cudaEventRecord(ev, side));
+  L->pending.push_back(ev);
+  return LORA_OK;
+}
+
+int set_batch_segments(lora_layer_t* L, const int32_t* token_slot_dev, int T, void* stream_) {
+  if (!L) return LORA_EINVAL;
+  if (T < 0 || T > L->T_max)
+    return fail(L, LORA_EINVAL, "T=%d outside [0, max_tokens=%d]", T, L->T_max);
+  if (T > 0 && !token_slot_dev) return fail(L, LORA_EINVAL, "null token_slot");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  // slot loads become visible to the builder (it reads the loaded flags)
+  for (cudaEvent_t e : L->pending) LORA_CUDA(L, cudaStreamWaitEvent(stream, e, 0));
+  L->spare.insert(L->spare.end(), L->pending.begin(), L->pending.end());
+  L->pending.clear();
+
+  BuilderArgs a;
+  a.token_slot = token_slot_dev;
+  a.T = T;
+  a.S = L->S;
+  a.loaded = L->loaded;
+  a.rows_per_tile = kShrinkRowsPerTile;
+  a.row_slot = L->row_slot;
+  a.perm = L->perm;
+  a.seg_offsets = L->seg_offsets;
+  a.seg_slot = L->seg_slot;
+  a.tile_seg = L->tile_seg;
+  a.tile_row0 = L->tile_row0;
+  a.meta = L->meta;
+  a.err = L->err;
+  LORA_CUDA(L, trace_mark(L, 0, stream));
+  LORA_CUDA(L, launch_segment_builder(a, stream));
+  LORA_CUDA(L, trace_mark(L, 1, stream));
+  L->T_batch = T;
+  return LORA_OK;
+}
+
+int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* stream_) {
+  if (!L) return LORA_EINVAL;
+  if (L->T_batch < 0) return fail(L, LORA_ESTATE, "lora_forward before set_batch_segments");
+  if (T != L->T_batch)
+    return fail(L, LORA_ESTATE, "T=%d differs from the batch's T=%d", T, L->T_batch);
+  if (T == 0) return LORA_OK;
+  if (!x_dev || !y_dev) return fail(L, LORA_EINVAL, "null x or y");
+  const size_t es = L->esize;
+  const char* xb = static_cast<const char*>(x_dev);
+  const char* yb = static_cast<const char*>(y_dev);
+  if (xb < yb + (size_t)T * L->N * es && yb < xb + (size_t)T * L->K * es)
+    return fail(L, LORA_EINVAL, "x and y overlap");
+  if (L->dtype == LORA_BF16 &&
+      (reinterpret_cast<uintptr_t>(x_dev) % 16 != 0 || reinterpret_cast<uintptr_t>(y_dev) % 16 != 0))
+    return fail(L, LORA_EINVAL, "bf16 x and y must be 16-byte aligned");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  for (cudaEvent_t e : L->pending) LORA_CUDA(L, cudaStreamWaitEvent(stream, e, 0));
+  L->spare.insert(L->spare.end(), L->pending.begin(), L->pending.end());
+  L->pending.clear();
+
+  int ksplit = 1, kchunk = L->K;
+  choose_ksplit(L, T, &ksplit, &kchunk);
+
+  ShrinkArgs sa;
+  sa.x = x_dev;
+  sa.T = T;
+  sa.K = L->K;
+  sa.R = L->R;
+  sa.At_pool = L->A_pool;
+  sa.rank = L->rank;
+  sa.perm = L->perm;
+  sa.seg_offsets = L->seg_offsets;
+  sa.seg_slot = L->seg_slot;
+  sa.tile_seg = L->tile_seg;
+  sa.tile_row0 = L->tile_row0;
+  sa.meta = L->meta;
+  sa.rows_per_tile = kShrinkRowsPerTile;
+  sa.ksplit = ksplit;
+  sa.kchunk = kchunk;
+  sa.vpart = L->vpart;
+  sa.v_stride_rows = L->T_max;
+  sa.max_items = ((T + kShrinkRowsPerTile - 1) / kShrinkRowsPerTile + std::min(T, L->S)) * ksplit;
+  sa.num_sms = L->num_sms;
+  LORA_CUDA(L, trace_mark(L, 2, stream));
+  LORA_CUDA(L, launch_shrink(sa, L->dtype == LORA_BF16, stream));
+  LORA_CUDA(L, trace_mark(L, 3, stream));
+
+  GemmArgs ga;
+  ga.M = T;
+  ga.N = L->N;
+  ga.K = L->K;
+  ga.x = x_dev;
+  ga.W = L->Wp;
+  ga.y = y_dev;
+  ga.ex.row_slot = L->row_slot;
+  ga.ex.vpart = L->vpart;
+  ga.ex.ksplit = ksplit;
+  ga.ex.v_stride_rows = L->T_max;
+  ga.ex.R = L->R;
+  ga.ex.B_pool = L->B_pool;
+  ga.ex.scale = L->scale;
+  ga.ex.rank = L->rank;
+  ga.err = L->err;
+  ga.num_sms = L->num_sms;
+  LORA_CUDA(L, trace_mark(L, 4, stream));
+  if (L->dtype == LORA_BF16)
+    LORA_CUDA(L, launch_gemm_tc(ga, L->tmap_w, stream));
+  else
+    LORA_CUDA(L, launch_gemm_simt_f32(ga, stream));
+  LORA_CUDA(L, trace_mark(L, 5, stream));
+
+  if (!is_capturing(stream)) {
+    LORA_CUDA(L, cudaEventRecord(L->last_forward, stream));
+    L->have_forward = true;
+  }
+  return LORA_OK;
+}
+
+int lora_forward_host(lora_layer_t* L, const void* x_host, const int32_t* token_slot_host,
+                      void* y_host, int T, void* stream_) {
+  if (!L) return LORA_EINVAL;
+  if (T < 0 || T > L->T_max)
+    return fail(L, LORA_EINVAL, "T=%d outside [0, max_tokens=%d]", T, L->T_max);
+  if (T > 0 && (!x_host || !token_slot_host || !y_host))
+    return fail(L, LORA_EINVAL, "null host buffer");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const size_t es = L->esize;
+  if (T > 0) {
+    LORA_CUDA(L, cudaMemcpyAsync(L->x_stage, x_host, (size_t)T * L->K * es, cudaMemcpyDefault,
+                                 stream));
+    LORA_CUDA(L, cudaMemcpyAsync(L->ids_stage, token_slot_host, (size_t)T * 4,
+                                 cudaMemcpyDefault, stream));
+  }
+  int rc = set_batch_segments(L, L->ids_stage, T, stream_);
+  if (rc != LORA_OK) return rc;
+  rc = lora_forward(L, L->x_stage, L->y_stage, T, stream_);
+  if (rc != LORA_OK) return rc;
+  if (T > 0)
+    LORA_CUDA(L, cudaMemcpyAsync(y_host, L->y_stage, (size_t)T * L->N * es, cudaMemcpyDefault,
+                                 stream));
+  return LORA_OK;
+}
+
+int lora_get_status(lora_layer_t* L, void* stream_) {
+  if (!L) return LORA_EINVAL;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int32_t flags = 0;
+  LORA_CUDA(L, cudaStreamSynchronize(stream));
+  LORA_CUDA(L, cudaMemcpy(&flags, L->err, 4, cudaMemcpyDeviceToHost));
+  LORA_CUDA(L, cudaMemset(L->err, 0, 4));
+  if (flags & LORA_ERRF_TIMEOUT)
+    return fail(L, LORA_ETIMEOUT, "a kernel pipeline wait timed out (flags=%d)", flags);
+  if (flags & (LORA_ERRF_BAD_ID | LORA_ERRF_EMPTY_SLOT))
+    return fail(L, LORA_EID, "token ids out of range or naming empty slots (flags=%d)", flags);
+  return LORA_OK;
+}
+
+int lora_get_segments(lora_layer_t* L, int32_t* perm, int32_t* seg_offsets, int32_t* seg_slot,
+                      int32_t* n_seg, int32_t* n_adapted, void* stream_) {
+  if (!L) return LORA_EINVAL;
+  if (!perm || !seg_offsets || !seg_slot || !n_seg || !n_adapted)
+    return fail(L, LORA_EINVAL, "null output pointer");
+  if (L->T_batch < 0) return fail(L, LORA_ESTATE, "no batch set");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  LORA_CUDA(L, cudaStreamSynchronize(stream));
+  int32_t meta[4];
+  LORA_CUDA(L, cudaMemcpy(meta, L->meta, sizeof(meta), cudaMemcpyDeviceToHost));
+  *n_seg = meta[0];
+  *n_adapted = meta[1];
+  if (meta[1] > 0)
+    LORA_CUDA(L, cudaMemcpy(perm, L->perm, (size_t)meta[1] * 4, cudaMemcpyDeviceToHost));
+  LORA_CUDA(L, cudaMemcpy(seg_offsets, L->seg_offsets, (size_t)(meta[0] + 1) * 4,
+                          cudaMemcpyDeviceToHost));
+  if (meta[0] > 0)
+    LORA_CUDA(L, cudaMemcpy(seg_slot, L->seg_slot, (size_t)meta[0] * 4, cudaMemcpyDeviceToHost));
+  return LORA_OK;
+}
+
+int lora_set_trace_events(lora_layer_t* L, void* const* events) {
+  if (!L) return LORA_EINVAL;
+  if (!events) {
+    L->tracing = false;
+    return LORA_OK;
+  }
+  for (int i = 0; i < 6; ++i)
+    if (!events[i]) return fail(L, LORA_EINVAL, "null trace event %d", i);
+  for (int i = 0; i < 6; ++i) L->trace[i] = static_cast<cudaEvent_t>(events[i]);
+  L->tracing = true;
+  return LORA_OK;
+}
+
+const char* lora_last_error(const lora_layer_t* L) { return L ? L->last_error : "null layer"; }
+
+void lora_layer_destroy(lora_layer_t* L) {
+  if (!L) return;
+  const int dev = L->device;
+  int cur = dev;
+  if (cudaGetDevice(&cur) == cudaSuccess && cur != dev) cudaSetDevice(dev);
+  cudaDeviceSynchronize();
+  free_all(L);
+  delete L;
+  if (cur != dev) cudaSetDevice(cur);
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// slots.cu -- slot table maintenance: the "activation" copy of an adapter into a slot and
+// the one-time packing of the base weight.
+//
+// "Serving LoRA adapters: from the model name to the wrapped layer" (vLLM), Step 3: the
+// activation copies each module's A and B into stacked buffers at the slot index; buffers
+// are sized for the maximum rank.  Here A [K,r] is stored transposed and zero-padded as
+// At [R][K] (K contiguous: the shrink streams it with coalesced vector loads) and B [r,N]
+// is copied as rows 0..r-1 of the slot's [R][N] block, rows r..R-1 zeroed.
+#include "lora_common.cuh"
+#include "lora_kernels.h"
+
+namespace lora {
+
+template <typename T>
+__global__ void transpose_pad_kernel(const T* __restrict__ A, T* __restrict__ At, int K, int r,
+                                     int R) {
+  // At[j][k] = A[k][j] for j < r, 0 for r <= j < R.  32x32 tiles through shared memory.
+  __shared__ T tile[32][33];
+  const int k0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+  for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+    const int k = k0 + dy, j = j0 + threadIdx.x;
+    tile[dy][threadIdx.x] = (k < K && j < r) ? A[(size_t)k * r + j] : T(0.f);
+  }
+  __syncthreads();
+  for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+    const int j = j0 + dy, k = k0 + threadIdx.x;
+    if (j < R && k < K) At[(size_t)j * K + k] = tile[threadIdx.x][dy];
+  }
+}
+
+cudaError_t launch_transpose_pad(const void* A_kr, void* At_rk, int K, int r, int R, bool bf16,
+                                 cudaStream_t stream) {
+  dim3 block(32, 8), grid((K + 31) / 32, (R + 31) / 32);
+  if (bf16)
+    transpose_pad_kernel<__nv_bfloat16><<<grid, block, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(A_kr), static_cast<__nv_bfloat16*>(At_rk), K, r, R);
+  else
+    transpose_pad_kernel<float><<<grid, block, 0, stream>>>(
+        static_cast<const float*>(A_kr), static_cast<float*>(At_rk), K, r, R);
+  return cudaGetLastError();
+}
+
+__global__ void pack_w_kernel(const __nv_bfloat16* __restrict__ W, __nv_bfloat16* __restrict__ Wt,
+                              int K, int N) {
+  // Wt[n][k] = W[k][n], 32x32 tiles.
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int n0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+  for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+    const int k = k0 + dy, n = n0 + threadIdx.x;
+    if (k < K && n < N) tile[dy][threadIdx.x] = W[(size_t)k * N + n];
+  }
+  __syncthreads();
+  for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+    const int n = n0 + dy, k = k0 + threadIdx.x;
+    if (n < N && k < K) Wt[(size_t)n * K + k] = tile[threadIdx.x][dy];
+  }
+}
+
+cudaError_t launch_pack_w_bf16(const void* W_kn, void* W_nk, int K, int N, cudaStream_t stream) {
+  dim3 block(32, 8), grid((N + 31) / 32, (K + 31) / 32);
+  pack_w_kernel<<<grid, block, 0, stream>>>(static_cast<const __nv_bfloat16*>(W_kn),
+                                            static_cast<__nv_bfloat16*>(W_nk), K, N);
+  return cudaGetLastError();
+}
+
+__global__ void slot_meta_kernel(float* scale, int32_t* rank, int32_t* loaded, int slot, float s,
+                                 int r, int is_loaded) {
+  scale[slot] = s;
+  rank[slot] = r;
+  loaded[slot] = is_loaded;
+}
+
+cudaError_t launch_slot_meta(float* scale, int32_t* rank, int32_t* loaded, int slot, float s,
+                             int r, int is_loaded, cudaStream_t stream) {
+  slot_meta_kernel<<<1, 1, 0, stream>>>(scale, rank, loaded, slot, s, r, is_loaded);
+  return cudaGetLastError();
+}
+
+}  // namespace lora
