@@ -1,0 +1,520 @@
+#!/usr/bin/env python
+"""Throughput of the mixed-adapter LoRA linear layer on GB300.
+
+One step = one pass of the whole hot path over one batch: the device segment builder
+(set_batch_segments) and the layer forward (shrink + tensor-core base GEMM with the
+fused expand), through the library's C ABI.  The default workload is the decode BGMV
+batch: T=256 tokens (one per request), K=N=4096, rank 16, 128 resident adapter slots,
+each token's slot uniform with 10% base-only rows, bf16 with fp32 accumulation.
+
+Timing: warm-up steps, then exactly --steps steps bracketed by a barrier and a device
+synchronize, CUDA events on the launching stream, max over ranks.  Each step uses the
+next of L independent layer instances (weights, slot table, inputs), so consecutive
+steps never find their data in L2 (L x ~66 MB >> 129 MB).  Steps are replayed from
+CUDA graphs captured once per instance.
+
+Prints one JSON line.  --impl reference times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "mixed-adapter LoRA layer tokens/s; SGMV/BGMV HBM GB/s and % of roofline"
+UNIT = "tokens/s"
+
+CONFIGS = {
+    "decode_bgmv": dict(seed=1002, desc="decode BGMV: T=256 tokens, K=N=4096, r=16, "
+                        "128 slots, 10% base-only, bf16 (fp32 accumulate)"),
+    "mixed_continuous": dict(seed=1004, desc="continuous batch: 8x448 prefill + 512 decode rows, "
+                             "unsorted, Zipf(1.1) over 1000 ids -> 100 slots, K=14336, "
+                             "N=4096, r=16, bf16"),
+    "prefill_sgmv": dict(seed=1003, desc="prefill SGMV: T=8192 in 32 geometric segments, "
+                         "K=4096, N=14336, r in {8,16,32,64} padded to 64, bf16"),
+}
+
+
+def make_workload(name, seed, device):
+    from segmented_rank_gemm_gb300 import workloads
+    fn = getattr(workloads, name)
+    return fn(seed=seed, device=device)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------------
+# algorithmic work per step (what the method must move / compute)
+# ------------------------------------------------------------------------------------
+
+def algorithmic(wl, ksplit_planes=None):
+    """Bytes and FLOPs per step: x, W, y once; each distinct adapter slice used in the
+    batch once at its true rank; ids; the fp32 rank-wide intermediate v once."""
+    T, K, N = wl.T, wl.K, wl.N
+    es = 2 if wl.dtype == torch.bfloat16 else 4
+    ids = wl.token_slot.cpu().numpy()
+    used = sorted(set(int(s) for s in ids if s >= 0))
+    ranks = {s: int(wl.adapters[s][0].shape[1]) for s in used}
+    adapted = ids >= 0
+    a_bytes = sum(K * ranks[s] * es for s in used)
+    b_bytes = sum(ranks[s] * N * es for s in used)
+    v_bytes = int(sum(ranks[int(s)] for s in ids[adapted])) * 4
+    base = {"x": T * K * es, "W": K * N * es, "y": T * N * es, "ids": T * 4}
+    lora_flops = 2 * sum(ranks[int(s)] * (K + N) for s in ids[adapted])
+    return {
+        "step_bytes": sum(base.values()) + a_bytes + b_bytes,
+        # the GEMM kernel: x, W, y, the distinct B slices, v (written by the shrink) once
+        "gemm_bytes": base["x"] + base["W"] + base["y"] + b_bytes + v_bytes + base["ids"],
+        "shrink_bytes": base["x"] + a_bytes + v_bytes,
+        "base_flops": 2 * T * K * N,
+        "lora_flops": lora_flops,
+        "distinct_slots": len(used),
+        "adapted_rows": int(adapted.sum()),
+    }
+
+
+# ------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, out_path=None):
+        self.out_path = out_path
+        self.proc = None
+        self.lines = []
+        self.t0 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t0 = time.time()
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.out_path:
+            with open(self.out_path, "w") as f:
+                f.write(self.FIELDS + "\n")
+                for t, l in self.lines:
+                    f.write("%.3f, %s\n" % (t, l))
+
+    def summary(self, t_from, t_to):
+        rows = []
+        for t, l in self.lines:
+            if not (t_from <= t <= t_to):
+                continue
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        gpu = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
+        idxs = sorted(set(r[0] for r in rows))
+        pick = gpu if gpu in idxs else idxs[0]
+        if len(idxs) > 1 and gpu not in idxs:  # the busiest GPU is ours
+            pick = max(idxs, key=lambda i: max(float(r[3]) for r in rows if r[0] == i))
+        rows = [r for r in rows if r[0] == pick]
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted(set(n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"))
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows)}
+
+
+# ------------------------------------------------------------------------------------
+# distributed helpers (one process per GPU; the layer needs no collective)
+# ------------------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: units processed by all ranks / the slowest rank's time."""
+    return units_per_rank * steps * world / max_seconds
+
+
+# ------------------------------------------------------------------------------------
+# our implementation
+# ------------------------------------------------------------------------------------
+
+def traffic_from_profile(kernel_src: str, config: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    entry = rec.get(config)
+    if not entry:
+        return None
+    with open(kernel_src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    if entry.get("kernel_sha256_16") != h:
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def run_ours(args):
+    from segmented_rank_gemm_gb300.lora import LoraLayer, lora_set_trace_events, LORA_OK
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = CONFIGS[args.config]
+
+    # L independent instances; instance 0 is drawn on the host (the oracle baseline uses
+    # the same values), the others on the device from their own seeds.
+    layers, inputs, wls = [], [], []
+    for i in range(args.layers):
+        seed = cfg["seed"] + 7919 * i + 104729 * rank
+        wl = make_workload(args.config, seed, "cpu" if i == 0 else dev)
+        layer = LoraLayer(wl.W.to(dev), wl.S, wl.R, wl.T)
+        for s, ad in enumerate(wl.adapters):
+            if ad is not None:
+                layer.load(s, ad[0].to(dev), ad[1].to(dev), ad[2])
+        x = wl.x.to(dev)
+        ids = wl.token_slot.to(dev)
+        y = torch.empty(wl.T, wl.N, dtype=wl.dtype, device=dev)
+        layers.append(layer)
+        inputs.append((x, ids, y))
+        if i == 0:
+            wl0 = wl
+        else:
+            del wl
+    torch.cuda.synchronize()
+    T, K, N = wl0.T, wl0.K, wl0.N
+    work = algorithmic(wl0)
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        layer = layers[i % len(layers)]
+        x, ids, y = inputs[i % len(layers)]
+        layer.set_batch(ids, stream)
+        layer.forward(x, y, stream)
+
+    # warm-up (eager), then capture one graph per instance
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1) * len(layers)):
+            step(i)
+    stream.synchronize()
+    for l in layers:
+        assert l.status(stream) == LORA_OK
+    graphs = []
+    if not args.no_graph:
+        for i in range(len(layers)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(i)
+            graphs.append(g)
+        for i in range(len(layers)):
+            graphs[i].replay()
+        torch.cuda.synchronize()
+
+    def run_steps(n, offset=0):
+        if graphs:
+            with torch.cuda.stream(stream):
+                for i in range(n):
+                    graphs[(i + offset) % len(graphs)].replay()
+        else:
+            with torch.cuda.stream(stream):
+                for i in range(n):
+                    step(i + offset)
+
+    # clocks: sample through a short soak and the timed region
+    sampler = ClockSampler(os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    sampler.start()
+    t_soak = time.time()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            run_steps(args.warmup)
+    stream.synchronize()
+    while time.time() - t_soak < args.soak_seconds:
+        run_steps(max(len(layers), 64))
+        stream.synchronize()
+
+    # ---- timed region: exactly args.steps steps ----
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    run_steps(args.steps)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    seconds = ev0.elapsed_time(ev1) / 1e3
+    seconds_max = max_over_ranks(seconds, world, dev)
+    value = aggregate(T, args.steps, world, seconds_max)
+    ms_per_step = seconds_max * 1e3 / args.steps
+
+    # ---- per-kernel durations: eager steps with the library's trace events ----
+    n_prof = min(args.steps, 400)
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_prof)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for c0 in range(0, n_prof, 32):
+            # a bounded device-side delay keeps the GPU behind the host while it enqueues
+            # the next 32 steps, so no host gap falls between a kernel's trace events
+            torch.cuda._sleep(int(4e6))
+            for i in range(c0, min(n_prof, c0 + 32)):
+                lora_set_trace_events(layers[i % len(layers)].handle, ev_sets[i])
+                step(i)
+    torch.cuda.synchronize()
+    for l in layers:
+        lora_set_trace_events(l.handle, None)
+    dur = {"builder": [], "shrink": [], "gemm": []}
+    for evs in ev_sets:
+        dur["builder"].append(evs[0].elapsed_time(evs[1]) * 1e3)
+        dur["shrink"].append(evs[2].elapsed_time(evs[3]) * 1e3)
+        dur["gemm"].append(evs[4].elapsed_time(evs[5]) * 1e3)
+    kern_us = {k: statistics.mean(v) for k, v in dur.items()}
+    t_clock_end = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_soak, t_clock_end)
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        x_h = [inp[0].cpu().pin_memory() for inp in inputs]
+        ids_h = [inp[1].cpu().pin_memory() for inp in inputs]
+        y_h = [torch.empty(T, N, dtype=wl0.dtype).pin_memory() for _ in inputs]
+        with torch.cuda.stream(stream):
+            for i in range(len(layers)):
+                layers[i].forward_host(x_h[i], ids_h[i], y_h[i], stream)
+        stream.synchronize()
+        n_e2e = args.steps
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(n_e2e):
+                j = i % len(layers)
+                layers[j].forward_host(x_h[j], ids_h[j], y_h[j], stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e_sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+        es = 2 if wl0.dtype == torch.bfloat16 else 4
+        e2e = {"value": aggregate(T, n_e2e, world, e_sec), "unit": UNIT,
+               "h2d_bytes_per_step": T * K * es + T * 4, "d2h_bytes_per_step": T * N * es,
+               "ms_per_step": e_sec * 1e3 / n_e2e,
+               "path": "lora_forward_host: pinned x/ids H2D, builder, shrink, GEMM, y D2H"}
+
+    for l in layers:
+        assert l.status(stream) == LORA_OK
+
+    pk = peaks()
+    gemm_s = kern_us["gemm"] * 1e-6
+    achieved = work["gemm_bytes"] / gemm_s / 1e9
+    kernel_src = os.path.join(ROOT, "segmented_rank_gemm_gb300", "csrc", "gemm_tc.cu")
+    roofline = {"kernel": "gemm_tc_kernel (base GEMM + fused expand)", "bound": "hbm",
+                "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"],
+                "traffic": traffic_from_profile(kernel_src, args.config),
+                "peak_source": pk["source"], "algorithmic_bytes_per_launch": work["gemm_bytes"],
+                "avg_launch_us": kern_us["gemm"]}
+    if args.config != "decode_bgmv":
+        tflops = work["base_flops"] / gemm_s / 1e12
+        roofline.update({"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tflops / pk["bf16_tflops"],
+                         "algorithmic_flops_per_launch": work["base_flops"]})
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl0.dtype == torch.bfloat16
+        else "f32", "data": "synthetic (seeded, shapes of the pages' 8B-class workloads)",
+        "config": {"workload": cfg["desc"], "T": T, "K": K, "N": N, "slots": wl0.S,
+                   "slot_rank_width": wl0.R, "distinct_slots": work["distinct_slots"],
+                   "adapted_rows": work["adapted_rows"], "parallelism": "replicas x%d" % world,
+                   "l2": "rotating %d independent layer instances (~%d MB of weights and slots)"
+                         " > 129 MB L2" % (len(layers), len(layers) * work["step_bytes"] // 10**6),
+                   "graphs": not args.no_graph},
+        "roofline": roofline,
+        "step_hbm": {"algorithmic_bytes": work["step_bytes"],
+                     "achieved_gbs": work["step_bytes"] / (ms_per_step * 1e-3) / 1e9,
+                     "frac_of_measured": work["step_bytes"] / (ms_per_step * 1e-3) / 1e9 / pk["hbm_gbs"],
+                     "frac_of_8tbs_spec": work["step_bytes"] / (ms_per_step * 1e-3) / 8e12},
+        "kernels_us": kern_us,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "wall_s_timed": t_wall1 - t_wall0,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl0, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out))
+    for l in layers:
+        l.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------
+# the CPU oracle as a baseline
+# ------------------------------------------------------------------------------------
+
+def _oracle_inputs(wl):
+    import oracle
+    table = oracle.SlotTable(wl.adapters, wl.K, wl.N)
+    x = wl.x.double().numpy()
+    W = wl.W.double().numpy()
+    ids = wl.token_slot.numpy().astype(np.int32)
+    return oracle, table, x, W, ids
+
+
+def cpu_baseline(wl, seconds: float):
+    """The oracle as it stands (plain C fp64, OpenMP over rows) on this host's cores:
+    whole batches repeated until ``seconds`` have passed."""
+    oracle, table, x, W, ids = _oracle_inputs(wl)
+    rows = np.arange(wl.T, dtype=np.int64)
+    t0 = time.time()
+    reps = 0
+    while True:
+        oracle.forward_rows(x, W, table, ids, rows=rows)
+        reps += 1
+        if time.time() - t0 >= seconds:
+            break
+    dt = time.time() - t0
+    return {"value": reps * wl.T / dt, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": "%d repetitions of the full %d-row batch (%.1f s)"
+            % (reps, wl.T, dt)}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return  # the oracle runs on rank 0's host cores only
+    cfg = CONFIGS[args.config]
+    wl = make_workload(args.config, cfg["seed"], "cpu")
+    oracle, table, x, W, ids = _oracle_inputs(wl)
+    threads = oracle.num_threads()
+    # size each step's sample so that the whole run stays within ~2 minutes
+    t0 = time.time()
+    oracle.forward_rows(x, W, table, ids, rows=np.arange(min(threads, wl.T), dtype=np.int64))
+    t_row = (time.time() - t0) / min(threads, wl.T)
+    budget = 120.0 / max(args.steps + args.warmup, 1)
+    n_rows = int(max(1, min(wl.T, budget / max(t_row, 1e-9))))
+    rng = np.random.default_rng(0)
+    samples = [np.sort(rng.choice(wl.T, size=n_rows, replace=False)).astype(np.int64)
+               for _ in range(args.steps + args.warmup)]
+    for i in range(args.warmup):
+        oracle.forward_rows(x, W, table, ids, rows=samples[i])
+    t0 = time.time()
+    for i in range(args.steps):
+        oracle.forward_rows(x, W, table, ids, rows=samples[args.warmup + i])
+    dt = time.time() - t0
+    value = n_rows * args.steps / dt
+    sample = "%d of %d rows per step (seeded), %d steps" % (n_rows, wl.T, args.steps)
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, shapes of the pages' 8B-class workloads)",
+        "config": {"workload": cfg["desc"], "T": wl.T, "K": wl.K, "N": wl.N, "slots": wl.S,
+                   "slot_rank_width": wl.R, "parallelism": "host cores, rank 0"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default="decode_bgmv")
+    ap.add_argument("--layers", type=int, default=8, help="independent instances rotated")
+    ap.add_argument("--soak-seconds", type=float, default=1.5)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3  # at least 3 warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

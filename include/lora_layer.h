@@ -114,9 +114,11 @@ int set_batch_segments(lora_layer_t* layer, const int32_t* token_slot_dev, int T
  * y = x W + per-row LoRA delta, for the batch described by the last set_batch_segments.
  *   x_dev   [T,K] device, y_dev [T,N] device (overwritten; must not overlap x_dev).
  *   T       must equal the T of the last set_batch_segments (else LORA_ESTATE).
- * Enqueues the shrink kernel (v = x A_slot into an fp32 rank-wide buffer, SGMV over the
- * segments) and the base GEMM, whose epilogue adds scale * v B_slot and writes y once.
- * No host synchronisation; no allocation.
+ * Enqueues the low-rank kernel (per segment tile: v = (alpha/r) x A_slot in fp32 and, for
+ * bf16 batches of at most 512 rows, the expand delta = v B_slot in fp32) and the base GEMM
+ * (bf16: tensor cores), whose epilogue adds the low-rank term (v B_slot, or delta) to the
+ * fp32 accumulator and writes y once.  No host synchronisation; no allocation; safe to
+ * capture in a CUDA graph.
  * Errors: LORA_EINVAL, LORA_ESTATE, LORA_ECUDA.
  */
 int lora_forward(lora_layer_t* layer, const void* x_dev, void* y_dev, int T, void* stream);
@@ -153,9 +155,11 @@ int lora_get_segments(lora_layer_t* layer, int32_t* perm, int32_t* seg_offsets,
  *   events   NULL to stop tracing, or an array of 6 cudaEvent_t (as void*) owned by the
  *            caller; afterwards every set_batch_segments records events[0] before and
  *            events[1] after the segment-builder launch, and every lora_forward records
- *            events[2] / events[3] around the shrink launch and events[4] / events[5]
- *            around the base-GEMM launch, each on the call's stream.
- * Tracing adds event records only; it changes no result.  Errors: LORA_EINVAL.
+ *            events[2] / events[3] around the low-rank kernel launch and events[4] /
+ *            events[5] around the base-GEMM launch, each on the call's stream.
+ * Tracing adds event records only; it changes no result (the records between kernels
+ * make each kernel wait for the previous one to finish, so traced kernels do not
+ * overlap).  Errors: LORA_EINVAL.
  */
 int lora_set_trace_events(lora_layer_t* layer, void* const* events);
 

@@ -61,6 +61,9 @@ __global__ void __launch_bounds__(kBuilderThreads, 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
+  // the tile kernel and the base GEMM may be scheduled now; both wait for this grid to
+  // finish before they read what it writes
+  griddep_launch_dependents();
 
   for (int i = tid; i < n_walk * S; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -193,8 +196,8 @@ int builder_smem_bytes(int S, int* n_walk_out) {
 cudaError_t launch_segment_builder(const BuilderArgs& a, cudaStream_t stream) {
   int n_walk = 1;
   const int smem = builder_smem_bytes(a.S, &n_walk);
-  cudaError_t e = cudaFuncSetAttribute(segment_builder_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static int limit = 0;
+  cudaError_t e = ensure_smem_limit(segment_builder_kernel, smem, &limit);
   if (e != cudaSuccess) return e;
   segment_builder_kernel<<<1, kBuilderThreads, smem, stream>>>(
       a.token_slot, a.T, a.S, a.loaded, n_walk, a.rows_per_tile, a.row_slot, a.perm,

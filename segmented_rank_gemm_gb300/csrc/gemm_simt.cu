@@ -60,18 +60,13 @@ __global__ void __launch_bounds__(kSimtThreads)
     __syncthreads();
   }
 
-  // scaled shrink of this tile's rows: vs[m][j] = scale_s * sum over K-chunks of vpart
+  // this tile's rows of v (fp32, already multiplied by alpha / r by the tile kernel)
   if (tid < kSimtTile) rs[tid] = (m0 + tid < a.M) ? ex.row_slot[m0 + tid] : -1;
   __syncthreads();
   for (int e = tid; e < kSimtTile * R; e += kSimtThreads) {
     const int m = e / R, j = e % R;
     const int s = rs[m];
-    if (s >= 0 && j < ex.rank[s]) {
-      float v = 0.f;
-      for (int kc = 0; kc < ex.ksplit; ++kc)
-        v += ex.vpart[((size_t)kc * ex.v_stride_rows + m0 + m) * R + j];
-      vs[m * (R + 1) + j] = ex.scale[s] * v;
-    }
+    if (s >= 0 && j < ex.rank[s]) vs[m * (R + 1) + j] = ex.v[(size_t)(m0 + m) * R + j];
   }
   __syncthreads();
 
@@ -98,8 +93,8 @@ __global__ void __launch_bounds__(kSimtThreads)
 
 cudaError_t launch_gemm_simt_f32(const GemmArgs& a, cudaStream_t stream) {
   const size_t smem = (size_t)kSimtTile * (a.ex.R + 1) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(gemm_simt_f32_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static int limit = 0;
+  cudaError_t e = ensure_smem_limit(gemm_simt_f32_kernel, (int)smem, &limit);
   if (e != cudaSuccess) return e;
   dim3 grid((a.M + kSimtTile - 1) / kSimtTile, (a.N + kSimtTile - 1) / kSimtTile);
   gemm_simt_f32_kernel<<<grid, kSimtThreads, smem, stream>>>(a);

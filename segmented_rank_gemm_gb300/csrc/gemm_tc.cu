@@ -11,11 +11,19 @@
 //               (both K-major, 128-byte swizzle) into a ring of shared-memory stages.
 //   warp 1      allocates BN TMEM columns; one lane issues tcgen05.mma (M=128, N=BN, K=16,
 //               bf16 x bf16 -> fp32 in TMEM) and frees each stage with tcgen05.commit.
-//   warps 2..5  epilogue: each thread owns one output row (one TMEM lane).  It sums the
-//               row's fp32 shrink partials over the K-chunks, scales them by alpha/r, reads
-//               the accumulator 32 columns at a time (tcgen05.ld), adds
-//               sum_j v_j B_slot[j, n] with 16-byte loads of B_slot, rounds to bf16 once and
-//               stores y.  Rows with slot -1 store the base product only.
+//   warps 2..5  epilogue: each thread owns one output row (one TMEM lane).  It reads the
+//               accumulator 32 columns at a time (tcgen05.ld), adds the row's low-rank term
+//               and rounds to bf16 once:
+//                 v mode     sum_j v_j B_slot[j, n], v (fp32, scaled by alpha / r) staged in
+//                            shared memory, B_slot read 4 rank rows x 32 columns at a time;
+//                 delta mode the fp32 delta[row, n] the tile kernel already expanded.
+//               Rows with slot -1 store the base product only.
+// Each CTA starts its K loop at a different K block (and wraps around), so the CTAs that
+// share an x tile (same rows) or a W tile (same columns) do not all request the same lines
+// from L2 at the same moment.
+// Launch: programmatic dependent launch after the tile kernel: the main loop reads only x and
+// W, so it runs while the low-rank kernels finish; the epilogue waits (griddepcontrol.wait)
+// before it reads their results.
 // Every mbarrier wait is bounded (lora_common.cuh): a broken pipeline sets an error flag.
 #include <cudaTypedefs.h>
 
@@ -50,6 +58,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * BN;
   const int nkb = (a.K + kBK - 1) / kBK;
+  const int kb0 = (int)((blockIdx.x + blockIdx.y) % (unsigned)nkb);  // rotated K start
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -74,7 +83,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int it = 0; it < nkb; ++it) {
+        const int kb = (kb0 + it) % nkb;
         if (!mbar_wait(&empty[s], ph ^ 1u, a.err)) break;
         uint8_t* sa = stage_base + (size_t)s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
@@ -93,7 +103,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
       int s = 0;
       uint32_t ph = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int it = 0; it < nkb; ++it) {
         if (!mbar_wait(&full[s], ph, a.err)) break;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(stage_base + (size_t)s * kStageBytes);
@@ -101,7 +111,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           tc_mma_bf16(tmem_base, smem_desc_sw128(a_addr + kk * 32),
-                      smem_desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+                      smem_desc_sw128(b_addr + kk * 32), idesc, (it | kk) != 0 ? 1u : 0u);
         }
         tc_commit(&empty[s]);
         if (++s == stages) {
@@ -113,29 +123,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue: expand + store ----------------
+    // ---------------- epilogue: low-rank term + store ----------------
     const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32) are this warp's
     const int rt = quad * 32 + lane;
     const int row = m0 + rt;
     const ExpandArgs& ex = a.ex;
+    griddep_wait();  // the segment builder and the tile kernel have finished
     int s = -1, r = 0;
     float* vrow = vs + rt * (R + 1);
     if (row < a.M) s = ex.row_slot[row];
-    if (s >= 0) {
+    if (s >= 0 && ex.mode == kExpandV) {
       r = ex.rank[s];
-      const float sc = ex.scale[s];
-      for (int j = 0; j < r; ++j) {
-        float acc = 0.f;
-        for (int kc = 0; kc < ex.ksplit; ++kc)
-          acc += ex.vpart[((size_t)kc * ex.v_stride_rows + row) * R + j];
-        vrow[j] = sc * acc;
-      }
+      const float* vsrc = ex.v + (size_t)row * R;
+      for (int j = 0; j < r; ++j) vrow[j] = vsrc[j];
     }
     mbar_wait(tmem_full, 0, a.err);
     tc_fence_after();
 
     const __nv_bfloat16* Bs =
         s >= 0 ? static_cast<const __nv_bfloat16*>(ex.B_pool) + (size_t)s * R * a.N : nullptr;
+    const float* drow = ex.delta + (size_t)row * a.N;
     __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.y) + (size_t)row * a.N;
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -146,23 +153,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(raw[i]);
       const int n = n0 + c0;
-      if (s >= 0) {
-#pragma unroll 1
-        for (int j = 0; j < r; ++j) {
-          const float vj = vrow[j];
-          const __nv_bfloat16* bj = Bs + (size_t)j * a.N + n;
+      if (s >= 0 && ex.mode == kExpandDelta) {
+        float4 d[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (n + q * 8 < a.N) {
-              const uint4 u = __ldg(reinterpret_cast<const uint4*>(bj + q * 8));
-              acc[q * 8 + 0] = fmaf(vj, bf16_lo(u.x), acc[q * 8 + 0]);
-              acc[q * 8 + 1] = fmaf(vj, bf16_hi(u.x), acc[q * 8 + 1]);
-              acc[q * 8 + 2] = fmaf(vj, bf16_lo(u.y), acc[q * 8 + 2]);
-              acc[q * 8 + 3] = fmaf(vj, bf16_hi(u.y), acc[q * 8 + 3]);
-              acc[q * 8 + 4] = fmaf(vj, bf16_lo(u.z), acc[q * 8 + 4]);
-              acc[q * 8 + 5] = fmaf(vj, bf16_hi(u.z), acc[q * 8 + 5]);
-              acc[q * 8 + 6] = fmaf(vj, bf16_lo(u.w), acc[q * 8 + 6]);
-              acc[q * 8 + 7] = fmaf(vj, bf16_hi(u.w), acc[q * 8 + 7]);
+        for (int q = 0; q < 8; ++q)
+          d[q] = (n + q * 4 < a.N) ? *reinterpret_cast<const float4*>(drow + n + q * 4)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          acc[q * 4 + 0] += d[q].x;
+          acc[q * 4 + 1] += d[q].y;
+          acc[q * 4 + 2] += d[q].z;
+          acc[q * 4 + 3] += d[q].w;
+        }
+      } else if (s >= 0) {
+#pragma unroll 1
+        for (int j0 = 0; j0 < r; j0 += 4) {
+          uint4 b[4][4];  // 4 rank rows x 32 columns, all loads in flight together
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              b[jj][q] = (j0 + jj < r && n + q * 8 < a.N)
+                             ? __ldg(reinterpret_cast<const uint4*>(Bs + (size_t)(j0 + jj) * a.N +
+                                                                    n + q * 8))
+                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const float vj = (j0 + jj < r) ? vrow[j0 + jj] : 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[q * 8 + 0] = fmaf(vj, bf16_lo(b[jj][q].x), acc[q * 8 + 0]);
+              acc[q * 8 + 1] = fmaf(vj, bf16_hi(b[jj][q].x), acc[q * 8 + 1]);
+              acc[q * 8 + 2] = fmaf(vj, bf16_lo(b[jj][q].y), acc[q * 8 + 2]);
+              acc[q * 8 + 3] = fmaf(vj, bf16_hi(b[jj][q].y), acc[q * 8 + 3]);
+              acc[q * 8 + 4] = fmaf(vj, bf16_lo(b[jj][q].z), acc[q * 8 + 4]);
+              acc[q * 8 + 5] = fmaf(vj, bf16_hi(b[jj][q].z), acc[q * 8 + 5]);
+              acc[q * 8 + 6] = fmaf(vj, bf16_lo(b[jj][q].w), acc[q * 8 + 6]);
+              acc[q * 8 + 7] = fmaf(vj, bf16_hi(b[jj][q].w), acc[q * 8 + 7]);
             }
           }
         }
@@ -246,12 +274,20 @@ static cudaError_t launch_tc(const GemmArgs& a, const CUtensorMap& tmap_x,
   const size_t smem = tc_smem_bytes(BN, a.ex.R, stages);
   if (smem > budget) return cudaErrorInvalidConfiguration;
   (void)stage;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static int limit = 0;
+  cudaError_t e = ensure_smem_limit(gemm_tc_kernel<BN>, (int)smem, &limit);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.M + kBM - 1) / kBM, (a.N + BN - 1) / BN);
-  gemm_tc_kernel<BN><<<grid, kTcThreads, smem, stream>>>(tmap_x, tmap_w, a, stages);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((a.M + kBM - 1) / kBM, (a.N + BN - 1) / BN);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmap_x, tmap_w, a, stages);
 }
 
 int gemm_tc_tile_index(int BN) { return BN == 256 ? 0 : (BN == 128 ? 1 : 2); }

@@ -185,6 +185,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 }
 
 // ------------------------------------------------------------------------------------
+// programmatic dependent launch
+// ------------------------------------------------------------------------------------
+// Let the next kernel in the stream (launched with programmatic stream serialization)
+// be scheduled now.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the previous kernel in the stream has completed and its writes are visible
+// (returns at once when this kernel was launched without the attribute).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------------------
 // small numeric helpers
 // ------------------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

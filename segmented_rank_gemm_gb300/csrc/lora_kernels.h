@@ -7,6 +7,18 @@
 
 namespace lora {
 
+constexpr int kTileRows = 16;  // rows per segment tile (builder cut, tile kernel work unit)
+
+// Raise a kernel's dynamic shared-memory limit only when a launch needs more than any
+// earlier launch in this process (so launches under stream capture set no attribute).
+template <typename Kernel>
+inline cudaError_t ensure_smem_limit(Kernel k, int bytes, int* cached) {
+  if (bytes <= *cached) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) *cached = bytes;
+  return e;
+}
+
 // ---- segment builder (builder.cu) ----
 struct BuilderArgs {
   const int32_t* token_slot;  // [T]
@@ -24,29 +36,31 @@ struct BuilderArgs {
 };
 cudaError_t launch_segment_builder(const BuilderArgs& a, cudaStream_t stream);
 
-// ---- shrink v = x A_slot (shrink.cu) ----
-struct ShrinkArgs {
+// ---- low-rank half per segment tile (lora_tile.cu) ----
+struct TileArgs {
   const void* x;  // [T,K] bf16 or f32
-  int T, K, R;
+  int K, N, R;
   const void* At_pool;  // [S][R][K] (transposed slot A, K contiguous)
-  const int32_t* rank;  // [S]
-  const int32_t* perm, *seg_offsets, *seg_slot, *tile_seg, *tile_row0, *meta;
-  int rows_per_tile;
-  int ksplit, kchunk;   // K cut into ksplit chunks of kchunk elements
-  float* vpart;         // [ksplit][v_stride_rows][R]
-  int v_stride_rows;    // rows per k-split plane (max_tokens)
-  int max_items;        // upper bound of tiles * ksplit (grid sizing)
-  int num_sms;
-};
-cudaError_t launch_shrink(const ShrinkArgs& a, bool bf16, cudaStream_t stream);
-
-// ---- base GEMM with the expand fused into its epilogue ----
-struct ExpandArgs {
-  const int32_t* row_slot;  // [T], -1 = base only
-  const float* vpart;       // [ksplit][v_stride_rows][R]
-  int ksplit, v_stride_rows, R;
   const void* B_pool;   // [S][R][N]
   const float* scale;   // [S]
+  const int32_t* rank;  // [S]
+  const int32_t* perm, *seg_offsets, *seg_slot, *tile_seg, *tile_row0, *meta;
+  float* out;           // v [T_max][R] (v mode) or delta [T_max][N] (delta mode), fp32
+  int max_tiles;        // upper bound of the builder's tile count (grid sizing)
+  int num_sms;
+};
+// Launched with programmatic stream serialization (it waits for the builder itself).
+cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStream_t stream);
+
+// ---- base GEMM with the low-rank term added in its epilogue ----
+enum ExpandMode { kExpandV = 0, kExpandDelta = 1 };
+struct ExpandArgs {
+  int mode;                 // kExpandV: y += v B_slot;  kExpandDelta: y += delta
+  const int32_t* row_slot;  // [T], -1 = base only
+  const float* v;           // [T_max][R] fp32, already scaled by alpha / r   (v mode)
+  const float* delta;       // [T_max][N] fp32                                (delta mode)
+  int R;
+  const void* B_pool;   // [S][R][N]
   const int32_t* rank;  // [S]
 };
 struct GemmArgs {

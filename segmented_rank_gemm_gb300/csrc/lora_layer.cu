@@ -3,9 +3,14 @@
 //
 // Every step of the computation runs in this library's kernels:
 //   set_batch_segments -> segment_builder_kernel            (builder.cu)
-//   lora_forward       -> shrink_kernel (SGMV/BGMV shrink)  (shrink.cu)
-//                      -> gemm_tc_kernel (bf16, tcgen05)    (gemm_tc.cu)  or
-//                         gemm_simt_f32_kernel (fp32)       (gemm_simt.cu)
+//   lora_forward       -> lora_tile_kernel (shrink; expand in delta mode)  (lora_tile.cu)
+//                      -> gemm_tc_kernel (bf16, tcgen05)                   (gemm_tc.cu)  or
+//                         gemm_simt_f32_kernel (fp32)                      (gemm_simt.cu)
+// Two regimes: batches of at most kDeltaMaxT rows (decode) use delta mode -- the tile
+// kernel expands the low-rank term into an fp32 [T,N] buffer the GEMM epilogue adds; larger
+// batches (prefill) use v mode -- the tile kernel writes v [T,r] and the GEMM epilogue
+// expands it.  bf16 launches chain with programmatic dependent launch (builder -> tile
+// kernel -> GEMM), so the GEMM main loop overlaps the low-rank kernels.
 //   load_adapter_slot  -> copy + transpose_pad_kernel + slot_meta_kernel (slots.cu)
 #include <cuda_runtime.h>
 
@@ -27,8 +32,7 @@ namespace {
 constexpr int kMaxSlots = 4096;
 constexpr int kMaxRank = 128;
 constexpr int kMaxTokens = 1 << 20;
-constexpr int kShrinkRowsPerTile = 16;
-constexpr int kMaxKSplit = 8;
+constexpr int kDeltaMaxT = 512;  // largest batch computed in delta mode
 
 }  // namespace
 
@@ -51,7 +55,8 @@ struct lora_layer {
   int32_t* tile_row0 = nullptr;  // [max_tiles]
   int32_t* meta = nullptr;       // [4]
   int32_t* err = nullptr;        // [1]
-  float* vpart = nullptr;        // [kMaxKSplit][T_max][R]
+  float* v = nullptr;            // [T_max][R]   fp32, scaled by alpha / r (v mode)
+  float* delta = nullptr;        // [min(T_max, kDeltaMaxT)][N] fp32 (delta mode, bf16)
   int max_tiles = 0;
   int T_batch = -1;              // T of the last set_batch_segments, -1 = none
   // staging for lora_forward_host
@@ -100,7 +105,7 @@ cudaError_t dmalloc(T** p, size_t count) {
 void free_all(lora_layer* L) {
   void* ptrs[] = {L->Wp, L->A_pool, L->B_pool, L->A_stage, L->scale, L->rank, L->loaded,
                   L->row_slot, L->perm, L->seg_offsets, L->seg_slot, L->tile_seg,
-                  L->tile_row0, L->meta, L->err, L->vpart, L->x_stage, L->ids_stage,
+                  L->tile_row0, L->meta, L->err, L->v, L->delta, L->x_stage, L->ids_stage,
                   L->y_stage};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -118,20 +123,6 @@ bool is_capturing(cudaStream_t s) {
   cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(s, &st) != cudaSuccess) return false;
   return st != cudaStreamCaptureStatusNone;
-}
-
-// Split K into chunks so that (expected tiles) x (chunks) covers the SMs a few times over.
-void choose_ksplit(const lora_layer* L, int T, int* ksplit, int* kchunk) {
-  const int vec = 256;  // a warp's 32 lanes x 8 bf16
-  const int est_tiles = std::max(1, std::min(T, L->S) + T / kShrinkRowsPerTile);
-  int ks = (4 * L->num_sms + est_tiles - 1) / est_tiles;
-  ks = std::max(1, std::min(ks, kMaxKSplit));
-  ks = std::min(ks, std::max(1, L->K / vec));
-  int kc = (L->K + ks - 1) / ks;
-  kc = ((kc + vec - 1) / vec) * vec;
-  ks = (L->K + kc - 1) / kc;
-  *ksplit = ks;
-  *kchunk = kc;
 }
 
 }  // namespace
@@ -171,7 +162,7 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
 
   const size_t es = L->esize;
   const size_t S = num_slots, R = max_rank;
-  L->max_tiles = (max_tokens + kShrinkRowsPerTile - 1) / kShrinkRowsPerTile + num_slots;
+  L->max_tiles = (max_tokens + kTileRows - 1) / kTileRows + num_slots;
   bool ok = cudaMalloc(&L->Wp, (size_t)K * N * es) == cudaSuccess &&
             cudaMalloc(&L->A_pool, S * R * K * es) == cudaSuccess &&
             cudaMalloc(&L->B_pool, S * R * N * es) == cudaSuccess &&
@@ -185,7 +176,9 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
             dmalloc(&L->tile_seg, L->max_tiles) == cudaSuccess &&
             dmalloc(&L->tile_row0, L->max_tiles) == cudaSuccess &&
             dmalloc(&L->meta, 4) == cudaSuccess && dmalloc(&L->err, 1) == cudaSuccess &&
-            dmalloc(&L->vpart, (size_t)kMaxKSplit * max_tokens * R) == cudaSuccess &&
+            dmalloc(&L->v, (size_t)max_tokens * R) == cudaSuccess &&
+            (dtype != LORA_BF16 ||
+             dmalloc(&L->delta, (size_t)std::min(max_tokens, kDeltaMaxT) * N) == cudaSuccess) &&
             cudaMalloc(&L->x_stage, (size_t)max_tokens * K * es) == cudaSuccess &&
             dmalloc(&L->ids_stage, max_tokens) == cudaSuccess &&
             cudaMalloc(&L->y_stage, (size_t)max_tokens * N * es) == cudaSuccess;
@@ -204,8 +197,7 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
        cudaMemsetAsync(L->loaded, 0, S * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->meta, 0, 16, stream) == cudaSuccess &&
        cudaMemsetAsync(L->err, 0, 4, stream) == cudaSuccess &&
-       cudaMemsetAsync(L->vpart, 0, (size_t)kMaxKSplit * max_tokens * R * 4, stream) ==
-           cudaSuccess;
+       cudaMemsetAsync(L->v, 0, (size_t)max_tokens * R * 4, stream) == cudaSuccess;
   if (!ok) return bail(LORA_ECUDA);
 
   if (dtype == LORA_BF16) {
@@ -296,7 +288,7 @@ int set_batch_segments(lora_layer_t* L, const int32_t* token_slot_dev, int T, vo
   a.T = T;
   a.S = L->S;
   a.loaded = L->loaded;
-  a.rows_per_tile = kShrinkRowsPerTile;
+  a.rows_per_tile = kTileRows;
   a.row_slot = L->row_slot;
   a.perm = L->perm;
   a.seg_offsets = L->seg_offsets;
@@ -332,31 +324,29 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   L->spare.insert(L->spare.end(), L->pending.begin(), L->pending.end());
   L->pending.clear();
 
-  int ksplit = 1, kchunk = L->K;
-  choose_ksplit(L, T, &ksplit, &kchunk);
+  const bool bf16 = L->dtype == LORA_BF16;
+  const bool delta_mode = bf16 && T <= kDeltaMaxT;
 
-  ShrinkArgs sa;
-  sa.x = x_dev;
-  sa.T = T;
-  sa.K = L->K;
-  sa.R = L->R;
-  sa.At_pool = L->A_pool;
-  sa.rank = L->rank;
-  sa.perm = L->perm;
-  sa.seg_offsets = L->seg_offsets;
-  sa.seg_slot = L->seg_slot;
-  sa.tile_seg = L->tile_seg;
-  sa.tile_row0 = L->tile_row0;
-  sa.meta = L->meta;
-  sa.rows_per_tile = kShrinkRowsPerTile;
-  sa.ksplit = ksplit;
-  sa.kchunk = kchunk;
-  sa.vpart = L->vpart;
-  sa.v_stride_rows = L->T_max;
-  sa.max_items = ((T + kShrinkRowsPerTile - 1) / kShrinkRowsPerTile + std::min(T, L->S)) * ksplit;
-  sa.num_sms = L->num_sms;
+  TileArgs ta;
+  ta.x = x_dev;
+  ta.K = L->K;
+  ta.N = L->N;
+  ta.R = L->R;
+  ta.At_pool = L->A_pool;
+  ta.B_pool = L->B_pool;
+  ta.scale = L->scale;
+  ta.rank = L->rank;
+  ta.perm = L->perm;
+  ta.seg_offsets = L->seg_offsets;
+  ta.seg_slot = L->seg_slot;
+  ta.tile_seg = L->tile_seg;
+  ta.tile_row0 = L->tile_row0;
+  ta.meta = L->meta;
+  ta.out = delta_mode ? L->delta : L->v;
+  ta.max_tiles = (T + kTileRows - 1) / kTileRows + std::min(T, L->S);
+  ta.num_sms = L->num_sms;
   LORA_CUDA(L, trace_mark(L, 2, stream));
-  LORA_CUDA(L, launch_shrink(sa, L->dtype == LORA_BF16, stream));
+  LORA_CUDA(L, launch_lora_tile(ta, bf16, delta_mode, stream));
   LORA_CUDA(L, trace_mark(L, 3, stream));
 
   GemmArgs ga;
@@ -366,18 +356,17 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.x = x_dev;
   ga.W = L->Wp;
   ga.y = y_dev;
+  ga.ex.mode = delta_mode ? kExpandDelta : kExpandV;
   ga.ex.row_slot = L->row_slot;
-  ga.ex.vpart = L->vpart;
-  ga.ex.ksplit = ksplit;
-  ga.ex.v_stride_rows = L->T_max;
+  ga.ex.v = L->v;
+  ga.ex.delta = L->delta;
   ga.ex.R = L->R;
   ga.ex.B_pool = L->B_pool;
-  ga.ex.scale = L->scale;
   ga.ex.rank = L->rank;
   ga.err = L->err;
   ga.num_sms = L->num_sms;
   LORA_CUDA(L, trace_mark(L, 4, stream));
-  if (L->dtype == LORA_BF16)
+  if (bf16)
     LORA_CUDA(L, launch_gemm_tc(ga, L->tmap_w, stream));
   else
     LORA_CUDA(L, launch_gemm_simt_f32(ga, stream));

@@ -1,0 +1,270 @@
+// lora_tile.cu -- the low-rank half of the layer per segment tile: shrink v = x A_slot and,
+// in delta mode, expand delta = scale * v B_slot.
+//
+// "Serving multiple LoRAs: segmented matrix multiplies and adapter scheduling", section
+// "Not merging the weights, computing in batches": SGMV groups the tokens of one adapter
+// and runs one small matrix multiply per segment; BGMV gathers each token's A and B; real
+// kernels shrink (x -> xA, down to r) and then expand ((xA)B) and add to the base output.
+// "Serving LoRA adapters ..." (vLLM) Step 4: the shrink result is an fp32 buffer of rank
+// width.
+//
+// Work list: the segment builder cut every segment into tiles of <= 16 rows sharing one
+// slot.  One CTA (8 warps) takes one tile at a time:
+//   shrink   warp w owns rank columns [w*JW, w*JW + JW); its lanes split K into 16-byte
+//            vectors and accumulate a block of RB rows x JW columns (RB * JW <= 16) in
+//            registers, so each A vector is loaded once per RB rows and each lane keeps
+//            RB + JW independent 16-byte loads in flight; a butterfly shuffle sums the
+//            lanes.  v (fp32, already multiplied by alpha / r) goes to shared memory.
+//   v mode   v is written to global memory [row][j]; the base GEMM's epilogue expands it.
+//   delta    each thread owns 8 consecutive output columns, loads up to 16 rank rows of
+//   mode     B_slot at once, and writes delta[row][n] = sum_j v[row][j] B[j][n] in fp32;
+//            the base GEMM's epilogue adds it before its single rounding of y.
+// Only the true rank r of the slot is read: the zero padding of the slot never is.
+//
+// Launch: programmatic dependent launch.  The kernel lets the next kernel (the base GEMM,
+// whose main loop needs nothing from it) launch at once, then waits for the segment
+// builder's results before reading them.
+#include "lora_common.cuh"
+#include "lora_kernels.h"
+
+namespace lora {
+
+static constexpr int kTileThreads = 256;
+
+template <typename T>
+struct Vec16;  // 16 bytes of T widened to fp32
+
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  uint4 raw;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+    raw = __ldg(reinterpret_cast<const uint4*>(p));
+  }
+  __device__ __forceinline__ float operator[](int e) const {
+    const uint32_t w = e < 2 ? raw.x : e < 4 ? raw.y : e < 6 ? raw.z : raw.w;
+    return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+  }
+};
+
+template <>
+struct Vec16<float> {  // 4 floats
+  static constexpr int N = 4;
+  float4 raw;
+  __device__ __forceinline__ void load(const float* p) {
+    raw = __ldg(reinterpret_cast<const float4*>(p));
+  }
+  __device__ __forceinline__ float operator[](int e) const {
+    return e == 0 ? raw.x : e == 1 ? raw.y : e == 2 ? raw.z : raw.w;
+  }
+};
+
+// One float: the fp32 path when K is not a multiple of 4 or x is not 16-byte aligned.
+struct Scalar32 {
+  static constexpr int N = 1;
+  float raw;
+  __device__ __forceinline__ void load(const float* p) { raw = __ldg(p); }
+  __device__ __forceinline__ float operator[](int) const { return raw; }
+};
+
+// Shrink of one tile by one warp: v_s[q][j] = sc * sum_k x[row_q][k] * At[j][k] for the
+// warp's JW rank columns.  K is a multiple of the vector width (checked on the host).
+template <typename T, typename V, int JW>
+__device__ __forceinline__ void shrink_tile_warp(const T* __restrict__ x, int K,
+                                                 const T* __restrict__ At, int r,
+                                                 const int* rows_s, int nr, float sc,
+                                                 float* v_s, int vstride, int warp, int lane) {
+  constexpr int RB = (16 / JW) < 8 ? (16 / JW) : 8;  // rows per register block
+  constexpr int VEC = V::N;
+  const int j0 = warp * JW;
+  if (j0 >= r) return;
+  const T* ar[JW];
+#pragma unroll
+  for (int jj = 0; jj < JW; ++jj) ar[jj] = At + (size_t)min(j0 + jj, r - 1) * K;
+
+  for (int q0 = 0; q0 < nr; q0 += RB) {
+    const T* xr[RB];
+#pragma unroll
+    for (int qq = 0; qq < RB; ++qq) xr[qq] = x + (size_t)rows_s[min(q0 + qq, nr - 1)] * K;
+    float acc[RB][JW];
+#pragma unroll
+    for (int qq = 0; qq < RB; ++qq)
+#pragma unroll
+      for (int jj = 0; jj < JW; ++jj) acc[qq][jj] = 0.f;
+
+    for (int k = lane * VEC; k < K; k += 32 * VEC) {
+      V xv[RB], av[JW];
+#pragma unroll
+      for (int qq = 0; qq < RB; ++qq) xv[qq].load(xr[qq] + k);
+#pragma unroll
+      for (int jj = 0; jj < JW; ++jj) av[jj].load(ar[jj] + k);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e)
+#pragma unroll
+        for (int qq = 0; qq < RB; ++qq)
+#pragma unroll
+          for (int jj = 0; jj < JW; ++jj) acc[qq][jj] = fmaf(xv[qq][e], av[jj][e], acc[qq][jj]);
+    }
+#pragma unroll
+    for (int qq = 0; qq < RB; ++qq)
+#pragma unroll
+      for (int jj = 0; jj < JW; ++jj) {
+        float s = acc[qq][jj];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        acc[qq][jj] = s;
+      }
+    if (lane == 0) {
+#pragma unroll
+      for (int qq = 0; qq < RB; ++qq)
+#pragma unroll
+        for (int jj = 0; jj < JW; ++jj)
+          if (q0 + qq < nr && j0 + jj < r) v_s[(q0 + qq) * vstride + j0 + jj] = sc * acc[qq][jj];
+    }
+  }
+}
+
+// Expand of one tile: delta[row_q][n..n+8) = sum_j v_s[q][j] * B[j][n..n+8), fp32 out.
+__device__ __forceinline__ void expand_tile_delta(const __nv_bfloat16* __restrict__ Bs, int N,
+                                                  int r, const float* v_s, int vstride,
+                                                  const int* rows_s, int nr,
+                                                  float* __restrict__ delta, int tid) {
+  for (int n = tid * 8; n < N; n += kTileThreads * 8) {
+    for (int q0 = 0; q0 < nr; q0 += 4) {
+      float acc[4][8];
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[qq][e] = 0.f;
+      for (int j0 = 0; j0 < r; j0 += 16) {
+        uint4 b[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          b[jj] = (j0 + jj < r) ? __ldg(reinterpret_cast<const uint4*>(Bs + (size_t)(j0 + jj) * N + n))
+                                : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const int q = min(q0 + qq, nr - 1);
+            const float vj = (j0 + jj < r) ? v_s[q * vstride + j0 + jj] : 0.f;
+            acc[qq][0] = fmaf(vj, bf16_lo(b[jj].x), acc[qq][0]);
+            acc[qq][1] = fmaf(vj, bf16_hi(b[jj].x), acc[qq][1]);
+            acc[qq][2] = fmaf(vj, bf16_lo(b[jj].y), acc[qq][2]);
+            acc[qq][3] = fmaf(vj, bf16_hi(b[jj].y), acc[qq][3]);
+            acc[qq][4] = fmaf(vj, bf16_lo(b[jj].z), acc[qq][4]);
+            acc[qq][5] = fmaf(vj, bf16_hi(b[jj].z), acc[qq][5]);
+            acc[qq][6] = fmaf(vj, bf16_lo(b[jj].w), acc[qq][6]);
+            acc[qq][7] = fmaf(vj, bf16_hi(b[jj].w), acc[qq][7]);
+          }
+        }
+      }
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        if (q0 + qq < nr) {
+          float4* d = reinterpret_cast<float4*>(delta + (size_t)rows_s[q0 + qq] * N + n);
+          d[0] = make_float4(acc[qq][0], acc[qq][1], acc[qq][2], acc[qq][3]);
+          d[1] = make_float4(acc[qq][4], acc[qq][5], acc[qq][6], acc[qq][7]);
+        }
+      }
+    }
+  }
+}
+
+// <= 128 registers a thread: two CTAs of this kernel, or one beside a base-GEMM CTA, fit
+// on an SM, so the GEMM launched after it can start while it runs.
+template <typename T, typename V, bool kDelta>
+__global__ void __launch_bounds__(kTileThreads, 2)
+    lora_tile_kernel(const T* __restrict__ x, int K, int N, int R,
+                     const T* __restrict__ At_pool, const T* __restrict__ B_pool,
+                     const float* __restrict__ scale, const int32_t* __restrict__ rank,
+                     const int32_t* __restrict__ perm, const int32_t* __restrict__ seg_offsets,
+                     const int32_t* __restrict__ seg_slot, const int32_t* __restrict__ tile_seg,
+                     const int32_t* __restrict__ tile_row0, const int32_t* __restrict__ meta,
+                     float* __restrict__ out /* v [T][R] or delta [T][N] */) {
+  griddep_launch_dependents();
+  griddep_wait();
+  __shared__ int rows_s[kTileRows];
+  __shared__ float v_s[kTileRows * 129];
+  const int vstride = R + 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_tiles = meta[2];
+
+  for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const int g = tile_seg[t];
+    const int s = seg_slot[g];
+    const int r = rank[s];
+    const float sc = scale[s];
+    const int p0 = tile_row0[t];
+    const int nr = min(kTileRows, seg_offsets[g + 1] - p0);
+    if (tid < nr) rows_s[tid] = perm[p0 + tid];
+    __syncthreads();
+    const T* At = At_pool + (size_t)s * R * K;
+    if (r <= 8)
+      shrink_tile_warp<T, V, 1>(x, K, At, r, rows_s, nr, sc, v_s, vstride, warp, lane);
+    else if (r <= 16)
+      shrink_tile_warp<T, V, 2>(x, K, At, r, rows_s, nr, sc, v_s, vstride, warp, lane);
+    else if (r <= 32)
+      shrink_tile_warp<T, V, 4>(x, K, At, r, rows_s, nr, sc, v_s, vstride, warp, lane);
+    else if (r <= 64)
+      shrink_tile_warp<T, V, 8>(x, K, At, r, rows_s, nr, sc, v_s, vstride, warp, lane);
+    else
+      shrink_tile_warp<T, V, 16>(x, K, At, r, rows_s, nr, sc, v_s, vstride, warp, lane);
+    __syncthreads();
+    if constexpr (kDelta) {
+      expand_tile_delta(reinterpret_cast<const __nv_bfloat16*>(B_pool) + (size_t)s * R * N, N, r,
+                        v_s, vstride, rows_s, nr, out, tid);
+    } else {
+      for (int i = tid; i < nr * r; i += kTileThreads) {
+        const int q = i / r, j = i - q * r;
+        out[(size_t)rows_s[q] * R + j] = v_s[q * vstride + j];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStream_t stream) {
+  int grid = a.max_tiles;
+  if (grid > a.num_sms * 4) grid = a.num_sms * 4;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTileThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (bf16) {
+    using T = __nv_bfloat16;
+    using V = Vec16<T>;
+    const T* x = static_cast<const T*>(a.x);
+    const T* At = static_cast<const T*>(a.At_pool);
+    const T* B = static_cast<const T*>(a.B_pool);
+    if (delta)
+      return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, V, true>, x, a.K, a.N, a.R, At, B,
+                                a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
+                                a.tile_row0, a.meta, a.out);
+    return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, V, false>, x, a.K, a.N, a.R, At, B,
+                              a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
+                              a.tile_row0, a.meta, a.out);
+  }
+  if (delta) return cudaErrorInvalidValue;  // delta mode is a bf16 path
+  using T = float;
+  const T* x = static_cast<const T*>(a.x);
+  const T* At = static_cast<const T*>(a.At_pool);
+  const T* B = static_cast<const T*>(a.B_pool);
+  const bool vec4 = a.K % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0;
+  if (vec4)
+    return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, Vec16<T>, false>, x, a.K, a.N, a.R, At, B,
+                              a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
+                              a.tile_row0, a.meta, a.out);
+  return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, Scalar32, false>, x, a.K, a.N, a.R, At, B,
+                            a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
+                            a.tile_row0, a.meta, a.out);
+}
+
+}  // namespace lora

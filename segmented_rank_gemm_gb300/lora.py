@@ -158,6 +158,9 @@ def lora_set_trace_events(layer, events) -> None:
     if events is None:
         _check(layer, _lib.lora_set_trace_events(layer, None))
         return
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on its first record
+            e.record()
     arr = (ctypes.c_void_p * 6)(*[e.cuda_event for e in events])
     _check(layer, _lib.lora_set_trace_events(layer, ctypes.cast(arr, ctypes.c_void_p)))
 
