@@ -1,30 +1,39 @@
-// gemm_tc.cu -- base GEMM y = x W on the fifth-generation tensor cores, with the LoRA expand
-// y += scale_slot * v B_slot fused into the epilogue so that y is written once.
+// gemm_tc.cu -- base GEMM y = x W on the fifth-generation tensor cores, with the layer's
+// low-rank term added in the epilogue so that y is written once.
 //
 // "LoRAX, in depth", section "Computing a batch that mixes adapters": the base term is the
 // same for every request, so it runs as one large GEMM over all tokens; only the low-rank
 // term differs by adapter.  "Serving LoRA adapters ..." (vLLM) Step 4: the expand multiplies
 // the fp32 rank buffer by B and adds it to the base output.
 //
-// Kernel structure (one 128 x BN output tile per CTA, 6 warps):
+// One CTA computes a 128 x BN block of y over a range of K blocks (6 warps):
 //   warp 0      TMA producer: 64-wide K blocks of x [M,K] and of the packed weight W^T [N,K]
 //               (both K-major, 128-byte swizzle) into a ring of shared-memory stages.
 //   warp 1      allocates BN TMEM columns; one lane issues tcgen05.mma (M=128, N=BN, K=16,
 //               bf16 x bf16 -> fp32 in TMEM) and frees each stage with tcgen05.commit.
-//   warps 2..5  epilogue: each thread owns one output row (one TMEM lane).  It reads the
+//   warps 2..5  epilogue: each thread owns one output row (one TMEM lane); it reads the
 //               accumulator 32 columns at a time (tcgen05.ld), adds the row's low-rank term
 //               and rounds to bf16 once:
-//                 v mode     sum_j v_j B_slot[j, n], v (fp32, scaled by alpha / r) staged in
-//                            shared memory, B_slot read 4 rank rows x 32 columns at a time;
+//                 v mode     sum_j v_j B_slot[j, n] (v fp32, already scaled by alpha / r,
+//                            staged in shared memory; B_slot read 4 rank rows x 32 columns
+//                            per batch of loads);
 //                 delta mode the fp32 delta[row, n] the tile kernel already expanded.
 //               Rows with slot -1 store the base product only.
-// Each CTA starts its K loop at a different K block (and wraps around), so the CTAs that
-// share an x tile (same rows) or a W tile (same columns) do not all request the same lines
-// from L2 at the same moment.
+// Split K (small batches): the grid's z dimension cuts K into `cs` <= 4 ranges and the cs
+// CTAs of one output block form a thread-block cluster.  After a cluster barrier (every main
+// loop done, so the stage buffers are idle) each CTA copies, for every other CTA d, its fp32
+// partial of the columns d owns from TMEM into a local send buffer and pushes it with one
+// bulk copy (cp.async.bulk shared::cta -> shared::cluster) into d's receive buffer,
+// completing on d's mbarrier; each CTA then adds the cs - 1 partials it received to its own
+// and runs the epilogue on its BN / cs columns.  A small batch thereby keeps W (not the
+// re-read x) dominant in every stage and needs 1/cs of the K range per SM.  Send and
+// receive rows are stored with their 16-byte chunks XOR-swizzled by row, so the row-per-
+// thread accesses avoid shared-memory bank conflicts.
+// Each CTA starts its K range at a rotated K block (and wraps around), so the CTAs that
+// share an x tile or a W tile do not all request the same lines from L2 at the same moment.
 // Launch: programmatic dependent launch after the tile kernel: the main loop reads only x and
 // W, so it runs while the low-rank kernels finish; the epilogue waits (griddepcontrol.wait)
-// before it reads their results.
-// Every mbarrier wait is bounded (lora_common.cuh): a broken pipeline sets an error flag.
+// before reading their results.  Every mbarrier wait is bounded (lora_common.cuh).
 #include <cudaTypedefs.h>
 
 #include "lora_common.cuh"
@@ -36,29 +45,97 @@ static constexpr int kTcThreads = 192;
 static constexpr int kBM = 128, kBK = 64;
 static constexpr int kABytes = kBM * kBK * 2;
 
+// Add the row's low-rank term to 32 accumulator columns starting at global column n and
+// store them as bf16 (d: the row's delta for these columns, loaded by the caller).
+__device__ __forceinline__ void epilogue_chunk32(float (&acc)[32], const GemmArgs& a, int row,
+                                                 int n, int s, int r, const float* vrow,
+                                                 const __nv_bfloat16* Bs, const float4* d,
+                                                 __nv_bfloat16* yrow) {
+  const ExpandArgs& ex = a.ex;
+  if (s >= 0 && ex.mode == kExpandDelta) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      acc[q * 4 + 0] += d[q].x;
+      acc[q * 4 + 1] += d[q].y;
+      acc[q * 4 + 2] += d[q].z;
+      acc[q * 4 + 3] += d[q].w;
+    }
+  } else if (s >= 0) {
+#pragma unroll 1
+    for (int j0 = 0; j0 < r; j0 += 4) {
+      uint4 b[4][4];  // 4 rank rows x 32 columns, all loads in flight together
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          b[jj][q] = (j0 + jj < r && n + q * 8 < a.N)
+                         ? __ldg(reinterpret_cast<const uint4*>(Bs + (size_t)(j0 + jj) * a.N + n +
+                                                                q * 8))
+                         : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const float vj = (j0 + jj < r) ? vrow[j0 + jj] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[q * 8 + 0] = fmaf(vj, bf16_lo(b[jj][q].x), acc[q * 8 + 0]);
+          acc[q * 8 + 1] = fmaf(vj, bf16_hi(b[jj][q].x), acc[q * 8 + 1]);
+          acc[q * 8 + 2] = fmaf(vj, bf16_lo(b[jj][q].y), acc[q * 8 + 2]);
+          acc[q * 8 + 3] = fmaf(vj, bf16_hi(b[jj][q].y), acc[q * 8 + 3]);
+          acc[q * 8 + 4] = fmaf(vj, bf16_lo(b[jj][q].z), acc[q * 8 + 4]);
+          acc[q * 8 + 5] = fmaf(vj, bf16_hi(b[jj][q].z), acc[q * 8 + 5]);
+          acc[q * 8 + 6] = fmaf(vj, bf16_lo(b[jj][q].w), acc[q * 8 + 6]);
+          acc[q * 8 + 7] = fmaf(vj, bf16_hi(b[jj][q].w), acc[q * 8 + 7]);
+        }
+      }
+    }
+  }
+  if (row < a.M) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (n + q * 8 < a.N) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[q * 8 + 0], acc[q * 8 + 1]);
+        o.y = pack_bf16x2(acc[q * 8 + 2], acc[q * 8 + 3]);
+        o.z = pack_bf16x2(acc[q * 8 + 4], acc[q * 8 + 5]);
+        o.w = pack_bf16x2(acc[q * 8 + 6], acc[q * 8 + 7]);
+        *reinterpret_cast<uint4*>(yrow + n + q * 8) = o;
+      }
+    }
+  }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                   const __grid_constant__ CUtensorMap tmap_w, GemmArgs a, int stages) {
+                   const __grid_constant__ CUtensorMap tmap_w, GemmArgs a, int stages,
+                   int v_smem_rank) {
   constexpr int kBBytes = BN * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
   const int R = a.ex.R;
+  const int vR = v_smem_rank;  // rank width staged in shared memory (0 in delta mode)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stage_base = smem;
   float* vs = reinterpret_cast<float*>(smem + (size_t)stages * kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(vs + kBM * (R + 1));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(vs + kBM * (vR + 1));
   uint64_t* full = bars;
   uint64_t* empty = bars + stages;
   uint64_t* tmem_full = bars + 2 * stages;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * stages + 1);
+  uint64_t* xchg_bar = bars + 2 * stages + 1;  // split K: partials received from the peers
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * stages + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * BN;
-  const int nkb = (a.K + kBK - 1) / kBK;
-  const int kb0 = (int)((blockIdx.x + blockIdx.y) % (unsigned)nkb);  // rotated K start
+  // split K: this CTA's range of K blocks (the host keeps every range non-empty)
+  const int cs = gridDim.z, z = blockIdx.z;
+  const int nkb_all = (a.K + kBK - 1) / kBK;
+  const int per = (nkb_all + cs - 1) / cs;
+  const int kb_begin = z * per;
+  const int nkb = min(nkb_all, kb_begin + per) - kb_begin;
+  const int rot = (int)((blockIdx.x + blockIdx.y) % (unsigned)nkb);
+  const int bnc = BN / cs;  // columns this CTA finishes
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -66,6 +143,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
+    mbar_init(xchg_bar, 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -84,7 +162,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       for (int it = 0; it < nkb; ++it) {
-        const int kb = (kb0 + it) % nkb;
+        const int kb = kb_begin + (rot + it) % nkb;
         if (!mbar_wait(&empty[s], ph ^ 1u, a.err)) break;
         uint8_t* sa = stage_base + (size_t)s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
@@ -122,93 +200,124 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_commit(tmem_full);
     }
     __syncwarp();
-  } else {
-    // ---------------- epilogue: low-rank term + store ----------------
-    const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32) are this warp's
-    const int rt = quad * 32 + lane;
-    const int row = m0 + rt;
-    const ExpandArgs& ex = a.ex;
-    griddep_wait();  // the segment builder and the tile kernel have finished
-    int s = -1, r = 0;
-    float* vrow = vs + rt * (R + 1);
-    if (row < a.M) s = ex.row_slot[row];
-    if (s >= 0 && ex.mode == kExpandV) {
-      r = ex.rank[s];
-      const float* vsrc = ex.v + (size_t)row * R;
+  }
+
+  // ---------------- epilogue warps: row data, then wait for the accumulator ----------------
+  const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32) belong to this warp
+  const int rt = quad * 32 + lane;
+  const int row = m0 + rt;
+  const bool epi = warp >= 2;
+  const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+  int s = -1, r = 0;
+  float* vrow = vs + rt * (vR + 1);
+  if (epi) {
+    griddep_wait();  // the low-rank kernel has finished
+    if (row < a.M) {
+      if (a.ex.mode == kExpandV) {
+        s = a.ex.row_slot[row];  // checked by the builder
+      } else {
+        const int t = a.ex.token_slot[row];
+        s = (t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0) ? t : -1;
+      }
+    }
+    if (s >= 0 && a.ex.mode == kExpandV) {
+      r = a.ex.rank[s];
+      const float* vsrc = a.ex.v + (size_t)row * R;
       for (int j = 0; j < r; ++j) vrow[j] = vsrc[j];
     }
     mbar_wait(tmem_full, 0, a.err);
     tc_fence_after();
+  }
 
-    const __nv_bfloat16* Bs =
-        s >= 0 ? static_cast<const __nv_bfloat16*>(ex.B_pool) + (size_t)s * R * a.N : nullptr;
-    const float* drow = ex.delta + (size_t)row * a.N;
-    __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.y) + (size_t)row * a.N;
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      uint32_t raw[32];
-      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + c0, raw);
-      tmem_ld_wait();
-      float acc[32];
+  // ---------------- split K: exchange partial accumulators inside the cluster ----------------
+  // stage buffers, reused: recv[cs-1][128 rows][bnc] then send[cs-1][128 rows][bnc], fp32,
+  // 16-byte chunks of a row XOR-swizzled by (row & 7)
+  const size_t slot_floats = (size_t)kBM * bnc;
+  float* recv = reinterpret_cast<float*>(stage_base);
+  float* send = recv + (size_t)(cs - 1) * slot_floats;
+  const int swz = rt & 7;
+  if (cs > 1) {
+    if (threadIdx.x == 64) mbar_arrive_expect_tx(xchg_bar, (uint32_t)((cs - 1) * slot_floats * 4));
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();  // every main loop of the cluster is done: stage buffers are idle
+    tc_fence_after();
+    if (epi) {
+      for (int d = 0; d < cs; ++d) {
+        if (d == z) continue;
+        float* srow = send + (size_t)(d < z ? d : d - 1) * slot_floats + (size_t)rt * bnc;
+        for (int c = 0; c < bnc; c += 32) {
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(tmem_row + d * bnc + c, raw);
+          tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(raw[i]);
-      const int n = n0 + c0;
-      if (s >= 0 && ex.mode == kExpandDelta) {
-        float4 d[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          d[q] = (n + q * 4 < a.N) ? *reinterpret_cast<const float4*>(drow + n + q * 4)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          acc[q * 4 + 0] += d[q].x;
-          acc[q * 4 + 1] += d[q].y;
-          acc[q * 4 + 2] += d[q].z;
-          acc[q * 4 + 3] += d[q].w;
-        }
-      } else if (s >= 0) {
-#pragma unroll 1
-        for (int j0 = 0; j0 < r; j0 += 4) {
-          uint4 b[4][4];  // 4 rank rows x 32 columns, all loads in flight together
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              b[jj][q] = (j0 + jj < r && n + q * 8 < a.N)
-                             ? __ldg(reinterpret_cast<const uint4*>(Bs + (size_t)(j0 + jj) * a.N +
-                                                                    n + q * 8))
-                             : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const float vj = (j0 + jj < r) ? vrow[j0 + jj] : 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              acc[q * 8 + 0] = fmaf(vj, bf16_lo(b[jj][q].x), acc[q * 8 + 0]);
-              acc[q * 8 + 1] = fmaf(vj, bf16_hi(b[jj][q].x), acc[q * 8 + 1]);
-              acc[q * 8 + 2] = fmaf(vj, bf16_lo(b[jj][q].y), acc[q * 8 + 2]);
-              acc[q * 8 + 3] = fmaf(vj, bf16_hi(b[jj][q].y), acc[q * 8 + 3]);
-              acc[q * 8 + 4] = fmaf(vj, bf16_lo(b[jj][q].z), acc[q * 8 + 4]);
-              acc[q * 8 + 5] = fmaf(vj, bf16_hi(b[jj][q].z), acc[q * 8 + 5]);
-              acc[q * 8 + 6] = fmaf(vj, bf16_lo(b[jj][q].w), acc[q * 8 + 6]);
-              acc[q * 8 + 7] = fmaf(vj, bf16_hi(b[jj][q].w), acc[q * 8 + 7]);
-            }
+          for (int i = 0; i < 8; ++i) {
+            const int chunk = ((c >> 2) + i) ^ swz;
+            *reinterpret_cast<float4*>(srow + chunk * 4) =
+                make_float4(__uint_as_float(raw[4 * i]), __uint_as_float(raw[4 * i + 1]),
+                            __uint_as_float(raw[4 * i + 2]), __uint_as_float(raw[4 * i + 3]));
           }
         }
       }
-      if (row < a.M) {
+      fence_proxy_async_smem();
+      named_barrier(1, 128);  // the four epilogue warps have staged every send row
+      if (threadIdx.x == 64) {
+        for (int d = 0; d < cs; ++d) {
+          if (d == z) continue;
+          const uint32_t src = smem_u32(send + (size_t)(d < z ? d : d - 1) * slot_floats);
+          const uint32_t dst =
+              dsmem_map(smem_u32(recv + (size_t)(z < d ? z : z - 1) * slot_floats), (uint32_t)d);
+          bulk_copy_s2cluster(dst, src, (uint32_t)(slot_floats * 4),
+                              dsmem_map(smem_u32(xchg_bar), (uint32_t)d));
+        }
+        bulk_commit_group();
+      }
+      mbar_wait(xchg_bar, 0, a.err);  // the cs - 1 partials of this CTA's columns are here
+    }
+  }
+
+  if (epi) {
+    const __nv_bfloat16* Bs =
+        s >= 0 ? static_cast<const __nv_bfloat16*>(a.ex.B_pool) + (size_t)s * R * a.N : nullptr;
+    const float* drow = a.ex.delta + (size_t)row * a.N;
+    __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.y) + (size_t)row * a.N;
+    const int cbase = z * bnc;  // first accumulator column this CTA finishes
+    const bool add_delta = s >= 0 && a.ex.mode == kExpandDelta;
+#pragma unroll 1
+    for (int c = 0; c < bnc; c += 64) {
+      // the row's delta for these 64 columns: all 16 loads in flight before the TMEM reads
+      float4 d[16];
+      const int nc = n0 + cbase + c;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (n + q * 8 < a.N) {
-            uint4 o;
-            o.x = pack_bf16x2(acc[q * 8 + 0], acc[q * 8 + 1]);
-            o.y = pack_bf16x2(acc[q * 8 + 2], acc[q * 8 + 3]);
-            o.z = pack_bf16x2(acc[q * 8 + 4], acc[q * 8 + 5]);
-            o.w = pack_bf16x2(acc[q * 8 + 6], acc[q * 8 + 7]);
-            *reinterpret_cast<uint4*>(yrow + n + q * 8) = o;
+      for (int q = 0; q < 16; ++q)
+        d[q] = (add_delta && nc + q * 4 < a.N) ? *reinterpret_cast<const float4*>(drow + nc + q * 4)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int cc = c + h * 32;
+        uint32_t raw[32];
+        tmem_ld_32x32b_x32(tmem_row + cbase + cc, raw);
+        tmem_ld_wait();
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(raw[i]);
+        for (int q = 0; q < cs - 1; ++q) {
+          const float* rrow = recv + (size_t)q * slot_floats + (size_t)rt * bnc;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int chunk = ((cc >> 2) + i) ^ swz;
+            const float4 v = *reinterpret_cast<const float4*>(rrow + chunk * 4);
+            acc[i * 4 + 0] += v.x;
+            acc[i * 4 + 1] += v.y;
+            acc[i * 4 + 2] += v.z;
+            acc[i * 4 + 3] += v.w;
           }
         }
+        epilogue_chunk32(acc, a, row, nc + h * 32, s, r, vrow, Bs, d + h * 8, yrow);
       }
     }
+    // the send buffers must stay intact until the bulk copies have read them
+    if (cs > 1 && threadIdx.x == 64) bulk_wait_read_all();
   }
 
   tc_fence_before();
@@ -248,60 +357,85 @@ cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Widest N tile that still gives at least one tile per SM, else the narrowest.
-int gemm_tc_block_n(int M, int N, int num_sms) {
+// Tile shape and K split.  Large problems: the widest N tile that still gives one tile per
+// SM, no split.  Small batches (when split is allowed): N tile 256 and the largest
+// power-of-two K split (cluster size, at most 4) that keeps the CTA count within the SMs.
+GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split) {
   const int mt = (M + kBM - 1) / kBM;
+  const int nkb = (K + kBK - 1) / kBK;
+  GemmPlan p{64, 1};
   const int cand[3] = {256, 128, 64};
   for (int i = 0; i < 3; ++i) {
     const int tiles = mt * ((N + cand[i] - 1) / cand[i]);
-    if (tiles >= num_sms) return cand[i];
+    if (tiles >= num_sms) {
+      p.block_n = cand[i];
+      return p;
+    }
   }
-  return 64;
-}
-
-static size_t tc_smem_bytes(int BN, int R, int stages) {
-  const size_t stage = (size_t)kABytes + (size_t)BN * kBK * 2;
-  return 1024 + stages * stage + (size_t)kBM * (R + 1) * 4 + (2 * stages + 2) * 8;
-}
-
-template <int BN>
-static cudaError_t launch_tc(const GemmArgs& a, const CUtensorMap& tmap_x,
-                             const CUtensorMap& tmap_w, cudaStream_t stream) {
-  const size_t stage = (size_t)kABytes + (size_t)BN * kBK * 2;
-  const size_t budget = 227 * 1024;
-  int stages = 8;
-  while (stages > 2 && tc_smem_bytes(BN, a.ex.R, stages) > budget) --stages;
-  const size_t smem = tc_smem_bytes(BN, a.ex.R, stages);
-  if (smem > budget) return cudaErrorInvalidConfiguration;
-  (void)stage;
-  static int limit = 0;
-  cudaError_t e = ensure_smem_limit(gemm_tc_kernel<BN>, (int)smem, &limit);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3((a.M + kBM - 1) / kBM, (a.N + BN - 1) / BN);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmap_x, tmap_w, a, stages);
+  if (!allow_split) return p;
+  const int tiles256 = mt * ((N + 255) / 256);
+  // every one of the cs K ranges of ceil(nkb / cs) blocks must be non-empty
+  auto ranges_ok = [nkb](int c) { return (c - 1) * ((nkb + c - 1) / c) < nkb; };
+  int cs = 1;
+  while (cs * 2 <= 4 && tiles256 * cs * 2 <= num_sms && ranges_ok(cs * 2)) cs *= 2;
+  if (cs > 1) {
+    p.block_n = 256;
+    p.ksplit = cs;
+  }
+  return p;
 }
 
 int gemm_tc_tile_index(int BN) { return BN == 256 ? 0 : (BN == 128 ? 1 : 2); }
 
+static size_t tc_smem_bytes(int BN, int vR, int stages) {
+  const size_t stage = (size_t)kABytes + (size_t)BN * kBK * 2;
+  return 1024 + stages * stage + (size_t)kBM * (vR + 1) * 4 + (2 * stages + 3) * 8;
+}
+
+template <int BN>
+static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUtensorMap& tmap_x,
+                             const CUtensorMap& tmap_w, cudaStream_t stream) {
+  const size_t budget = 227 * 1024;
+  const int vR = a.ex.mode == kExpandV ? a.ex.R : 0;
+  const int cs = plan.ksplit;
+  // the split-K send and receive buffers reuse the stage buffers
+  const size_t recv = cs > 1 ? (size_t)2 * (cs - 1) * kBM * (BN / cs) * 4 : 0;
+  const size_t stage = (size_t)kABytes + (size_t)BN * kBK * 2;
+  int stages = 8;
+  while (stages > 2 && tc_smem_bytes(BN, vR, stages) > budget) --stages;
+  if ((size_t)stages * stage < recv) return cudaErrorInvalidConfiguration;
+  const size_t smem = tc_smem_bytes(BN, vR, stages);
+  if (smem > budget) return cudaErrorInvalidConfiguration;
+  static int limit = 0;
+  cudaError_t e = ensure_smem_limit(gemm_tc_kernel<BN>, (int)smem, &limit);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = cs;
+  cfg.gridDim = dim3((a.M + kBM - 1) / kBM, (a.N + BN - 1) / BN, cs);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = cs > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmap_x, tmap_w, a, stages, vR);
+}
+
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3, cudaStream_t stream) {
-  const int BN = gemm_tc_block_n(a.M, a.N, a.num_sms);
+  const GemmPlan plan = gemm_tc_plan(a.M, a.N, a.K, a.num_sms, a.ex.mode == kExpandDelta);
   CUtensorMap tmap_x;
   cudaError_t e = encode_tmap_bf16(&tmap_x, a.x, a.M, a.K, kBM);
   if (e != cudaSuccess) return e;
-  const CUtensorMap& tw = tmap_w3[gemm_tc_tile_index(BN)];
-  switch (BN) {
-    case 256: return launch_tc<256>(a, tmap_x, tw, stream);
-    case 128: return launch_tc<128>(a, tmap_x, tw, stream);
-    default: return launch_tc<64>(a, tmap_x, tw, stream);
+  const CUtensorMap& tw = tmap_w3[gemm_tc_tile_index(plan.block_n)];
+  switch (plan.block_n) {
+    case 256: return launch_tc<256>(a, plan, tmap_x, tw, stream);
+    case 128: return launch_tc<128>(a, plan, tmap_x, tw, stream);
+    default: return launch_tc<64>(a, plan, tmap_x, tw, stream);
   }
 }
 

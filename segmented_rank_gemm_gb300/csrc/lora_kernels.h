@@ -52,11 +52,30 @@ struct TileArgs {
 // Launched with programmatic stream serialization (it waits for the builder itself).
 cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStream_t stream);
 
+// ---- decode batches: BGMV shrink + expand into an fp32 delta (lora_tile.cu) ----
+struct BgmvArgs {
+  const void* x;  // [T,K] bf16
+  const int32_t* token_slot;  // [T] as given by the caller
+  const int32_t* loaded;      // [S]
+  int T, K, N, R, S;
+  const void* At_pool;  // [S][R][K]
+  const void* B_pool;   // [S][R][N]
+  const float* scale;   // [S]
+  const int32_t* rank;  // [S]
+  float* delta;         // [T_max][N] fp32
+  int num_sms;
+};
+// Launched with programmatic stream serialization; it does not wait for the builder.
+cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream);
+
 // ---- base GEMM with the low-rank term added in its epilogue ----
 enum ExpandMode { kExpandV = 0, kExpandDelta = 1 };
 struct ExpandArgs {
   int mode;                 // kExpandV: y += v B_slot;  kExpandDelta: y += delta
-  const int32_t* row_slot;  // [T], -1 = base only
+  const int32_t* row_slot;  // [T] builder-checked slots, -1 = base only (v mode)
+  const int32_t* token_slot;  // [T] caller's ids, checked against loaded (delta mode)
+  const int32_t* loaded;      // [S]
+  int S;
   const float* v;           // [T_max][R] fp32, already scaled by alpha / r   (v mode)
   const float* delta;       // [T_max][N] fp32                                (delta mode)
   int R;
@@ -78,7 +97,11 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3, cudaSt
 constexpr int kTcTileN[3] = {256, 128, 64};
 // Encode a 2-D bf16 tensor map for a K-major [rows, K] matrix with a (64 x box_rows) box.
 cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
-int gemm_tc_block_n(int M, int N, int num_sms);
+struct GemmPlan {
+  int block_n;  // N tile: 256, 128 or 64
+  int ksplit;   // K ranges per output tile (= cluster size), 1..4
+};
+GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split);
 
 // fp32 SIMT path (gemm_simt.cu)
 cudaError_t launch_gemm_simt_f32(const GemmArgs& a, cudaStream_t stream);

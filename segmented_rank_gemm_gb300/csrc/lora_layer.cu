@@ -3,14 +3,16 @@
 //
 // Every step of the computation runs in this library's kernels:
 //   set_batch_segments -> segment_builder_kernel            (builder.cu)
-//   lora_forward       -> lora_tile_kernel (shrink; expand in delta mode)  (lora_tile.cu)
-//                      -> gemm_tc_kernel (bf16, tcgen05)                   (gemm_tc.cu)  or
-//                         gemm_simt_f32_kernel (fp32)                      (gemm_simt.cu)
-// Two regimes: batches of at most kDeltaMaxT rows (decode) use delta mode -- the tile
-// kernel expands the low-rank term into an fp32 [T,N] buffer the GEMM epilogue adds; larger
-// batches (prefill) use v mode -- the tile kernel writes v [T,r] and the GEMM epilogue
-// expands it.  bf16 launches chain with programmatic dependent launch (builder -> tile
-// kernel -> GEMM), so the GEMM main loop overlaps the low-rank kernels.
+//   lora_forward       -> bgmv_delta_kernel (decode: BGMV shrink + expand)  (lora_tile.cu)
+//                         or lora_tile_kernel (SGMV shrink per segment tile)
+//                      -> gemm_tc_kernel (bf16, tcgen05)                    (gemm_tc.cu)  or
+//                         gemm_simt_f32_kernel (fp32)                       (gemm_simt.cu)
+// Two regimes.  bf16 batches of at most kDeltaMaxT rows (decode) use delta mode: the BGMV
+// kernel gathers each row's A and B by its slot id and writes the expanded low-rank term to
+// an fp32 [T,N] buffer that the GEMM epilogue adds; it needs nothing from the segment
+// builder, so builder, BGMV kernel and GEMM main loop all run at once.  Larger batches
+// (prefill) and fp32 use v mode: the SGMV tile kernel (after the builder) writes v [T,r]
+// and the GEMM epilogue expands it.  bf16 launches chain with programmatic dependent launch.
 //   load_adapter_slot  -> copy + transpose_pad_kernel + slot_meta_kernel (slots.cu)
 #include <cuda_runtime.h>
 
@@ -59,6 +61,7 @@ struct lora_layer {
   float* delta = nullptr;        // [min(T_max, kDeltaMaxT)][N] fp32 (delta mode, bf16)
   int max_tiles = 0;
   int T_batch = -1;              // T of the last set_batch_segments, -1 = none
+  const int32_t* token_slot = nullptr;  // the caller's ids of that batch
   // staging for lora_forward_host
   void* x_stage = nullptr;
   int32_t* ids_stage = nullptr;
@@ -301,6 +304,7 @@ int set_batch_segments(lora_layer_t* L, const int32_t* token_slot_dev, int T, vo
   LORA_CUDA(L, launch_segment_builder(a, stream));
   LORA_CUDA(L, trace_mark(L, 1, stream));
   L->T_batch = T;
+  L->token_slot = token_slot_dev;
   return LORA_OK;
 }
 
@@ -327,26 +331,45 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   const bool bf16 = L->dtype == LORA_BF16;
   const bool delta_mode = bf16 && T <= kDeltaMaxT;
 
-  TileArgs ta;
-  ta.x = x_dev;
-  ta.K = L->K;
-  ta.N = L->N;
-  ta.R = L->R;
-  ta.At_pool = L->A_pool;
-  ta.B_pool = L->B_pool;
-  ta.scale = L->scale;
-  ta.rank = L->rank;
-  ta.perm = L->perm;
-  ta.seg_offsets = L->seg_offsets;
-  ta.seg_slot = L->seg_slot;
-  ta.tile_seg = L->tile_seg;
-  ta.tile_row0 = L->tile_row0;
-  ta.meta = L->meta;
-  ta.out = delta_mode ? L->delta : L->v;
-  ta.max_tiles = (T + kTileRows - 1) / kTileRows + std::min(T, L->S);
-  ta.num_sms = L->num_sms;
   LORA_CUDA(L, trace_mark(L, 2, stream));
-  LORA_CUDA(L, launch_lora_tile(ta, bf16, delta_mode, stream));
+  if (delta_mode) {
+    BgmvArgs ba;
+    ba.x = x_dev;
+    ba.token_slot = L->token_slot;
+    ba.loaded = L->loaded;
+    ba.T = T;
+    ba.K = L->K;
+    ba.N = L->N;
+    ba.R = L->R;
+    ba.S = L->S;
+    ba.At_pool = L->A_pool;
+    ba.B_pool = L->B_pool;
+    ba.scale = L->scale;
+    ba.rank = L->rank;
+    ba.delta = L->delta;
+    ba.num_sms = L->num_sms;
+    LORA_CUDA(L, launch_bgmv_delta(ba, stream));
+  } else {
+    TileArgs ta;
+    ta.x = x_dev;
+    ta.K = L->K;
+    ta.N = L->N;
+    ta.R = L->R;
+    ta.At_pool = L->A_pool;
+    ta.B_pool = L->B_pool;
+    ta.scale = L->scale;
+    ta.rank = L->rank;
+    ta.perm = L->perm;
+    ta.seg_offsets = L->seg_offsets;
+    ta.seg_slot = L->seg_slot;
+    ta.tile_seg = L->tile_seg;
+    ta.tile_row0 = L->tile_row0;
+    ta.meta = L->meta;
+    ta.out = L->v;
+    ta.max_tiles = (T + kTileRows - 1) / kTileRows + std::min(T, L->S);
+    ta.num_sms = L->num_sms;
+    LORA_CUDA(L, launch_lora_tile(ta, bf16, false, stream));
+  }
   LORA_CUDA(L, trace_mark(L, 3, stream));
 
   GemmArgs ga;
@@ -358,6 +381,9 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.y = y_dev;
   ga.ex.mode = delta_mode ? kExpandDelta : kExpandV;
   ga.ex.row_slot = L->row_slot;
+  ga.ex.token_slot = L->token_slot;
+  ga.ex.loaded = L->loaded;
+  ga.ex.S = L->S;
   ga.ex.v = L->v;
   ga.ex.delta = L->delta;
   ga.ex.R = L->R;

@@ -224,6 +224,157 @@ __global__ void __launch_bounds__(kTileThreads, 2)
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Delta mode for small (decode) batches: BGMV, one row per thread-block cluster of CS CTAs.
+// "Serving multiple LoRAs ...": BGMV -- each token gathers its own adapter's A and B by
+// index and does a small matrix x vector.  The row's ids are checked here (slot in range
+// and loaded), so the kernel needs nothing from the segment builder and runs alongside it.
+// CTA c of the cluster:
+//   1. partial v over K range c: warp w owns rank columns [w*JW, w*JW + JW) in groups of 4;
+//      its lanes split the range into 16-byte vectors, with the K loop unrolled so a lane's
+//      loads of the group's A rows and of x are in flight together;
+//   2. the CS partials are summed through distributed shared memory (double-buffered, one
+//      cluster barrier per row) and scaled by alpha / r;
+//   3. delta[row][n] = sum_j v_j B_slot[j][n] over N range c, fp32, each thread loading up
+//      to 16 rank rows of B for its 8 columns at once.
+// ---------------------------------------------------------------------------------------
+static constexpr int kBgmvThreads = 128;
+
+__global__ void __launch_bounds__(kBgmvThreads)
+    bgmv_delta_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ token_slot,
+                      const int32_t* __restrict__ loaded, int T, int K, int N, int R, int S,
+                      const __nv_bfloat16* __restrict__ At_pool,
+                      const __nv_bfloat16* __restrict__ B_pool, const float* __restrict__ scale,
+                      const int32_t* __restrict__ rank, float* __restrict__ delta, int kchunk,
+                      int nchunk) {
+  griddep_launch_dependents();  // the base GEMM's main loop may start now
+  __shared__ float v_part[2][128];
+  __shared__ float v_s[128];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t csize;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
+  const uint32_t c = cluster_ctarank();
+  const int n_clusters = gridDim.x / csize;
+  const int k0 = c * kchunk, k1 = min(K, k0 + kchunk);
+  const int nb0 = c * nchunk, nb1 = min(N, nb0 + nchunk);
+
+  int buf = 0;
+  for (int row = blockIdx.x / csize; row < T; row += n_clusters) {
+    const int s = token_slot[row];
+    if (s < 0 || s >= S || loaded[s] == 0) continue;  // base only (same decision in all CTAs)
+    const int r = rank[s];
+    const float sc = scale[s];
+    const __nv_bfloat16* xr = x + (size_t)row * K;
+    const __nv_bfloat16* At = At_pool + (size_t)s * R * K;
+    float* vp = v_part[buf];
+    buf ^= 1;
+
+    // ---- 1. partial v over [k0, k1) ----
+    const int jw = (r + 3) / 4;  // rank columns per warp
+    for (int g0 = warp * jw; g0 < min(r, warp * jw + jw); g0 += 4) {
+      const __nv_bfloat16* ar[4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) ar[jj] = At + (size_t)min(g0 + jj, r - 1) * K;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int k = k0 + lane * 8; k < k1; k += 256) {
+        Vec16<__nv_bfloat16> xv, av[4];
+        xv.load(xr + k);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) av[jj].load(ar[jj] + k);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) acc[jj] = fmaf(xv[e], av[jj][e], acc[jj]);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[jj] += __shfl_xor_sync(0xffffffffu, acc[jj], o);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          if (g0 + jj < min(r, warp * jw + jw)) vp[g0 + jj] = acc[jj];
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();  // every CTA's partial of this row is in its shared memory
+
+    // ---- 2. sum the partials of the cluster ----
+    if (tid < r) {
+      const uint32_t local = smem_u32(vp + tid);
+      float sum = 0.f;
+      for (uint32_t d = 0; d < csize; ++d) sum += dsmem_ld(dsmem_map(local, d));
+      v_s[tid] = sc * sum;
+    }
+    __syncthreads();
+
+    // ---- 3. delta over [nb0, nb1) ----
+    const __nv_bfloat16* Bs = B_pool + (size_t)s * R * N;
+    float* drow = delta + (size_t)row * N;
+    for (int n = nb0 + tid * 8; n < nb1; n += kBgmvThreads * 8) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int j0 = 0; j0 < r; j0 += 16) {
+        uint4 b[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          b[jj] = (j0 + jj < r)
+                      ? __ldg(reinterpret_cast<const uint4*>(Bs + (size_t)(j0 + jj) * N + n))
+                      : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const float vj = (j0 + jj < r) ? v_s[j0 + jj] : 0.f;
+          acc[0] = fmaf(vj, bf16_lo(b[jj].x), acc[0]);
+          acc[1] = fmaf(vj, bf16_hi(b[jj].x), acc[1]);
+          acc[2] = fmaf(vj, bf16_lo(b[jj].y), acc[2]);
+          acc[3] = fmaf(vj, bf16_hi(b[jj].y), acc[3]);
+          acc[4] = fmaf(vj, bf16_lo(b[jj].z), acc[4]);
+          acc[5] = fmaf(vj, bf16_hi(b[jj].z), acc[5]);
+          acc[6] = fmaf(vj, bf16_lo(b[jj].w), acc[6]);
+          acc[7] = fmaf(vj, bf16_hi(b[jj].w), acc[7]);
+        }
+      }
+      float4* d = reinterpret_cast<float4*>(drow + n);
+      d[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      d[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    __syncthreads();  // v_s is rewritten by the next row
+  }
+  __syncwarp();
+  cluster_sync_all();  // no CTA leaves while a peer may still read its partials
+}
+
+cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream) {
+  // cluster of cs CTAs per row: 4 normally, fewer when K or N is small
+  int cs = 4;
+  while (cs > 1 && (a.K < cs * 256 || a.N < cs * 64)) cs >>= 1;
+  const int kchunk = ((a.K + cs - 1) / cs + 255) / 256 * 256;
+  const int nchunk = ((a.N + cs - 1) / cs + 7) / 8 * 8;
+  int clusters = a.T;
+  const int cap = a.num_sms * 6 / cs;  // co-resident with the base GEMM
+  if (clusters > cap) clusters = cap;
+  if (clusters < 1) clusters = 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cs;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(clusters * cs);
+  cfg.blockDim = dim3(kBgmvThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, bgmv_delta_kernel, static_cast<const __nv_bfloat16*>(a.x),
+                            a.token_slot, a.loaded, a.T, a.K, a.N, a.R, a.S,
+                            static_cast<const __nv_bfloat16*>(a.At_pool),
+                            static_cast<const __nv_bfloat16*>(a.B_pool), a.scale, a.rank, a.delta,
+                            kchunk, nchunk);
+}
+
 cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStream_t stream) {
   int grid = a.max_tiles;
   if (grid > a.num_sms * 4) grid = a.num_sms * 4;
@@ -244,10 +395,7 @@ cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStrea
     const T* x = static_cast<const T*>(a.x);
     const T* At = static_cast<const T*>(a.At_pool);
     const T* B = static_cast<const T*>(a.B_pool);
-    if (delta)
-      return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, V, true>, x, a.K, a.N, a.R, At, B,
-                                a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
-                                a.tile_row0, a.meta, a.out);
+    if (delta) return cudaErrorInvalidValue;  // delta mode runs bgmv_delta_kernel
     return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, V, false>, x, a.K, a.N, a.R, At, B,
                               a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
                               a.tile_row0, a.meta, a.out);
