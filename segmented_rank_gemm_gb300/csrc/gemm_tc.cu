@@ -31,9 +31,10 @@
 // thread accesses avoid shared-memory bank conflicts.
 // Each CTA starts its K range at a rotated K block (and wraps around), so the CTAs that
 // share an x tile or a W tile do not all request the same lines from L2 at the same moment.
-// Launch: programmatic dependent launch after the tile kernel: the main loop reads only x and
-// W, so it runs while the low-rank kernels finish; the epilogue waits (griddepcontrol.wait)
-// before reading their results.  Every mbarrier wait is bounded (lora_common.cuh).
+// Launch: programmatic dependent launch after the low-rank kernel: the main loop and the
+// split-K exchange read only x, W and the accumulators, so they run while the low-rank
+// kernel is still working; the epilogue waits (griddepcontrol.wait) only before it reads
+// the low-rank results.  Every mbarrier wait is bounded (lora_common.cuh).
 #include <cudaTypedefs.h>
 
 #include "lora_common.cuh"
@@ -211,20 +212,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   int s = -1, r = 0;
   float* vrow = vs + rt * (vR + 1);
   if (epi) {
-    griddep_wait();  // the low-rank kernel has finished
-    if (row < a.M) {
-      if (a.ex.mode == kExpandV) {
-        s = a.ex.row_slot[row];  // checked by the builder
-      } else {
-        const int t = a.ex.token_slot[row];
-        s = (t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0) ? t : -1;
-      }
-    }
-    if (s >= 0 && a.ex.mode == kExpandV) {
-      r = a.ex.rank[s];
-      const float* vsrc = a.ex.v + (size_t)row * R;
-      for (int j = 0; j < r; ++j) vrow[j] = vsrc[j];
-    }
     mbar_wait(tmem_full, 0, a.err);
     tc_fence_after();
   }
@@ -277,6 +264,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   if (epi) {
+    // only now the low-rank kernel's results are needed: the main loop and the split-K
+    // exchange ran while it was still working
+    griddep_wait();
+    if (row < a.M) {
+      if (a.ex.mode == kExpandV) {
+        s = a.ex.row_slot[row];  // checked by the builder
+      } else {
+        const int t = a.ex.token_slot[row];
+        s = (t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0) ? t : -1;
+      }
+    }
+    if (s >= 0 && a.ex.mode == kExpandV) {
+      r = a.ex.rank[s];
+      const float* vsrc = a.ex.v + (size_t)row * R;
+      for (int j = 0; j < r; ++j) vrow[j] = vsrc[j];
+    }
     const __nv_bfloat16* Bs =
         s >= 0 ? static_cast<const __nv_bfloat16*>(a.ex.B_pool) + (size_t)s * R * a.N : nullptr;
     const float* drow = a.ex.delta + (size_t)row * a.N;
@@ -284,37 +287,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int cbase = z * bnc;  // first accumulator column this CTA finishes
     const bool add_delta = s >= 0 && a.ex.mode == kExpandDelta;
 #pragma unroll 1
-    for (int c = 0; c < bnc; c += 64) {
-      // the row's delta for these 64 columns: all 16 loads in flight before the TMEM reads
-      float4 d[16];
+    for (int c = 0; c < bnc; c += 32) {
       const int nc = n0 + cbase + c;
+      float4 d[8];  // the row's delta for these 32 columns, in flight during the TMEM read
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
+      for (int q = 0; q < 8; ++q)
         d[q] = (add_delta && nc + q * 4 < a.N) ? *reinterpret_cast<const float4*>(drow + nc + q * 4)
                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+      uint32_t raw[32];
+      tmem_ld_32x32b_x32(tmem_row + cbase + c, raw);
+      tmem_ld_wait();
+      float acc[32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int cc = c + h * 32;
-        uint32_t raw[32];
-        tmem_ld_32x32b_x32(tmem_row + cbase + cc, raw);
-        tmem_ld_wait();
-        float acc[32];
+      for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(raw[i]);
+      for (int q = 0; q < cs - 1; ++q) {
+        const float* rrow = recv + (size_t)q * slot_floats + (size_t)rt * bnc;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(raw[i]);
-        for (int q = 0; q < cs - 1; ++q) {
-          const float* rrow = recv + (size_t)q * slot_floats + (size_t)rt * bnc;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int chunk = ((cc >> 2) + i) ^ swz;
-            const float4 v = *reinterpret_cast<const float4*>(rrow + chunk * 4);
-            acc[i * 4 + 0] += v.x;
-            acc[i * 4 + 1] += v.y;
-            acc[i * 4 + 2] += v.z;
-            acc[i * 4 + 3] += v.w;
-          }
+        for (int i = 0; i < 8; ++i) {
+          const int chunk = ((c >> 2) + i) ^ swz;
+          const float4 v = *reinterpret_cast<const float4*>(rrow + chunk * 4);
+          acc[i * 4 + 0] += v.x;
+          acc[i * 4 + 1] += v.y;
+          acc[i * 4 + 2] += v.z;
+          acc[i * 4 + 3] += v.w;
         }
-        epilogue_chunk32(acc, a, row, nc + h * 32, s, r, vrow, Bs, d + h * 8, yrow);
       }
+      epilogue_chunk32(acc, a, row, nc, s, r, vrow, Bs, d, yrow);
     }
     // the send buffers must stay intact until the bulk copies have read them
     if (cs > 1 && threadIdx.x == 64) bulk_wait_read_all();

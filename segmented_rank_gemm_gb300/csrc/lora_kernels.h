@@ -9,6 +9,19 @@ namespace lora {
 
 constexpr int kTileRows = 16;  // rows per segment tile (builder cut, tile kernel work unit)
 
+// Kernels that run beside the base GEMM prefer the largest shared-memory carveout: an SM can
+// only take a GEMM CTA (~200 KB of shared memory) while it holds CTAs of other kernels if
+// its L1/shared split is already the one the GEMM needs.  Set once per kernel, outside
+// stream capture.
+template <typename Kernel>
+inline cudaError_t prefer_max_smem_carveout(Kernel k, bool* done) {
+  if (*done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess) *done = true;
+  return e;
+}
+
 // Raise a kernel's dynamic shared-memory limit only when a launch needs more than any
 // earlier launch in this process (so launches under stream capture set no attribute).
 template <typename Kernel>

@@ -23,7 +23,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/lora_layer.h"
+#include "lora_layer.h"
 #include "lora_common.cuh"
 #include "lora_kernels.h"
 

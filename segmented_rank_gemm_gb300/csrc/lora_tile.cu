@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
 // ---------------------------------------------------------------------------------------
 static constexpr int kBgmvThreads = 128;
 
-__global__ void __launch_bounds__(kBgmvThreads)
+__global__ void __launch_bounds__(kBgmvThreads, 8)  // <= 64 registers: 4 CTAs fit beside a GEMM CTA
     bgmv_delta_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ token_slot,
                       const int32_t* __restrict__ loaded, int T, int K, int N, int R, int S,
                       const __nv_bfloat16* __restrict__ At_pool,
@@ -345,16 +345,251 @@ __global__ void __launch_bounds__(kBgmvThreads)
   cluster_sync_all();  // no CTA leaves while a peer may still read its partials
 }
 
+// ---------------------------------------------------------------------------------------
+// Delta mode, slot-major (slot width <= 32): one loaded slot per cluster of CS CTAs.  The
+// cluster finds the rows that name its slot by scanning the id vector (no segment builder
+// needed), so each A and B slice is read once per slot, however many rows share it.
+// CTA c of the cluster:
+//   0. stages, with 16-byte cp.async copies (many in flight, no register cost), its K range
+//      of A_slot and of the slot's x rows in shared memory;
+//   1. partial v over its K range: a warp per (row, group of 8 rank columns), lanes over
+//      16-byte chunks, 8 independent accumulators; then stages its N range of B_slot into
+//      the buffer A used, so that copy lands while the cluster reduces;
+//   2. the CS partials summed through distributed shared memory, scaled by alpha / r;
+//   3. delta over its N range from the staged B, fp32.
+// Rows of a slot go through in groups of kSlotRows.
+// ---------------------------------------------------------------------------------------
+static constexpr int kSlotThreads = 128;
+static constexpr int kSlotRows = 4;
+static constexpr int kSlotMaxRank = 32;
+static constexpr int kSlotMaxT = 512;
+
+__global__ void __launch_bounds__(kSlotThreads)
+    bgmv_slot_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ token_slot,
+                     const int32_t* __restrict__ loaded, int T, int K, int N, int R, int S,
+                     const __nv_bfloat16* __restrict__ At_pool,
+                     const __nv_bfloat16* __restrict__ B_pool, const float* __restrict__ scale,
+                     const int32_t* __restrict__ rank, float* __restrict__ delta, int kchunk,
+                     int nchunk) {
+  griddep_launch_dependents();  // the base GEMM's main loop may start now
+  extern __shared__ __align__(16) uint8_t smem[];
+  // [R][max(kchunk, nchunk)]: A's K range, then B's N range; then [kSlotRows][kchunk] of x
+  const int wchunk = max(kchunk, nchunk);
+  __nv_bfloat16* AB_s = reinterpret_cast<__nv_bfloat16*>(smem);
+  __nv_bfloat16* x_s = AB_s + (size_t)R * wchunk;
+  __shared__ int rows_s[kSlotMaxT];
+  __shared__ int warp_cnt[kSlotThreads / 32];
+  __shared__ float v_part[2][kSlotRows * (kSlotMaxRank + 1)];
+  __shared__ float v_s[kSlotRows * (kSlotMaxRank + 1)];
+  constexpr int vstride = kSlotMaxRank + 1;
+  constexpr int kIdsPerThread = kSlotMaxT / kSlotThreads;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t csize;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
+  const uint32_t c = cluster_ctarank();
+  const int n_clusters = gridDim.x / csize;
+  const int k0 = c * kchunk, kc = max(0, min(K - k0, kchunk));
+  const int nb0 = c * nchunk, nc = max(0, min(N - nb0, nchunk));
+  const int kv = kc / 8, nv = nc / 8;  // 16-byte chunks per staged row
+
+  // the id vector, read once: thread t holds ids t*kIdsPerThread ... (+kIdsPerThread)
+  int ids[kIdsPerThread];
+#pragma unroll
+  for (int u = 0; u < kIdsPerThread; ++u) {
+    const int i = tid * kIdsPerThread + u;
+    ids[u] = i < T ? token_slot[i] : -1;
+  }
+
+  int buf = 0;
+  for (int s = blockIdx.x / csize; s < S; s += n_clusters) {
+    if (loaded[s] == 0) continue;  // the same decision in every CTA of the cluster
+    // ---- rows naming slot s, in row order (one block-wide exclusive scan) ----
+    int mine = 0;
+#pragma unroll
+    for (int u = 0; u < kIdsPerThread; ++u) mine += ids[u] == s;
+    int inc = mine;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, inc, d);
+      if (lane >= d) inc += v;
+    }
+    if (lane == 31) warp_cnt[warp] = inc;
+    __syncthreads();
+    int pos = inc - mine, nrows = 0;
+    for (int w = 0; w < kSlotThreads / 32; ++w) {
+      if (w < warp) pos += warp_cnt[w];
+      nrows += warp_cnt[w];
+    }
+#pragma unroll
+    for (int u = 0; u < kIdsPerThread; ++u)
+      if (ids[u] == s) rows_s[pos++] = tid * kIdsPerThread + u;
+    __syncthreads();
+    if (nrows == 0) continue;  // same in every CTA
+    const int r = rank[s];
+    const float sc = scale[s];
+    const __nv_bfloat16* At = At_pool + (size_t)s * R * K + k0;
+    const __nv_bfloat16* Bs = B_pool + (size_t)s * R * N + nb0;
+
+    for (int q0 = 0; q0 < nrows; q0 += kSlotRows) {
+      const int nq = min(kSlotRows, nrows - q0);
+      // ---- 0. stage A (K range) and the group's x rows ----
+      for (int i = tid; i < r * kv; i += kSlotThreads) {
+        const int j = i / kv, e = i - j * kv;
+        cp_async_16(AB_s + (size_t)j * wchunk + e * 8, At + (size_t)j * K + e * 8);
+      }
+      for (int i = tid; i < nq * kv; i += kSlotThreads) {
+        const int q = i / kv, e = i - q * kv;
+        cp_async_16(x_s + (size_t)q * kchunk + e * 8, x + (size_t)rows_s[q0 + q] * K + k0 + e * 8);
+      }
+      cp_async_wait_all();
+      __syncthreads();
+
+      // ---- 1. partial v: warp per (row, 8 rank columns) ----
+      float* vp = v_part[buf];
+      buf ^= 1;
+      const int ngr = (r + 7) / 8;
+      for (int o = warp; o < nq * ngr; o += kSlotThreads / 32) {
+        const int q = o / ngr, j0 = (o - q * ngr) * 8;
+        const __nv_bfloat16* xs = x_s + (size_t)q * kchunk;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int e = lane; e < kv; e += 32) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + e * 8);
+          const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
+                               bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const uint4 av =
+                *reinterpret_cast<const uint4*>(AB_s + (size_t)min(j0 + jj, r - 1) * wchunk + e * 8);
+            acc[jj] = fmaf(xf[0], bf16_lo(av.x), acc[jj]);
+            acc[jj] = fmaf(xf[1], bf16_hi(av.x), acc[jj]);
+            acc[jj] = fmaf(xf[2], bf16_lo(av.y), acc[jj]);
+            acc[jj] = fmaf(xf[3], bf16_hi(av.y), acc[jj]);
+            acc[jj] = fmaf(xf[4], bf16_lo(av.z), acc[jj]);
+            acc[jj] = fmaf(xf[5], bf16_hi(av.z), acc[jj]);
+            acc[jj] = fmaf(xf[6], bf16_lo(av.w), acc[jj]);
+            acc[jj] = fmaf(xf[7], bf16_hi(av.w), acc[jj]);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) acc[jj] += __shfl_xor_sync(0xffffffffu, acc[jj], off);
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+            if (j0 + jj < r) vp[q * vstride + j0 + jj] = acc[jj];
+        }
+      }
+      __syncthreads();  // A is no longer read: stage B (N range) in its place
+      for (int i = tid; i < r * nv; i += kSlotThreads) {
+        const int j = i / nv, e = i - j * nv;
+        cp_async_16(AB_s + (size_t)j * wchunk + e * 8, Bs + (size_t)j * N + e * 8);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      __syncwarp();
+      cluster_sync_all();  // every CTA's partials of this row group are written
+
+      // ---- 2. sum the partials of the cluster ----
+      if (tid < nq * r) {
+        const int q = tid / r, j = tid - q * r;
+        const uint32_t local = smem_u32(vp + q * vstride + j);
+        float sum = 0.f;
+        for (uint32_t d = 0; d < csize; ++d) sum += dsmem_ld(dsmem_map(local, d));
+        v_s[q * vstride + j] = sc * sum;
+      }
+      asm volatile("cp.async.wait_group 0;" ::: "memory");  // B is here
+      __syncthreads();
+
+      // ---- 3. delta over this CTA's N range ----
+      for (int e = tid; e < nv; e += kSlotThreads) {
+        float acc[kSlotRows][8];
+#pragma unroll
+        for (int q = 0; q < kSlotRows; ++q)
+#pragma unroll
+          for (int i2 = 0; i2 < 8; ++i2) acc[q][i2] = 0.f;
+        for (int j = 0; j < r; ++j) {
+          const uint4 b = *reinterpret_cast<const uint4*>(AB_s + (size_t)j * wchunk + e * 8);
+          const float bf[8] = {bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y),
+                               bf16_lo(b.z), bf16_hi(b.z), bf16_lo(b.w), bf16_hi(b.w)};
+#pragma unroll
+          for (int q = 0; q < kSlotRows; ++q) {
+            const float vj = v_s[min(q, nq - 1) * vstride + j];
+#pragma unroll
+            for (int i2 = 0; i2 < 8; ++i2) acc[q][i2] = fmaf(vj, bf[i2], acc[q][i2]);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kSlotRows; ++q) {
+          if (q < nq) {
+            float4* d = reinterpret_cast<float4*>(delta + (size_t)rows_s[q0 + q] * N + nb0 + e * 8);
+            d[0] = make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
+            d[1] = make_float4(acc[q][4], acc[q][5], acc[q][6], acc[q][7]);
+          }
+        }
+      }
+      __syncthreads();  // the staging buffers and v_s are rewritten next
+    }
+  }
+  __syncwarp();
+  cluster_sync_all();  // no CTA leaves while a peer may still read its partials
+}
+
+static size_t bgmv_slot_smem(int R, int kchunk, int nchunk) {
+  return ((size_t)R * (kchunk > nchunk ? kchunk : nchunk) + (size_t)kSlotRows * kchunk) * 2;
+}
+
 cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream) {
-  // cluster of cs CTAs per row: 4 normally, fewer when K or N is small
+  if (a.R <= kSlotMaxRank && a.T <= kSlotMaxT) {
+    // slot-major: cluster of 4 CTAs per slot (8 for slot widths above 16), fewer when K or N
+    // is small; each CTA stages R x (K/cs) of A -- then R x (N/cs) of B in the same buffer --
+    // and kSlotRows x (K/cs) of x
+    int cs = a.R <= 16 ? 4 : 8;
+    while (cs > 1 && (a.K < cs * 64 || a.N < cs * 64)) cs >>= 1;
+    const int kchunk = ((a.K + cs - 1) / cs + 7) / 8 * 8;
+    const int nchunk = ((a.N + cs - 1) / cs + 7) / 8 * 8;
+    const size_t smem = bgmv_slot_smem(a.R, kchunk, nchunk);
+    if (smem <= 200 * 1024) {
+      static int limit = 0;
+      static bool carveout = false;
+      cudaError_t e = ensure_smem_limit(bgmv_slot_kernel, (int)smem, &limit);
+      if (e == cudaSuccess) e = prefer_max_smem_carveout(bgmv_slot_kernel, &carveout);
+      if (e != cudaSuccess) return e;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      attr[1].id = cudaLaunchAttributeClusterDimension;
+      attr[1].val.clusterDim.x = cs;
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(a.S * cs);
+      cfg.blockDim = dim3(kSlotThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cfg.attrs = attr;
+      cfg.numAttrs = 2;
+      return cudaLaunchKernelEx(&cfg, bgmv_slot_kernel, static_cast<const __nv_bfloat16*>(a.x),
+                                a.token_slot, a.loaded, a.T, a.K, a.N, a.R, a.S,
+                                static_cast<const __nv_bfloat16*>(a.At_pool),
+                                static_cast<const __nv_bfloat16*>(a.B_pool), a.scale, a.rank,
+                                a.delta, kchunk, nchunk);
+    }
+  }
+  // row-major: cluster of cs CTAs per row: 4 normally, fewer when K or N is small
   int cs = 4;
   while (cs > 1 && (a.K < cs * 256 || a.N < cs * 64)) cs >>= 1;
   const int kchunk = ((a.K + cs - 1) / cs + 255) / 256 * 256;
   const int nchunk = ((a.N + cs - 1) / cs + 7) / 8 * 8;
   int clusters = a.T;
-  const int cap = a.num_sms * 6 / cs;  // co-resident with the base GEMM
+  // at most 4 of these CTAs per SM, so that the base GEMM launched after this kernel still
+  // finds room for its CTA on every SM and runs concurrently
+  const int cap = a.num_sms * 4 / cs;
   if (clusters > cap) clusters = cap;
   if (clusters < 1) clusters = 1;
+  static bool carveout = false;
+  cudaError_t e = prefer_max_smem_carveout(bgmv_delta_kernel, &carveout);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -389,6 +624,14 @@ cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStrea
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  static bool carveout[3] = {false, false, false};
+  cudaError_t e = bf16 ? prefer_max_smem_carveout(lora_tile_kernel<__nv_bfloat16, Vec16<__nv_bfloat16>, false>, &carveout[0])
+                       : cudaSuccess;
+  if (e == cudaSuccess && !bf16)
+    e = prefer_max_smem_carveout(lora_tile_kernel<float, Vec16<float>, false>, &carveout[1]);
+  if (e == cudaSuccess && !bf16)
+    e = prefer_max_smem_carveout(lora_tile_kernel<float, Scalar32, false>, &carveout[2]);
+  if (e != cudaSuccess) return e;
   if (bf16) {
     using T = __nv_bfloat16;
     using V = Vec16<T>;
