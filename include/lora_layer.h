@@ -163,6 +163,33 @@ int lora_get_segments(lora_layer_t* layer, int32_t* perm, int32_t* seg_offsets,
  */
 int lora_set_trace_events(lora_layer_t* layer, void* const* events);
 
+/*
+ * The segment builder of set_batch_segments for callers that cannot allocate device memory
+ * (a framework or engine that owns all device memory through its own pool and forbids
+ * allocations behind its back, or a latency-critical path that cannot afford cudaMalloc's
+ * implicit synchronisation).  The pages have no counterpart to this entry point: it is a
+ * deployment aid of this library.
+ *   token_slot_dev   [T] int32 device ids, -1 = base only; 0 <= T <= 16384.
+ *   num_slots        1 <= num_slots <= 1024.
+ *   slot_loaded_dev  [num_slots] int32 device flags (0 = slot empty) or NULL (every slot in
+ *                    range holds an adapter).
+ *   perm_dev [T], seg_offsets_dev [num_slots + 1], seg_slot_dev [num_slots],
+ *   counts_dev [3]   caller-owned device outputs: the same permutation, offsets and
+ *                    per-segment slots as set_batch_segments computes, and counts_dev =
+ *                    {n_seg, n_adapted, error flags} (flags nonzero when an id is outside
+ *                    [-1, num_slots) or names an empty slot; such rows count as base only).
+ * Allocates nothing: the builder's scratch is one static device array (96 KB on every GPU
+ * that loads the library, held until exit).  The first call on a device looks up that
+ * array's address with the device current; make it before any stream capture.  Calls
+ * share the array and it keeps the last call's contents; calls that overlap on the GPU
+ * race on it.  Enqueued on `stream`, no synchronisation.
+ * Errors: LORA_EINVAL (sizes above the limits, null pointers), LORA_ECUDA.
+ */
+int lora_build_segments_static(const int32_t* token_slot_dev, int T, int num_slots,
+                               const int32_t* slot_loaded_dev, int32_t* perm_dev,
+                               int32_t* seg_offsets_dev, int32_t* seg_slot_dev,
+                               int32_t* counts_dev, void* stream);
+
 /* Text of the last error raised on this layer ("" if none).  Owned by the layer. */
 const char* lora_last_error(const lora_layer_t* layer);
 

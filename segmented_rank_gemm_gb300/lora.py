@@ -27,7 +27,7 @@ LORA_ECUDA, LORA_ENOMEM, LORA_ESTATE, LORA_ETIMEOUT = -5, -6, -7, -8
 ABI_FUNCTIONS = ("lora_layer_create", "load_adapter_slot", "unload_adapter_slot",
                  "set_batch_segments", "lora_forward", "lora_forward_host", "lora_get_status",
                  "lora_get_segments", "lora_set_trace_events", "lora_last_error",
-                 "lora_layer_destroy")
+                 "lora_layer_destroy", "lora_build_segments_static")
 
 
 class LoraError(RuntimeError):
@@ -51,6 +51,7 @@ def _load() -> ctypes.CDLL:
     L.lora_get_status.argtypes = [vp, vp]
     L.lora_get_segments.argtypes = [vp, vp, vp, vp, vp, vp, vp]
     L.lora_set_trace_events.argtypes = [vp, vp]
+    L.lora_build_segments_static.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp]
     L.lora_last_error.argtypes = [vp]
     L.lora_last_error.restype = ctypes.c_char_p
     L.lora_layer_destroy.argtypes = [vp]
@@ -163,6 +164,17 @@ def lora_set_trace_events(layer, events) -> None:
             e.record()
     arr = (ctypes.c_void_p * 6)(*[e.cuda_event for e in events])
     _check(layer, _lib.lora_set_trace_events(layer, ctypes.cast(arr, ctypes.c_void_p)))
+
+
+def lora_build_segments_static(token_slot, T, num_slots, slot_loaded, perm, seg_offsets,
+                               seg_slot, counts, stream=None) -> None:
+    """Segment builder without any device allocation (scratch in a static device array);
+    all tensors are caller-owned CUDA int32 tensors, ``slot_loaded`` may be None."""
+    rc = _lib.lora_build_segments_static(_ptr(token_slot), T, num_slots, _ptr(slot_loaded),
+                                         _ptr(perm), _ptr(seg_offsets), _ptr(seg_slot),
+                                         _ptr(counts), _stream(stream))
+    if rc < 0:
+        raise LoraError(rc, "lora_build_segments_static")
 
 
 def lora_last_error(layer) -> str:
