@@ -45,6 +45,9 @@ CONFIGS = {
                              "N=4096, r=16, bf16"),
     "prefill_sgmv": dict(seed=1003, desc="prefill SGMV: T=8192 in 32 geometric segments, "
                          "K=4096, N=14336, r in {8,16,32,64} padded to 64, bf16"),
+    "stack_8b": dict(seed=1005, desc="8B-class LoRA stack: 32 layers x 7 projections (q/o "
+                     "4096->4096, k/v 4096->1024, gate/up 4096->14336, down 14336->4096), rank 16 "
+                     "on all 7, 100 resident slots, 512 decode tokens, outputs chained, bf16"),
 }
 
 
@@ -185,8 +188,11 @@ def barrier(world):
 
 
 def max_over_ranks(value: float, world: int, device) -> float:
+    """The slowest rank's value (host timing reduction; no data of the layer moves)."""
     if world == 1:
         return value
+    if torch.distributed.get_backend() == "gloo":
+        device = "cpu"
     t = torch.tensor([value], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
@@ -219,8 +225,82 @@ def traffic_from_profile(kernel_src: str, config: str):
     return entry.get("dram_bytes_per_launch")
 
 
+def run_stack(args):
+    """The 8B-class stack: one step = one chained pass over its 224 projections (captured
+    in one CUDA graph); every pass streams ~22 GB of weights and slots, far beyond L2."""
+    from segmented_rank_gemm_gb300.stack import LoraStack
+    from segmented_rank_gemm_gb300.workloads import STACK_PROJECTIONS
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    st = LoraStack(seed=CONFIGS["stack_8b"]["seed"] + 104729 * rank, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    g = st.capture(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            g.replay()
+    stream.synchronize()
+    sampler = ClockSampler(os.path.join(ROOT, "gpurun_out", "clocks_bench_stack.csv")
+                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    sampler.start()
+    t_soak = time.time()
+    while time.time() - t_soak < args.soak_seconds:
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler.stop()
+    clocks = sampler.summary(t_soak, time.time())
+    seconds = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    T = st.T
+    flops = sum(2 * T * k * n for _, k, n in STACK_PROJECTIONS) * st.n_layers
+    base_bytes = sum(k * n * 2 for _, k, n in STACK_PROJECTIONS) * st.n_layers
+    ad_bytes = sum(16 * (k + n) * 2 for _, k, n in STACK_PROJECTIONS) * st.n_layers * st.S
+    step_s = seconds / args.steps
+    pk = peaks()
+    tf = flops / step_s / 1e12
+    peak = pk["bf16_tflops_sustained"] or pk["bf16_tflops"]
+    out = {
+        "metric": METRIC, "value": aggregate(T, args.steps, world, seconds), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": CONFIGS["stack_8b"]["desc"], "T": T, "layers": st.n_layers,
+                   "projections": 7 * st.n_layers, "slots": st.S, "graphs": True,
+                   "parallelism": "replicas x%d" % world,
+                   "l2": "each pass streams %.1f GB" % ((base_bytes + ad_bytes) / 1e9)},
+        "roofline": {"kernel": "whole chained pass (224 x builder + BGMV + tcgen05 GEMM)",
+                     "bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tf / peak, "traffic": None, "peak_source": pk["source"] + " sustained",
+                     "algorithmic_flops_per_step": flops},
+        "step_hbm": {"algorithmic_bytes": base_bytes + ad_bytes,
+                     "achieved_gbs": (base_bytes + ad_bytes) / step_s / 1e9},
+        "gpu_launches": 3 * 7 * st.n_layers * args.steps + args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(out))
+    st.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def run_ours(args):
     from segmented_rank_gemm_gb300.lora import LoraLayer, lora_set_trace_events, LORA_OK
+    if args.config == "stack_8b":
+        return run_stack(args)
 
     world, rank, local = dist_env()
     if world > 1:

@@ -128,6 +128,19 @@ bool is_capturing(cudaStream_t s) {
   return st != cudaStreamCaptureStatusNone;
 }
 
+// Order `stream` after every slot load not yet waited on.  Under stream capture the loads
+// are outside the graph, so the waits become external-event nodes of the graph.
+cudaError_t wait_pending_loads(lora_layer* L, cudaStream_t stream) {
+  const unsigned flags = is_capturing(stream) ? cudaEventWaitExternal : cudaEventWaitDefault;
+  for (cudaEvent_t e : L->pending) {
+    cudaError_t err = cudaStreamWaitEvent(stream, e, flags);
+    if (err != cudaSuccess) return err;
+  }
+  L->spare.insert(L->spare.end(), L->pending.begin(), L->pending.end());
+  L->pending.clear();
+  return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -282,9 +295,7 @@ int set_batch_segments(lora_layer_t* L, const int32_t* token_slot_dev, int T, vo
   if (T > 0 && !token_slot_dev) return fail(L, LORA_EINVAL, "null token_slot");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   // slot loads become visible to the builder (it reads the loaded flags)
-  for (cudaEvent_t e : L->pending) LORA_CUDA(L, cudaStreamWaitEvent(stream, e, 0));
-  L->spare.insert(L->spare.end(), L->pending.begin(), L->pending.end());
-  L->pending.clear();
+  LORA_CUDA(L, wait_pending_loads(L, stream));
 
   BuilderArgs a;
   a.token_slot = token_slot_dev;
@@ -324,9 +335,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
       (reinterpret_cast<uintptr_t>(x_dev) % 16 != 0 || reinterpret_cast<uintptr_t>(y_dev) % 16 != 0))
     return fail(L, LORA_EINVAL, "bf16 x and y must be 16-byte aligned");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  for (cudaEvent_t e : L->pending) LORA_CUDA(L, cudaStreamWaitEvent(stream, e, 0));
-  L->spare.insert(L->spare.end(), L->pending.begin(), L->pending.end());
-  L->pending.clear();
+  LORA_CUDA(L, wait_pending_loads(L, stream));
 
   const bool bf16 = L->dtype == LORA_BF16;
   const bool delta_mode = bf16 && T <= kDeltaMaxT;

@@ -241,6 +241,15 @@ def stack_projection(layer: int, proj: int, seed: int = 1005, S: int = 100, r: i
     return W, adapters
 
 
+def stack_input(proj: int, T: int = 512, seed: int = 1005, dtype=BF16, device="cpu"):
+    """A fresh N(0,1) input [T, K] for projection ``proj`` of the stack: the per-projection
+    parity cases feed every projection an input of its own instead of the previous
+    projection's output."""
+    _, K, _ = STACK_PROJECTIONS[proj]
+    g = _gen(seed * 7919 + proj + 17, device)
+    return _randn(g, (T, K), 1.0, dtype, device)
+
+
 # ---------------------------------------------------------------------------------
 # Generic seeded cases for the tests
 # ---------------------------------------------------------------------------------
