@@ -72,29 +72,40 @@ def peaks():
 # algorithmic work per step (what the method must move / compute)
 # ------------------------------------------------------------------------------------
 
-def algorithmic(wl, ksplit_planes=None):
+def algorithmic(wl, delta_mode=None):
     """Bytes and FLOPs per step: x, W, y once; each distinct adapter slice used in the
-    batch once at its true rank; ids; the fp32 rank-wide intermediate v once."""
+    batch once at its true rank; ids; the fp32 intermediate of the low-rank term once
+    (v [T_a, r] in v mode; delta [T_a, N] in delta mode, batches of <= 512 bf16 rows)."""
     T, K, N = wl.T, wl.K, wl.N
     es = 2 if wl.dtype == torch.bfloat16 else 4
+    if delta_mode is None:
+        delta_mode = wl.dtype == torch.bfloat16 and T <= 512
     ids = wl.token_slot.cpu().numpy()
     used = sorted(set(int(s) for s in ids if s >= 0))
     ranks = {s: int(wl.adapters[s][0].shape[1]) for s in used}
     adapted = ids >= 0
+    n_ad = int(adapted.sum())
     a_bytes = sum(K * ranks[s] * es for s in used)
     b_bytes = sum(ranks[s] * N * es for s in used)
     v_bytes = int(sum(ranks[int(s)] for s in ids[adapted])) * 4
+    d_bytes = n_ad * N * 4
     base = {"x": T * K * es, "W": K * N * es, "y": T * N * es, "ids": T * 4}
     lora_flops = 2 * sum(ranks[int(s)] * (K + N) for s in ids[adapted])
+    if delta_mode:  # low-rank kernel: x, A, B -> delta; GEMM: x, W, delta -> y
+        gemm = base["x"] + base["W"] + base["y"] + d_bytes + base["ids"]
+        lowrank = base["x"] + a_bytes + b_bytes + d_bytes + base["ids"]
+    else:  # tile kernel: x, A -> v; GEMM: x, W, v, B -> y
+        gemm = base["x"] + base["W"] + base["y"] + b_bytes + v_bytes + base["ids"]
+        lowrank = base["x"] + a_bytes + v_bytes
     return {
         "step_bytes": sum(base.values()) + a_bytes + b_bytes,
-        # the GEMM kernel: x, W, y, the distinct B slices, v (written by the shrink) once
-        "gemm_bytes": base["x"] + base["W"] + base["y"] + b_bytes + v_bytes + base["ids"],
-        "shrink_bytes": base["x"] + a_bytes + v_bytes,
+        "gemm_bytes": gemm,
+        "lowrank_bytes": lowrank,
         "base_flops": 2 * T * K * N,
         "lora_flops": lora_flops,
         "distinct_slots": len(used),
-        "adapted_rows": int(adapted.sum()),
+        "adapted_rows": n_ad,
+        "mode": "delta" if delta_mode else "v",
     }
 
 
@@ -489,6 +500,9 @@ def run_ours(args):
                      "frac_of_measured": work["step_bytes"] / (ms_per_step * 1e-3) / 1e9 / pk["hbm_gbs"],
                      "frac_of_8tbs_spec": work["step_bytes"] / (ms_per_step * 1e-3) / 8e12},
         "kernels_us": kern_us,
+        "lowrank_kernel": {"algorithmic_bytes": work["lowrank_bytes"],
+                           "achieved_gbs": work["lowrank_bytes"] / (kern_us["shrink"] * 1e-6) / 1e9,
+                           "mode": work["mode"]},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "e2e": e2e,
