@@ -11,7 +11,11 @@
 //   perm[T_a]        adapted rows sorted by ascending slot, original order within a slot
 //   seg_offsets[n_seg+1], seg_slot[n_seg]   one segment per slot that owns rows
 //   tile_seg/tile_row0[n_tiles]             the shrink kernel's work list: each segment
-//                                           cut into pieces of at most rows_per_tile rows
+//                                           cut into pieces of at most rows_per_tile rows,
+//                                           or (window mode) units: a window of window_rows
+//                                           consecutive perm positions (tile_row0 = its
+//                                           first position) and the first of at most
+//                                           window_groups of its segments (tile_seg)
 //   meta = {n_seg, T_a, n_tiles}
 // Method (a counting sort that needs no atomics, so the order is unique):
 //   1. W "walker" warps each own a contiguous range of rows and count, per slot, the rows
@@ -26,6 +30,8 @@
 namespace lora {
 
 static constexpr int kBuilderThreads = 1024;
+// windows per thread in window mode: 1024 * 8 windows of 128 rows cover 2^20 rows
+static constexpr int kMaxWinPerThread = 8;
 
 struct Scan3 {
   int a, b, c;
@@ -49,6 +55,7 @@ __device__ __forceinline__ Scan3 warp_inclusive_scan3(Scan3 v, int lane) {
 __global__ void __launch_bounds__(kBuilderThreads, 1)
     segment_builder_kernel(const int32_t* __restrict__ token_slot, int T, int S,
                            const int32_t* __restrict__ loaded, int n_walk, int rows_per_tile,
+                           int window_rows, int window_groups,
                            int32_t* __restrict__ row_slot, int32_t* __restrict__ perm,
                            int32_t* __restrict__ seg_offsets, int32_t* __restrict__ seg_slot,
                            int32_t* __restrict__ tile_seg, int32_t* __restrict__ tile_row0,
@@ -119,7 +126,7 @@ __global__ void __launch_bounds__(kBuilderThreads, 1)
     const int t = total[s];
     mine.a += t;
     mine.b += t > 0;
-    mine.c += (t + rows_per_tile - 1) / rows_per_tile;
+    if (window_rows == 0) mine.c += (t + rows_per_tile - 1) / rows_per_tile;
   }
   const Scan3 inc = warp_inclusive_scan3(mine, lane);
   if (lane == 31) warp_tot[warp] = inc;
@@ -141,14 +148,24 @@ __global__ void __launch_bounds__(kBuilderThreads, 1)
     if (t > 0) {
       seg_slot[pre.b] = s;
       seg_offsets[pre.b] = pre.a;
-      const int nt = (t + rows_per_tile - 1) / rows_per_tile;
-      for (int q = 0; q < nt; ++q) {
-        tile_seg[pre.c + q] = pre.b;
-        tile_row0[pre.c + q] = pre.a + q * rows_per_tile;
+      if (window_rows == 0) {
+        const int nt = (t + rows_per_tile - 1) / rows_per_tile;
+        for (int q = 0; q < nt; ++q) {
+          tile_seg[pre.c + q] = pre.b;
+          tile_row0[pre.c + q] = pre.a + q * rows_per_tile;
+        }
+        pre.c += nt;
+      } else {
+        // per window, provisionally: tile_seg = the segment holding its first position,
+        // tile_row0 = the segment holding its last position (T_a - 1 for the last window)
+        const int T_a = grand.a, W = window_rows;
+        const int nwin = (T_a + W - 1) / W;
+        for (int q = (pre.a + W - 1) / W; q * W < pre.a + t; ++q) tile_seg[q] = pre.b;
+        for (int q = pre.a / W; q < nwin && min(q * W + W - 1, T_a - 1) < pre.a + t; ++q)
+          tile_row0[q] = pre.b;
       }
       for (int w = 0; w < n_walk; ++w) hist[(size_t)w * S + s] += pre.a;  // -> cursors
       pre.b += 1;
-      pre.c += nt;
     }
     pre.a += t;
   }
@@ -156,9 +173,50 @@ __global__ void __launch_bounds__(kBuilderThreads, 1)
     seg_offsets[grand.b] = grand.a;
     meta[0] = grand.b;  // n_seg
     meta[1] = grand.a;  // T_a
-    meta[2] = grand.c;  // n_tiles
+    if (window_rows == 0) meta[2] = grand.c;  // n_tiles
   }
   __syncthreads();
+
+  // ---- 2c. window mode: one work unit per window and group of <= window_groups of its
+  //      segments (a window spans segments tile_seg .. tile_row0 of step 2b) ----
+  if (window_rows > 0) {
+    const int W = window_rows, G = window_groups;
+    const int nwin = (grand.a + W - 1) / W;
+    const int wpt = (nwin + (int)blockDim.x - 1) / (int)blockDim.x;  // <= kMaxWinPerThread
+    int first[kMaxWinPerThread], units[kMaxWinPerThread];
+    int my_units = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxWinPerThread; ++i) {
+      const int w = tid * wpt + i;
+      units[i] = 0;
+      first[i] = 0;
+      if (i < wpt && w < nwin) {
+        first[i] = tile_seg[w];
+        units[i] = (tile_row0[w] - first[i] + G) / G;
+        my_units += units[i];
+      }
+    }
+    const Scan3 uinc = warp_inclusive_scan3(Scan3{my_units, 0, 0}, lane);
+    __syncthreads();  // every window read; warp_tot free again
+    if (lane == 31) warp_tot[warp] = uinc;
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = blockDim.x >> 5;
+      Scan3 v = lane < nw ? warp_tot[lane] : Scan3{0, 0, 0};
+      const Scan3 vinc = warp_inclusive_scan3(v, lane);
+      if (lane < nw) warp_tot[lane] = Scan3{vinc.a - v.a, 0, 0};
+      if (lane == 31) meta[2] = vinc.a;  // n_units
+    }
+    __syncthreads();
+    int u = warp_tot[warp].a + uinc.a - my_units;
+#pragma unroll
+    for (int i = 0; i < kMaxWinPerThread; ++i) {
+      for (int q = 0; q < units[i]; ++q, ++u) {
+        tile_seg[u] = first[i] + q * G;
+        tile_row0[u] = (tid * wpt + i) * W;
+      }
+    }
+  }
 
   // ---- 3. stable scatter: walkers re-walk their rows in order ----
   if (warp < n_walk) {
@@ -194,6 +252,10 @@ int builder_smem_bytes(int S, int* n_walk_out) {
 }
 
 cudaError_t launch_segment_builder(const BuilderArgs& a, cudaStream_t stream) {
+  if (a.window_rows > 0 &&
+      (a.window_groups < 1 ||
+       (a.T + a.window_rows - 1) / a.window_rows > kBuilderThreads * kMaxWinPerThread))
+    return cudaErrorInvalidValue;
   int n_walk = 1;
   const int smem = builder_smem_bytes(a.S, &n_walk);
   static int limit = 0;
@@ -202,7 +264,8 @@ cudaError_t launch_segment_builder(const BuilderArgs& a, cudaStream_t stream) {
   if (e == cudaSuccess) e = prefer_max_smem_carveout(segment_builder_kernel, &carveout);
   if (e != cudaSuccess) return e;
   segment_builder_kernel<<<1, kBuilderThreads, smem, stream>>>(
-      a.token_slot, a.T, a.S, a.loaded, n_walk, a.rows_per_tile, a.row_slot, a.perm,
+      a.token_slot, a.T, a.S, a.loaded, n_walk, a.rows_per_tile, a.window_rows,
+      a.window_groups, a.row_slot, a.perm,
       a.seg_offsets, a.seg_slot, a.tile_seg, a.tile_row0, a.meta, a.err);
   return cudaGetLastError();
 }

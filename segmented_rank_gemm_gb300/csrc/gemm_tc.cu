@@ -12,13 +12,18 @@
 //   warp 1      allocates BN TMEM columns; one lane issues tcgen05.mma (M=128, N=BN, K=16,
 //               bf16 x bf16 -> fp32 in TMEM) and frees each stage with tcgen05.commit.
 //   warps 2..5  epilogue: each thread owns one output row (one TMEM lane); it reads the
-//               accumulator 32 columns at a time (tcgen05.ld), adds the row's low-rank term
-//               and rounds to bf16 once:
-//                 v mode     sum_j v_j B_slot[j, n] (v fp32, already scaled by alpha / r,
-//                            staged in shared memory; B_slot read 4 rank rows x 32 columns
-//                            per batch of loads);
-//                 delta mode the fp32 delta[row, n] the tile kernel already expanded.
-//               Rows with slot -1 store the base product only.
+//               accumulator 32 columns at a time (tcgen05.ld) and rounds to bf16 once.
+//               In delta mode it first adds the fp32 delta[row, n] the BGMV kernel
+//               expanded (rows with slot -1 store the base product only).
+// v mode (the expand on the tensor cores): while the main loop runs, the epilogue warps list
+// the tile's distinct slots u (ascending) and then write extra K blocks into the same ring,
+// after the base blocks: y_tile += sum_u [V_u^hi | V_u^lo] [B_u^T ; B_u^T], where V_u is v
+// (fp32, already scaled by alpha / r, summed over its K-split planes) on the rows of slot u
+// and zero elsewhere, V^hi = bf16(V) and V^lo = bf16(V - V^hi), and B_u^T comes from the
+// transposed slot pool.  Each 64-wide block holds 8 chunks of 8 rank columns: the hi then lo
+// halves of consecutive slots' R columns.  The MMA lane runs those blocks after the base
+// ones, so base and low-rank products meet in the one fp32 accumulator.  Rows with slot -1
+// match no slot and keep the base product only.
 // Split K (small batches): the grid's z dimension cuts K into `cs` <= 4 ranges and the cs
 // CTAs of one output block form a thread-block cluster.  After a cluster barrier (every main
 // loop done, so the stage buffers are idle) each CTA copies, for every other CTA d, its fp32
@@ -46,48 +51,18 @@ static constexpr int kTcThreads = 192;
 static constexpr int kBM = 128, kBK = 64;
 static constexpr int kABytes = kBM * kBK * 2;
 
-// Add the row's low-rank term to 32 accumulator columns starting at global column n and
-// store them as bf16 (d: the row's delta for these columns, loaded by the caller).
+// Add the row's delta (delta mode, adapted rows) to 32 accumulator columns starting at
+// global column n and store them as bf16.
 __device__ __forceinline__ void epilogue_chunk32(float (&acc)[32], const GemmArgs& a, int row,
-                                                 int n, int s, int r, const float* vrow,
-                                                 const __nv_bfloat16* Bs, const float4* d,
+                                                 int n, bool add_delta, const float4* d,
                                                  __nv_bfloat16* yrow) {
-  const ExpandArgs& ex = a.ex;
-  if (s >= 0 && ex.mode == kExpandDelta) {
+  if (add_delta) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       acc[q * 4 + 0] += d[q].x;
       acc[q * 4 + 1] += d[q].y;
       acc[q * 4 + 2] += d[q].z;
       acc[q * 4 + 3] += d[q].w;
-    }
-  } else if (s >= 0) {
-#pragma unroll 1
-    for (int j0 = 0; j0 < r; j0 += 4) {
-      uint4 b[4][4];  // 4 rank rows x 32 columns, all loads in flight together
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          b[jj][q] = (j0 + jj < r && n + q * 8 < a.N)
-                         ? __ldg(reinterpret_cast<const uint4*>(Bs + (size_t)(j0 + jj) * a.N + n +
-                                                                q * 8))
-                         : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const float vj = (j0 + jj < r) ? vrow[j0 + jj] : 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[q * 8 + 0] = fmaf(vj, bf16_lo(b[jj][q].x), acc[q * 8 + 0]);
-          acc[q * 8 + 1] = fmaf(vj, bf16_hi(b[jj][q].x), acc[q * 8 + 1]);
-          acc[q * 8 + 2] = fmaf(vj, bf16_lo(b[jj][q].y), acc[q * 8 + 2]);
-          acc[q * 8 + 3] = fmaf(vj, bf16_hi(b[jj][q].y), acc[q * 8 + 3]);
-          acc[q * 8 + 4] = fmaf(vj, bf16_lo(b[jj][q].z), acc[q * 8 + 4]);
-          acc[q * 8 + 5] = fmaf(vj, bf16_hi(b[jj][q].z), acc[q * 8 + 5]);
-          acc[q * 8 + 6] = fmaf(vj, bf16_lo(b[jj][q].w), acc[q * 8 + 6]);
-          acc[q * 8 + 7] = fmaf(vj, bf16_hi(b[jj][q].w), acc[q * 8 + 7]);
-        }
-      }
     }
   }
   if (row < a.M) {
@@ -105,27 +80,58 @@ __device__ __forceinline__ void epilogue_chunk32(float (&acc)[32], const GemmArg
   }
 }
 
+// 8 consecutive v values of a row (the sum of its K-split planes), as 8 bf16: the high
+// parts (bf16 of v) or the low parts (bf16 of v - high), so that hi + lo carries v to
+// about 16 significant bits through a bf16 x bf16 product.
+__device__ __forceinline__ uint4 v_chunk_bf16(const ExpandArgs& ex, int row, int j0, bool hi) {
+  const float* vr = ex.v + (size_t)row * ex.R + j0;
+  float4 v0 = __ldg(reinterpret_cast<const float4*>(vr));
+  float4 v1 = __ldg(reinterpret_cast<const float4*>(vr + 4));
+  for (int p = 1; p < ex.v_planes; ++p) {
+    const float* vp = vr + (size_t)p * ex.v_plane_stride;
+    const float4 a0 = __ldg(reinterpret_cast<const float4*>(vp));
+    const float4 a1 = __ldg(reinterpret_cast<const float4*>(vp + 4));
+    v0.x += a0.x; v0.y += a0.y; v0.z += a0.z; v0.w += a0.w;
+    v1.x += a1.x; v1.y += a1.y; v1.z += a1.z; v1.w += a1.w;
+  }
+  const float f[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float e0 = f[2 * i], e1 = f[2 * i + 1];
+    if (!hi) {
+      e0 -= __bfloat162float(__float2bfloat16_rn(e0));
+      e1 -= __bfloat162float(__float2bfloat16_rn(e1));
+    }
+    w[i] = pack_bf16x2(e0, e1);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                   const __grid_constant__ CUtensorMap tmap_w, GemmArgs a, int stages,
-                   int v_smem_rank) {
+                   const __grid_constant__ CUtensorMap tmap_w, GemmArgs a, int stages) {
   constexpr int kBBytes = BN * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
-  const int R = a.ex.R;
-  const int vR = v_smem_rank;  // rank width staged in shared memory (0 in delta mode)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stage_base = smem;
-  float* vs = reinterpret_cast<float*>(smem + (size_t)stages * kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(vs + kBM * (vR + 1));
+  // v mode: the tile's distinct slots (a bitmap over slots, then the ascending list)
+  uint32_t* slot_bits = reinterpret_cast<uint32_t*>(smem + (size_t)stages * kStageBytes);
+  int* uslot = reinterpret_cast<int*>(slot_bits + kBM);  // [128]
+  int* wsum = uslot + kBM;                               // [4] per epilogue warp
+  int* x_blocks = wsum + 4;                              // expand blocks of this tile
+  uint64_t* bars = reinterpret_cast<uint64_t*>(x_blocks + 2);
   uint64_t* full = bars;
   uint64_t* empty = bars + stages;
   uint64_t* tmem_full = bars + 2 * stages;
   uint64_t* xchg_bar = bars + 2 * stages + 1;  // split K: partials received from the peers
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * stages + 2);
+  uint64_t* xinfo_bar = bars + 2 * stages + 2;  // v mode: x_blocks written
+  uint64_t* xgrant = bars + 2 * stages + 3;     // [stages] v mode: a free stage for the expand
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * stages + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * BN;
@@ -145,6 +151,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(tmem_full, 1);
     mbar_init(xchg_bar, 1);
+    mbar_init(xinfo_bar, 1);
+    for (int s = 0; s < stages; ++s) mbar_init(&xgrant[s], 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -174,28 +182,66 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ph ^= 1u;
         }
       }
+      // v mode: claim the ring stages of the expand blocks in order (a wait on the
+      // adjacent phase of empty, as for the base blocks) and hand each to the epilogue
+      // warps, which fill it.  Their own waits are on xgrant: two grants of one stage are
+      // separated by their fill, so those waits are on adjacent phases too.
+      if (a.ex.mode == kExpandV && mbar_wait(xinfo_bar, 0, a.err)) {
+        const int nx = *x_blocks;
+        for (int e = 0; e < nx; ++e) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, a.err)) break;
+          mbar_arrive(&xgrant[s]);
+          if (++s == stages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      // descriptors built once: the start-address field counts 16-byte units, so a stage
+      // is + s * kStageBytes / 16 and a 16-wide K step inside the 128-byte row is + 2
+      const uint64_t a_desc0 = smem_desc_sw128(smem_u32(stage_base));
+      const uint64_t b_desc0 = smem_desc_sw128(smem_u32(stage_base + kABytes));
       int s = 0;
       uint32_t ph = 0;
       for (int it = 0; it < nkb; ++it) {
         if (!mbar_wait(&full[s], ph, a.err)) break;
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(stage_base + (size_t)s * kStageBytes);
-        const uint32_t b_addr = a_addr + kABytes;
+        const uint64_t stage_off = (uint64_t)(s * (kStageBytes >> 4));
+        const uint64_t a_desc = a_desc0 + stage_off, b_desc = b_desc0 + stage_off;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          tc_mma_bf16(tmem_base, smem_desc_sw128(a_addr + kk * 32),
-                      smem_desc_sw128(b_addr + kk * 32), idesc, (it | kk) != 0 ? 1u : 0u);
+          tc_mma_bf16(tmem_base, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2), idesc,
+                      (it | kk) != 0 ? 1u : 0u);
         }
         tc_commit(&empty[s]);
         if (++s == stages) {
           s = 0;
           ph ^= 1u;
+        }
+      }
+      if (a.ex.mode == kExpandV && mbar_wait(xinfo_bar, 0, a.err)) {
+        // the low-rank expand: blocks the epilogue warps write into the same ring
+        const int nx = *x_blocks;
+        for (int e = 0; e < nx; ++e) {
+          if (!mbar_wait(&full[s], ph, a.err)) break;
+          tc_fence_after();
+          const uint64_t stage_off = (uint64_t)(s * (kStageBytes >> 4));
+          const uint64_t a_desc = a_desc0 + stage_off, b_desc = b_desc0 + stage_off;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_bf16(tmem_base, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
+                        idesc, 1u);
+          tc_commit(&empty[s]);
+          if (++s == stages) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
       }
       tc_commit(tmem_full);
@@ -209,8 +255,77 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int row = m0 + rt;
   const bool epi = warp >= 2;
   const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-  int s = -1, r = 0;
-  float* vrow = vs + rt * (vR + 1);
+  if (epi && a.ex.mode == kExpandV) {
+    // ---- v mode: write the low-rank expand as extra K blocks of the ring ----
+    // y_tile += sum over the tile's distinct slots u of [v_u^hi | v_u^lo] [B_u^T ; B_u^T],
+    // where v_u holds the v rows of slot u's rows and zeros elsewhere.  A block's 8 chunks
+    // of 8 K-columns hold, in order, the hi then lo halves of each slot's R rank columns.
+    const int et = threadIdx.x - 64;  // 0..127
+    griddep_wait();                   // v and the checked slots come from earlier kernels
+    const int srow = m0 + et < a.M ? a.ex.row_slot[m0 + et] : -1;
+    slot_bits[et] = 0u;
+    named_barrier(1, 128);
+    if (srow >= 0) atomicOr(&slot_bits[srow >> 5], 1u << (srow & 31));
+    named_barrier(1, 128);
+    uint32_t word = et < (a.ex.S + 31) / 32 ? slot_bits[et] : 0u;
+    const int cnt = __popc(word);
+    int incl = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += t;
+    }
+    if (lane == 31) wsum[et >> 5] = incl;
+    named_barrier(1, 128);
+    int pos = incl - cnt, m = 0;
+    for (int i = 0; i < 4; ++i) {
+      if (i < (et >> 5)) pos += wsum[i];
+      m += wsum[i];
+    }
+    while (word) {
+      const int b = __ffs(word) - 1;
+      uslot[pos++] = et * 32 + b;
+      word &= word - 1;
+    }
+    named_barrier(1, 128);
+    const int R = a.ex.R, R8 = R >> 3, per = 2 * R8;  // chunks per slot: hi, then lo
+    const int nx = (m * per + 7) / 8;
+    if (et == 0) {
+      *x_blocks = nx;
+      mbar_arrive(xinfo_bar);
+    }
+    const __nv_bfloat16* Bt = static_cast<const __nv_bfloat16*>(a.ex.Bt_pool);
+    for (int e = 0; e < nx; ++e) {
+      const int st = (nkb + e) % stages;  // ring position nkb + e, after the base blocks
+      // the e / stages earlier grants of this stage were for this loop's earlier blocks
+      if (!mbar_wait(&xgrant[st], (uint32_t)(e / stages) & 1u, a.err)) break;
+      uint8_t* sa = stage_base + (size_t)st * kStageBytes;
+      uint8_t* sb = sa + kABytes;
+      // A rows: this thread's row of the tile, 8 chunks
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        const int q = e * 8 + c, u = q / per, wq = q - u * per;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (u < m && uslot[u] == srow) val = v_chunk_bf16(a.ex, m0 + et, (wq % R8) * 8, wq < R8);
+        *reinterpret_cast<uint4*>(sa + et * 128 + ((c ^ (et & 7)) << 4)) = val;
+      }
+      // B rows: rank columns of B_u^T for this tile's N columns
+      for (int n = et; n < BN; n += 128) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int q = e * 8 + c, u = q / per, wq = q - u * per;
+          const bool ok = u < m && n0 + n < a.N;
+          const __nv_bfloat16* src =
+              ok ? Bt + ((size_t)uslot[u] * a.N + n0 + n) * R + (wq % R8) * 8 : Bt;
+          cp_async_16_zfill(sb + n * 128 + ((c ^ (n & 7)) << 4), src, ok ? 16u : 0u);
+        }
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async-proxy reads
+      named_barrier(1, 128);
+      if (et == 0) mbar_arrive(&full[st]);
+    }
+  }
   if (epi) {
     mbar_wait(tmem_full, 0, a.err);
     tc_fence_after();
@@ -266,34 +381,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (epi) {
     // only now the low-rank kernel's results are needed: the main loop and the split-K
     // exchange ran while it was still working
-    griddep_wait();
-    if (row < a.M) {
-      if (a.ex.mode == kExpandV) {
-        s = a.ex.row_slot[row];  // checked by the builder
-      } else {
+    bool add_delta = false;
+    if (a.ex.mode == kExpandDelta) {
+      griddep_wait();
+      if (row < a.M) {
         const int t = a.ex.token_slot[row];
-        s = (t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0) ? t : -1;
+        add_delta = t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0;
       }
     }
-    if (s >= 0 && a.ex.mode == kExpandV) {
-      r = a.ex.rank[s];
-      const float* vsrc = a.ex.v + (size_t)row * R;
-      for (int j = 0; j < r; ++j) vrow[j] = vsrc[j];
-    }
-    const __nv_bfloat16* Bs =
-        s >= 0 ? static_cast<const __nv_bfloat16*>(a.ex.B_pool) + (size_t)s * R * a.N : nullptr;
-    const float* drow = a.ex.delta + (size_t)row * a.N;
+    // the delta buffer holds the first 512 rows only: a row that adds no delta never forms
+    // an address into it beyond row 0
+    const float* drow = a.ex.delta + (add_delta ? (size_t)row * a.N : 0);
     __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.y) + (size_t)row * a.N;
     const int cbase = z * bnc;  // first accumulator column this CTA finishes
-    const bool add_delta = s >= 0 && a.ex.mode == kExpandDelta;
 #pragma unroll 1
     for (int c = 0; c < bnc; c += 32) {
       const int nc = n0 + cbase + c;
       float4 d[8];  // the row's delta for these 32 columns, in flight during the TMEM read
+      if (add_delta) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        d[q] = (add_delta && nc + q * 4 < a.N) ? *reinterpret_cast<const float4*>(drow + nc + q * 4)
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < 8; ++q)
+          d[q] = nc + q * 4 < a.N ? *reinterpret_cast<const float4*>(drow + nc + q * 4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) d[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       uint32_t raw[32];
       tmem_ld_32x32b_x32(tmem_row + cbase + c, raw);
       tmem_ld_wait();
@@ -312,7 +425,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           acc[i * 4 + 3] += v.w;
         }
       }
-      epilogue_chunk32(acc, a, row, nc, s, r, vrow, Bs, d, yrow);
+      epilogue_chunk32(acc, a, row, nc, add_delta, d, yrow);
     }
     // the send buffers must stay intact until the bulk copies have read them
     if (cs > 1 && threadIdx.x == 64) bulk_wait_read_all();
@@ -385,24 +498,25 @@ GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split) {
 
 int gemm_tc_tile_index(int BN) { return BN == 256 ? 0 : (BN == 128 ? 1 : 2); }
 
-static size_t tc_smem_bytes(int BN, int vR, int stages) {
+static size_t tc_smem_bytes(int BN, int stages) {
   const size_t stage = (size_t)kABytes + (size_t)BN * kBK * 2;
-  return 1024 + stages * stage + (size_t)kBM * (vR + 1) * 4 + (2 * stages + 3) * 8;
+  return 1024 + stages * stage + (2 * kBM + 6) * 4 + (3 * stages + 4) * 8;
 }
 
 template <int BN>
 static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUtensorMap& tmap_x,
                              const CUtensorMap& tmap_w, cudaStream_t stream) {
   const size_t budget = 227 * 1024;
-  const int vR = a.ex.mode == kExpandV ? a.ex.R : 0;
   const int cs = plan.ksplit;
+  if (a.ex.mode == kExpandV && (cs != 1 || a.ex.R % 8 != 0 || a.ex.S > 32 * kBM || !a.ex.Bt_pool))
+    return cudaErrorInvalidValue;
   // the split-K send and receive buffers reuse the stage buffers
   const size_t recv = cs > 1 ? (size_t)2 * (cs - 1) * kBM * (BN / cs) * 4 : 0;
   const size_t stage = (size_t)kABytes + (size_t)BN * kBK * 2;
   int stages = 8;
-  while (stages > 2 && tc_smem_bytes(BN, vR, stages) > budget) --stages;
+  while (stages > 2 && tc_smem_bytes(BN, stages) > budget) --stages;
   if ((size_t)stages * stage < recv) return cudaErrorInvalidConfiguration;
-  const size_t smem = tc_smem_bytes(BN, vR, stages);
+  const size_t smem = tc_smem_bytes(BN, stages);
   if (smem > budget) return cudaErrorInvalidConfiguration;
   static int limit = 0;
   cudaError_t e = ensure_smem_limit(gemm_tc_kernel<BN>, (int)smem, &limit);
@@ -421,7 +535,7 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = cs > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmap_x, tmap_w, a, stages, vR);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmap_x, tmap_w, a, stages);
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3, cudaStream_t stream) {

@@ -7,7 +7,8 @@
 
 namespace lora {
 
-constexpr int kTileRows = 16;  // rows per segment tile (builder cut, tile kernel work unit)
+constexpr int kTileRows = 16;     // rows per segment tile of the CUDA-core tile kernel
+constexpr int kTcTileRows = 128;  // rows per segment tile of the tensor-core shrink (MMA M)
 
 // Kernels that run beside the base GEMM prefer the largest shared-memory carveout: an SM can
 // only take a GEMM CTA (~200 KB of shared memory) while it holds CTAs of other kernels if
@@ -38,6 +39,12 @@ struct BuilderArgs {
   int T, S;
   const int32_t* loaded;  // [S]
   int rows_per_tile;
+  // 0: the work list cuts every segment into tiles of <= rows_per_tile rows.  > 0: it lists
+  // units instead: a window of window_rows consecutive positions of perm (tile_row0 = its
+  // first position) with the first (tile_seg) of at most window_groups segments that
+  // overlap it; a window spanning more segments gives several units.
+  int window_rows;
+  int window_groups;
   int32_t* row_slot;     // [T]
   int32_t* perm;         // [T]
   int32_t* seg_offsets;  // [S+1]
@@ -65,6 +72,29 @@ struct TileArgs {
 // Launched with programmatic stream serialization (it waits for the builder itself).
 cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStream_t stream);
 
+// ---- SGMV shrink on the tensor cores (sgmv_tc.cu) ----
+struct ShrinkTcArgs {
+  const void* x;  // [T,K] bf16
+  int T, K, R;    // R: slot rank width (multiple of 8); v has R columns
+  int Rt;         // MMA N: R rounded up to 16
+  const float* scale;  // [S]
+  const int32_t* perm, *seg_offsets, *seg_slot, *tile_seg, *tile_row0, *meta;
+  float* v;            // [max_planes][T_max][R] fp32 partial sums over K ranges, scaled
+  size_t plane_stride; // floats between planes (T_max * R)
+  int ks;              // K split (planes written), from sgmv_shrink_tc_split
+  int32_t* err;
+  int num_sms;
+};
+// Segments per window unit (the MMA stacks their A blocks along N) for a rank width Rt.
+int sgmv_shrink_tc_groups(int Rt);
+// The K split for a batch of T rows over S slots (the number of v planes the shrink writes),
+// at most max_planes.
+int sgmv_shrink_tc_split(int T, int K, int S, int num_sms, int max_planes);
+// tmap_a: the A pool [S*R rows][K] bf16 with a (64 x Rt) box.  Writes planes 0 .. ks - 1 of
+// v.  Launched with programmatic stream serialization (it waits for the builder itself).
+cudaError_t launch_sgmv_shrink_tc(const ShrinkTcArgs& a, const CUtensorMap& tmap_a,
+                                  cudaStream_t stream);
+
 // ---- decode batches: BGMV shrink + expand into an fp32 delta (lora_tile.cu) ----
 struct BgmvArgs {
   const void* x;  // [T,K] bf16
@@ -89,10 +119,13 @@ struct ExpandArgs {
   const int32_t* token_slot;  // [T] caller's ids, checked against loaded (delta mode)
   const int32_t* loaded;      // [S]
   int S;
-  const float* v;           // [T_max][R] fp32, already scaled by alpha / r   (v mode)
+  const float* v;           // [planes][T_max][R] fp32, scaled by alpha / r   (v mode):
+  int v_planes;             //   v of a row = the sum of its planes, in plane order
+  size_t v_plane_stride;    //   floats between planes
   const float* delta;       // [T_max][N] fp32                                (delta mode)
   int R;
   const void* B_pool;   // [S][R][N]
+  const void* Bt_pool;  // [S][N][R] bf16: B transposed (v mode, tensor-core expand)
   const int32_t* rank;  // [S]
 };
 struct GemmArgs {

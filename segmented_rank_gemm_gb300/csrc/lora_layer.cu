@@ -39,11 +39,14 @@ constexpr int kDeltaMaxT = 512;  // largest batch computed in delta mode
 }  // namespace
 
 struct lora_layer {
-  int K = 0, N = 0, S = 0, R = 0, T_max = 0, dtype = 0, device = 0, num_sms = 0;
+  int K = 0, N = 0, S = 0, T_max = 0, dtype = 0, device = 0, num_sms = 0;
+  int max_rank = 0;  // largest adapter rank a slot accepts
+  int R = 0;         // slot rank width: max_rank rounded up to a multiple of 8 (zero padded)
   size_t esize = 0;
   void* Wp = nullptr;      // packed base weight: bf16 [N][K], f32 [K][N]
   void* A_pool = nullptr;  // [S][R][K]
   void* B_pool = nullptr;  // [S][R][N]
+  void* Bt_pool = nullptr; // [S][N][R] bf16, B transposed: the tensor-core expand (v mode)
   void* A_stage = nullptr; // [K][R] staging for the transposition of a loaded A
   float* scale = nullptr;  // [S]
   int32_t* rank = nullptr;    // [S]
@@ -57,7 +60,8 @@ struct lora_layer {
   int32_t* tile_row0 = nullptr;  // [max_tiles]
   int32_t* meta = nullptr;       // [4]
   int32_t* err = nullptr;        // [1]
-  float* v = nullptr;            // [T_max][R]   fp32, scaled by alpha / r (v mode)
+  float* v = nullptr;            // [v_planes][T_max][R] fp32, scaled by alpha / r (v mode)
+  int v_planes = 1;              // K-split partial planes of v (bf16: tensor-core shrink)
   float* delta = nullptr;        // [min(T_max, kDeltaMaxT)][N] fp32 (delta mode, bf16)
   int max_tiles = 0;
   int T_batch = -1;              // T of the last set_batch_segments, -1 = none
@@ -73,6 +77,7 @@ struct lora_layer {
   std::vector<cudaEvent_t> pending;    // loads not yet waited on by a forward
   std::vector<cudaEvent_t> spare;
   CUtensorMap tmap_w[3];
+  CUtensorMap tmap_a;  // A pool [S*R rows][K] with a (64 x round_up(R, 16)) box (bf16)
   cudaEvent_t trace[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   bool tracing = false;
   char last_error[512] = {0};
@@ -106,7 +111,7 @@ cudaError_t dmalloc(T** p, size_t count) {
 }
 
 void free_all(lora_layer* L) {
-  void* ptrs[] = {L->Wp, L->A_pool, L->B_pool, L->A_stage, L->scale, L->rank, L->loaded,
+  void* ptrs[] = {L->Wp, L->A_pool, L->B_pool, L->Bt_pool, L->A_stage, L->scale, L->rank, L->loaded,
                   L->row_slot, L->perm, L->seg_offsets, L->seg_slot, L->tile_seg,
                   L->tile_row0, L->meta, L->err, L->v, L->delta, L->x_stage, L->ids_stage,
                   L->y_stage};
@@ -160,7 +165,8 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
   L->K = K;
   L->N = N;
   L->S = num_slots;
-  L->R = max_rank;
+  L->max_rank = max_rank;
+  L->R = (max_rank + 7) / 8 * 8;
   L->T_max = max_tokens;
   L->dtype = dtype;
   L->esize = dtype == LORA_BF16 ? 2 : 4;
@@ -177,8 +183,10 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
   if (e != cudaSuccess) return bail(LORA_ECUDA);
 
   const size_t es = L->esize;
-  const size_t S = num_slots, R = max_rank;
+  const size_t S = num_slots, R = L->R;
   L->max_tiles = (max_tokens + kTileRows - 1) / kTileRows + num_slots;
+  // small batches split the shrink's K range over up to 8 planes of v; large ones need none
+  L->v_planes = dtype == LORA_BF16 ? std::max(1, std::min(8, 65536 / max_tokens)) : 1;
   bool ok = cudaMalloc(&L->Wp, (size_t)K * N * es) == cudaSuccess &&
             cudaMalloc(&L->A_pool, S * R * K * es) == cudaSuccess &&
             cudaMalloc(&L->B_pool, S * R * N * es) == cudaSuccess &&
@@ -192,12 +200,15 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
             dmalloc(&L->tile_seg, L->max_tiles) == cudaSuccess &&
             dmalloc(&L->tile_row0, L->max_tiles) == cudaSuccess &&
             dmalloc(&L->meta, 4) == cudaSuccess && dmalloc(&L->err, 1) == cudaSuccess &&
-            dmalloc(&L->v, (size_t)max_tokens * R) == cudaSuccess &&
+            dmalloc(&L->v, (size_t)L->v_planes * max_tokens * R) == cudaSuccess &&
             (dtype != LORA_BF16 ||
              dmalloc(&L->delta, (size_t)std::min(max_tokens, kDeltaMaxT) * N) == cudaSuccess) &&
             cudaMalloc(&L->x_stage, (size_t)max_tokens * K * es) == cudaSuccess &&
             dmalloc(&L->ids_stage, max_tokens) == cudaSuccess &&
-            cudaMalloc(&L->y_stage, (size_t)max_tokens * N * es) == cudaSuccess;
+            cudaMalloc(&L->y_stage, (size_t)max_tokens * N * es) == cudaSuccess &&
+            // batches beyond kDeltaMaxT rows expand v on the tensor cores from B^T
+            (dtype != LORA_BF16 || max_tokens <= kDeltaMaxT ||
+             cudaMalloc(&L->Bt_pool, S * R * N * es) == cudaSuccess);
   if (!ok) {
     cudaGetLastError();
     return bail(LORA_ENOMEM);
@@ -208,12 +219,13 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
 
   ok = cudaMemsetAsync(L->A_pool, 0, S * R * K * es, stream) == cudaSuccess &&
        cudaMemsetAsync(L->B_pool, 0, S * R * N * es, stream) == cudaSuccess &&
+       (!L->Bt_pool || cudaMemsetAsync(L->Bt_pool, 0, S * R * N * es, stream) == cudaSuccess) &&
        cudaMemsetAsync(L->scale, 0, S * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->rank, 0, S * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->loaded, 0, S * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->meta, 0, 16, stream) == cudaSuccess &&
        cudaMemsetAsync(L->err, 0, 4, stream) == cudaSuccess &&
-       cudaMemsetAsync(L->v, 0, (size_t)max_tokens * R * 4, stream) == cudaSuccess;
+       cudaMemsetAsync(L->v, 0, (size_t)L->v_planes * max_tokens * R * 4, stream) == cudaSuccess;
   if (!ok) return bail(LORA_ECUDA);
 
   if (dtype == LORA_BF16) {
@@ -221,6 +233,9 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
     for (int i = 0; i < 3; ++i)
       if (encode_tmap_bf16(&L->tmap_w[i], L->Wp, N, K, kTcTileN[i]) != cudaSuccess)
         return bail(LORA_ECUDA);
+    if (encode_tmap_bf16(&L->tmap_a, L->A_pool, (int)(S * R), K, (L->R + 15) / 16 * 16) !=
+        cudaSuccess)
+      return bail(LORA_ECUDA);
   } else {
     if (cudaMemcpyAsync(L->Wp, W_dev, (size_t)K * N * es, cudaMemcpyDefault, stream) !=
         cudaSuccess)
@@ -246,7 +261,8 @@ int load_adapter_slot(lora_layer_t* L, int slot, const void* A_src, const void* 
                       float alpha, void* side_) {
   if (!L) return LORA_EINVAL;
   if (slot < 0 || slot >= L->S) return fail(L, LORA_ESLOT, "slot %d outside [0, %d)", slot, L->S);
-  if (r < 1 || r > L->R) return fail(L, LORA_ERANK, "rank %d outside [1, %d]", r, L->R);
+  if (r < 1 || r > L->max_rank)
+    return fail(L, LORA_ERANK, "rank %d outside [1, %d]", r, L->max_rank);
   if (!A_src || !B_src) return fail(L, LORA_EINVAL, "null adapter pointer");
   cudaStream_t side = static_cast<cudaStream_t>(side_);
   const size_t es = L->esize;
@@ -266,6 +282,9 @@ int load_adapter_slot(lora_layer_t* L, int slot, const void* A_src, const void* 
   LORA_CUDA(L, cudaMemcpyAsync(Bs, B_src, (size_t)r * N * es, cudaMemcpyDefault, side));
   if ((size_t)r < R)
     LORA_CUDA(L, cudaMemsetAsync(Bs + (size_t)r * N * es, 0, (R - r) * N * es, side));
+  if (L->Bt_pool)  // B^T [N][R] of the slot (rank rows beyond r are the zeros just set)
+    LORA_CUDA(L, launch_pack_w_bf16(Bs, static_cast<char*>(L->Bt_pool) + (size_t)slot * N * R * es,
+                                    (int)R, (int)N, side));
   LORA_CUDA(L, launch_slot_meta(L->scale, L->rank, L->loaded, slot, alpha / (float)r, r, 1,
                                 side));
   cudaEvent_t ev = take_event(L);
@@ -302,7 +321,11 @@ int set_batch_segments(lora_layer_t* L, const int32_t* token_slot_dev, int T, vo
   a.T = T;
   a.S = L->S;
   a.loaded = L->loaded;
+  // work list: 128-row windows of perm for the tensor-core shrink (bf16), segment tiles of
+  // the CUDA-core tile kernel (fp32)
   a.rows_per_tile = kTileRows;
+  a.window_rows = L->dtype == LORA_BF16 ? kTcTileRows : 0;
+  a.window_groups = L->dtype == LORA_BF16 ? sgmv_shrink_tc_groups((L->R + 15) / 16 * 16) : 0;
   a.row_slot = L->row_slot;
   a.perm = L->perm;
   a.seg_offsets = L->seg_offsets;
@@ -339,6 +362,10 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
 
   const bool bf16 = L->dtype == LORA_BF16;
   const bool delta_mode = bf16 && T <= kDeltaMaxT;
+  // planes of v the tensor-core shrink writes (its K split); the GEMM sums them
+  const int v_split = bf16 && !delta_mode
+                          ? sgmv_shrink_tc_split(T, L->K, L->S, L->num_sms, L->v_planes)
+                          : 1;
 
   LORA_CUDA(L, trace_mark(L, 2, stream));
   if (delta_mode) {
@@ -358,6 +385,26 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     ba.delta = L->delta;
     ba.num_sms = L->num_sms;
     LORA_CUDA(L, launch_bgmv_delta(ba, stream));
+  } else if (bf16) {
+    ShrinkTcArgs sa;
+    sa.x = x_dev;
+    sa.T = T;
+    sa.K = L->K;
+    sa.R = L->R;
+    sa.Rt = (L->R + 15) / 16 * 16;
+    sa.scale = L->scale;
+    sa.perm = L->perm;
+    sa.seg_offsets = L->seg_offsets;
+    sa.seg_slot = L->seg_slot;
+    sa.tile_seg = L->tile_seg;
+    sa.tile_row0 = L->tile_row0;
+    sa.meta = L->meta;
+    sa.v = L->v;
+    sa.plane_stride = (size_t)L->T_max * L->R;
+    sa.ks = v_split;
+    sa.err = L->err;
+    sa.num_sms = L->num_sms;
+    LORA_CUDA(L, launch_sgmv_shrink_tc(sa, L->tmap_a, stream));
   } else {
     TileArgs ta;
     ta.x = x_dev;
@@ -394,9 +441,12 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.ex.loaded = L->loaded;
   ga.ex.S = L->S;
   ga.ex.v = L->v;
+  ga.ex.v_planes = v_split;
+  ga.ex.v_plane_stride = (size_t)L->T_max * L->R;
   ga.ex.delta = L->delta;
   ga.ex.R = L->R;
   ga.ex.B_pool = L->B_pool;
+  ga.ex.Bt_pool = L->Bt_pool;
   ga.ex.rank = L->rank;
   ga.err = L->err;
   ga.num_sms = L->num_sms;

@@ -98,6 +98,8 @@ extern "C" int lora_build_segments_static(const int32_t* token_slot_dev, int T, 
   a.S = num_slots;
   a.loaded = loaded;
   a.rows_per_tile = lora::kTileRows;
+  a.window_rows = 0;
+  a.window_groups = 0;
   a.row_slot = scratch + kOffRowSlot;
   a.perm = perm_dev;
   a.seg_offsets = seg_offsets_dev;
