@@ -80,10 +80,11 @@ __device__ __forceinline__ void epilogue_chunk32(float (&acc)[32], const GemmArg
   }
 }
 
-// 8 consecutive v values of a row (the sum of its K-split planes), as 8 bf16: the high
-// parts (bf16 of v) or the low parts (bf16 of v - high), so that hi + lo carries v to
-// about 16 significant bits through a bf16 x bf16 product.
-__device__ __forceinline__ uint4 v_chunk_bf16(const ExpandArgs& ex, int row, int j0, bool hi) {
+// The row's v (the sum of its K-split planes) at rank columns j0 .. j0 + 7, split into bf16
+// high parts (bf16 of v) and low parts (bf16 of v - high): hi + lo carries v to about 16
+// significant bits through a bf16 x bf16 product.
+__device__ __forceinline__ void v_hi_lo8(const ExpandArgs& ex, int row, int j0, uint4& hi,
+                                         uint4& lo) {
   const float* vr = ex.v + (size_t)row * ex.R + j0;
   float4 v0 = __ldg(reinterpret_cast<const float4*>(vr));
   float4 v1 = __ldg(reinterpret_cast<const float4*>(vr + 4));
@@ -95,23 +96,23 @@ __device__ __forceinline__ uint4 v_chunk_bf16(const ExpandArgs& ex, int row, int
     v1.x += a1.x; v1.y += a1.y; v1.z += a1.z; v1.w += a1.w;
   }
   const float f[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-  uint32_t w[4];
+  uint32_t h[4], l[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float e0 = f[2 * i], e1 = f[2 * i + 1];
-    if (!hi) {
-      e0 -= __bfloat162float(__float2bfloat16_rn(e0));
-      e1 -= __bfloat162float(__float2bfloat16_rn(e1));
-    }
-    w[i] = pack_bf16x2(e0, e1);
+    const float e0 = f[2 * i], e1 = f[2 * i + 1];
+    h[i] = pack_bf16x2(e0, e1);
+    l[i] = pack_bf16x2(e0 - bf16_lo(h[i]), e1 - bf16_hi(h[i]));
   }
-  return make_uint4(w[0], w[1], w[2], w[3]);
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                   const __grid_constant__ CUtensorMap tmap_w, GemmArgs a, int stages) {
+                   const __grid_constant__ CUtensorMap tmap_w,
+                   const __grid_constant__ CUtensorMap tmap_bx, GemmArgs a, int stages,
+                   int xscr_bytes) {
   constexpr int kBBytes = BN * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
 
@@ -119,8 +120,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stage_base = smem;
+  // v mode: each tile row's hi / lo v halves in the expand block layout (128 B per block)
+  uint8_t* xscr = smem + (size_t)stages * kStageBytes;
   // v mode: the tile's distinct slots (a bitmap over slots, then the ascending list)
-  uint32_t* slot_bits = reinterpret_cast<uint32_t*>(smem + (size_t)stages * kStageBytes);
+  uint32_t* slot_bits = reinterpret_cast<uint32_t*>(xscr + xscr_bytes);
   int* uslot = reinterpret_cast<int*>(slot_bits + kBM);  // [128]
   int* wsum = uslot + kBM;                               // [4] per epilogue warp
   int* x_blocks = wsum + 4;                              // expand blocks of this tile
@@ -130,8 +133,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* tmem_full = bars + 2 * stages;
   uint64_t* xchg_bar = bars + 2 * stages + 1;  // split K: partials received from the peers
   uint64_t* xinfo_bar = bars + 2 * stages + 2;  // v mode: x_blocks written
-  uint64_t* xgrant = bars + 2 * stages + 3;     // [stages] v mode: a free stage for the expand
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * stages + 3);
+  uint64_t* xgrant = bars + 2 * stages + 3;     // [stages] v mode: stage handed to the epilogue
+  uint64_t* xa_full = bars + 3 * stages + 3;    // [stages] v mode: its A half written
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * stages + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * BN;
@@ -152,12 +156,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(tmem_full, 1);
     mbar_init(xchg_bar, 1);
     mbar_init(xinfo_bar, 1);
-    for (int s = 0; s < stages; ++s) mbar_init(&xgrant[s], 1);
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&xgrant[s], 1);
+      mbar_init(&xa_full[s], 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_x);
     tma_prefetch_desc(&tmap_w);
+    if (a.ex.mode == kExpandV) tma_prefetch_desc(&tmap_bx);
   }
   if (warp == 1) tmem_alloc(tmem_holder, BN);
   tc_fence_before();
@@ -182,14 +190,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ph ^= 1u;
         }
       }
-      // v mode: claim the ring stages of the expand blocks in order (a wait on the
-      // adjacent phase of empty, as for the base blocks) and hand each to the epilogue
-      // warps, which fill it.  Their own waits are on xgrant: two grants of one stage are
-      // separated by their fill, so those waits are on adjacent phases too.
+      // v mode: the expand blocks follow in the same ring.  The producer claims each
+      // stage in order (a wait on the adjacent phase of empty, as for the base blocks),
+      // loads its B half (the slot's rows of the B expand pool) with TMA and hands the
+      // stage to the epilogue warps for the A half.  Their waits are on xgrant: two grants
+      // of one stage are separated by their own fill, so those waits are on adjacent
+      // phases too.
       if (a.ex.mode == kExpandV && mbar_wait(xinfo_bar, 0, a.err)) {
         const int nx = *x_blocks;
+        const ExpandLayout xl = expand_layout(a.ex.R);
         for (int e = 0; e < nx; ++e) {
           if (!mbar_wait(&empty[s], ph ^ 1u, a.err)) break;
+          const int u = e / xl.nbs, b = e - u * xl.nbs;
+          const int col = xl.nbs == 1 ? 0 : (b % (xl.rx / 64)) * 64;
+          uint8_t* sa = stage_base + (size_t)s * kStageBytes;
+          mbar_arrive_expect_tx(&full[s], kBBytes);
+          tma_load_2d(sa + kABytes, &tmap_bx, &full[s], col, uslot[u] * a.N + n0);
           mbar_arrive(&xgrant[s]);
           if (++s == stages) {
             s = 0;
@@ -229,7 +245,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the low-rank expand: blocks the epilogue warps write into the same ring
         const int nx = *x_blocks;
         for (int e = 0; e < nx; ++e) {
+          // B half (TMA) and A half (written by the epilogue warps)
           if (!mbar_wait(&full[s], ph, a.err)) break;
+          if (!mbar_wait(&xa_full[s], (uint32_t)(e / stages) & 1u, a.err)) break;
           tc_fence_after();
           const uint64_t stage_off = (uint64_t)(s * (kStageBytes >> 4));
           const uint64_t a_desc = a_desc0 + stage_off, b_desc = b_desc0 + stage_off;
@@ -288,42 +306,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       word &= word - 1;
     }
     named_barrier(1, 128);
-    const int R = a.ex.R, R8 = R >> 3, per = 2 * R8;  // chunks per slot: hi, then lo
-    const int nx = (m * per + 7) / 8;
+    const ExpandLayout xl = expand_layout(a.ex.R);
+    const int nx = m * xl.nbs;
     if (et == 0) {
       *x_blocks = nx;
       mbar_arrive(xinfo_bar);
     }
-    const __nv_bfloat16* Bt = static_cast<const __nv_bfloat16*>(a.ex.Bt_pool);
+    // this row's hi and lo halves in the block layout (while the main loop runs)
+    uint8_t* mine = xscr + (size_t)et * xl.nbs * 128;
+    if (srow >= 0) {
+      for (int j0 = 0; j0 < xl.rx; j0 += 8) {
+        uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
+        if (j0 < a.ex.R) v_hi_lo8(a.ex, m0 + et, j0, hi, lo);
+        const int hb = xl.nbs == 1 ? 0 : j0 / 64;                   // block of the hi part
+        const int lb = xl.nbs == 1 ? 0 : xl.rx / 64 + j0 / 64;      // block of the lo part
+        const int off = xl.nbs == 1 ? j0 * 2 : (j0 % 64) * 2;        // byte in the block
+        *reinterpret_cast<uint4*>(mine + hb * 128 + off) = hi;
+        *reinterpret_cast<uint4*>(mine + lb * 128 + off + (xl.nbs == 1 ? 64 : 0)) = lo;
+      }
+    }
     for (int e = 0; e < nx; ++e) {
       const int st = (nkb + e) % stages;  // ring position nkb + e, after the base blocks
       // the e / stages earlier grants of this stage were for this loop's earlier blocks
       if (!mbar_wait(&xgrant[st], (uint32_t)(e / stages) & 1u, a.err)) break;
+      const int u = e / xl.nbs, b = e - u * xl.nbs;
+      const bool own = uslot[u] == srow;  // rows of other slots contribute zeros
       uint8_t* sa = stage_base + (size_t)st * kStageBytes;
-      uint8_t* sb = sa + kABytes;
-      // A rows: this thread's row of the tile, 8 chunks
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const int q = e * 8 + c, u = q / per, wq = q - u * per;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (u < m && uslot[u] == srow) val = v_chunk_bf16(a.ex, m0 + et, (wq % R8) * 8, wq < R8);
+        const uint4 val = own ? *reinterpret_cast<const uint4*>(mine + b * 128 + c * 16)
+                              : make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(sa + et * 128 + ((c ^ (et & 7)) << 4)) = val;
       }
-      // B rows: rank columns of B_u^T for this tile's N columns
-      for (int n = et; n < BN; n += 128) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int q = e * 8 + c, u = q / per, wq = q - u * per;
-          const bool ok = u < m && n0 + n < a.N;
-          const __nv_bfloat16* src =
-              ok ? Bt + ((size_t)uslot[u] * a.N + n0 + n) * R + (wq % R8) * 8 : Bt;
-          cp_async_16_zfill(sb + n * 128 + ((c ^ (n & 7)) << 4), src, ok ? 16u : 0u);
-        }
-      }
-      cp_async_wait_all();
       fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async-proxy reads
       named_barrier(1, 128);
-      if (et == 0) mbar_arrive(&full[st]);
+      if (et == 0) mbar_arrive(&xa_full[st]);
     }
   }
   if (epi) {
@@ -498,25 +515,27 @@ GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split) {
 
 int gemm_tc_tile_index(int BN) { return BN == 256 ? 0 : (BN == 128 ? 1 : 2); }
 
-static size_t tc_smem_bytes(int BN, int stages) {
+static size_t tc_smem_bytes(int BN, int stages, int xscr_bytes) {
   const size_t stage = (size_t)kABytes + (size_t)BN * kBK * 2;
-  return 1024 + stages * stage + (2 * kBM + 6) * 4 + (3 * stages + 4) * 8;
+  return 1024 + stages * stage + xscr_bytes + (2 * kBM + 6) * 4 + (4 * stages + 4) * 8;
 }
 
 template <int BN>
 static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUtensorMap& tmap_x,
-                             const CUtensorMap& tmap_w, cudaStream_t stream) {
+                             const CUtensorMap& tmap_w, const CUtensorMap& tmap_bx,
+                             cudaStream_t stream) {
   const size_t budget = 227 * 1024;
   const int cs = plan.ksplit;
-  if (a.ex.mode == kExpandV && (cs != 1 || a.ex.R % 8 != 0 || a.ex.S > 32 * kBM || !a.ex.Bt_pool))
+  if (a.ex.mode == kExpandV && (cs != 1 || a.ex.R % 8 != 0 || a.ex.R > 128 || a.ex.S > 32 * kBM))
     return cudaErrorInvalidValue;
+  const int xscr = a.ex.mode == kExpandV ? kBM * expand_layout(a.ex.R).nbs * 128 : 0;
   // the split-K send and receive buffers reuse the stage buffers
   const size_t recv = cs > 1 ? (size_t)2 * (cs - 1) * kBM * (BN / cs) * 4 : 0;
   const size_t stage = (size_t)kABytes + (size_t)BN * kBK * 2;
   int stages = 8;
-  while (stages > 2 && tc_smem_bytes(BN, stages) > budget) --stages;
+  while (stages > 2 && tc_smem_bytes(BN, stages, xscr) > budget) --stages;
   if ((size_t)stages * stage < recv) return cudaErrorInvalidConfiguration;
-  const size_t smem = tc_smem_bytes(BN, stages);
+  const size_t smem = tc_smem_bytes(BN, stages, xscr);
   if (smem > budget) return cudaErrorInvalidConfiguration;
   static int limit = 0;
   cudaError_t e = ensure_smem_limit(gemm_tc_kernel<BN>, (int)smem, &limit);
@@ -535,19 +554,23 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = cs > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmap_x, tmap_w, a, stages);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmap_x, tmap_w, tmap_bx, a, stages, xscr);
 }
 
-cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3, cudaStream_t stream) {
+cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
+                           const CUtensorMap* tmap_bx3, cudaStream_t stream) {
+  if (a.ex.mode == kExpandV && !tmap_bx3) return cudaErrorInvalidValue;
   const GemmPlan plan = gemm_tc_plan(a.M, a.N, a.K, a.num_sms, a.ex.mode == kExpandDelta);
   CUtensorMap tmap_x;
   cudaError_t e = encode_tmap_bf16(&tmap_x, a.x, a.M, a.K, kBM);
   if (e != cudaSuccess) return e;
-  const CUtensorMap& tw = tmap_w3[gemm_tc_tile_index(plan.block_n)];
+  const int ti = gemm_tc_tile_index(plan.block_n);
+  const CUtensorMap& tw = tmap_w3[ti];
+  const CUtensorMap& tb = tmap_bx3 ? tmap_bx3[ti] : tw;  // unused in delta mode
   switch (plan.block_n) {
-    case 256: return launch_tc<256>(a, plan, tmap_x, tw, stream);
-    case 128: return launch_tc<128>(a, plan, tmap_x, tw, stream);
-    default: return launch_tc<64>(a, plan, tmap_x, tw, stream);
+    case 256: return launch_tc<256>(a, plan, tmap_x, tw, tb, stream);
+    case 128: return launch_tc<128>(a, plan, tmap_x, tw, tb, stream);
+    default: return launch_tc<64>(a, plan, tmap_x, tw, tb, stream);
   }
 }
 

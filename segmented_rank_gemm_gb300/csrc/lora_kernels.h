@@ -111,6 +111,23 @@ struct BgmvArgs {
 // Launched with programmatic stream serialization; it does not wait for the builder.
 cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream);
 
+// ---- the tensor-core expand's layout of a slot's rank columns ----
+// v of a row is split as v = hi + lo (two bf16) and multiplied by the slot's B^T on the
+// tensor cores in 64-wide K blocks.  Rank width R <= 32: one block per slot, columns
+// [0, 32) = hi (zero beyond R) and [32, 64) = lo, against [B^T | B^T].  R > 32: the halves
+// are padded to rx = 64 or 128 and take rx / 64 blocks each (hi blocks, then lo blocks),
+// all against B^T padded to rx columns.  wx = columns of a slot's row in the B expand pool.
+struct ExpandLayout {
+  int wx;   // B expand pool width: 64 (R <= 32) or rx
+  int nbs;  // K blocks per slot
+  int rx;   // padded width of each half
+};
+__host__ __device__ inline ExpandLayout expand_layout(int R) {
+  if (R <= 32) return ExpandLayout{64, 1, 32};
+  const int rx = R <= 64 ? 64 : 128;
+  return ExpandLayout{rx, 2 * rx / 64, rx};
+}
+
 // ---- base GEMM with the low-rank term added in its epilogue ----
 enum ExpandMode { kExpandV = 0, kExpandDelta = 1 };
 struct ExpandArgs {
@@ -125,7 +142,6 @@ struct ExpandArgs {
   const float* delta;       // [T_max][N] fp32                                (delta mode)
   int R;
   const void* B_pool;   // [S][R][N]
-  const void* Bt_pool;  // [S][N][R] bf16: B transposed (v mode, tensor-core expand)
   const int32_t* rank;  // [S]
 };
 struct GemmArgs {
@@ -138,8 +154,11 @@ struct GemmArgs {
   int num_sms;
 };
 // tcgen05 / TMEM / TMA kernel (gemm_tc.cu).  tmap_w3 holds the layer's cached maps of the
-// packed weight for N tiles of 256, 128 and 64 rows (in that order).
-cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3, cudaStream_t stream);
+// packed weight for N tiles of 256, 128 and 64 rows (in that order); tmap_bx3 the maps of
+// the B expand pool [S*N rows][wx] with (64 x 256/128/64) boxes (v mode; may be null in
+// delta mode).
+cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
+                           const CUtensorMap* tmap_bx3, cudaStream_t stream);
 constexpr int kTcTileN[3] = {256, 128, 64};
 // Encode a 2-D bf16 tensor map for a K-major [rows, K] matrix with a (64 x box_rows) box.
 cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
@@ -158,6 +177,8 @@ cudaError_t launch_transpose_pad(const void* A_kr, void* At_rk, int K, int r, in
                                  cudaStream_t stream);
 // Wp[n][k] = W[k][n] (bf16 base weight packing).
 cudaError_t launch_pack_w_bf16(const void* W_kn, void* W_nk, int K, int N, cudaStream_t stream);
+// B expand pool row block of one slot: Bx[n][j] from B [R][N] (see expand_layout).
+cudaError_t launch_pack_bx(const void* B_rn, void* Bx_nw, int R, int N, cudaStream_t stream);
 cudaError_t launch_slot_meta(float* scale, int32_t* rank, int32_t* loaded, int slot, float s,
                              int r, int is_loaded, cudaStream_t stream);
 

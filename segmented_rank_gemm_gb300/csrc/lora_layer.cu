@@ -46,7 +46,7 @@ struct lora_layer {
   void* Wp = nullptr;      // packed base weight: bf16 [N][K], f32 [K][N]
   void* A_pool = nullptr;  // [S][R][K]
   void* B_pool = nullptr;  // [S][R][N]
-  void* Bt_pool = nullptr; // [S][N][R] bf16, B transposed: the tensor-core expand (v mode)
+  void* Bx_pool = nullptr; // [S][N][wx] bf16, the B expand pool of the tensor-core expand
   void* A_stage = nullptr; // [K][R] staging for the transposition of a loaded A
   float* scale = nullptr;  // [S]
   int32_t* rank = nullptr;    // [S]
@@ -78,6 +78,7 @@ struct lora_layer {
   std::vector<cudaEvent_t> spare;
   CUtensorMap tmap_w[3];
   CUtensorMap tmap_a;  // A pool [S*R rows][K] with a (64 x round_up(R, 16)) box (bf16)
+  CUtensorMap tmap_bx[3];  // B expand pool [S*N rows][wx], boxes of 256/128/64 rows
   cudaEvent_t trace[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   bool tracing = false;
   char last_error[512] = {0};
@@ -111,7 +112,7 @@ cudaError_t dmalloc(T** p, size_t count) {
 }
 
 void free_all(lora_layer* L) {
-  void* ptrs[] = {L->Wp, L->A_pool, L->B_pool, L->Bt_pool, L->A_stage, L->scale, L->rank, L->loaded,
+  void* ptrs[] = {L->Wp, L->A_pool, L->B_pool, L->Bx_pool, L->A_stage, L->scale, L->rank, L->loaded,
                   L->row_slot, L->perm, L->seg_offsets, L->seg_slot, L->tile_seg,
                   L->tile_row0, L->meta, L->err, L->v, L->delta, L->x_stage, L->ids_stage,
                   L->y_stage};
@@ -206,9 +207,9 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
             cudaMalloc(&L->x_stage, (size_t)max_tokens * K * es) == cudaSuccess &&
             dmalloc(&L->ids_stage, max_tokens) == cudaSuccess &&
             cudaMalloc(&L->y_stage, (size_t)max_tokens * N * es) == cudaSuccess &&
-            // batches beyond kDeltaMaxT rows expand v on the tensor cores from B^T
+            // batches beyond kDeltaMaxT rows expand v on the tensor cores
             (dtype != LORA_BF16 || max_tokens <= kDeltaMaxT ||
-             cudaMalloc(&L->Bt_pool, S * R * N * es) == cudaSuccess);
+             cudaMalloc(&L->Bx_pool, S * expand_layout((int)R).wx * N * es) == cudaSuccess);
   if (!ok) {
     cudaGetLastError();
     return bail(LORA_ENOMEM);
@@ -219,7 +220,9 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
 
   ok = cudaMemsetAsync(L->A_pool, 0, S * R * K * es, stream) == cudaSuccess &&
        cudaMemsetAsync(L->B_pool, 0, S * R * N * es, stream) == cudaSuccess &&
-       (!L->Bt_pool || cudaMemsetAsync(L->Bt_pool, 0, S * R * N * es, stream) == cudaSuccess) &&
+       (!L->Bx_pool ||
+        cudaMemsetAsync(L->Bx_pool, 0, S * expand_layout((int)R).wx * N * es, stream) ==
+            cudaSuccess) &&
        cudaMemsetAsync(L->scale, 0, S * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->rank, 0, S * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->loaded, 0, S * 4, stream) == cudaSuccess &&
@@ -236,6 +239,11 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
     if (encode_tmap_bf16(&L->tmap_a, L->A_pool, (int)(S * R), K, (L->R + 15) / 16 * 16) !=
         cudaSuccess)
       return bail(LORA_ECUDA);
+    if (L->Bx_pool)
+      for (int i = 0; i < 3; ++i)
+        if (encode_tmap_bf16(&L->tmap_bx[i], L->Bx_pool, (int)(S * N),
+                             expand_layout((int)R).wx, kTcTileN[i]) != cudaSuccess)
+          return bail(LORA_ECUDA);
   } else {
     if (cudaMemcpyAsync(L->Wp, W_dev, (size_t)K * N * es, cudaMemcpyDefault, stream) !=
         cudaSuccess)
@@ -282,9 +290,11 @@ int load_adapter_slot(lora_layer_t* L, int slot, const void* A_src, const void* 
   LORA_CUDA(L, cudaMemcpyAsync(Bs, B_src, (size_t)r * N * es, cudaMemcpyDefault, side));
   if ((size_t)r < R)
     LORA_CUDA(L, cudaMemsetAsync(Bs + (size_t)r * N * es, 0, (R - r) * N * es, side));
-  if (L->Bt_pool)  // B^T [N][R] of the slot (rank rows beyond r are the zeros just set)
-    LORA_CUDA(L, launch_pack_w_bf16(Bs, static_cast<char*>(L->Bt_pool) + (size_t)slot * N * R * es,
-                                    (int)R, (int)N, side));
+  if (L->Bx_pool)  // the slot's rows of the B expand pool (rank rows >= r: the zeros just set)
+    LORA_CUDA(L, launch_pack_bx(Bs,
+                                static_cast<char*>(L->Bx_pool) +
+                                    (size_t)slot * N * expand_layout((int)R).wx * es,
+                                (int)R, (int)N, side));
   LORA_CUDA(L, launch_slot_meta(L->scale, L->rank, L->loaded, slot, alpha / (float)r, r, 1,
                                 side));
   cudaEvent_t ev = take_event(L);
@@ -446,13 +456,12 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.ex.delta = L->delta;
   ga.ex.R = L->R;
   ga.ex.B_pool = L->B_pool;
-  ga.ex.Bt_pool = L->Bt_pool;
   ga.ex.rank = L->rank;
   ga.err = L->err;
   ga.num_sms = L->num_sms;
   LORA_CUDA(L, trace_mark(L, 4, stream));
   if (bf16)
-    LORA_CUDA(L, launch_gemm_tc(ga, L->tmap_w, stream));
+    LORA_CUDA(L, launch_gemm_tc(ga, L->tmap_w, L->Bx_pool ? L->tmap_bx : nullptr, stream));
   else
     LORA_CUDA(L, launch_gemm_simt_f32(ga, stream));
   LORA_CUDA(L, trace_mark(L, 5, stream));

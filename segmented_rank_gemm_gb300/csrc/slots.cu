@@ -63,6 +63,34 @@ cudaError_t launch_pack_w_bf16(const void* W_kn, void* W_nk, int K, int N, cudaS
   return cudaGetLastError();
 }
 
+__global__ void pack_bx_kernel(const __nv_bfloat16* __restrict__ B, __nv_bfloat16* __restrict__ Bx,
+                               int R, int N, int wx, int half) {
+  // Bx[n][j] = B[j mod half][n] for j < wx (half = wx / 2 when both halves repeat B^T,
+  // else half = wx), 0 where that rank index is >= R.  32x32 tiles through shared memory.
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int n0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+  for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+    const int j = j0 + dy, n = n0 + threadIdx.x;
+    const int jj = j % half;
+    tile[dy][threadIdx.x] =
+        (j < wx && jj < R && n < N) ? B[(size_t)jj * N + n] : __float2bfloat16(0.f);
+  }
+  __syncthreads();
+  for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+    const int n = n0 + dy, j = j0 + threadIdx.x;
+    if (n < N && j < wx) Bx[(size_t)n * wx + j] = tile[threadIdx.x][dy];
+  }
+}
+
+cudaError_t launch_pack_bx(const void* B_rn, void* Bx_nw, int R, int N, cudaStream_t stream) {
+  const ExpandLayout L = expand_layout(R);
+  dim3 block(32, 8), grid((N + 31) / 32, (L.wx + 31) / 32);
+  pack_bx_kernel<<<grid, block, 0, stream>>>(static_cast<const __nv_bfloat16*>(B_rn),
+                                             static_cast<__nv_bfloat16*>(Bx_nw), R, N, L.wx,
+                                             L.nbs == 1 ? L.wx / 2 : L.wx);
+  return cudaGetLastError();
+}
+
 __global__ void slot_meta_kernel(float* scale, int32_t* rank, int32_t* loaded, int slot, float s,
                                  int r, int is_loaded) {
   scale[slot] = s;
