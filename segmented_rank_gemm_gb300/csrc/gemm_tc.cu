@@ -343,6 +343,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (et == 0) mbar_arrive(&xa_full[st]);
     }
   }
+  bool add_delta = false;  // delta mode: the row adds the low-rank term of the delta buffer
+  if (epi && a.ex.mode != kExpandV) {
+    // the low-rank kernel's results are needed from here on: the main loop keeps running
+    griddep_wait();
+    if (row < a.M) {
+      const int t = a.ex.token_slot[row];
+      add_delta = t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0;
+      // one CTA per row block reports ids outside [-1, S) or naming empty slots
+      if (blockIdx.y == 0 && z == 0) {
+        if (t < -1 || t >= a.ex.S) atomicOr(a.err, LORA_ERRF_BAD_ID);
+        else if (t >= 0 && !add_delta) atomicOr(a.err, LORA_ERRF_EMPTY_SLOT);
+      }
+    }
+  }
   if (epi) {
     mbar_wait(tmem_full, 0, a.err);
     tc_fence_after();
@@ -398,24 +412,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (epi) {
     // only now the low-rank kernel's results are needed: the main loop and the split-K
     // exchange ran while it was still working
-    bool add_delta = false;
-    if (a.ex.mode == kExpandDelta) {
-      griddep_wait();
-      if (row < a.M) {
-        const int t = a.ex.token_slot[row];
-        add_delta = t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0;
-      }
-    }
     // the delta buffer holds the first 512 rows only: a row that adds no delta never forms
     // an address into it beyond row 0
-    const float* drow = a.ex.delta + (add_delta ? (size_t)row * a.N : 0);
+    const bool from_delta = add_delta && a.ex.mode == kExpandDelta;
+    const float* drow = a.ex.delta + (from_delta ? (size_t)row * a.N : 0);
     __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.y) + (size_t)row * a.N;
     const int cbase = z * bnc;  // first accumulator column this CTA finishes
 #pragma unroll 1
     for (int c = 0; c < bnc; c += 32) {
       const int nc = n0 + cbase + c;
       float4 d[8];  // the row's delta for these 32 columns, in flight during the TMEM read
-      if (add_delta) {
+      if (from_delta) {
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           d[q] = nc + q * 4 < a.N ? *reinterpret_cast<const float4*>(drow + nc + q * 4)
@@ -486,8 +493,11 @@ cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K
 }
 
 // Tile shape and K split.  Large problems: the widest N tile that still gives one tile per
-// SM, no split.  Small batches (when split is allowed): N tile 256 and the largest
-// power-of-two K split (cluster size, at most 4) that keeps the CTA count within the SMs.
+// SM, no split.  Small batches (when split is allowed): N tile 128 and the largest
+// power-of-two K split (cluster size, at most 4) that keeps the CTA count within the SMs;
+// N tile 256 when even the unsplit 128-wide tiles leave most SMs idle.  (A 128-wide tile
+// with a 2-way split moves a third of the partials a 256-wide one with a 4-way split
+// does, and its CTA leaves room on its SM for a CTA of the low-rank kernel.)
 GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split) {
   const int mt = (M + kBM - 1) / kBM;
   const int nkb = (K + kBK - 1) / kBK;
@@ -501,14 +511,17 @@ GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split) {
     }
   }
   if (!allow_split) return p;
-  const int tiles256 = mt * ((N + 255) / 256);
   // every one of the cs K ranges of ceil(nkb / cs) blocks must be non-empty
   auto ranges_ok = [nkb](int c) { return (c - 1) * ((nkb + c - 1) / c) < nkb; };
-  int cs = 1;
-  while (cs * 2 <= 4 && tiles256 * cs * 2 <= num_sms && ranges_ok(cs * 2)) cs *= 2;
-  if (cs > 1) {
-    p.block_n = 256;
-    p.ksplit = cs;
+  for (int bn : {128, 256}) {
+    const int tiles = mt * ((N + bn - 1) / bn);
+    int cs = 1;
+    while (cs * 2 <= 4 && tiles * cs * 2 <= num_sms && ranges_ok(cs * 2)) cs *= 2;
+    if (cs > 1 && tiles * cs * 2 > num_sms / 2) {
+      p.block_n = bn;
+      p.ksplit = cs;
+      return p;
+    }
   }
   return p;
 }
@@ -524,7 +537,9 @@ template <int BN>
 static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUtensorMap& tmap_x,
                              const CUtensorMap& tmap_w, const CUtensorMap& tmap_bx,
                              cudaStream_t stream) {
-  const size_t budget = 227 * 1024;
+  // delta mode leaves ~8 KB of the SM's shared memory to a CTA of the BGMV kernel, which
+  // then runs on the same SM while the main loop does
+  const size_t budget = a.ex.mode == kExpandDelta ? 219 * 1024 : 227 * 1024;
   const int cs = plan.ksplit;
   if (a.ex.mode == kExpandV && (cs != 1 || a.ex.R % 8 != 0 || a.ex.R > 128 || a.ex.S > 32 * kBM))
     return cudaErrorInvalidValue;
@@ -560,7 +575,7 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
                            const CUtensorMap* tmap_bx3, cudaStream_t stream) {
   if (a.ex.mode == kExpandV && !tmap_bx3) return cudaErrorInvalidValue;
-  const GemmPlan plan = gemm_tc_plan(a.M, a.N, a.K, a.num_sms, a.ex.mode == kExpandDelta);
+  const GemmPlan plan = gemm_tc_plan(a.M, a.N, a.K, a.num_sms, a.ex.mode != kExpandV);
   CUtensorMap tmap_x;
   cudaError_t e = encode_tmap_bf16(&tmap_x, a.x, a.M, a.K, kBM);
   if (e != cudaSuccess) return e;

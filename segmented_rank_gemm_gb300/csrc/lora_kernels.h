@@ -129,6 +129,8 @@ __host__ __device__ inline ExpandLayout expand_layout(int R) {
 }
 
 // ---- base GEMM with the low-rank term added in its epilogue ----
+// kExpandV: y += [v^hi | v^lo] [B^T ; B^T] as extra tensor-core K blocks (large batches).
+// kExpandDelta: y += delta, the fp32 [T,N] low-rank term a BGMV kernel expanded.
 enum ExpandMode { kExpandV = 0, kExpandDelta = 1 };
 struct ExpandArgs {
   int mode;                 // kExpandV: y += v B_slot;  kExpandDelta: y += delta

@@ -65,6 +65,7 @@ struct lora_layer {
   float* delta = nullptr;        // [min(T_max, kDeltaMaxT)][N] fp32 (delta mode, bf16)
   int max_tiles = 0;
   int T_batch = -1;              // T of the last set_batch_segments, -1 = none
+  bool segments_pending = false;  // that batch's builder has not run yet (decode batches)
   const int32_t* token_slot = nullptr;  // the caller's ids of that batch
   // staging for lora_forward_host
   void* x_stage = nullptr;
@@ -317,6 +318,8 @@ int unload_adapter_slot(lora_layer_t* L, int slot, void* side_) {
   return LORA_OK;
 }
 
+static int run_builder(lora_layer_t* L, cudaStream_t stream);
+
 int set_batch_segments(lora_layer_t* L, const int32_t* token_slot_dev, int T, void* stream_) {
   if (!L) return LORA_EINVAL;
   if (T < 0 || T > L->T_max)
@@ -326,9 +329,24 @@ int set_batch_segments(lora_layer_t* L, const int32_t* token_slot_dev, int T, vo
   // slot loads become visible to the builder (it reads the loaded flags)
   LORA_CUDA(L, wait_pending_loads(L, stream));
 
+  L->T_batch = T;
+  L->token_slot = token_slot_dev;
+  // A bf16 batch of at most kDeltaMaxT rows is computed without its segments (the BGMV
+  // kernel and the base GEMM read the ids directly, and the GEMM reports bad ids), so the
+  // builder runs only if lora_get_segments asks for them.
+  L->segments_pending = L->dtype == LORA_BF16 && T <= kDeltaMaxT;
+  if (L->segments_pending) {
+    LORA_CUDA(L, trace_mark(L, 0, stream));
+    LORA_CUDA(L, trace_mark(L, 1, stream));
+    return LORA_OK;
+  }
+  return run_builder(L, stream);
+}
+
+static int run_builder(lora_layer_t* L, cudaStream_t stream) {
   BuilderArgs a;
-  a.token_slot = token_slot_dev;
-  a.T = T;
+  a.token_slot = L->token_slot;
+  a.T = L->T_batch;
   a.S = L->S;
   a.loaded = L->loaded;
   // work list: 128-row windows of perm for the tensor-core shrink (bf16), segment tiles of
@@ -347,8 +365,7 @@ int set_batch_segments(lora_layer_t* L, const int32_t* token_slot_dev, int T, vo
   LORA_CUDA(L, trace_mark(L, 0, stream));
   LORA_CUDA(L, launch_segment_builder(a, stream));
   LORA_CUDA(L, trace_mark(L, 1, stream));
-  L->T_batch = T;
-  L->token_slot = token_slot_dev;
+  L->segments_pending = false;
   return LORA_OK;
 }
 
@@ -519,6 +536,10 @@ int lora_get_segments(lora_layer_t* L, int32_t* perm, int32_t* seg_offsets, int3
     return fail(L, LORA_EINVAL, "null output pointer");
   if (L->T_batch < 0) return fail(L, LORA_ESTATE, "no batch set");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (L->segments_pending) {
+    const int rc = run_builder(L, stream);
+    if (rc != LORA_OK) return rc;
+  }
   LORA_CUDA(L, cudaStreamSynchronize(stream));
   int32_t meta[4];
   LORA_CUDA(L, cudaMemcpy(meta, L->meta, sizeof(meta), cudaMemcpyDeviceToHost));

@@ -24,6 +24,8 @@
 // Launch: programmatic dependent launch.  The kernel lets the next kernel (the base GEMM,
 // whose main loop needs nothing from it) launch at once, then waits for the segment
 // builder's results before reading them.
+#include <algorithm>
+
 #include "lora_common.cuh"
 #include "lora_kernels.h"
 
@@ -345,237 +347,240 @@ __global__ void __launch_bounds__(kBgmvThreads, 8)  // <= 64 registers: 4 CTAs f
   cluster_sync_all();  // no CTA leaves while a peer may still read its partials
 }
 
-// ---------------------------------------------------------------------------------------
-// Delta mode, slot-major (slot width <= 32): one loaded slot per cluster of CS CTAs.  The
-// cluster finds the rows that name its slot by scanning the id vector (no segment builder
-// needed), so each A and B slice is read once per slot, however many rows share it.
-// CTA c of the cluster:
-//   0. stages, with 16-byte cp.async copies (many in flight, no register cost), its K range
-//      of A_slot and of the slot's x rows in shared memory;
-//   1. partial v over its K range: a warp per (row, group of 8 rank columns), lanes over
-//      16-byte chunks, 8 independent accumulators; then stages its N range of B_slot into
-//      the buffer A used, so that copy lands while the cluster reduces;
-//   2. the CS partials summed through distributed shared memory, scaled by alpha / r;
-//   3. delta over its N range from the staged B, fp32.
-// Rows of a slot go through in groups of kSlotRows.
-// ---------------------------------------------------------------------------------------
-static constexpr int kSlotThreads = 128;
-static constexpr int kSlotRows = 4;
-static constexpr int kSlotMaxRank = 32;
-static constexpr int kSlotMaxT = 512;
+static constexpr int kSlotMaxT = 512;  // largest decode batch (the delta buffer's rows)
 
-__global__ void __launch_bounds__(kSlotThreads)
-    bgmv_slot_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ token_slot,
-                     const int32_t* __restrict__ loaded, int T, int K, int N, int R, int S,
-                     const __nv_bfloat16* __restrict__ At_pool,
-                     const __nv_bfloat16* __restrict__ B_pool, const float* __restrict__ scale,
-                     const int32_t* __restrict__ rank, float* __restrict__ delta, int kchunk,
-                     int nchunk) {
-  griddep_launch_dependents();  // the base GEMM's main loop may start now
-  extern __shared__ __align__(16) uint8_t smem[];
-  // [R][max(kchunk, nchunk)]: A's K range, then B's N range; then [kSlotRows][kchunk] of x
-  const int wchunk = max(kchunk, nchunk);
-  __nv_bfloat16* AB_s = reinterpret_cast<__nv_bfloat16*>(smem);
-  __nv_bfloat16* x_s = AB_s + (size_t)R * wchunk;
-  __shared__ int rows_s[kSlotMaxT];
-  __shared__ int warp_cnt[kSlotThreads / 32];
-  __shared__ float v_part[2][kSlotRows * (kSlotMaxRank + 1)];
-  __shared__ float v_s[kSlotRows * (kSlotMaxRank + 1)];
-  constexpr int vstride = kSlotMaxRank + 1;
-  constexpr int kIdsPerThread = kSlotMaxT / kSlotThreads;
+// ---------------------------------------------------------------------------------------
+// BGMV for decode batches (rank width <= 32, T <= 512): one CTA per slot at a time (CTAs
+// loop over slots), delta[row, :] = (alpha/r) (x[row] A_s) B_s for the slot's rows.
+// The rows are found with one scan of the id vector.  Both halves stream the slot's
+// matrices through registers, each read once per group of rows:
+//   shrink  thread t takes 16-byte chunks t, t + 256, ... of K; the loads of a chunk (the
+//           rows' x and a batch of 16 rank rows of A_s^T) are issued together; the block
+//           sums the partials (warp shuffles, then one shared-memory pass) into v (fp32).
+//   expand  thread t takes 8-column chunks t, t + 256, ... of N; a batch of 16 rank rows of
+//           B_s is loaded together and applied to the group's rows; the fp32 delta rows
+//           are written once.
+// At most 128 registers a thread and ~4 KB of shared memory, so that a CTA fits on an SM
+// beside a base GEMM CTA and runs while its main loop does.
+// ---------------------------------------------------------------------------------------
+static constexpr int kStrThreads = 256;
+static constexpr int kStrExpRows = 4;  // rows per group (shrink, then expand)
+static constexpr int kStrRedMax = 64;  // rows x rank columns of one shrink pass
+
+// v of NQ rows (rank columns < RMAX) into vdst[q][j], scaled by sc; all threads of the CTA.
+template <int RMAX, int NQ>
+__device__ __forceinline__ void stream_shrink(const __nv_bfloat16* __restrict__ x,
+                                              const int* rows, int K, const __nv_bfloat16* At,
+                                              int r, float sc, float (*red)[kStrRedMax],
+                                              float (*vdst)[32]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t csize;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
-  const uint32_t c = cluster_ctarank();
-  const int n_clusters = gridDim.x / csize;
-  const int k0 = c * kchunk, kc = max(0, min(K - k0, kchunk));
-  const int nb0 = c * nchunk, nc = max(0, min(N - nb0, nchunk));
-  const int kv = kc / 8, nv = nc / 8;  // 16-byte chunks per staged row
-
-  // the id vector, read once: thread t holds ids t*kIdsPerThread ... (+kIdsPerThread)
-  int ids[kIdsPerThread];
+  float acc[NQ][RMAX];
 #pragma unroll
-  for (int u = 0; u < kIdsPerThread; ++u) {
-    const int i = tid * kIdsPerThread + u;
+  for (int q = 0; q < NQ; ++q)
+#pragma unroll
+    for (int j = 0; j < RMAX; ++j) acc[q][j] = 0.f;
+  for (int e = tid; e < K / 8; e += kStrThreads) {
+    // the loads of a chunk go out together: the rows' x, then a batch of 16 rank rows of A
+    uint4 xv[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+      xv[q] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)rows[q] * K + e * 8));
+#pragma unroll
+    for (int j0 = 0; j0 < RMAX; j0 += 16) {
+      if (j0 >= r) break;
+      uint4 av[16];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj)
+        av[jj] = j0 + jj < r
+                     ? __ldg(reinterpret_cast<const uint4*>(At + (size_t)(j0 + jj) * K + e * 8))
+                     : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        const float xf[8] = {bf16_lo(xv[q].x), bf16_hi(xv[q].x), bf16_lo(xv[q].y),
+                             bf16_hi(xv[q].y), bf16_lo(xv[q].z), bf16_hi(xv[q].z),
+                             bf16_lo(xv[q].w), bf16_hi(xv[q].w)};
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          float t = acc[q][j0 + jj];
+          t = fmaf(xf[0], bf16_lo(av[jj].x), t);
+          t = fmaf(xf[1], bf16_hi(av[jj].x), t);
+          t = fmaf(xf[2], bf16_lo(av[jj].y), t);
+          t = fmaf(xf[3], bf16_hi(av[jj].y), t);
+          t = fmaf(xf[4], bf16_lo(av[jj].z), t);
+          t = fmaf(xf[5], bf16_hi(av[jj].z), t);
+          t = fmaf(xf[6], bf16_lo(av[jj].w), t);
+          t = fmaf(xf[7], bf16_hi(av[jj].w), t);
+          acc[q][j0 + jj] = t;
+        }
+      }
+    }
+  }
+  // block sum: warp shuffles, then one shared-memory pass
+#pragma unroll
+  for (int q = 0; q < NQ; ++q)
+#pragma unroll
+    for (int j = 0; j < RMAX; ++j) {
+      float t = acc[q][j];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+      if (lane == 0) red[warp][q * RMAX + j] = t;
+    }
+  __syncthreads();
+  for (int i = tid; i < NQ * RMAX; i += kStrThreads) {
+    const int q = i / RMAX, j = i - q * RMAX;
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kStrThreads / 32; ++w) sum += red[w][i];
+    vdst[q][j] = j < r ? sc * sum : 0.f;
+  }
+  __syncthreads();  // red is rewritten by the next pass
+}
+
+// delta rows of NG rows from v_s[0 .. NG) and the slot's B rows; all threads of the CTA.
+template <int RMAX, int NG>
+__device__ __forceinline__ void stream_expand(const __nv_bfloat16* __restrict__ Bs, int N, int r,
+                                              const float (*v_s)[32], const int* rows,
+                                              float* __restrict__ delta) {
+  for (int e = threadIdx.x; e < N / 8; e += kStrThreads) {
+    float o[NG][8];
+#pragma unroll
+    for (int q = 0; q < NG; ++q)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[q][i] = 0.f;
+#pragma unroll
+    for (int j0 = 0; j0 < RMAX; j0 += 16) {
+      if (j0 >= r) break;
+      uint4 b[16];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj)
+        b[jj] = j0 + jj < r
+                    ? __ldg(reinterpret_cast<const uint4*>(Bs + (size_t)(j0 + jj) * N + e * 8))
+                    : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const float bf[8] = {bf16_lo(b[jj].x), bf16_hi(b[jj].x), bf16_lo(b[jj].y),
+                             bf16_hi(b[jj].y), bf16_lo(b[jj].z), bf16_hi(b[jj].z),
+                             bf16_lo(b[jj].w), bf16_hi(b[jj].w)};
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+          const float vj = v_s[q][j0 + jj];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[q][i] = fmaf(vj, bf[i], o[q][i]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < NG; ++q) {
+      float4* d = reinterpret_cast<float4*>(delta + (size_t)rows[q] * N + e * 8);
+      d[0] = make_float4(o[q][0], o[q][1], o[q][2], o[q][3]);
+      d[1] = make_float4(o[q][4], o[q][5], o[q][6], o[q][7]);
+    }
+  }
+}
+
+template <int RMAX, int ROWS>
+__global__ void __launch_bounds__(kStrThreads, 2)
+    bgmv_stream_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ token_slot,
+                       const int32_t* __restrict__ loaded, int T, int K, int N, int R, int S,
+                       const __nv_bfloat16* __restrict__ At_pool,
+                       const __nv_bfloat16* __restrict__ B_pool, const float* __restrict__ scale,
+                       const int32_t* __restrict__ rank, float* __restrict__ delta) {
+  griddep_launch_dependents();  // the base GEMM's main loop may start now
+  __shared__ int rows_s[kSlotMaxT];
+  __shared__ int warp_cnt[kStrThreads / 32];
+  __shared__ float red[kStrThreads / 32][kStrRedMax];
+  __shared__ float v_s[kStrExpRows][32];
+  constexpr int kIds = kSlotMaxT / kStrThreads;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int ids[kIds];
+#pragma unroll
+  for (int u = 0; u < kIds; ++u) {
+    const int i = tid * kIds + u;
     ids[u] = i < T ? token_slot[i] : -1;
   }
-
-  int buf = 0;
-  for (int s = blockIdx.x / csize; s < S; s += n_clusters) {
-    if (loaded[s] == 0) continue;  // the same decision in every CTA of the cluster
-    // ---- rows naming slot s, in row order (one block-wide exclusive scan) ----
+  const int kv = K / 8, nv = N / 8;  // 16-byte chunks of a row of x / 8-column chunks of N
+  for (int s = blockIdx.x; s < S; s += gridDim.x) {
+    if (loaded[s] == 0) continue;
+    // every 16-byte chunk of A_s and B_s this thread will read, requested into L2 now: the
+    // DRAM round trips overlap the row scan below, and the loads after it hit L2
+    const int rs = min(R, RMAX);
+    for (int e = tid; e < kv; e += kStrThreads)
+      for (int j = 0; j < rs; ++j)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(At_pool + ((size_t)s * R + j) * K + e * 8));
+    for (int e = tid; e < nv; e += kStrThreads)
+      for (int j = 0; j < rs; ++j)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(B_pool + ((size_t)s * R + j) * N + e * 8));
+    // ---- rows naming slot s, in row order ----
     int mine = 0;
 #pragma unroll
-    for (int u = 0; u < kIdsPerThread; ++u) mine += ids[u] == s;
+    for (int u = 0; u < kIds; ++u) mine += ids[u] == s;
     int inc = mine;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, inc, d);
-      if (lane >= d) inc += v;
+      const int t = __shfl_up_sync(0xffffffffu, inc, d);
+      if (lane >= d) inc += t;
     }
     if (lane == 31) warp_cnt[warp] = inc;
     __syncthreads();
     int pos = inc - mine, nrows = 0;
-    for (int w = 0; w < kSlotThreads / 32; ++w) {
+    for (int w = 0; w < kStrThreads / 32; ++w) {
       if (w < warp) pos += warp_cnt[w];
       nrows += warp_cnt[w];
     }
 #pragma unroll
-    for (int u = 0; u < kIdsPerThread; ++u)
-      if (ids[u] == s) rows_s[pos++] = tid * kIdsPerThread + u;
+    for (int u = 0; u < kIds; ++u)
+      if (ids[u] == s) rows_s[pos++] = tid * kIds + u;
     __syncthreads();
-    if (nrows == 0) continue;  // same in every CTA
+    if (nrows == 0) continue;
     const int r = rank[s];
     const float sc = scale[s];
-    const __nv_bfloat16* At = At_pool + (size_t)s * R * K + k0;
-    const __nv_bfloat16* Bs = B_pool + (size_t)s * R * N + nb0;
-
-    for (int q0 = 0; q0 < nrows; q0 += kSlotRows) {
-      const int nq = min(kSlotRows, nrows - q0);
-      // ---- 0. stage A (K range) and the group's x rows ----
-      for (int i = tid; i < r * kv; i += kSlotThreads) {
-        const int j = i / kv, e = i - j * kv;
-        cp_async_16(AB_s + (size_t)j * wchunk + e * 8, At + (size_t)j * K + e * 8);
+    const __nv_bfloat16* At = At_pool + (size_t)s * R * K;
+    const __nv_bfloat16* Bs = B_pool + (size_t)s * R * N;
+    for (int g0 = 0; g0 < nrows; g0 += kStrExpRows) {
+      const int ng = min(kStrExpRows, nrows - g0);
+      // shrink: v_s[0 .. ng), ROWS rows a pass (the last pass may take one)
+      for (int q0 = 0; q0 < ng; q0 += ROWS) {
+        if (ng - q0 >= ROWS)
+          stream_shrink<RMAX, ROWS>(x, rows_s + g0 + q0, K, At, r, sc, red, v_s + q0);
+        else
+          stream_shrink<RMAX, 1>(x, rows_s + g0 + q0, K, At, r, sc, red, v_s + q0);
       }
-      for (int i = tid; i < nq * kv; i += kSlotThreads) {
-        const int q = i / kv, e = i - q * kv;
-        cp_async_16(x_s + (size_t)q * kchunk + e * 8, x + (size_t)rows_s[q0 + q] * K + k0 + e * 8);
+      // expand: the group's delta rows
+      switch (ng) {
+        case 1: stream_expand<RMAX, 1>(Bs, N, r, v_s, rows_s + g0, delta); break;
+        case 2: stream_expand<RMAX, 2>(Bs, N, r, v_s, rows_s + g0, delta); break;
+        case 3: stream_expand<RMAX, 3>(Bs, N, r, v_s, rows_s + g0, delta); break;
+        default: stream_expand<RMAX, 4>(Bs, N, r, v_s, rows_s + g0, delta); break;
       }
-      cp_async_wait_all();
-      __syncthreads();
-
-      // ---- 1. partial v: warp per (row, 8 rank columns) ----
-      float* vp = v_part[buf];
-      buf ^= 1;
-      const int ngr = (r + 7) / 8;
-      for (int o = warp; o < nq * ngr; o += kSlotThreads / 32) {
-        const int q = o / ngr, j0 = (o - q * ngr) * 8;
-        const __nv_bfloat16* xs = x_s + (size_t)q * kchunk;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int e = lane; e < kv; e += 32) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(xs + e * 8);
-          const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
-                               bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const uint4 av =
-                *reinterpret_cast<const uint4*>(AB_s + (size_t)min(j0 + jj, r - 1) * wchunk + e * 8);
-            acc[jj] = fmaf(xf[0], bf16_lo(av.x), acc[jj]);
-            acc[jj] = fmaf(xf[1], bf16_hi(av.x), acc[jj]);
-            acc[jj] = fmaf(xf[2], bf16_lo(av.y), acc[jj]);
-            acc[jj] = fmaf(xf[3], bf16_hi(av.y), acc[jj]);
-            acc[jj] = fmaf(xf[4], bf16_lo(av.z), acc[jj]);
-            acc[jj] = fmaf(xf[5], bf16_hi(av.z), acc[jj]);
-            acc[jj] = fmaf(xf[6], bf16_lo(av.w), acc[jj]);
-            acc[jj] = fmaf(xf[7], bf16_hi(av.w), acc[jj]);
-          }
-        }
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) acc[jj] += __shfl_xor_sync(0xffffffffu, acc[jj], off);
-        }
-        if (lane == 0) {
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj)
-            if (j0 + jj < r) vp[q * vstride + j0 + jj] = acc[jj];
-        }
-      }
-      __syncthreads();  // A is no longer read: stage B (N range) in its place
-      for (int i = tid; i < r * nv; i += kSlotThreads) {
-        const int j = i / nv, e = i - j * nv;
-        cp_async_16(AB_s + (size_t)j * wchunk + e * 8, Bs + (size_t)j * N + e * 8);
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-      __syncwarp();
-      cluster_sync_all();  // every CTA's partials of this row group are written
-
-      // ---- 2. sum the partials of the cluster ----
-      if (tid < nq * r) {
-        const int q = tid / r, j = tid - q * r;
-        const uint32_t local = smem_u32(vp + q * vstride + j);
-        float sum = 0.f;
-        for (uint32_t d = 0; d < csize; ++d) sum += dsmem_ld(dsmem_map(local, d));
-        v_s[q * vstride + j] = sc * sum;
-      }
-      asm volatile("cp.async.wait_group 0;" ::: "memory");  // B is here
-      __syncthreads();
-
-      // ---- 3. delta over this CTA's N range ----
-      for (int e = tid; e < nv; e += kSlotThreads) {
-        float acc[kSlotRows][8];
-#pragma unroll
-        for (int q = 0; q < kSlotRows; ++q)
-#pragma unroll
-          for (int i2 = 0; i2 < 8; ++i2) acc[q][i2] = 0.f;
-        for (int j = 0; j < r; ++j) {
-          const uint4 b = *reinterpret_cast<const uint4*>(AB_s + (size_t)j * wchunk + e * 8);
-          const float bf[8] = {bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y),
-                               bf16_lo(b.z), bf16_hi(b.z), bf16_lo(b.w), bf16_hi(b.w)};
-#pragma unroll
-          for (int q = 0; q < kSlotRows; ++q) {
-            const float vj = v_s[min(q, nq - 1) * vstride + j];
-#pragma unroll
-            for (int i2 = 0; i2 < 8; ++i2) acc[q][i2] = fmaf(vj, bf[i2], acc[q][i2]);
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < kSlotRows; ++q) {
-          if (q < nq) {
-            float4* d = reinterpret_cast<float4*>(delta + (size_t)rows_s[q0 + q] * N + nb0 + e * 8);
-            d[0] = make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
-            d[1] = make_float4(acc[q][4], acc[q][5], acc[q][6], acc[q][7]);
-          }
-        }
-      }
-      __syncthreads();  // the staging buffers and v_s are rewritten next
+      __syncthreads();  // v_s is rewritten by the next group
     }
   }
-  __syncwarp();
-  cluster_sync_all();  // no CTA leaves while a peer may still read its partials
 }
 
-static size_t bgmv_slot_smem(int R, int kchunk, int nchunk) {
-  return ((size_t)R * (kchunk > nchunk ? kchunk : nchunk) + (size_t)kSlotRows * kchunk) * 2;
+static cudaError_t launch_bgmv_stream(const BgmvArgs& a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(std::max(1, std::min(a.S, a.num_sms)));
+  cfg.blockDim = dim3(kStrThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
+  const __nv_bfloat16* At = static_cast<const __nv_bfloat16*>(a.At_pool);
+  const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(a.B_pool);
+  if (a.R <= 16)
+    return cudaLaunchKernelEx(&cfg, bgmv_stream_kernel<16, 2>, x, a.token_slot, a.loaded, a.T,
+                              a.K, a.N, a.R, a.S, At, B, a.scale, a.rank, a.delta);
+  return cudaLaunchKernelEx(&cfg, bgmv_stream_kernel<32, 1>, x, a.token_slot, a.loaded, a.T, a.K,
+                            a.N, a.R, a.S, At, B, a.scale, a.rank, a.delta);
 }
 
 cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream) {
-  if (a.R <= kSlotMaxRank && a.T <= kSlotMaxT) {
-    // slot-major: cluster of 4 CTAs per slot (8 for slot widths above 16), fewer when K or N
-    // is small; each CTA stages R x (K/cs) of A -- then R x (N/cs) of B in the same buffer --
-    // and kSlotRows x (K/cs) of x
-    int cs = a.R <= 16 ? 4 : 8;
-    while (cs > 1 && (a.K < cs * 64 || a.N < cs * 64)) cs >>= 1;
-    const int kchunk = ((a.K + cs - 1) / cs + 7) / 8 * 8;
-    const int nchunk = ((a.N + cs - 1) / cs + 7) / 8 * 8;
-    const size_t smem = bgmv_slot_smem(a.R, kchunk, nchunk);
-    if (smem <= 200 * 1024) {
-      static int limit = 0;
-      static bool carveout = false;
-      cudaError_t e = ensure_smem_limit(bgmv_slot_kernel, (int)smem, &limit);
-      if (e == cudaSuccess) e = prefer_max_smem_carveout(bgmv_slot_kernel, &carveout);
-      if (e != cudaSuccess) return e;
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[2];
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-      attr[1].id = cudaLaunchAttributeClusterDimension;
-      attr[1].val.clusterDim.x = cs;
-      attr[1].val.clusterDim.y = 1;
-      attr[1].val.clusterDim.z = 1;
-      cfg.gridDim = dim3(a.S * cs);
-      cfg.blockDim = dim3(kSlotThreads);
-      cfg.dynamicSmemBytes = smem;
-      cfg.stream = stream;
-      cfg.attrs = attr;
-      cfg.numAttrs = 2;
-      return cudaLaunchKernelEx(&cfg, bgmv_slot_kernel, static_cast<const __nv_bfloat16*>(a.x),
-                                a.token_slot, a.loaded, a.T, a.K, a.N, a.R, a.S,
-                                static_cast<const __nv_bfloat16*>(a.At_pool),
-                                static_cast<const __nv_bfloat16*>(a.B_pool), a.scale, a.rank,
-                                a.delta, kchunk, nchunk);
-    }
-  }
+  if (a.R <= 32 && a.T <= kSlotMaxT && a.K % 8 == 0 && a.N % 8 == 0)
+    return launch_bgmv_stream(a, stream);  // slot-major, registers only
   // row-major: cluster of cs CTAs per row: 4 normally, fewer when K or N is small
   int cs = 4;
   while (cs > 1 && (a.K < cs * 256 || a.N < cs * 64)) cs >>= 1;
