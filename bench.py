@@ -298,7 +298,8 @@ def run_stack(args):
                      "algorithmic_flops_per_step": flops},
         "step_hbm": {"algorithmic_bytes": base_bytes + ad_bytes,
                      "achieved_gbs": (base_bytes + ad_bytes) / step_s / 1e9},
-        "gpu_launches": 3 * 7 * st.n_layers * args.steps + args.steps,
+        # per projection: BGMV + GEMM (decode batch: no segment builder)
+        "gpu_launches": 2 * 7 * st.n_layers * args.steps,
         "clocks": clocks,
     }
     if rank == 0:
@@ -462,7 +463,8 @@ def run_ours(args):
         e2e = {"value": aggregate(T, n_e2e, world, e_sec), "unit": UNIT,
                "h2d_bytes_per_step": T * K * es + T * 4, "d2h_bytes_per_step": T * N * es,
                "ms_per_step": e_sec * 1e3 / n_e2e,
-               "path": "lora_forward_host: pinned x/ids H2D, builder, shrink, GEMM, y D2H"}
+               "path": "lora_forward_host: pinned x/ids H2D, %s, y D2H" % (
+                   "BGMV, GEMM" if work["mode"] == "delta" else "builder, SGMV shrink, GEMM")}
 
     for l in layers:
         assert l.status(stream) == LORA_OK
@@ -503,7 +505,8 @@ def run_ours(args):
         "lowrank_kernel": {"algorithmic_bytes": work["lowrank_bytes"],
                            "achieved_gbs": work["lowrank_bytes"] / (kern_us["shrink"] * 1e-6) / 1e9,
                            "mode": work["mode"]},
-        "gpu_launches": 3 * args.steps,
+        # decode batches (bf16, <= 512 rows): BGMV + GEMM; larger: builder + shrink + GEMM
+        "gpu_launches": (2 if work["mode"] == "delta" else 3) * args.steps,
         "clocks": clocks,
         "e2e": e2e,
         "wall_s_timed": t_wall1 - t_wall0,

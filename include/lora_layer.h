@@ -98,14 +98,18 @@ int load_adapter_slot(lora_layer_t* layer, int slot, const void* A_src, const vo
 int unload_adapter_slot(lora_layer_t* layer, int slot, void* side_stream);
 
 /*
- * Build the segment layout of a batch on the device.
+ * Set the batch: each row's slot, and its segment layout on the device.
  *   token_slot_dev  [T] int32 in device memory: each row's slot, -1 = base only.
  *   T               0 <= T <= max_tokens (T = 0 is an empty batch).
- * Enqueues one kernel on `stream` that stably sorts the adapted rows by slot
- * (ascending slot, original row order within a slot; base-only rows excluded; slots with
- * no rows get no segment) into a row permutation, segment offsets (n_seg + 1) and each
- * segment's slot, in layer-owned device memory.  The next lora_forward on the same
- * stream uses this layout; token_slot_dev must stay valid until that forward has run.
+ * The layout stably sorts the adapted rows by slot (ascending slot, original row order
+ * within a slot; base-only rows excluded; slots with no rows get no segment) into a row
+ * permutation, segment offsets (n_seg + 1) and each segment's slot, in layer-owned device
+ * memory, built by one kernel on `stream`.  bf16 batches of more than 512 rows (and every
+ * fp32 batch) need it and get it here; bf16 batches of at most 512 rows are computed from
+ * the ids alone, so their layout is built only when lora_get_segments asks for it.
+ * The next lora_forward on the same stream uses this batch.  token_slot_dev is borrowed:
+ * it must stay valid until that forward has run, and, for batches of at most 512 bf16
+ * rows, until the next set_batch_segments (lora_get_segments may read it).
  * Errors: LORA_EINVAL, LORA_ECUDA.
  */
 int set_batch_segments(lora_layer_t* layer, const int32_t* token_slot_dev, int T, void* stream);
@@ -114,11 +118,18 @@ int set_batch_segments(lora_layer_t* layer, const int32_t* token_slot_dev, int T
  * y = x W + per-row LoRA delta, for the batch described by the last set_batch_segments.
  *   x_dev   [T,K] device, y_dev [T,N] device (overwritten; must not overlap x_dev).
  *   T       must equal the T of the last set_batch_segments (else LORA_ESTATE).
- * Enqueues the low-rank kernel (per segment tile: v = (alpha/r) x A_slot in fp32 and, for
- * bf16 batches of at most 512 rows, the expand delta = v B_slot in fp32) and the base GEMM
- * (bf16: tensor cores), whose epilogue adds the low-rank term (v B_slot, or delta) to the
- * fp32 accumulator and writes y once.  No host synchronisation; no allocation; safe to
- * capture in a CUDA graph.
+ * Enqueues the low-rank kernel and the base GEMM (bf16: tensor cores), which adds the
+ * low-rank term to its fp32 accumulator and writes y once:
+ *   bf16, T <= 512 (decode)  BGMV: per slot, v = (alpha/r) x A_slot and delta = v B_slot in
+ *                            fp32 for the slot's rows; the GEMM epilogue adds delta.  Rows
+ *                            whose id is outside [-1, S) or names an empty slot are
+ *                            computed base only and flagged (lora_get_status).
+ *   bf16, T > 512 (prefill)  SGMV shrink on the tensor cores per window of the segment
+ *                            layout, v in fp32; the GEMM multiplies v (split into two bf16
+ *                            parts) by B_slot as extra K blocks of its own accumulation.
+ *   fp32                     SGMV shrink per segment tile, v in fp32; the GEMM epilogue
+ *                            expands it.
+ * No host synchronisation; no allocation; safe to capture in a CUDA graph.
  * Errors: LORA_EINVAL, LORA_ESTATE, LORA_ECUDA.
  */
 int lora_forward(lora_layer_t* layer, const void* x_dev, void* y_dev, int T, void* stream);
@@ -141,7 +152,8 @@ int lora_forward_host(lora_layer_t* layer, const void* x_host, const int32_t* to
 int lora_get_status(lora_layer_t* layer, void* stream);
 
 /*
- * Copy the current segment layout to host memory (synchronises `stream`).
+ * Copy the current segment layout to host memory (synchronises `stream`; first builds the
+ * layout on `stream` if the batch's set_batch_segments did not).
  *   perm [max_tokens], seg_offsets [num_slots + 1], seg_slot [num_slots]: caller-owned
  *   host arrays; *n_seg and *n_adapted receive the segment count and the number of
  *   adapted rows (perm[0..n_adapted) and seg_offsets[0..n_seg] are meaningful).
@@ -154,7 +166,8 @@ int lora_get_segments(lora_layer_t* layer, int32_t* perm, int32_t* seg_offsets,
  * Optional tracing of the layer's kernel launches (for timing on the launch stream).
  *   events   NULL to stop tracing, or an array of 6 cudaEvent_t (as void*) owned by the
  *            caller; afterwards every set_batch_segments records events[0] before and
- *            events[1] after the segment-builder launch, and every lora_forward records
+ *            events[1] after the segment-builder launch (back to back when the batch
+ *            needs no builder), and every lora_forward records
  *            events[2] / events[3] around the low-rank kernel launch and events[4] /
  *            events[5] around the base-GEMM launch, each on the call's stream.
  * Tracing adds event records only; it changes no result (the records between kernels
