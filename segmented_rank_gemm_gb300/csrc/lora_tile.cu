@@ -360,11 +360,10 @@ static constexpr int kSlotMaxT = 512;  // largest decode batch (the delta buffer
 //   expand  thread t takes 8-column chunks t, t + 256, ... of N; a batch of 16 rank rows of
 //           B_s is loaded together and applied to the group's rows; the fp32 delta rows
 //           are written once.
-// At most 128 registers a thread and ~4 KB of shared memory, so that a CTA fits on an SM
-// beside a base GEMM CTA and runs while its main loop does.
+// Few registers (see below) and ~5 KB of shared memory, so that a CTA fits on an SM beside
+// a base GEMM CTA and runs while its main loop does.
 // ---------------------------------------------------------------------------------------
 static constexpr int kStrThreads = 256;
-static constexpr int kStrExpRows = 4;  // rows per group (shrink, then expand)
 static constexpr int kStrRedMax = 64;  // rows x rank columns of one shrink pass
 
 // v of NQ rows (rank columns < RMAX) into vdst[q][j], scaled by sc; all threads of the CTA.
@@ -478,18 +477,29 @@ __device__ __forceinline__ void stream_expand(const __nv_bfloat16* __restrict__ 
   }
 }
 
+// Work items: (slot, group of kStrGroup of its rows, in row order), so that a slot with many
+// rows is spread over several CTAs instead of making one CTA the kernel's tail.  Every CTA
+// derives the same item list from the ids (a shared-memory histogram over slots and an
+// exclusive scan of the groups per slot) and takes items blockIdx.x, + gridDim.x, ...
+static constexpr int kStrGroup = 2;
+
+// At most 120 registers a thread: the register file is split between the SM's four warp
+// schedulers, each holding the registers of its own warps (16K), and a GEMM CTA's 6 warps
+// put 2 warps of ~136 registers on two of them; 2 warps of this kernel must fit beside
+// those for the two kernels to share the SM.
 template <int RMAX, int ROWS>
-__global__ void __launch_bounds__(kStrThreads, 2)
+__global__ void __maxnreg__(120)
     bgmv_stream_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ token_slot,
                        const int32_t* __restrict__ loaded, int T, int K, int N, int R, int S,
                        const __nv_bfloat16* __restrict__ At_pool,
                        const __nv_bfloat16* __restrict__ B_pool, const float* __restrict__ scale,
                        const int32_t* __restrict__ rank, float* __restrict__ delta) {
   griddep_launch_dependents();  // the base GEMM's main loop may start now
-  __shared__ int rows_s[kSlotMaxT];
+  extern __shared__ int grp_off[];  // [S + 1]: rows per slot, then first item of each slot
+  __shared__ int rows_s[kStrGroup];
   __shared__ int warp_cnt[kStrThreads / 32];
   __shared__ float red[kStrThreads / 32][kStrRedMax];
-  __shared__ float v_s[kStrExpRows][32];
+  __shared__ float v_s[kStrGroup][32];
   constexpr int kIds = kSlotMaxT / kStrThreads;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int ids[kIds];
@@ -498,9 +508,52 @@ __global__ void __launch_bounds__(kStrThreads, 2)
     const int i = tid * kIds + u;
     ids[u] = i < T ? token_slot[i] : -1;
   }
+  // ---- the item list: rows per slot, then groups per loaded slot, exclusive scan ----
+  for (int q = tid; q <= S; q += kStrThreads) grp_off[q] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kIds; ++u)
+    if (ids[u] >= 0 && ids[u] < S) atomicAdd(&grp_off[ids[u]], 1);
+  __syncthreads();
+  const int per = (S + kStrThreads - 1) / kStrThreads;  // consecutive slots per thread
+  const int q_begin = min(S, tid * per), q_end = min(S, q_begin + per);
+  int mine = 0;
+  for (int q = q_begin; q < q_end; ++q) {
+    const int g = loaded[q] != 0 ? (grp_off[q] + kStrGroup - 1) / kStrGroup : 0;
+    grp_off[q] = g;
+    mine += g;
+  }
+  int inc = mine;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, d);
+    if (lane >= d) inc += t;
+  }
+  if (lane == 31) warp_cnt[warp] = inc;
+  __syncthreads();
+  int base = inc - mine, n_items = 0;
+  for (int w = 0; w < kStrThreads / 32; ++w) {
+    if (w < warp) base += warp_cnt[w];
+    n_items += warp_cnt[w];
+  }
+  for (int q = q_begin; q < q_end; ++q) {  // groups -> first item of the slot
+    const int g = grp_off[q];
+    grp_off[q] = base;
+    base += g;
+  }
+  if (tid == 0) grp_off[S] = n_items;
+  __syncthreads();
+
   const int kv = K / 8, nv = N / 8;  // 16-byte chunks of a row of x / 8-column chunks of N
-  for (int s = blockIdx.x; s < S; s += gridDim.x) {
-    if (loaded[s] == 0) continue;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    // the item's slot: the last s with grp_off[s] <= it
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (grp_off[mid] <= it) lo = mid;
+      else hi = mid - 1;
+    }
+    const int s = lo, g0 = (it - grp_off[s]) * kStrGroup;  // first row (in slot order)
     // every 16-byte chunk of A_s and B_s this thread will read, requested into L2 now: the
     // DRAM round trips overlap the row scan below, and the loads after it hit L2
     const int rs = min(R, RMAX);
@@ -510,61 +563,66 @@ __global__ void __launch_bounds__(kStrThreads, 2)
     for (int e = tid; e < nv; e += kStrThreads)
       for (int j = 0; j < rs; ++j)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(B_pool + ((size_t)s * R + j) * N + e * 8));
-    // ---- rows naming slot s, in row order ----
-    int mine = 0;
+    // ---- the slot's rows g0 .. g0 + kStrGroup - 1, in row order ----
+    int cnt = 0;
 #pragma unroll
-    for (int u = 0; u < kIds; ++u) mine += ids[u] == s;
-    int inc = mine;
+    for (int u = 0; u < kIds; ++u) cnt += ids[u] == s;
+    int inc2 = cnt;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, inc, d);
-      if (lane >= d) inc += t;
+      const int t = __shfl_up_sync(0xffffffffu, inc2, d);
+      if (lane >= d) inc2 += t;
     }
-    if (lane == 31) warp_cnt[warp] = inc;
+    if (lane == 31) warp_cnt[warp] = inc2;
     __syncthreads();
-    int pos = inc - mine, nrows = 0;
+    int pos = inc2 - cnt, nrows = 0;
     for (int w = 0; w < kStrThreads / 32; ++w) {
       if (w < warp) pos += warp_cnt[w];
       nrows += warp_cnt[w];
     }
 #pragma unroll
     for (int u = 0; u < kIds; ++u)
-      if (ids[u] == s) rows_s[pos++] = tid * kIds + u;
+      if (ids[u] == s) {
+        if (pos >= g0 && pos < g0 + kStrGroup) rows_s[pos - g0] = tid * kIds + u;
+        ++pos;
+      }
     __syncthreads();
-    if (nrows == 0) continue;
+    const int ng = min(kStrGroup, nrows - g0);
     const int r = rank[s];
     const float sc = scale[s];
     const __nv_bfloat16* At = At_pool + (size_t)s * R * K;
     const __nv_bfloat16* Bs = B_pool + (size_t)s * R * N;
-    for (int g0 = 0; g0 < nrows; g0 += kStrExpRows) {
-      const int ng = min(kStrExpRows, nrows - g0);
-      // shrink: v_s[0 .. ng), ROWS rows a pass (the last pass may take one)
-      for (int q0 = 0; q0 < ng; q0 += ROWS) {
-        if (ng - q0 >= ROWS)
-          stream_shrink<RMAX, ROWS>(x, rows_s + g0 + q0, K, At, r, sc, red, v_s + q0);
-        else
-          stream_shrink<RMAX, 1>(x, rows_s + g0 + q0, K, At, r, sc, red, v_s + q0);
-      }
-      // expand: the group's delta rows
-      switch (ng) {
-        case 1: stream_expand<RMAX, 1>(Bs, N, r, v_s, rows_s + g0, delta); break;
-        case 2: stream_expand<RMAX, 2>(Bs, N, r, v_s, rows_s + g0, delta); break;
-        case 3: stream_expand<RMAX, 3>(Bs, N, r, v_s, rows_s + g0, delta); break;
-        default: stream_expand<RMAX, 4>(Bs, N, r, v_s, rows_s + g0, delta); break;
-      }
-      __syncthreads();  // v_s is rewritten by the next group
+    // shrink: v_s[0 .. ng), ROWS rows a pass (the last pass may take one)
+    for (int q0 = 0; q0 < ng; q0 += ROWS) {
+      if (ng - q0 >= ROWS)
+        stream_shrink<RMAX, ROWS>(x, rows_s + q0, K, At, r, sc, red, v_s + q0);
+      else
+        stream_shrink<RMAX, 1>(x, rows_s + q0, K, At, r, sc, red, v_s + q0);
     }
+    // expand: the group's delta rows
+    if (ng == 1)
+      stream_expand<RMAX, 1>(Bs, N, r, v_s, rows_s, delta);
+    else
+      stream_expand<RMAX, kStrGroup>(Bs, N, r, v_s, rows_s, delta);
+    __syncthreads();  // rows_s and v_s are rewritten by the next item
   }
 }
 
 static cudaError_t launch_bgmv_stream(const BgmvArgs& a, cudaStream_t stream) {
+  // the SMs it runs on must keep the shared-memory split a GEMM CTA needs, or that CTA
+  // waits for them to drain
+  static bool carveout16 = false, carveout32 = false;
+  cudaError_t e = a.R <= 16 ? prefer_max_smem_carveout(bgmv_stream_kernel<16, 2>, &carveout16)
+                            : prefer_max_smem_carveout(bgmv_stream_kernel<32, 1>, &carveout32);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(std::max(1, std::min(a.S, a.num_sms)));
+  // one CTA per SM: every CTA derives the item list, so idle ones leave right after that
+  cfg.gridDim = dim3(std::max(1, a.num_sms));
   cfg.blockDim = dim3(kStrThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = (size_t)(a.S + 1) * sizeof(int);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
