@@ -343,20 +343,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (et == 0) mbar_arrive(&xa_full[st]);
     }
   }
-  bool add_delta = false;  // delta mode: the row adds the low-rank term of the delta buffer
-  if (epi && a.ex.mode != kExpandV) {
-    // the low-rank kernel's results are needed from here on: the main loop keeps running
-    griddep_wait();
-    if (row < a.M) {
-      const int t = a.ex.token_slot[row];
-      add_delta = t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0;
-      // one CTA per row block reports ids outside [-1, S) or naming empty slots
-      if (blockIdx.y == 0 && z == 0) {
-        if (t < -1 || t >= a.ex.S) atomicOr(a.err, LORA_ERRF_BAD_ID);
-        else if (t >= 0 && !add_delta) atomicOr(a.err, LORA_ERRF_EMPTY_SLOT);
-      }
-    }
-  }
   if (epi) {
     mbar_wait(tmem_full, 0, a.err);
     tc_fence_after();
@@ -409,9 +395,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
-  if (epi) {
+  bool add_delta = false;  // delta mode: the row adds the low-rank term of the delta buffer
+  if (epi && a.ex.mode == kExpandDelta) {
     // only now the low-rank kernel's results are needed: the main loop and the split-K
     // exchange ran while it was still working
+    griddep_wait();
+    if (row < a.M) {
+      const int t = a.ex.token_slot[row];
+      add_delta = t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0;
+      // one CTA per row block reports ids outside [-1, S) or naming empty slots
+      if (blockIdx.y == 0 && z == 0) {
+        if (t < -1 || t >= a.ex.S) atomicOr(a.err, LORA_ERRF_BAD_ID);
+        else if (t >= 0 && !add_delta) atomicOr(a.err, LORA_ERRF_EMPTY_SLOT);
+      }
+    }
+  }
+  if (epi) {
     // the delta buffer holds the first 512 rows only: a row that adds no delta never forms
     // an address into it beyond row 0
     const bool from_delta = add_delta && a.ex.mode == kExpandDelta;
