@@ -491,35 +491,47 @@ cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Tile shape and K split.  Large problems: the widest N tile that still gives one tile per
-// SM, no split.  Small batches (when split is allowed): N tile 128 and the largest
-// power-of-two K split (cluster size, at most 4) that keeps the CTA count within the SMs;
-// N tile 256 when even the unsplit 128-wide tiles leave most SMs idle.  (A 128-wide tile
-// with a 2-way split moves a third of the partials a 256-wide one with a 4-way split
-// does, and its CTA leaves room on its SM for a CTA of the low-rank kernel.)
+// Tile shape and K split.  Large problems (no split allowed): the widest N tile that still
+// gives one tile per SM.  Small batches (split allowed): the (N tile, K split) of least
+// estimated time, from per-K-block costs measured on this kernel: an MMA of N <= 128 costs
+// its issue time (~440 cycles for the 4 MMAs of a 64-wide K block), a 256-wide block waits
+// on its 48 KB of operands (~660 cycles at ~75 B/cycle of TMA ingress per SM); plus ~3k
+// cycles of epilogue per wave and the split-K exchange at ~10 B/cycle per CTA.
 GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split) {
   const int mt = (M + kBM - 1) / kBM;
   const int nkb = (K + kBK - 1) / kBK;
   GemmPlan p{64, 1};
   const int cand[3] = {256, 128, 64};
-  for (int i = 0; i < 3; ++i) {
-    const int tiles = mt * ((N + cand[i] - 1) / cand[i]);
-    if (tiles >= num_sms) {
-      p.block_n = cand[i];
-      return p;
+  if (!allow_split) {
+    for (int i = 0; i < 3; ++i) {
+      const int tiles = mt * ((N + cand[i] - 1) / cand[i]);
+      if (tiles >= num_sms) {
+        p.block_n = cand[i];
+        return p;
+      }
     }
+    return p;
   }
-  if (!allow_split) return p;
   // every one of the cs K ranges of ceil(nkb / cs) blocks must be non-empty
   auto ranges_ok = [nkb](int c) { return (c - 1) * ((nkb + c - 1) / c) < nkb; };
-  for (int bn : {128, 256}) {
+  double best = 1e30;
+  for (int i = 0; i < 3; ++i) {
+    const int bn = cand[i];
+    const double per_kb = bn == 256 ? 660.0 : 440.0;
     const int tiles = mt * ((N + bn - 1) / bn);
-    int cs = 1;
-    while (cs * 2 <= 4 && tiles * cs * 2 <= num_sms && ranges_ok(cs * 2)) cs *= 2;
-    if (cs > 1 && tiles * cs * 2 > num_sms / 2) {
-      p.block_n = bn;
-      p.ksplit = cs;
-      return p;
+    // each CTA finishes bn / cs >= 32 columns (its epilogue and the split-K exchange work
+    // in 32-column chunks)
+    for (int cs = 1; cs <= 4 && bn / cs >= 32; cs *= 2) {
+      if (cs > 1 && !ranges_ok(cs)) break;
+      const int waves = (tiles * cs + num_sms - 1) / num_sms;
+      const int kb = (nkb + cs - 1) / cs;
+      const double exch = cs > 1 ? (cs - 1) * (double)kBM * (bn / cs) * 4.0 / 10.0 : 0.0;
+      const double cost = waves * (kb * per_kb + 3000.0 + exch);
+      if (cost < best * 0.999) {
+        best = cost;
+        p.block_n = bn;
+        p.ksplit = cs;
+      }
     }
   }
   return p;
@@ -540,6 +552,7 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   // then runs on the same SM while the main loop does
   const size_t budget = a.ex.mode == kExpandDelta ? 219 * 1024 : 227 * 1024;
   const int cs = plan.ksplit;
+  if (cs < 1 || cs > 4 || BN / cs < 32) return cudaErrorInvalidConfiguration;
   if (a.ex.mode == kExpandV && (cs != 1 || a.ex.R % 8 != 0 || a.ex.R > 128 || a.ex.S > 32 * kBM))
     return cudaErrorInvalidValue;
   const int xscr = a.ex.mode == kExpandV ? kBM * expand_layout(a.ex.R).nbs * 128 : 0;
