@@ -42,6 +42,8 @@
 // the low-rank results.  Every mbarrier wait is bounded (lora_common.cuh).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "lora_common.cuh"
 #include "lora_kernels.h"
 
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_bx, GemmArgs a, int stages,
-                   int xscr_bytes) {
+                   int xscr_bytes, int group_m) {
   constexpr int kBBytes = BN * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
 
@@ -138,14 +140,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * stages + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * BN;
+  // Tile order: bands of group_m row tiles, column tiles in turn within a band, row tiles
+  // fastest.  A wave of CTAs then shares one band of x (which stays in L2) instead of
+  // streaming all of x from DRAM again for every few column tiles.
+  int mt_i = blockIdx.x, nt_i = blockIdx.y;
+  {
+    const int mt = gridDim.x, nt = gridDim.y;
+    const int id = blockIdx.x + blockIdx.y * mt;
+    const int band = id / (group_m * nt);
+    const int gm = min(group_m, mt - band * group_m);  // rows of the last band may be fewer
+    const int w = id - band * group_m * nt;
+    mt_i = band * group_m + w % gm;
+    nt_i = w / gm;
+  }
+  const int m0 = mt_i * kBM, n0 = nt_i * BN;
   // split K: this CTA's range of K blocks (the host keeps every range non-empty)
   const int cs = gridDim.z, z = blockIdx.z;
   const int nkb_all = (a.K + kBK - 1) / kBK;
   const int per = (nkb_all + cs - 1) / cs;
   const int kb_begin = z * per;
   const int nkb = min(nkb_all, kb_begin + per) - kb_begin;
-  const int rot = (int)((blockIdx.x + blockIdx.y) % (unsigned)nkb);
+  const int rot = (int)((mt_i + nt_i) % (unsigned)nkb);
   const int bnc = BN / cs;  // columns this CTA finishes
 
   if (threadIdx.x == 0) {
@@ -404,7 +419,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int t = a.ex.token_slot[row];
       add_delta = t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0;
       // one CTA per row block reports ids outside [-1, S) or naming empty slots
-      if (blockIdx.y == 0 && z == 0) {
+      if (nt_i == 0 && z == 0) {
         if (t < -1 || t >= a.ex.S) atomicOr(a.err, LORA_ERRF_BAD_ID);
         else if (t >= 0 && !add_delta) atomicOr(a.err, LORA_ERRF_EMPTY_SLOT);
       }
@@ -581,7 +596,11 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = cs > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmap_x, tmap_w, tmap_bx, a, stages, xscr);
+  // row tiles per band: x of a band at most ~32 MB
+  const int mt = (a.M + kBM - 1) / kBM;
+  const int group_m = std::max(1, std::min(mt, (int)((32u << 20) / ((size_t)a.K * kBM * 2))));
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmap_x, tmap_w, tmap_bx, a, stages, xscr,
+                            group_m);
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
