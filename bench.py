@@ -359,22 +359,38 @@ def run_ours(args):
     stream.synchronize()
     for l in layers:
         assert l.status(stream) == LORA_OK
-    graphs = []
+    # one graph per step and instance, and one graph of a whole rotation (one step on each
+    # instance in turn, as the layers of a model's decode step are captured together)
+    graphs, rot_graph = [], None
     if not args.no_graph:
         for i in range(len(layers)):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 step(i)
             graphs.append(g)
+        rot_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(rot_graph, stream=stream):
+            for i in range(len(layers)):
+                step(i)
         for i in range(len(layers)):
             graphs[i].replay()
+        rot_graph.replay()
         torch.cuda.synchronize()
 
     def run_steps(n, offset=0):
+        """Exactly n steps: whole rotations from the rotation graph, the rest one by one."""
         if graphs:
             with torch.cuda.stream(stream):
-                for i in range(n):
+                i = 0
+                while i < n and (i + offset) % len(graphs) != 0:
                     graphs[(i + offset) % len(graphs)].replay()
+                    i += 1
+                while n - i >= len(graphs):
+                    rot_graph.replay()
+                    i += len(graphs)
+                while i < n:
+                    graphs[(i + offset) % len(graphs)].replay()
+                    i += 1
         else:
             with torch.cuda.stream(stream):
                 for i in range(n):
@@ -495,7 +511,8 @@ def run_ours(args):
                    "adapted_rows": work["adapted_rows"], "parallelism": "replicas x%d" % world,
                    "l2": "rotating %d independent layer instances (~%d MB of weights and slots)"
                          " > 129 MB L2" % (len(layers), len(layers) * work["step_bytes"] // 10**6),
-                   "graphs": not args.no_graph},
+                   "graphs": ("one graph per rotation of %d steps (one per instance)" % len(layers))
+                             if not args.no_graph else False},
         "roofline": roofline,
         "step_hbm": {"algorithmic_bytes": work["step_bytes"],
                      "achieved_gbs": work["step_bytes"] / (ms_per_step * 1e-3) / 1e9,
