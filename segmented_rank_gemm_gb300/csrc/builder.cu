@@ -205,7 +205,11 @@ __global__ void __launch_bounds__(kBuilderThreads, 1)
       Scan3 v = lane < nw ? warp_tot[lane] : Scan3{0, 0, 0};
       const Scan3 vinc = warp_inclusive_scan3(v, lane);
       if (lane < nw) warp_tot[lane] = Scan3{vinc.a - v.a, 0, 0};
-      if (lane == 31) meta[2] = vinc.a;  // n_units
+      if (lane == 31) {
+        meta[2] = vinc.a;  // n_units
+        meta[4] = 0;       // the shrink's work and exit counters start at zero
+        meta[5] = 0;
+      }
     }
     __syncthreads();
     int u = warp_tot[warp].a + uinc.a - my_units;

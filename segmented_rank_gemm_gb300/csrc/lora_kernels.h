@@ -51,7 +51,7 @@ struct BuilderArgs {
   int32_t* seg_slot;     // [S]
   int32_t* tile_seg;     // [T/rows_per_tile + S]
   int32_t* tile_row0;    // [T/rows_per_tile + S]
-  int32_t* meta;         // [4] n_seg, T_a, n_tiles
+  int32_t* meta;         // [4] n_seg, T_a, n_tiles (window mode: [8], [4..5] zeroed)
   int32_t* err;
 };
 cudaError_t launch_segment_builder(const BuilderArgs& a, cudaStream_t stream);
@@ -79,6 +79,7 @@ struct ShrinkTcArgs {
   int Rt;         // MMA N: R rounded up to 16
   const float* scale;  // [S]
   const int32_t* perm, *seg_offsets, *seg_slot, *tile_seg, *tile_row0, *meta;
+  int32_t* work;       // [2] item and exit counters, zero between launches (builder zeroes)
   float* v;            // [max_planes][T_max][R] fp32 partial sums over K ranges, scaled
   size_t plane_stride; // floats between planes (T_max * R)
   int ks;              // K split (planes written), from sgmv_shrink_tc_split

@@ -58,7 +58,7 @@ struct lora_layer {
   int32_t* seg_slot = nullptr;   // [S]
   int32_t* tile_seg = nullptr;   // [max_tiles]
   int32_t* tile_row0 = nullptr;  // [max_tiles]
-  int32_t* meta = nullptr;       // [4]
+  int32_t* meta = nullptr;       // [8]: builder counts, shrink work counters
   int32_t* err = nullptr;        // [1]
   float* v = nullptr;            // [v_planes][T_max][R] fp32, scaled by alpha / r (v mode)
   int v_planes = 1;              // K-split partial planes of v (bf16: tensor-core shrink)
@@ -201,7 +201,7 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
             dmalloc(&L->seg_slot, S) == cudaSuccess &&
             dmalloc(&L->tile_seg, L->max_tiles) == cudaSuccess &&
             dmalloc(&L->tile_row0, L->max_tiles) == cudaSuccess &&
-            dmalloc(&L->meta, 4) == cudaSuccess && dmalloc(&L->err, 1) == cudaSuccess &&
+            dmalloc(&L->meta, 8) == cudaSuccess && dmalloc(&L->err, 1) == cudaSuccess &&
             dmalloc(&L->v, (size_t)L->v_planes * max_tokens * R) == cudaSuccess &&
             (dtype != LORA_BF16 ||
              dmalloc(&L->delta, (size_t)std::min(max_tokens, kDeltaMaxT) * N) == cudaSuccess) &&
@@ -227,7 +227,7 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
        cudaMemsetAsync(L->scale, 0, S * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->rank, 0, S * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->loaded, 0, S * 4, stream) == cudaSuccess &&
-       cudaMemsetAsync(L->meta, 0, 16, stream) == cudaSuccess &&
+       cudaMemsetAsync(L->meta, 0, 32, stream) == cudaSuccess &&
        cudaMemsetAsync(L->err, 0, 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->v, 0, (size_t)L->v_planes * max_tokens * R * 4, stream) == cudaSuccess;
   if (!ok) return bail(LORA_ECUDA);
@@ -426,6 +426,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     sa.tile_seg = L->tile_seg;
     sa.tile_row0 = L->tile_row0;
     sa.meta = L->meta;
+    sa.work = L->meta + 4;
     sa.v = L->v;
     sa.plane_stride = (size_t)L->T_max * L->R;
     sa.ks = v_split;

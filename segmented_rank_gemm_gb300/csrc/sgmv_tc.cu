@@ -13,7 +13,10 @@
 // spans more segments gives several units.  A work item is one unit and one of `ks` K
 // ranges; its partial product goes to plane kp of v, and the consumer of v (the base
 // GEMM's epilogue) sums a row's planes in plane order, so the result does not depend on
-// which CTA ran which item.  The kernel is persistent: CTA b takes items b, b + grid, ...
+// which CTA ran which item.  The kernel is persistent and schedules items dynamically: a
+// CTA's producer takes the next item from a device counter and passes it to the CTA's MMA
+// and epilogue warps through the unit description ring (items differ in cost: windows with
+// one or two segments, partial windows); the last CTA to finish resets the counters.
 // One MMA serves all segments of a unit: the B operand stacks their transposed A blocks
 // (Rt rows each), D[128, G*Rt] = X_win[128, K] * [A_s1 .. A_sG], and each row of the unit's
 // segments keeps the Rt columns of its own slot (Gp * Rt <= 128, Gp <= 8).  The stacked A
@@ -122,12 +125,22 @@ __global__ void __launch_bounds__(kShThreads, 1)
     uint32_t ph = 0;
     bool ok = true;
     int item = 0;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++item) {
-      const int u = w / ks;
+    for (; ok; ++item) {
+      int w = 0;
+      if (lane == 0) w = atomicAdd(a.work, 1);  // the next item
+      w = __shfl_sync(0xffffffffu, w, 0);
       // ---- the unit's description ----
       const int ib = item % kShInfo;
       if (!mbar_wait(&info_empty[ib], ((uint32_t)(item / kShInfo) & 1u) ^ 1u, a.err)) break;
       UnitInfo& ui = info[ib];
+      if (w >= n_items) {  // no items left: tell the other roles
+        if (lane == 0) {
+          ui.G = 0;
+          mbar_arrive(&info_full[ib]);
+        }
+        break;
+      }
+      const int u = w / ks;
       const int p0 = a.tile_row0[u], p1 = min(p0 + kTcTileRows, T_a);
       const int gs = a.tile_seg[u];
       // lanes g <= Gp: start of segment gs + g (seg_offsets[n_seg] = T_a ends the list)
@@ -194,12 +207,12 @@ __global__ void __launch_bounds__(kShThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      int item = 0;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++item) {
+      for (int item = 0; ok; ++item) {
         const int ib = item % kShInfo;
         if (!mbar_wait(&info_full[ib], (uint32_t)(item / kShInfo) & 1u, a.err)) break;
         const int G = info[ib].G, kp = info[ib].kp;
         mbar_arrive(&info_empty[ib]);
+        if (G == 0) break;  // no items left
         const int kb0 = kp * kpb, kb1 = min(nkb, kb0 + kpb);
         const uint32_t idesc = idesc_bf16_f32(kTcTileRows, G * Rt);
         const int buf = item & 1;
@@ -234,14 +247,17 @@ __global__ void __launch_bounds__(kShThreads, 1)
     const int quad = warp & 3;  // TMEM lanes [32 quad, 32 quad + 32)
     const int rt = quad * 32 + lane;
     const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    int item = 0;
-    for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++item) {
+    for (int item = 0;; ++item) {
       const int ib = item % kShInfo;
       if (!__all_sync(0xffffffffu,
                       mbar_wait(&info_full[ib], (uint32_t)(item / kShInfo) & 1u, a.err)))
         break;
       const UnitInfo& ui = info[ib];
       const int G = ui.G, p = ui.p0 + rt, kp = ui.kp;
+      if (G == 0) {  // no items left
+        mbar_arrive(&info_empty[ib]);
+        break;
+      }
       const bool live = p >= ui.off[0] && p < ui.off[G];
       int g = 0;  // the row's segment in the unit: the last g with off[g] <= p
       for (int j = 1; j < G; ++j) g += ui.off[j] <= p ? 1 : 0;
@@ -279,6 +295,12 @@ __global__ void __launch_bounds__(kShThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * kShNmax);
+  }
+  // every CTA has taken its last item: the last one to get here resets the counters for
+  // the next launch
+  if (threadIdx.x == 0 && atomicAdd(a.work + 1, 1) == (int)gridDim.x - 1) {
+    atomicExch(a.work, 0);
+    atomicExch(a.work + 1, 0);
   }
 }
 
