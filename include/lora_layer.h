@@ -177,6 +177,21 @@ int lora_get_segments(lora_layer_t* layer, int32_t* perm, int32_t* seg_offsets,
 int lora_set_trace_events(lora_layer_t* layer, void* const* events);
 
 /*
+ * Tuning and testing hook: fix the tiling of the bf16 base GEMM (y = x W plus the low-rank
+ * term) for the layer's later forwards, instead of the automatic plan.  It changes no
+ * result beyond fp32 summation order; the automatic plan is the fast choice.
+ *   block_n    N tile of a CTA: 64, 128 or 256; 0 restores the automatic plan.
+ *   k_split    K ranges per output tile: 1, 2 or 4, with block_n / k_split >= 32; used for
+ *              batches of at most 512 rows (larger ones never split K).
+ *   cta_pair   1: pairs of CTAs share 256-row tiles (tcgen05 cta_group::2); needs
+ *              block_n >= 128.
+ * A forward fails with LORA_ECUDA when the fixed plan cannot run its batch (a K range that
+ * would be empty).  Growing the split-K scratch for the new plan synchronises the device.
+ * Errors: LORA_EINVAL (other values), LORA_ENOMEM, LORA_ECUDA.
+ */
+int lora_set_gemm_plan(lora_layer_t* layer, int block_n, int k_split, int cta_pair);
+
+/*
  * The segment builder of set_batch_segments for callers that cannot allocate device memory
  * (a framework or engine that owns all device memory through its own pool and forbids
  * allocations behind its back, or a latency-critical path that cannot afford cudaMalloc's

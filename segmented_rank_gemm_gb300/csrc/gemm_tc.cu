@@ -25,21 +25,27 @@
 // ones, so base and low-rank products meet in the one fp32 accumulator.  Rows with slot -1
 // match no slot and keep the base product only.
 // Split K (small batches): the grid's z dimension cuts K into `cs` <= 4 ranges and the cs
-// CTAs of one output block form a thread-block cluster.  After a cluster barrier (every main
-// loop done, so the stage buffers are idle) each CTA copies, for every other CTA d, its fp32
-// partial of the columns d owns from TMEM into a local send buffer and pushes it with one
-// bulk copy (cp.async.bulk shared::cta -> shared::cluster) into d's receive buffer,
-// completing on d's mbarrier; each CTA then adds the cs - 1 partials it received to its own
-// and runs the epilogue on its BN / cs columns.  A small batch thereby keeps W (not the
-// re-read x) dominant in every stage and needs 1/cs of the K range per SM.  Send and
-// receive rows are stored with their 16-byte chunks XOR-swizzled by row, so the row-per-
-// thread accesses avoid shared-memory bank conflicts.
+// CTAs of one output block form a thread-block cluster (with CTA pairs, the 2 cs CTAs of a
+// 256-row block).  After its main loop each CTA writes, for every other CTA d of its block,
+// its fp32 partial of the columns d finishes into an L2-resident scratch block; after a
+// cluster barrier (release / acquire) each CTA adds the cs - 1 blocks addressed to it and
+// runs the epilogue on its BN / cs columns.  L2 carries these blocks several times faster
+// than distributed shared memory.  A small batch thereby keeps W (not the re-read x)
+// dominant in every stage and needs 1/cs of the K range per SM.
+// CTA pairs (cta_group::2): two CTAs of a cluster share a 256 x BN tile; each loads its 128
+// rows of x and half of the W tile, the even CTA issues M = 256 MMAs that read both CTAs'
+// shared memory and write both CTAs' TMEM, and its commits arrive on both CTAs' barriers.
+// A pair thereby moves the same operand bytes per SM as a 128 x BN/2 tile while every MMA
+// instruction does the work of a 128 x BN one (the issue rate, ~124 cycles per instruction
+// however narrow, bounds tiles below 256 columns).
 // Each CTA starts its K range at a rotated K block (and wraps around), so the CTAs that
 // share an x tile or a W tile do not all request the same lines from L2 at the same moment.
 // Launch: programmatic dependent launch after the low-rank kernel: the main loop and the
 // split-K exchange read only x, W and the accumulators, so they run while the low-rank
 // kernel is still working; the epilogue waits (griddepcontrol.wait) only before it reads
-// the low-rank results.  Every mbarrier wait is bounded (lora_common.cuh).
+// the low-rank results.  It lets no dependent launch early (measured: the next forward's
+// low-rank kernel, resident early, slowed the step), so the next kernel on the stream sees
+// y complete.  Every mbarrier wait is bounded (lora_common.cuh).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -109,13 +115,14 @@ __device__ __forceinline__ void v_hi_lo8(const ExpandArgs& ex, int row, int j0, 
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_bx, GemmArgs a, int stages,
                    int xscr_bytes, int group_m) {
-  constexpr int kBBytes = BN * kBK * 2;
+  constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of the W (or B expand) tile this CTA loads
+  constexpr int kBBytes = kBRows * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
 
   extern __shared__ uint8_t smem_raw[];
@@ -133,34 +140,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* full = bars;
   uint64_t* empty = bars + stages;
   uint64_t* tmem_full = bars + 2 * stages;
-  uint64_t* xchg_bar = bars + 2 * stages + 1;  // split K: partials received from the peers
-  uint64_t* xinfo_bar = bars + 2 * stages + 2;  // v mode: x_blocks written
-  uint64_t* xgrant = bars + 2 * stages + 3;     // [stages] v mode: stage handed to the epilogue
-  uint64_t* xa_full = bars + 3 * stages + 3;    // [stages] v mode: its A half written
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * stages + 3);
+  uint64_t* xinfo_bar = bars + 2 * stages + 1;  // v mode: x_blocks written
+  uint64_t* xgrant = bars + 2 * stages + 2;     // [stages] v mode: stage handed to the epilogue
+  uint64_t* xa_full = bars + 3 * stages + 2;    // [stages] v mode: its A half written
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * stages + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Tile order: bands of group_m row tiles, column tiles in turn within a band, row tiles
   // fastest.  A wave of CTAs then shares one band of x (which stays in L2) instead of
   // streaming all of x from DRAM again for every few column tiles.
-  int mt_i = blockIdx.x, nt_i = blockIdx.y;
+  // CTA pairs: the two CTAs of a pair are neighbours in x, take one tile order (counted in
+  // pairs) and cover 256 consecutive rows, CTA pr of the pair rows [128 pr, 128 pr + 128).
+  const int pr = PAIR ? (int)(blockIdx.x & 1u) : 0;
+  int pm_i, nt_i;
   {
-    const int mt = gridDim.x, nt = gridDim.y;
-    const int id = blockIdx.x + blockIdx.y * mt;
+    const int mt = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x, nt = gridDim.y;
+    const int id = (PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x) + blockIdx.y * mt;
     const int band = id / (group_m * nt);
     const int gm = min(group_m, mt - band * group_m);  // rows of the last band may be fewer
     const int w = id - band * group_m * nt;
-    mt_i = band * group_m + w % gm;
+    pm_i = band * group_m + w % gm;
     nt_i = w / gm;
   }
+  const int mt_i = PAIR ? 2 * pm_i + pr : pm_i;
   const int m0 = mt_i * kBM, n0 = nt_i * BN;
+  // cluster ranks (x fastest): CTA (pr, z) is rank pr + 2 z with pairs, z without; the even
+  // CTA of a pair issues its MMAs, and its barriers count both CTAs' loads
+  const uint32_t lead_rank = PAIR ? 2u * blockIdx.z : 0u;
+  const uint16_t pair_mask = (uint16_t)(3u << lead_rank);
   // split K: this CTA's range of K blocks (the host keeps every range non-empty)
   const int cs = gridDim.z, z = blockIdx.z;
   const int nkb_all = (a.K + kBK - 1) / kBK;
   const int per = (nkb_all + cs - 1) / cs;
   const int kb_begin = z * per;
   const int nkb = min(nkb_all, kb_begin + per) - kb_begin;
-  const int rot = (int)((mt_i + nt_i) % (unsigned)nkb);
+  const int rot = (int)((pm_i + nt_i) % (unsigned)nkb);  // the same for both CTAs of a pair
   const int bnc = BN / cs;  // columns this CTA finishes
 
   if (threadIdx.x == 0) {
@@ -169,11 +183,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(xchg_bar, 1);
     mbar_init(xinfo_bar, 1);
     for (int s = 0; s < stages; ++s) {
       mbar_init(&xgrant[s], 1);
-      mbar_init(&xa_full[s], 1);
+      mbar_init(&xa_full[s], PAIR ? 2 : 1);  // pairs: one arrival from each CTA's epilogue
     }
     fence_mbar_init();
   }
@@ -182,11 +195,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tma_prefetch_desc(&tmap_w);
     if (a.ex.mode == kExpandV) tma_prefetch_desc(&tmap_bx);
   }
-  if (warp == 1) tmem_alloc(tmem_holder, BN);
+  if (warp == 1) {
+    if (PAIR)
+      tmem_alloc_pair(tmem_holder, BN);
+    else
+      tmem_alloc(tmem_holder, BN);
+  }
   tc_fence_before();
   __syncthreads();
+  // pairs: the peer's barriers are initialised before this CTA's loads and MMAs signal them
+  if (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -197,9 +218,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int kb = kb_begin + (rot + it) % nkb;
         if (!mbar_wait(&empty[s], ph ^ 1u, a.err)) break;
         uint8_t* sa = stage_base + (size_t)s * kStageBytes;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        tma_load_2d(sa, &tmap_x, &full[s], kb * kBK, m0);
-        tma_load_2d(sa + kABytes, &tmap_w, &full[s], kb * kBK, n0);
+        if (PAIR) {
+          // this CTA's 128 rows of x and its half of the W tile; the bytes of both CTAs
+          // are counted on the even CTA's barrier, which its MMA lane waits on
+          if (pr == 0) mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
+          const uint32_t fb = dsmem_map(smem_u32(&full[s]), lead_rank);
+          tma_load_2d_pair(sa, &tmap_x, fb, kb * kBK, m0);
+          tma_load_2d_pair(sa + kABytes, &tmap_w, fb, kb * kBK, n0 + pr * kBRows);
+        } else {
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          tma_load_2d(sa, &tmap_x, &full[s], kb * kBK, m0);
+          tma_load_2d(sa + kABytes, &tmap_w, &full[s], kb * kBK, n0);
+        }
         if (++s == stages) {
           s = 0;
           ph ^= 1u;
@@ -219,8 +249,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int u = e / xl.nbs, b = e - u * xl.nbs;
           const int col = xl.nbs == 1 ? 0 : (b % (xl.rx / 64)) * 64;
           uint8_t* sa = stage_base + (size_t)s * kStageBytes;
-          mbar_arrive_expect_tx(&full[s], kBBytes);
-          tma_load_2d(sa + kABytes, &tmap_bx, &full[s], col, uslot[u] * a.N + n0);
+          const int brow = uslot[u] * a.N + n0 + pr * kBRows;
+          if (PAIR) {
+            if (pr == 0) mbar_arrive_expect_tx(&full[s], 2 * kBBytes);
+            tma_load_2d_pair(sa + kABytes, &tmap_bx, dsmem_map(smem_u32(&full[s]), lead_rank),
+                             col, brow);
+          } else {
+            mbar_arrive_expect_tx(&full[s], kBBytes);
+            tma_load_2d(sa + kABytes, &tmap_bx, &full[s], col, brow);
+          }
           mbar_arrive(&xgrant[s]);
           if (++s == stages) {
             s = 0;
@@ -231,9 +268,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+    // ---------------- MMA issuer (pairs: the even CTA's lane, for both CTAs) ----------------
+    if (lane == 0 && pr == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN);
       // descriptors built once: the start-address field counts 16-byte units, so a stage
       // is + s * kStageBytes / 16 and a 16-wide K step inside the 128-byte row is + 2
       const uint64_t a_desc0 = smem_desc_sw128(smem_u32(stage_base));
@@ -247,10 +284,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint64_t a_desc = a_desc0 + stage_off, b_desc = b_desc0 + stage_off;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          tc_mma_bf16(tmem_base, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2), idesc,
-                      (it | kk) != 0 ? 1u : 0u);
+          const uint32_t acc = (it | kk) != 0 ? 1u : 0u;
+          if (PAIR)
+            tc_mma_bf16_pair(tmem_base, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
+                             idesc, acc);
+          else
+            tc_mma_bf16(tmem_base, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
+                        idesc, acc);
         }
-        tc_commit(&empty[s]);
+        if (PAIR)
+          tc_commit_pair_mc(&empty[s], pair_mask);  // frees the stage in both CTAs
+        else
+          tc_commit(&empty[s]);
         if (++s == stages) {
           s = 0;
           ph ^= 1u;
@@ -262,22 +307,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int e = 0; e < nx; ++e) {
           // B half (TMA) and A half (written by the epilogue warps)
           if (!mbar_wait(&full[s], ph, a.err)) break;
-          if (!mbar_wait(&xa_full[s], (uint32_t)(e / stages) & 1u, a.err)) break;
+          // pairs: the peer's epilogue wrote its A half, then arrived here across the cluster
+          if (!(PAIR ? mbar_wait_cluster(&xa_full[s], (uint32_t)(e / stages) & 1u, a.err)
+                     : mbar_wait(&xa_full[s], (uint32_t)(e / stages) & 1u, a.err)))
+            break;
           tc_fence_after();
           const uint64_t stage_off = (uint64_t)(s * (kStageBytes >> 4));
           const uint64_t a_desc = a_desc0 + stage_off, b_desc = b_desc0 + stage_off;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma_bf16(tmem_base, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
-                        idesc, 1u);
-          tc_commit(&empty[s]);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            if (PAIR)
+              tc_mma_bf16_pair(tmem_base, a_desc + (uint64_t)(kk * 2),
+                               b_desc + (uint64_t)(kk * 2), idesc, 1u);
+            else
+              tc_mma_bf16(tmem_base, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
+                          idesc, 1u);
+          }
+          if (PAIR)
+            tc_commit_pair_mc(&empty[s], pair_mask);
+          else
+            tc_commit(&empty[s]);
           if (++s == stages) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
-      tc_commit(tmem_full);
+      if (PAIR)
+        tc_commit_pair_mc(tmem_full, pair_mask);  // both CTAs' accumulators are complete
+      else
+        tc_commit(tmem_full);
     }
     __syncwarp();
   }
@@ -296,9 +355,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int et = threadIdx.x - 64;  // 0..127
     griddep_wait();                   // v and the checked slots come from earlier kernels
     const int srow = m0 + et < a.M ? a.ex.row_slot[m0 + et] : -1;
+    // pairs: both CTAs list the slots of all 256 rows, so they agree on the expand blocks
+    const int pm0 = m0 + (pr == 0 ? kBM : -kBM);  // the peer's first row
+    const int orow = PAIR && pm0 + et < a.M ? a.ex.row_slot[pm0 + et] : -1;
     slot_bits[et] = 0u;
     named_barrier(1, 128);
     if (srow >= 0) atomicOr(&slot_bits[srow >> 5], 1u << (srow & 31));
+    if (orow >= 0) atomicOr(&slot_bits[orow >> 5], 1u << (orow & 31));
     named_barrier(1, 128);
     uint32_t word = et < (a.ex.S + 31) / 32 ? slot_bits[et] : 0u;
     const int cnt = __popc(word);
@@ -355,7 +418,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async-proxy reads
       named_barrier(1, 128);
-      if (et == 0) mbar_arrive(&xa_full[st]);
+      if (et == 0) {
+        if (PAIR && pr != 0)
+          mbar_arrive_remote(dsmem_map(smem_u32(&xa_full[st]), lead_rank));
+        else
+          mbar_arrive(&xa_full[st]);
+      }
     }
   }
   if (epi) {
@@ -363,55 +431,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
   }
 
-  // ---------------- split K: exchange partial accumulators inside the cluster ----------------
-  // stage buffers, reused: recv[cs-1][128 rows][bnc] then send[cs-1][128 rows][bnc], fp32,
-  // 16-byte chunks of a row XOR-swizzled by (row & 7)
-  const size_t slot_floats = (size_t)kBM * bnc;
-  float* recv = reinterpret_cast<float*>(stage_base);
-  float* send = recv + (size_t)(cs - 1) * slot_floats;
-  const int swz = rt & 7;
+  // ---------------- split K: exchange partial accumulators through L2 ----------------
+  // scratch of this output block: [d][z] blocks (CTA z's partial of CTA d's columns) of
+  // [bnc / 4][128 rows] float4, rows fastest, so a warp's 32 rows move 512 contiguous bytes
+  const int nq = bnc / 4;
+  const float4* xk_in = nullptr;  // the cs blocks addressed to this CTA: [q][nq][128]
   if (cs > 1) {
-    if (threadIdx.x == 64) mbar_arrive_expect_tx(xchg_bar, (uint32_t)((cs - 1) * slot_floats * 4));
-    __syncwarp();
-    tc_fence_before();
-    cluster_sync_all();  // every main loop of the cluster is done: stage buffers are idle
-    tc_fence_after();
+    float4* xk_tile = reinterpret_cast<float4*>(a.xk) +
+                      (size_t)(mt_i * (int)gridDim.y + nt_i) * cs * cs * nq * kBM;
+    xk_in = xk_tile + (size_t)z * cs * nq * kBM + rt;
     if (epi) {
       for (int d = 0; d < cs; ++d) {
         if (d == z) continue;
-        float* srow = send + (size_t)(d < z ? d : d - 1) * slot_floats + (size_t)rt * bnc;
+        float4* blk = xk_tile + (size_t)(d * cs + z) * nq * kBM + rt;
         for (int c = 0; c < bnc; c += 32) {
           uint32_t raw[32];
           tmem_ld_32x32b_x32(tmem_row + d * bnc + c, raw);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int chunk = ((c >> 2) + i) ^ swz;
-            *reinterpret_cast<float4*>(srow + chunk * 4) =
-                make_float4(__uint_as_float(raw[4 * i]), __uint_as_float(raw[4 * i + 1]),
-                            __uint_as_float(raw[4 * i + 2]), __uint_as_float(raw[4 * i + 3]));
-          }
+          for (int i = 0; i < 8; ++i)
+            __stcg(blk + (size_t)((c >> 2) + i) * kBM,
+                   make_float4(__uint_as_float(raw[4 * i]), __uint_as_float(raw[4 * i + 1]),
+                               __uint_as_float(raw[4 * i + 2]), __uint_as_float(raw[4 * i + 3])));
         }
       }
-      fence_proxy_async_smem();
-      named_barrier(1, 128);  // the four epilogue warps have staged every send row
-      if (threadIdx.x == 64) {
-        for (int d = 0; d < cs; ++d) {
-          if (d == z) continue;
-          const uint32_t src = smem_u32(send + (size_t)(d < z ? d : d - 1) * slot_floats);
-          const uint32_t dst =
-              dsmem_map(smem_u32(recv + (size_t)(z < d ? z : z - 1) * slot_floats), (uint32_t)d);
-          bulk_copy_s2cluster(dst, src, (uint32_t)(slot_floats * 4),
-                              dsmem_map(smem_u32(xchg_bar), (uint32_t)d));
-        }
-        bulk_commit_group();
-      }
-      mbar_wait(xchg_bar, 0, a.err);  // the cs - 1 partials of this CTA's columns are here
     }
+    tc_fence_before();
+    cluster_sync_all();  // release / acquire: every block addressed to this CTA is written
+    tc_fence_after();
   }
 
+  // ---------------- the epilogue's inputs, landed in shared memory ----------------
+  // The ring is idle once the accumulator is complete.  xin: the cs - 1 partial blocks
+  // addressed to this CTA ([j][bnc / 4][128 rows] float4, as in the scratch); dsm: the
+  // tile's delta rows ([128][bnc] fp32, 16-byte chunks XOR-swizzled by row & 7).  Both
+  // arrive by cp.async and are waited for once, so their latencies overlap instead of
+  // following one another chunk by chunk.
+  const bool delta_mode = a.ex.mode == kExpandDelta;
+  float4* xin = reinterpret_cast<float4*>(stage_base);
+  float* dsm = reinterpret_cast<float*>(stage_base + (size_t)(cs - 1) * nq * kBM * 16);
+  if (epi && cs > 1) {
+    for (int q = 0, j = 0; q < cs; ++q) {
+      if (q == z) continue;
+      const float4* src = xk_in + (size_t)q * nq * kBM;
+      float4* dst = xin + (size_t)j * nq * kBM + rt;
+      for (int c4 = 0; c4 < nq; ++c4) cp_async_16(dst + (size_t)c4 * kBM, src + (size_t)c4 * kBM);
+      ++j;
+    }
+  }
   bool add_delta = false;  // delta mode: the row adds the low-rank term of the delta buffer
-  if (epi && a.ex.mode == kExpandDelta) {
+  if (epi && delta_mode) {
     // only now the low-rank kernel's results are needed: the main loop and the split-K
     // exchange ran while it was still working
     griddep_wait();
@@ -424,56 +493,66 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         else if (t >= 0 && !add_delta) atomicOr(a.err, LORA_ERRF_EMPTY_SLOT);
       }
     }
+    // the tile's delta rows (the buffer holds the batch's rows, at most 512): consecutive
+    // threads fetch consecutive 16-byte chunks of a row
+    const int et = threadIdx.x - 64;
+    const int cfirst = n0 + z * bnc;  // first column this CTA finishes
+    for (int idx = et; idx < kBM * nq; idx += 128) {
+      const int r = idx / nq, ch = idx - r * nq;
+      const int gr = m0 + r, gc = cfirst + ch * 4;
+      if (gr < a.M && gc < a.N)
+        cp_async_16(dsm + (size_t)r * bnc + ((ch ^ (r & 7)) << 2),
+                    a.ex.delta + (size_t)gr * a.N + gc);
+    }
+  }
+  if (epi && (cs > 1 || delta_mode)) {
+    cp_async_wait_all();
+    named_barrier(1, 128);  // delta rows fetched by the other epilogue threads
   }
   if (epi) {
-    // the delta buffer holds the first 512 rows only: a row that adds no delta never forms
-    // an address into it beyond row 0
-    const bool from_delta = add_delta && a.ex.mode == kExpandDelta;
-    const float* drow = a.ex.delta + (from_delta ? (size_t)row * a.N : 0);
     __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.y) + (size_t)row * a.N;
     const int cbase = z * bnc;  // first accumulator column this CTA finishes
+    const float* drow = dsm + (size_t)rt * bnc;
 #pragma unroll 1
     for (int c = 0; c < bnc; c += 32) {
       const int nc = n0 + cbase + c;
-      float4 d[8];  // the row's delta for these 32 columns, in flight during the TMEM read
-      if (from_delta) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          d[q] = nc + q * 4 < a.N ? *reinterpret_cast<const float4*>(drow + nc + q * 4)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) d[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
       uint32_t raw[32];
       tmem_ld_32x32b_x32(tmem_row + cbase + c, raw);
       tmem_ld_wait();
       float acc[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(raw[i]);
-      for (int q = 0; q < cs - 1; ++q) {
-        const float* rrow = recv + (size_t)q * slot_floats + (size_t)rt * bnc;
+      for (int j = 0; j < cs - 1; ++j) {
+        const float4* blk = xin + (size_t)j * nq * kBM + rt;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int chunk = ((c >> 2) + i) ^ swz;
-          const float4 v = *reinterpret_cast<const float4*>(rrow + chunk * 4);
+          const float4 v = blk[(size_t)((c >> 2) + i) * kBM];
           acc[i * 4 + 0] += v.x;
           acc[i * 4 + 1] += v.y;
           acc[i * 4 + 2] += v.z;
           acc[i * 4 + 3] += v.w;
         }
       }
+      float4 d[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        d[q] = add_delta
+                   ? *reinterpret_cast<const float4*>(drow + ((((c >> 2) + q) ^ (rt & 7)) << 2))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
       epilogue_chunk32(acc, a, row, nc, add_delta, d, yrow);
     }
-    // the send buffers must stay intact until the bulk copies have read them
-    if (cs > 1 && threadIdx.x == 64) bulk_wait_read_all();
   }
 
   tc_fence_before();
   __syncthreads();
+  // pairs: the peer is done with this CTA's TMEM, shared memory and barriers
+  if (PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, BN);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, BN);
+    else
+      tmem_dealloc(tmem_base, BN);
   }
 }
 
@@ -506,60 +585,112 @@ cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Tile shape and K split.  Large problems (no split allowed): the widest N tile that still
-// gives one tile per SM.  Small batches (split allowed): the (N tile, K split) of least
-// estimated time, from per-K-block costs measured on this kernel: an MMA of N <= 128 costs
-// its issue time (~440 cycles for the 4 MMAs of a 64-wide K block), a 256-wide block waits
-// on its 48 KB of operands (~660 cycles at ~75 B/cycle of TMA ingress per SM); plus ~3k
-// cycles of epilogue per wave and the split-K exchange at ~10 B/cycle per CTA.
+// CTAs of this GEMM that can be resident at once in clusters of `csize` CTAs (every variant
+// holds one CTA per SM; a cluster must fit in one GPC, whose sizes differ).  Queried once.
+static int resident_ctas(int csize, int num_sms) {
+  static int cache[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+  if (csize < 1 || csize > 8) return 0;
+  if (cache[csize] == 0) {
+    static int limit = 0;
+    const int smem = 200 * 1024;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(csize * 64);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (ensure_smem_limit(gemm_tc_kernel<256, false>, smem, &limit) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<256, false>, &cfg) == cudaSuccess &&
+        n > 0) {
+      cache[csize] = std::min(num_sms, n * csize);
+    } else {
+      cudaGetLastError();
+      cache[csize] = csize == 1 ? num_sms : 8 * (num_sms / 8 / csize) * csize;
+    }
+  }
+  return cache[csize];
+}
+
+// Tile shape, K split and CTA pairs, by least estimated time (cycles).  Measured on this
+// kernel: a 64-wide K block costs ~550 cycles whatever the tile (4 MMA instructions at
+// ~124 cycles each below N = 256, 128 at N = 256, plus ~50 of barrier hand-off), unless
+// its operands arrive slower than ~100 B per cycle per SM; CTA pairs halve the W rows a
+// CTA loads.  Each wave adds ~3k cycles of prologue, pipeline fill and epilogue; a split
+// K adds the exchange of fp32 partials through L2 (written and read at ~50 B per cycle per
+// SM).  Large problems (no split allowed) weigh the same costs without the split.
 GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split) {
   const int mt = (M + kBM - 1) / kBM;
   const int nkb = (K + kBK - 1) / kBK;
-  GemmPlan p{64, 1};
-  const int cand[3] = {256, 128, 64};
-  if (!allow_split) {
-    for (int i = 0; i < 3; ++i) {
-      const int tiles = mt * ((N + cand[i] - 1) / cand[i]);
-      if (tiles >= num_sms) {
-        p.block_n = cand[i];
-        return p;
-      }
-    }
-    return p;
-  }
   // every one of the cs K ranges of ceil(nkb / cs) blocks must be non-empty
   auto ranges_ok = [nkb](int c) { return (c - 1) * ((nkb + c - 1) / c) < nkb; };
+  GemmPlan p{64, 1, 0};
   double best = 1e30;
-  for (int i = 0; i < 3; ++i) {
-    const int bn = cand[i];
-    const double per_kb = bn == 256 ? 660.0 : 440.0;
-    const int tiles = mt * ((N + bn - 1) / bn);
-    // each CTA finishes bn / cs >= 32 columns (its epilogue and the split-K exchange work
-    // in 32-column chunks)
-    for (int cs = 1; cs <= 4 && bn / cs >= 32; cs *= 2) {
-      if (cs > 1 && !ranges_ok(cs)) break;
-      const int waves = (tiles * cs + num_sms - 1) / num_sms;
-      const int kb = (nkb + cs - 1) / cs;
-      const double exch = cs > 1 ? (cs - 1) * (double)kBM * (bn / cs) * 4.0 / 10.0 : 0.0;
-      const double cost = waves * (kb * per_kb + 3000.0 + exch);
-      if (cost < best * 0.999) {
-        best = cost;
-        p.block_n = bn;
-        p.ksplit = cs;
+  const int cand[3] = {256, 128, 64};
+  // single CTAs first: a pair is taken only where it is estimated faster (its epilogue ends
+  // on a cluster barrier, ~1 us slower per tile)
+  for (int pair = 0; pair <= 1; ++pair) {
+    if (pair && mt < 2) continue;  // a pair over one row tile would leave a CTA idle
+    for (int i = 0; i < 3; ++i) {
+      const int bn = cand[i];
+      if (pair && bn < 128) continue;
+      const double bytes = kABytes + (double)(pair ? bn / 2 : bn) * kBK * 2;
+      const double per_kb = std::max(bytes / 100.0, 4.0 * std::max(124.0, 0.5 * bn)) + 50.0;
+      const int ctas_m = pair ? 2 * ((mt + 1) / 2) : mt;
+      const int tiles = ctas_m * ((N + bn - 1) / bn);
+      // each CTA finishes bn / cs >= 32 columns (its epilogue and the split-K exchange work
+      // in 32-column chunks)
+      for (int cs = 1; cs <= (allow_split ? 4 : 1) && bn / cs >= 32; cs *= 2) {
+        if (cs > 1 && !ranges_ok(cs)) break;
+        const int conc = resident_ctas((pair ? 2 : 1) * cs, num_sms);
+        if (conc < 1) continue;
+        const int waves = (tiles * cs + conc - 1) / conc;
+        const int kb = (nkb + cs - 1) / cs;
+        const double exch = cs > 1 ? 2.0 * (cs - 1) * kBM * (bn / cs) * 4.0 / 50.0 : 0.0;
+        const double cost = waves * (kb * per_kb + 3000.0 + exch);
+        if (cost < best * 0.999) {
+          best = cost;
+          p.block_n = bn;
+          p.ksplit = cs;
+          p.pair = pair;
+        }
       }
     }
   }
   return p;
 }
 
-int gemm_tc_tile_index(int BN) { return BN == 256 ? 0 : (BN == 128 ? 1 : 2); }
-
-static size_t tc_smem_bytes(int BN, int stages, int xscr_bytes) {
-  const size_t stage = (size_t)kABytes + (size_t)BN * kBK * 2;
-  return 1024 + stages * stage + xscr_bytes + (2 * kBM + 6) * 4 + (4 * stages + 4) * 8;
+// Split-K scratch of a plan: per output block (one per CTA of a K range) cs x cs blocks of
+// 128 rows x BN / cs columns.
+static size_t exchange_floats(const GemmPlan& p, int M, int N) {
+  if (p.ksplit <= 1) return 0;
+  const int mt = (M + kBM - 1) / kBM;
+  const size_t gx = p.pair ? 2 * ((mt + 1) / 2) : mt;
+  const size_t gy = (N + p.block_n - 1) / p.block_n;
+  return gx * gy * p.ksplit * p.block_n * kBM;
 }
 
-template <int BN>
+size_t gemm_tc_exchange_floats(int M, int N, int K, int num_sms) {
+  return exchange_floats(gemm_tc_plan(M, N, K, num_sms, true), M, N);
+}
+
+size_t gemm_tc_plan_exchange_floats(const GemmPlan& p, int M, int N) {
+  return exchange_floats(p, M, N);
+}
+
+int gemm_tc_tile_index(int BN) { return BN == 256 ? 0 : (BN == 128 ? 1 : 2); }
+
+static size_t tc_smem_bytes(int BN, bool pair, int stages, int xscr_bytes) {
+  const size_t stage = (size_t)kABytes + (size_t)(pair ? BN / 2 : BN) * kBK * 2;
+  return 1024 + stages * stage + xscr_bytes + (2 * kBM + 6) * 4 + (4 * stages + 3) * 8;
+}
+
+template <int BN, bool PAIR>
 static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUtensorMap& tmap_x,
                              const CUtensorMap& tmap_w, const CUtensorMap& tmap_bx,
                              cudaStream_t stream) {
@@ -571,52 +702,70 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   if (a.ex.mode == kExpandV && (cs != 1 || a.ex.R % 8 != 0 || a.ex.R > 128 || a.ex.S > 32 * kBM))
     return cudaErrorInvalidValue;
   const int xscr = a.ex.mode == kExpandV ? kBM * expand_layout(a.ex.R).nbs * 128 : 0;
-  // the split-K send and receive buffers reuse the stage buffers
-  const size_t recv = cs > 1 ? (size_t)2 * (cs - 1) * kBM * (BN / cs) * 4 : 0;
-  const size_t stage = (size_t)kABytes + (size_t)BN * kBK * 2;
+  if (cs > 1 && (!a.xk || a.xk_floats < exchange_floats(plan, a.M, a.N)))
+    return cudaErrorInvalidValue;
   int stages = 8;
-  while (stages > 2 && tc_smem_bytes(BN, stages, xscr) > budget) --stages;
-  if ((size_t)stages * stage < recv) return cudaErrorInvalidConfiguration;
-  const size_t smem = tc_smem_bytes(BN, stages, xscr);
+  while (stages > 2 && tc_smem_bytes(BN, PAIR, stages, xscr) > budget) --stages;
+  const size_t smem = tc_smem_bytes(BN, PAIR, stages, xscr);
   if (smem > budget) return cudaErrorInvalidConfiguration;
+  // the epilogue lands its split-K partials and delta rows (128 x BN fp32) in the ring
+  const size_t stage = (size_t)kABytes + (size_t)(PAIR ? BN / 2 : BN) * kBK * 2;
+  if ((cs > 1 || a.ex.mode == kExpandDelta) && (size_t)stages * stage < (size_t)kBM * BN * 4)
+    return cudaErrorInvalidConfiguration;
   static int limit = 0;
-  cudaError_t e = ensure_smem_limit(gemm_tc_kernel<BN>, (int)smem, &limit);
+  cudaError_t e = ensure_smem_limit(gemm_tc_kernel<BN, PAIR>, (int)smem, &limit);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.x = PAIR ? 2 : 1;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = cs;
-  cfg.gridDim = dim3((a.M + kBM - 1) / kBM, (a.N + BN - 1) / BN, cs);
+  // pairs: an even number of row tiles (a last CTA past M loads zeros and stores nothing)
+  const int mt = (a.M + kBM - 1) / kBM;
+  const int mtp = PAIR ? (mt + 1) / 2 : mt;  // row tiles, or pairs of them
+  cfg.gridDim = dim3(PAIR ? 2 * mtp : mt, (a.N + BN - 1) / BN, cs);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = cs > 1 ? 2 : 1;
-  // row tiles per band: x of a band at most ~32 MB
-  const int mt = (a.M + kBM - 1) / kBM;
-  const int group_m = std::max(1, std::min(mt, (int)((32u << 20) / ((size_t)a.K * kBM * 2))));
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmap_x, tmap_w, tmap_bx, a, stages, xscr,
-                            group_m);
+  cfg.numAttrs = (PAIR || cs > 1) ? 2 : 1;
+  // row tiles (pairs) per band: x of a band at most ~32 MB
+  const size_t band_rows = (size_t)kBM * (PAIR ? 2 : 1);
+  const int group_m =
+      std::max(1, std::min(mtp, (int)((32u << 20) / ((size_t)a.K * band_rows * 2))));
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, PAIR>, tmap_x, tmap_w, tmap_bx, a, stages,
+                            xscr, group_m);
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
                            const CUtensorMap* tmap_bx3, cudaStream_t stream) {
   if (a.ex.mode == kExpandV && !tmap_bx3) return cudaErrorInvalidValue;
-  const GemmPlan plan = gemm_tc_plan(a.M, a.N, a.K, a.num_sms, a.ex.mode != kExpandV);
+  GemmPlan plan = gemm_tc_plan(a.M, a.N, a.K, a.num_sms, a.ex.mode != kExpandV);
+  if (a.force_bn != 0) {
+    // v mode never splits K: its expand blocks run after the base ones in one accumulator
+    plan = GemmPlan{a.force_bn, a.ex.mode == kExpandV ? 1 : a.force_cs, a.force_pair};
+    const int nkb = (a.K + kBK - 1) / kBK, c = plan.ksplit;
+    if (c > 1 && (c - 1) * ((nkb + c - 1) / c) >= nkb) return cudaErrorInvalidConfiguration;
+  }
   CUtensorMap tmap_x;
   cudaError_t e = encode_tmap_bf16(&tmap_x, a.x, a.M, a.K, kBM);
   if (e != cudaSuccess) return e;
-  const int ti = gemm_tc_tile_index(plan.block_n);
+  // a CTA of a pair loads half of the N tile's rows: the map with boxes of block_n / 2 rows
+  const int ti = gemm_tc_tile_index(plan.pair ? plan.block_n / 2 : plan.block_n);
   const CUtensorMap& tw = tmap_w3[ti];
   const CUtensorMap& tb = tmap_bx3 ? tmap_bx3[ti] : tw;  // unused in delta mode
+  if (plan.pair) {
+    if (plan.block_n == 256) return launch_tc<256, true>(a, plan, tmap_x, tw, tb, stream);
+    if (plan.block_n == 128) return launch_tc<128, true>(a, plan, tmap_x, tw, tb, stream);
+    return cudaErrorInvalidConfiguration;
+  }
   switch (plan.block_n) {
-    case 256: return launch_tc<256>(a, plan, tmap_x, tw, tb, stream);
-    case 128: return launch_tc<128>(a, plan, tmap_x, tw, tb, stream);
-    default: return launch_tc<64>(a, plan, tmap_x, tw, tb, stream);
+    case 256: return launch_tc<256, false>(a, plan, tmap_x, tw, tb, stream);
+    case 128: return launch_tc<128, false>(a, plan, tmap_x, tw, tb, stream);
+    default: return launch_tc<64, false>(a, plan, tmap_x, tw, tb, stream);
   }
 }
 

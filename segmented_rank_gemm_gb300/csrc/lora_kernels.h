@@ -155,6 +155,9 @@ struct GemmArgs {
   ExpandArgs ex;
   int32_t* err;
   int num_sms;
+  float* xk;         // split K: scratch for the exchanged fp32 partials (L2-resident)
+  size_t xk_floats;  // its capacity (gemm_tc_exchange_floats of the batch)
+  int force_bn, force_cs, force_pair;  // tcgen05 tiling fixed by the caller (force_bn 0: auto)
 };
 // tcgen05 / TMEM / TMA kernel (gemm_tc.cu).  tmap_w3 holds the layer's cached maps of the
 // packed weight for N tiles of 256, 128 and 64 rows (in that order); tmap_bx3 the maps of
@@ -167,9 +170,15 @@ constexpr int kTcTileN[3] = {256, 128, 64};
 cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
 struct GemmPlan {
   int block_n;  // N tile: 256, 128 or 64
-  int ksplit;   // K ranges per output tile (= cluster size), 1..4
+  int ksplit;   // K ranges per output tile, 1..4
+  int pair;     // 1: CTA pairs (cta_group::2 MMAs, 256-row tiles, N tile 256 or 128)
 };
 GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split);
+// Floats of split-K exchange scratch the tcgen05 GEMM needs for an M-row batch with the
+// K split allowed (0 when its plan does not split K).
+size_t gemm_tc_exchange_floats(int M, int N, int K, int num_sms);
+// The same for a given plan.
+size_t gemm_tc_plan_exchange_floats(const GemmPlan& p, int M, int N);
 
 // fp32 SIMT path (gemm_simt.cu)
 cudaError_t launch_gemm_simt_f32(const GemmArgs& a, cudaStream_t stream);

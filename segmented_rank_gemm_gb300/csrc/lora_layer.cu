@@ -63,6 +63,9 @@ struct lora_layer {
   float* v = nullptr;            // [v_planes][T_max][R] fp32, scaled by alpha / r (v mode)
   int v_planes = 1;              // K-split partial planes of v (bf16: tensor-core shrink)
   float* delta = nullptr;        // [min(T_max, kDeltaMaxT)][N] fp32 (delta mode, bf16)
+  float* xk = nullptr;           // split-K exchange scratch of the base GEMM (delta mode)
+  size_t xk_floats = 0;
+  GemmPlan gemm_plan{0, 0, 0};   // fixed by lora_set_gemm_plan (block_n 0: automatic)
   int max_tiles = 0;
   int T_batch = -1;              // T of the last set_batch_segments, -1 = none
   bool segments_pending = false;  // that batch's builder has not run yet (decode batches)
@@ -115,8 +118,8 @@ cudaError_t dmalloc(T** p, size_t count) {
 void free_all(lora_layer* L) {
   void* ptrs[] = {L->Wp, L->A_pool, L->B_pool, L->Bx_pool, L->A_stage, L->scale, L->rank, L->loaded,
                   L->row_slot, L->perm, L->seg_offsets, L->seg_slot, L->tile_seg,
-                  L->tile_row0, L->meta, L->err, L->v, L->delta, L->x_stage, L->ids_stage,
-                  L->y_stage};
+                  L->tile_row0, L->meta, L->err, L->v, L->delta, L->xk, L->x_stage,
+                  L->ids_stage, L->y_stage};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (L->stage_free) cudaEventDestroy(L->stage_free);
@@ -189,6 +192,10 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
   L->max_tiles = (max_tokens + kTileRows - 1) / kTileRows + num_slots;
   // small batches split the shrink's K range over up to 8 planes of v; large ones need none
   L->v_planes = dtype == LORA_BF16 ? std::max(1, std::min(8, 65536 / max_tokens)) : 1;
+  // the base GEMM of a delta-mode batch may split K: scratch for its largest exchange
+  if (dtype == LORA_BF16)
+    for (int m = 1; m <= std::min(max_tokens, kDeltaMaxT); ++m)
+      L->xk_floats = std::max(L->xk_floats, gemm_tc_exchange_floats(m, N, K, L->num_sms));
   bool ok = cudaMalloc(&L->Wp, (size_t)K * N * es) == cudaSuccess &&
             cudaMalloc(&L->A_pool, S * R * K * es) == cudaSuccess &&
             cudaMalloc(&L->B_pool, S * R * N * es) == cudaSuccess &&
@@ -205,6 +212,7 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
             dmalloc(&L->v, (size_t)L->v_planes * max_tokens * R) == cudaSuccess &&
             (dtype != LORA_BF16 ||
              dmalloc(&L->delta, (size_t)std::min(max_tokens, kDeltaMaxT) * N) == cudaSuccess) &&
+            (L->xk_floats == 0 || dmalloc(&L->xk, L->xk_floats) == cudaSuccess) &&
             cudaMalloc(&L->x_stage, (size_t)max_tokens * K * es) == cudaSuccess &&
             dmalloc(&L->ids_stage, max_tokens) == cudaSuccess &&
             cudaMalloc(&L->y_stage, (size_t)max_tokens * N * es) == cudaSuccess &&
@@ -477,6 +485,11 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.ex.rank = L->rank;
   ga.err = L->err;
   ga.num_sms = L->num_sms;
+  ga.xk = L->xk;
+  ga.xk_floats = L->xk_floats;
+  ga.force_bn = L->gemm_plan.block_n;
+  ga.force_cs = L->gemm_plan.ksplit;
+  ga.force_pair = L->gemm_plan.pair;
   LORA_CUDA(L, trace_mark(L, 4, stream));
   if (bf16)
     LORA_CUDA(L, launch_gemm_tc(ga, L->tmap_w, L->Bx_pool ? L->tmap_bx : nullptr, stream));
@@ -565,6 +578,38 @@ int lora_set_trace_events(lora_layer_t* L, void* const* events) {
     if (!events[i]) return fail(L, LORA_EINVAL, "null trace event %d", i);
   for (int i = 0; i < 6; ++i) L->trace[i] = static_cast<cudaEvent_t>(events[i]);
   L->tracing = true;
+  return LORA_OK;
+}
+
+int lora_set_gemm_plan(lora_layer_t* L, int block_n, int k_split, int cta_pair) {
+  if (!L) return LORA_EINVAL;
+  if (block_n == 0) {
+    L->gemm_plan = GemmPlan{0, 0, 0};
+    return LORA_OK;
+  }
+  if ((block_n != 64 && block_n != 128 && block_n != 256) ||
+      (k_split != 1 && k_split != 2 && k_split != 4) || block_n / k_split < 32 ||
+      (cta_pair != 0 && cta_pair != 1) || (cta_pair && block_n < 128))
+    return fail(L, LORA_EINVAL, "invalid GEMM plan (block_n %d, k_split %d, cta_pair %d)",
+                block_n, k_split, cta_pair);
+  const GemmPlan p{block_n, k_split, cta_pair};
+  // the scratch must hold the exchange of every batch that may split K with this plan
+  size_t need = 0;
+  if (L->dtype == LORA_BF16)
+    for (int m = 1; m <= std::min(L->T_max, kDeltaMaxT); ++m)
+      need = std::max(need, gemm_tc_plan_exchange_floats(p, m, L->N));
+  if (need > L->xk_floats) {
+    LORA_CUDA(L, cudaDeviceSynchronize());  // earlier forwards may still use the scratch
+    float* grown = nullptr;
+    if (dmalloc(&grown, need) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(L, LORA_ENOMEM, "split-K scratch of %zu floats", need);
+    }
+    if (L->xk) cudaFree(L->xk);
+    L->xk = grown;
+    L->xk_floats = need;
+  }
+  L->gemm_plan = p;
   return LORA_OK;
 }
 

@@ -184,8 +184,8 @@ __global__ void __launch_bounds__(kTileThreads, 2)
                      const int32_t* __restrict__ seg_slot, const int32_t* __restrict__ tile_seg,
                      const int32_t* __restrict__ tile_row0, const int32_t* __restrict__ meta,
                      float* __restrict__ out /* v [T][R] or delta [T][N] */) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   __shared__ int rows_s[kTileRows];
   __shared__ float v_s[kTileRows * 129];
   const int vstride = R + 1;
@@ -249,6 +249,7 @@ __global__ void __launch_bounds__(kBgmvThreads, 8)  // <= 64 registers: 4 CTAs f
                       const __nv_bfloat16* __restrict__ B_pool, const float* __restrict__ scale,
                       const int32_t* __restrict__ rank, float* __restrict__ delta, int kchunk,
                       int nchunk) {
+  griddep_wait();  // the previous kernel's writes (x, the delta it read) are settled
   griddep_launch_dependents();  // the base GEMM's main loop may start now
   __shared__ float v_part[2][128];
   __shared__ float v_s[128];
@@ -494,7 +495,11 @@ __global__ void __maxnreg__(120)
                        const __nv_bfloat16* __restrict__ At_pool,
                        const __nv_bfloat16* __restrict__ B_pool, const float* __restrict__ scale,
                        const int32_t* __restrict__ rank, float* __restrict__ delta) {
-  griddep_launch_dependents();  // the base GEMM's main loop may start now
+  // launched while the previous kernel (the previous forward's base GEMM) still runs: wait
+  // for it before reading x or writing delta, and only then let the base GEMM start (its
+  // main loop reads x, which that kernel may have written)
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ int grp_off[];  // [S + 1]: rows per slot, then first item of each slot
   __shared__ int rows_s[kStrGroup];
   __shared__ int warp_cnt[kStrThreads / 32];

@@ -26,8 +26,8 @@ LORA_ECUDA, LORA_ENOMEM, LORA_ESTATE, LORA_ETIMEOUT = -5, -6, -7, -8
 # every entry point declared in include/lora_layer.h
 ABI_FUNCTIONS = ("lora_layer_create", "load_adapter_slot", "unload_adapter_slot",
                  "set_batch_segments", "lora_forward", "lora_forward_host", "lora_get_status",
-                 "lora_get_segments", "lora_set_trace_events", "lora_last_error",
-                 "lora_layer_destroy", "lora_build_segments_static")
+                 "lora_get_segments", "lora_set_trace_events", "lora_set_gemm_plan",
+                 "lora_last_error", "lora_layer_destroy", "lora_build_segments_static")
 
 
 class LoraError(RuntimeError):
@@ -51,6 +51,7 @@ def _load() -> ctypes.CDLL:
     L.lora_get_status.argtypes = [vp, vp]
     L.lora_get_segments.argtypes = [vp, vp, vp, vp, vp, vp, vp]
     L.lora_set_trace_events.argtypes = [vp, vp]
+    L.lora_set_gemm_plan.argtypes = [vp, i32, i32, i32]
     L.lora_build_segments_static.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp]
     L.lora_last_error.argtypes = [vp]
     L.lora_last_error.restype = ctypes.c_char_p
@@ -166,6 +167,12 @@ def lora_set_trace_events(layer, events) -> None:
     _check(layer, _lib.lora_set_trace_events(layer, ctypes.cast(arr, ctypes.c_void_p)))
 
 
+def lora_set_gemm_plan(layer, block_n: int, k_split: int = 1, cta_pair: int = 0) -> None:
+    """Fix the base GEMM's N tile, K split and CTA pairing; ``block_n=0`` restores the
+    automatic plan."""
+    _check(layer, _lib.lora_set_gemm_plan(layer, int(block_n), int(k_split), int(cta_pair)))
+
+
 def lora_build_segments_static(token_slot, T, num_slots, slot_loaded, perm, seg_offsets,
                                seg_slot, counts, stream=None) -> None:
     """Segment builder without any device allocation (scratch in a static device array);
@@ -244,6 +251,9 @@ class LoraLayer:
 
     def segments(self, stream=None):
         return lora_get_segments(self.handle, self.max_tokens, self.num_slots, stream)
+
+    def set_gemm_plan(self, block_n: int, k_split: int = 1, cta_pair: int = 0):
+        lora_set_gemm_plan(self.handle, block_n, k_split, cta_pair)
 
     def close(self):
         if getattr(self, "handle", None):
