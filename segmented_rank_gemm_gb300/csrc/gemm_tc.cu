@@ -115,12 +115,28 @@ __device__ __forceinline__ void v_hi_lo8(const ExpandArgs& ex, int row, int j0, 
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// Output tile (pm, nt) of work unit u: bands of group_m row tiles (pairs of them with CTA
+// pairs), column tiles in turn within a band, row tiles fastest.  Consecutive units (those
+// the resident CTAs run at the same time) then share one band of x, which stays in L2,
+// instead of streaming all of x from DRAM again for every few column tiles.
+__device__ __forceinline__ void unit_tile(int u, int mtp, int nt, int group_m, int& pm,
+                                          int& ntile) {
+  const int band = u / (group_m * nt);
+  const int gm = min(group_m, mtp - band * group_m);  // rows of the last band may be fewer
+  const int w = u - band * group_m * nt;
+  pm = band * group_m + w % gm;
+  ntile = w / gm;
+}
+
+// Registers capped at 136: two warps of this kernel and two of the decode BGMV kernel
+// (120 registers) share each of an SM's four 16K-register files, so the two kernels run
+// side by side.
 template <int BN, bool PAIR>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __maxnreg__(136)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_bx, GemmArgs a, int stages,
-                   int xscr_bytes, int group_m) {
+                   int xscr_bytes, int group_m, int mtp, int nt) {
   constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of the W (or B expand) tile this CTA loads
   constexpr int kBBytes = kBRows * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
@@ -139,31 +155,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(x_blocks + 2);
   uint64_t* full = bars;
   uint64_t* empty = bars + stages;
-  uint64_t* tmem_full = bars + 2 * stages;
-  uint64_t* xinfo_bar = bars + 2 * stages + 1;  // v mode: x_blocks written
-  uint64_t* xgrant = bars + 2 * stages + 2;     // [stages] v mode: stage handed to the epilogue
-  uint64_t* xa_full = bars + 3 * stages + 2;    // [stages] v mode: its A half written
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * stages + 2);
+  uint64_t* tmem_full = bars + 2 * stages;       // [2] accumulator buffer complete
+  uint64_t* tmem_empty = bars + 2 * stages + 2;  // [2] accumulator buffer drained
+  uint64_t* xinfo_bar = bars + 2 * stages + 4;   // v mode: the tile's x_blocks written
+  uint64_t* xgrant = bars + 2 * stages + 5;      // [stages] v mode: stage handed to the epilogue
+  uint64_t* xa_full = bars + 3 * stages + 5;     // [stages] v mode: its A half written
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * stages + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Tile order: bands of group_m row tiles, column tiles in turn within a band, row tiles
-  // fastest.  A wave of CTAs then shares one band of x (which stays in L2) instead of
-  // streaming all of x from DRAM again for every few column tiles.
-  // CTA pairs: the two CTAs of a pair are neighbours in x, take one tile order (counted in
-  // pairs) and cover 256 consecutive rows, CTA pr of the pair rows [128 pr, 128 pr + 128).
+  // Work units: output tiles, one per CTA (pair) slot and round: slot g runs units
+  // g, g + G, g + 2 G, ... (delta mode: G is the number of units, one each).  CTA pairs:
+  // the two CTAs of a pair are neighbours in x and cover 256 consecutive rows, CTA pr of
+  // the pair rows [128 pr, 128 pr + 128).
   const int pr = PAIR ? (int)(blockIdx.x & 1u) : 0;
-  int pm_i, nt_i;
-  {
-    const int mt = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x, nt = gridDim.y;
-    const int id = (PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x) + blockIdx.y * mt;
-    const int band = id / (group_m * nt);
-    const int gm = min(group_m, mt - band * group_m);  // rows of the last band may be fewer
-    const int w = id - band * group_m * nt;
-    pm_i = band * group_m + w % gm;
-    nt_i = w / gm;
-  }
-  const int mt_i = PAIR ? 2 * pm_i + pr : pm_i;
-  const int m0 = mt_i * kBM, n0 = nt_i * BN;
+  const int g0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int G = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
+  const int U = mtp * nt;
   // cluster ranks (x fastest): CTA (pr, z) is rank pr + 2 z with pairs, z without; the even
   // CTA of a pair issues its MMAs, and its barriers count both CTAs' loads
   const uint32_t lead_rank = PAIR ? 2u * blockIdx.z : 0u;
@@ -174,15 +181,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int per = (nkb_all + cs - 1) / cs;
   const int kb_begin = z * per;
   const int nkb = min(nkb_all, kb_begin + per) - kb_begin;
-  const int rot = (int)((pm_i + nt_i) % (unsigned)nkb);  // the same for both CTAs of a pair
   const int bnc = BN / cs;  // columns this CTA finishes
+  const bool vmode = a.ex.mode == kExpandV;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tmem_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], PAIR ? 2 : 1);  // pairs: one arrival from each CTA's epilogue
+    }
     mbar_init(xinfo_bar, 1);
     for (int s = 0; s < stages; ++s) {
       mbar_init(&xgrant[s], 1);
@@ -193,13 +203,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_x);
     tma_prefetch_desc(&tmap_w);
-    if (a.ex.mode == kExpandV) tma_prefetch_desc(&tmap_bx);
+    if (vmode) tma_prefetch_desc(&tmap_bx);
   }
+  // two accumulator buffers of BN columns: the epilogue drains one while the MMAs fill the
+  // other with the next tile
   if (warp == 1) {
     if (PAIR)
-      tmem_alloc_pair(tmem_holder, BN);
+      tmem_alloc_pair(tmem_holder, 2 * BN);
     else
-      tmem_alloc(tmem_holder, BN);
+      tmem_alloc(tmem_holder, 2 * BN);
   }
   tc_fence_before();
   __syncthreads();
@@ -208,48 +220,62 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      for (int it = 0; it < nkb; ++it) {
-        const int kb = kb_begin + (rot + it) % nkb;
-        if (!mbar_wait(&empty[s], ph ^ 1u, a.err)) break;
-        uint8_t* sa = stage_base + (size_t)s * kStageBytes;
-        if (PAIR) {
-          // this CTA's 128 rows of x and its half of the W tile; the bytes of both CTAs
-          // are counted on the even CTA's barrier, which its MMA lane waits on
-          if (pr == 0) mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
-          const uint32_t fb = dsmem_map(smem_u32(&full[s]), lead_rank);
-          tma_load_2d_pair(sa, &tmap_x, fb, kb * kBK, m0);
-          tma_load_2d_pair(sa + kABytes, &tmap_w, fb, kb * kBK, n0 + pr * kBRows);
-        } else {
-          mbar_arrive_expect_tx(&full[s], kStageBytes);
-          tma_load_2d(sa, &tmap_x, &full[s], kb * kBK, m0);
-          tma_load_2d(sa + kABytes, &tmap_w, &full[s], kb * kBK, n0);
+      bool ok = true;
+      for (int u = g0, k = 0; ok && u < U; u += G, ++k) {
+        int pm_i, nt_i;
+        unit_tile(u, mtp, nt, group_m, pm_i, nt_i);
+        const int m0 = (PAIR ? 2 * pm_i + pr : pm_i) * kBM, n0 = nt_i * BN;
+        // each tile starts its K range at a rotated block (the same for both CTAs of a
+        // pair), so tiles sharing an x or W tile do not request the same lines at once
+        const int rot = (int)((pm_i + nt_i) % (unsigned)nkb);
+        for (int it = 0; it < nkb; ++it) {
+          const int kb = kb_begin + (rot + it) % nkb;
+          if (!mbar_wait(&empty[s], ph ^ 1u, a.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stage_base + (size_t)s * kStageBytes;
+          if (PAIR) {
+            // this CTA's 128 rows of x and its half of the W tile; the bytes of both CTAs
+            // are counted on the even CTA's barrier, which its MMA lane waits on
+            if (pr == 0) mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
+            const uint32_t fb = dsmem_map(smem_u32(&full[s]), lead_rank);
+            tma_load_2d_pair(sa, &tmap_x, fb, kb * kBK, m0);
+            tma_load_2d_pair(sa + kABytes, &tmap_w, fb, kb * kBK, n0 + pr * kBRows);
+          } else {
+            mbar_arrive_expect_tx(&full[s], kStageBytes);
+            tma_load_2d(sa, &tmap_x, &full[s], kb * kBK, m0);
+            tma_load_2d(sa + kABytes, &tmap_w, &full[s], kb * kBK, n0);
+          }
+          if (++s == stages) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
-        if (++s == stages) {
-          s = 0;
-          ph ^= 1u;
-        }
-      }
-      // v mode: the expand blocks follow in the same ring.  The producer claims each
-      // stage in order (a wait on the adjacent phase of empty, as for the base blocks),
-      // loads its B half (the slot's rows of the B expand pool) with TMA and hands the
-      // stage to the epilogue warps for the A half.  Their waits are on xgrant: two grants
-      // of one stage are separated by their own fill, so those waits are on adjacent
-      // phases too.
-      if (a.ex.mode == kExpandV && mbar_wait(xinfo_bar, 0, a.err)) {
+        // v mode: the tile's expand blocks follow in the same ring.  The producer claims
+        // each stage in order (a wait on the adjacent phase of empty, as for the base
+        // blocks), loads its B half (the slot's rows of the B expand pool) with TMA and
+        // hands the stage to the epilogue warps for the A half.  Their waits are on xgrant:
+        // two grants of one stage are separated by their own fill, so those waits are on
+        // adjacent phases too.
+        if (!ok || !vmode) continue;
+        if (!mbar_wait(xinfo_bar, (uint32_t)k & 1u, a.err)) break;
         const int nx = *x_blocks;
         const ExpandLayout xl = expand_layout(a.ex.R);
         for (int e = 0; e < nx; ++e) {
-          if (!mbar_wait(&empty[s], ph ^ 1u, a.err)) break;
-          const int u = e / xl.nbs, b = e - u * xl.nbs;
+          if (!mbar_wait(&empty[s], ph ^ 1u, a.err)) {
+            ok = false;
+            break;
+          }
+          const int uu = e / xl.nbs, b = e - uu * xl.nbs;
           const int col = xl.nbs == 1 ? 0 : (b % (xl.rx / 64)) * 64;
           uint8_t* sa = stage_base + (size_t)s * kStageBytes;
-          const int brow = uslot[u] * a.N + n0 + pr * kBRows;
+          const int brow = uslot[uu] * a.N + n0 + pr * kBRows;
           if (PAIR) {
             if (pr == 0) mbar_arrive_expect_tx(&full[s], 2 * kBBytes);
             tma_load_2d_pair(sa + kABytes, &tmap_bx, dsmem_map(smem_u32(&full[s]), lead_rank),
@@ -276,273 +302,320 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t a_desc0 = smem_desc_sw128(smem_u32(stage_base));
       const uint64_t b_desc0 = smem_desc_sw128(smem_u32(stage_base + kABytes));
       int s = 0;
-      uint32_t ph = 0;
-      for (int it = 0; it < nkb; ++it) {
-        if (!mbar_wait(&full[s], ph, a.err)) break;
-        tc_fence_after();
-        const uint64_t stage_off = (uint64_t)(s * (kStageBytes >> 4));
+      uint32_t ph = 0, xa_par = 0;  // xa_par: bit s = parity of stage s's next xa_full phase
+      bool ok = true;
+      // the 16-wide K chunks of `chunks` (bit kk) of a stage; `first` starts the accumulator
+      auto mma4 = [&](uint32_t d_tmem, int stage, bool first, unsigned chunks) {
+        const uint64_t stage_off = (uint64_t)(stage * (kStageBytes >> 4));
         const uint64_t a_desc = a_desc0 + stage_off, b_desc = b_desc0 + stage_off;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint32_t acc = (it | kk) != 0 ? 1u : 0u;
+          if (!((chunks >> kk) & 1u)) continue;
+          const uint32_t acc = (first && kk == 0) ? 0u : 1u;
           if (PAIR)
-            tc_mma_bf16_pair(tmem_base, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
+            tc_mma_bf16_pair(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
                              idesc, acc);
           else
-            tc_mma_bf16(tmem_base, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
-                        idesc, acc);
+            tc_mma_bf16(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2), idesc,
+                        acc);
         }
         if (PAIR)
-          tc_commit_pair_mc(&empty[s], pair_mask);  // frees the stage in both CTAs
+          tc_commit_pair_mc(&empty[stage], pair_mask);  // frees the stage in both CTAs
         else
-          tc_commit(&empty[s]);
-        if (++s == stages) {
-          s = 0;
-          ph ^= 1u;
-        }
-      }
-      if (a.ex.mode == kExpandV && mbar_wait(xinfo_bar, 0, a.err)) {
-        // the low-rank expand: blocks the epilogue warps write into the same ring
-        const int nx = *x_blocks;
-        for (int e = 0; e < nx; ++e) {
-          // B half (TMA) and A half (written by the epilogue warps)
-          if (!mbar_wait(&full[s], ph, a.err)) break;
-          // pairs: the peer's epilogue wrote its A half, then arrived here across the cluster
-          if (!(PAIR ? mbar_wait_cluster(&xa_full[s], (uint32_t)(e / stages) & 1u, a.err)
-                     : mbar_wait(&xa_full[s], (uint32_t)(e / stages) & 1u, a.err)))
+          tc_commit(&empty[stage]);
+      };
+      for (int u = g0, k = 0; ok && u < U; u += G, ++k) {
+        const int b = k & 1;
+        const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+        // the epilogue has drained this buffer's previous tile (tile k - 2); pairs: both
+        // CTAs' epilogues, the peer's across the cluster
+        if (!(PAIR ? mbar_wait_cluster(&tmem_empty[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, a.err)
+                   : mbar_wait(&tmem_empty[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, a.err)))
+          break;
+        tc_fence_after();
+        for (int it = 0; it < nkb; ++it) {
+          if (!mbar_wait(&full[s], ph, a.err)) {
+            ok = false;
             break;
-          tc_fence_after();
-          const uint64_t stage_off = (uint64_t)(s * (kStageBytes >> 4));
-          const uint64_t a_desc = a_desc0 + stage_off, b_desc = b_desc0 + stage_off;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            if (PAIR)
-              tc_mma_bf16_pair(tmem_base, a_desc + (uint64_t)(kk * 2),
-                               b_desc + (uint64_t)(kk * 2), idesc, 1u);
-            else
-              tc_mma_bf16(tmem_base, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
-                          idesc, 1u);
           }
-          if (PAIR)
-            tc_commit_pair_mc(&empty[s], pair_mask);
-          else
-            tc_commit(&empty[s]);
+          tc_fence_after();
+          mma4(d_tmem, s, it == 0, 0xFu);
           if (++s == stages) {
             s = 0;
             ph ^= 1u;
           }
         }
+        if (ok && vmode && mbar_wait(xinfo_bar, (uint32_t)k & 1u, a.err)) {
+          // the low-rank expand: blocks the epilogue warps write into the same ring; only
+          // the K chunks that hold rank columns are multiplied
+          const int nx = *x_blocks;
+          const ExpandLayout xl = expand_layout(a.ex.R);
+          for (int e = 0; e < nx; ++e) {
+            // B half (TMA) and A half (written by the epilogue warps; pairs: by both CTAs')
+            if (!mbar_wait(&full[s], ph, a.err)) {
+              ok = false;
+              break;
+            }
+            const uint32_t xp = (xa_par >> s) & 1u;
+            xa_par ^= 1u << s;
+            if (!(PAIR ? mbar_wait_cluster(&xa_full[s], xp, a.err)
+                       : mbar_wait(&xa_full[s], xp, a.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            mma4(d_tmem, s, false, expand_chunks(xl, a.ex.R, e % xl.nbs));
+            if (++s == stages) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+        if (PAIR)
+          tc_commit_pair_mc(&tmem_full[b], pair_mask);  // both CTAs' accumulators complete
+        else
+          tc_commit(&tmem_full[b]);
       }
-      if (PAIR)
-        tc_commit_pair_mc(tmem_full, pair_mask);  // both CTAs' accumulators are complete
-      else
-        tc_commit(tmem_full);
     }
     __syncwarp();
-  }
-
-  // ---------------- epilogue warps: row data, then wait for the accumulator ----------------
-  const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32) belong to this warp
-  const int rt = quad * 32 + lane;
-  const int row = m0 + rt;
-  const bool epi = warp >= 2;
-  const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-  if (epi && a.ex.mode == kExpandV) {
-    // ---- v mode: write the low-rank expand as extra K blocks of the ring ----
-    // y_tile += sum over the tile's distinct slots u of [v_u^hi | v_u^lo] [B_u^T ; B_u^T],
-    // where v_u holds the v rows of slot u's rows and zeros elsewhere.  A block's 8 chunks
-    // of 8 K-columns hold, in order, the hi then lo halves of each slot's R rank columns.
+  } else {
+    // ---------------- epilogue warps ----------------
+    const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32) belong to this warp
+    const int rt = quad * 32 + lane;
     const int et = threadIdx.x - 64;  // 0..127
-    griddep_wait();                   // v and the checked slots come from earlier kernels
-    const int srow = m0 + et < a.M ? a.ex.row_slot[m0 + et] : -1;
-    // pairs: both CTAs list the slots of all 256 rows, so they agree on the expand blocks
-    const int pm0 = m0 + (pr == 0 ? kBM : -kBM);  // the peer's first row
-    const int orow = PAIR && pm0 + et < a.M ? a.ex.row_slot[pm0 + et] : -1;
-    slot_bits[et] = 0u;
-    named_barrier(1, 128);
-    if (srow >= 0) atomicOr(&slot_bits[srow >> 5], 1u << (srow & 31));
-    if (orow >= 0) atomicOr(&slot_bits[orow >> 5], 1u << (orow & 31));
-    named_barrier(1, 128);
-    uint32_t word = et < (a.ex.S + 31) / 32 ? slot_bits[et] : 0u;
-    const int cnt = __popc(word);
-    int incl = cnt;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += t;
-    }
-    if (lane == 31) wsum[et >> 5] = incl;
-    named_barrier(1, 128);
-    int pos = incl - cnt, m = 0;
-    for (int i = 0; i < 4; ++i) {
-      if (i < (et >> 5)) pos += wsum[i];
-      m += wsum[i];
-    }
-    while (word) {
-      const int b = __ffs(word) - 1;
-      uslot[pos++] = et * 32 + b;
-      word &= word - 1;
-    }
-    named_barrier(1, 128);
     const ExpandLayout xl = expand_layout(a.ex.R);
-    const int nx = m * xl.nbs;
-    if (et == 0) {
-      *x_blocks = nx;
-      mbar_arrive(xinfo_bar);
-    }
-    // this row's hi and lo halves in the block layout (while the main loop runs)
-    uint8_t* mine = xscr + (size_t)et * xl.nbs * 128;
-    if (srow >= 0) {
-      for (int j0 = 0; j0 < xl.rx; j0 += 8) {
-        uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
-        if (j0 < a.ex.R) v_hi_lo8(a.ex, m0 + et, j0, hi, lo);
-        const int hb = xl.nbs == 1 ? 0 : j0 / 64;                   // block of the hi part
-        const int lb = xl.nbs == 1 ? 0 : xl.rx / 64 + j0 / 64;      // block of the lo part
-        const int off = xl.nbs == 1 ? j0 * 2 : (j0 % 64) * 2;        // byte in the block
-        *reinterpret_cast<uint4*>(mine + hb * 128 + off) = hi;
-        *reinterpret_cast<uint4*>(mine + lb * 128 + off + (xl.nbs == 1 ? 64 : 0)) = lo;
-      }
-    }
-    for (int e = 0; e < nx; ++e) {
-      const int st = (nkb + e) % stages;  // ring position nkb + e, after the base blocks
-      // the e / stages earlier grants of this stage were for this loop's earlier blocks
-      if (!mbar_wait(&xgrant[st], (uint32_t)(e / stages) & 1u, a.err)) break;
-      const int u = e / xl.nbs, b = e - u * xl.nbs;
-      const bool own = uslot[u] == srow;  // rows of other slots contribute zeros
-      uint8_t* sa = stage_base + (size_t)st * kStageBytes;
+    uint32_t gpar = 0;  // bit s = parity of stage s's next xgrant phase
+    int ring = 0;       // ring blocks (base and expand) of this CTA's earlier tiles
+    if (vmode) griddep_wait();  // v and the checked slots come from earlier kernels
+    for (int u = g0, k = 0; u < U; u += G, ++k) {
+      int pm_i, nt_i;
+      unit_tile(u, mtp, nt, group_m, pm_i, nt_i);
+      const int mt_i = PAIR ? 2 * pm_i + pr : pm_i;
+      const int m0 = mt_i * kBM, n0 = nt_i * BN;
+      const int row = m0 + rt;
+      const int b = k & 1;
+      const uint32_t tmem_row =
+          tmem_base + (uint32_t)(b * BN) + (static_cast<uint32_t>(quad * 32) << 16);
+      bool ok = true;
+      if (vmode) {
+        // ---- v mode: write the low-rank expand as extra K blocks of the ring ----
+        // y_tile += sum over the tile's distinct slots u of [v_u^hi | v_u^lo] [B_u^T ; B_u^T],
+        // where v_u holds the v rows of slot u's rows and zeros elsewhere.  A block's 8
+        // chunks of 8 K-columns hold, in order, the hi then lo halves of each slot's R rank
+        // columns.  The previous tile's expand blocks are all consumed (its accumulator was
+        // drained), so uslot, x_blocks and the scratch are free.
+        const int srow = m0 + et < a.M ? a.ex.row_slot[m0 + et] : -1;
+        // pairs: both CTAs list the slots of all 256 rows, so they agree on the expand blocks
+        const int pm0 = m0 + (pr == 0 ? kBM : -kBM);  // the peer's first row
+        const int orow = PAIR && pm0 + et < a.M ? a.ex.row_slot[pm0 + et] : -1;
+        slot_bits[et] = 0u;
+        named_barrier(1, 128);
+        if (srow >= 0) atomicOr(&slot_bits[srow >> 5], 1u << (srow & 31));
+        if (orow >= 0) atomicOr(&slot_bits[orow >> 5], 1u << (orow & 31));
+        named_barrier(1, 128);
+        uint32_t word = et < (a.ex.S + 31) / 32 ? slot_bits[et] : 0u;
+        const int cnt = __popc(word);
+        int incl = cnt;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 val = own ? *reinterpret_cast<const uint4*>(mine + b * 128 + c * 16)
-                              : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sa + et * 128 + ((c ^ (et & 7)) << 4)) = val;
+        for (int d = 1; d < 32; d <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += t;
+        }
+        if (lane == 31) wsum[et >> 5] = incl;
+        named_barrier(1, 128);
+        int pos = incl - cnt, m = 0;
+        for (int i = 0; i < 4; ++i) {
+          if (i < (et >> 5)) pos += wsum[i];
+          m += wsum[i];
+        }
+        while (word) {
+          const int bit = __ffs(word) - 1;
+          uslot[pos++] = et * 32 + bit;
+          word &= word - 1;
+        }
+        named_barrier(1, 128);
+        const int nx = m * xl.nbs;
+        if (et == 0) {
+          *x_blocks = nx;
+          mbar_arrive(xinfo_bar);
+        }
+        // this row's hi and lo halves in the block layout (while the main loop runs)
+        uint8_t* mine = xscr + (size_t)et * xl.nbs * 128;
+        if (srow >= 0) {
+          for (int j0 = 0; j0 < xl.rx; j0 += 8) {
+            uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
+            if (j0 < a.ex.R) v_hi_lo8(a.ex, m0 + et, j0, hi, lo);
+            const int hb = xl.nbs == 1 ? 0 : j0 / 64;                // block of the hi part
+            const int lb = xl.nbs == 1 ? 0 : xl.rx / 64 + j0 / 64;   // block of the lo part
+            const int off = xl.nbs == 1 ? j0 * 2 : (j0 % 64) * 2;     // byte in the block
+            *reinterpret_cast<uint4*>(mine + hb * 128 + off) = hi;
+            *reinterpret_cast<uint4*>(mine + lb * 128 + off + (xl.nbs == 1 ? 64 : 0)) = lo;
+          }
+        }
+        for (int e = 0; e < nx; ++e) {
+          const int st = (ring + nkb + e) % stages;  // after the tile's base blocks
+          const uint32_t gp = (gpar >> st) & 1u;
+          gpar ^= 1u << st;
+          if (!mbar_wait(&xgrant[st], gp, a.err)) {
+            ok = false;
+            break;
+          }
+          const int uu = e / xl.nbs, blk = e - uu * xl.nbs;
+          const bool own = uslot[uu] == srow;  // rows of other slots contribute zeros
+          uint8_t* sa = stage_base + (size_t)st * kStageBytes;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 val = own ? *reinterpret_cast<const uint4*>(mine + blk * 128 + c * 16)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sa + et * 128 + ((c ^ (et & 7)) << 4)) = val;
+          }
+          fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async-proxy reads
+          named_barrier(1, 128);
+          if (et == 0) {
+            if (PAIR && pr != 0)
+              mbar_arrive_remote(dsmem_map(smem_u32(&xa_full[st]), lead_rank));
+            else
+              mbar_arrive(&xa_full[st]);
+          }
+        }
+        ring += nkb + nx;
       }
-      fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async-proxy reads
+      const bool full_ok = ok && mbar_wait(&tmem_full[b], (uint32_t)(k >> 1) & 1u, a.err);
+      // a split K (one tile per CTA) must still meet its cluster barrier below, whatever
+      // the error (the flag is set); otherwise stop here
+      if (!full_ok && cs == 1) break;
+      tc_fence_after();
+
+      // ---------------- split K: exchange partial accumulators through L2 ----------------
+      // (delta mode, one tile per CTA.)  Scratch of this output block: [d][z] blocks (CTA
+      // z's partial of CTA d's columns) of [bnc / 4][128 rows] float4, rows fastest, so a
+      // warp's 32 rows move 512 contiguous bytes.
+      const int nq = bnc / 4;
+      const float4* xk_in = nullptr;  // the cs blocks addressed to this CTA: [q][nq][128]
+      if (cs > 1) {
+        float4* xk_tile =
+            reinterpret_cast<float4*>(a.xk) + (size_t)(mt_i * nt + nt_i) * cs * cs * nq * kBM;
+        xk_in = xk_tile + (size_t)z * cs * nq * kBM + rt;
+        for (int d = 0; d < cs; ++d) {
+          if (d == z) continue;
+          float4* blk = xk_tile + (size_t)(d * cs + z) * nq * kBM + rt;
+          for (int c = 0; c < bnc; c += 32) {
+            uint32_t raw[32];
+            tmem_ld_32x32b_x32(tmem_row + d * bnc + c, raw);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              __stcg(blk + (size_t)((c >> 2) + i) * kBM,
+                     make_float4(__uint_as_float(raw[4 * i]), __uint_as_float(raw[4 * i + 1]),
+                                 __uint_as_float(raw[4 * i + 2]),
+                                 __uint_as_float(raw[4 * i + 3])));
+          }
+        }
+        // release / acquire across the cluster: every block addressed to this CTA is
+        // written (the producer and MMA warps, done with their single tile, arrive at the
+        // matching barrier after their loops)
+        tc_fence_before();
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        tc_fence_after();
+      }
+
+      // ---------------- the epilogue's inputs, landed in shared memory ----------------
+      // (delta mode, one tile per CTA: the ring is idle once the accumulator is complete.)
+      // xin: the cs - 1 partial blocks addressed to this CTA ([j][bnc / 4][128 rows] float4,
+      // as in the scratch); dsm: the tile's delta rows ([128][bnc] fp32, 16-byte chunks
+      // XOR-swizzled by row & 7).  Both arrive by cp.async and are waited for once, so
+      // their latencies overlap instead of following one another chunk by chunk.
+      float4* xin = reinterpret_cast<float4*>(stage_base);
+      float* dsm = reinterpret_cast<float*>(stage_base + (size_t)(cs - 1) * nq * kBM * 16);
+      if (cs > 1) {
+        for (int q = 0, j = 0; q < cs; ++q) {
+          if (q == z) continue;
+          const float4* src = xk_in + (size_t)q * nq * kBM;
+          float4* dst = xin + (size_t)j * nq * kBM + rt;
+          for (int c4 = 0; c4 < nq; ++c4)
+            cp_async_16(dst + (size_t)c4 * kBM, src + (size_t)c4 * kBM);
+          ++j;
+        }
+      }
+      bool add_delta = false;  // delta mode: the row adds the low-rank term of the delta buffer
+      if (!vmode) {
+        // only now the low-rank kernel's results are needed: the main loop and the split-K
+        // exchange ran while it was still working
+        griddep_wait();
+        if (row < a.M) {
+          const int t = a.ex.token_slot[row];
+          add_delta = t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0;
+          // one CTA per row block reports ids outside [-1, S) or naming empty slots
+          if (nt_i == 0 && z == 0) {
+            if (t < -1 || t >= a.ex.S) atomicOr(a.err, LORA_ERRF_BAD_ID);
+            else if (t >= 0 && !add_delta) atomicOr(a.err, LORA_ERRF_EMPTY_SLOT);
+          }
+        }
+        // the tile's delta rows (the buffer holds the batch's rows, at most 512):
+        // consecutive threads fetch consecutive 16-byte chunks of a row
+        const int cfirst = n0 + z * bnc;  // first column this CTA finishes
+        for (int idx = et; idx < kBM * nq; idx += 128) {
+          const int r = idx / nq, ch = idx - r * nq;
+          const int gr = m0 + r, gc = cfirst + ch * 4;
+          if (gr < a.M && gc < a.N)
+            cp_async_16(dsm + (size_t)r * bnc + ((ch ^ (r & 7)) << 2),
+                        a.ex.delta + (size_t)gr * a.N + gc);
+        }
+      }
+      if (cs > 1 || !vmode) {
+        cp_async_wait_all();
+        named_barrier(1, 128);  // delta rows fetched by the other epilogue threads
+      }
+      __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.y) + (size_t)row * a.N;
+      const int cbase = z * bnc;  // first accumulator column this CTA finishes
+      const float* drow = dsm + (size_t)rt * bnc;
+#pragma unroll 1
+      for (int c = 0; c < bnc; c += 32) {
+        const int nc = n0 + cbase + c;
+        uint32_t raw[32];
+        tmem_ld_32x32b_x32(tmem_row + cbase + c, raw);
+        tmem_ld_wait();
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(raw[i]);
+        for (int j = 0; j < cs - 1; ++j) {
+          const float4* blk = xin + (size_t)j * nq * kBM + rt;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 v = blk[(size_t)((c >> 2) + i) * kBM];
+            acc[i * 4 + 0] += v.x;
+            acc[i * 4 + 1] += v.y;
+            acc[i * 4 + 2] += v.z;
+            acc[i * 4 + 3] += v.w;
+          }
+        }
+        float4 d[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          d[q] = add_delta
+                     ? *reinterpret_cast<const float4*>(drow + ((((c >> 2) + q) ^ (rt & 7)) << 2))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        epilogue_chunk32(acc, a, row, nc, add_delta, d, yrow);
+      }
+      // this buffer is drained: the MMAs may fill it with tile k + 2 (pairs: both CTAs'
+      // epilogues arrive on the even CTA's barrier)
+      tc_fence_before();
       named_barrier(1, 128);
       if (et == 0) {
         if (PAIR && pr != 0)
-          mbar_arrive_remote(dsmem_map(smem_u32(&xa_full[st]), lead_rank));
+          mbar_arrive_remote(dsmem_map(smem_u32(&tmem_empty[b]), lead_rank));
         else
-          mbar_arrive(&xa_full[st]);
+          mbar_arrive(&tmem_empty[b]);
       }
-    }
-  }
-  if (epi) {
-    mbar_wait(tmem_full, 0, a.err);
-    tc_fence_after();
-  }
-
-  // ---------------- split K: exchange partial accumulators through L2 ----------------
-  // scratch of this output block: [d][z] blocks (CTA z's partial of CTA d's columns) of
-  // [bnc / 4][128 rows] float4, rows fastest, so a warp's 32 rows move 512 contiguous bytes
-  const int nq = bnc / 4;
-  const float4* xk_in = nullptr;  // the cs blocks addressed to this CTA: [q][nq][128]
-  if (cs > 1) {
-    float4* xk_tile = reinterpret_cast<float4*>(a.xk) +
-                      (size_t)(mt_i * (int)gridDim.y + nt_i) * cs * cs * nq * kBM;
-    xk_in = xk_tile + (size_t)z * cs * nq * kBM + rt;
-    if (epi) {
-      for (int d = 0; d < cs; ++d) {
-        if (d == z) continue;
-        float4* blk = xk_tile + (size_t)(d * cs + z) * nq * kBM + rt;
-        for (int c = 0; c < bnc; c += 32) {
-          uint32_t raw[32];
-          tmem_ld_32x32b_x32(tmem_row + d * bnc + c, raw);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            __stcg(blk + (size_t)((c >> 2) + i) * kBM,
-                   make_float4(__uint_as_float(raw[4 * i]), __uint_as_float(raw[4 * i + 1]),
-                               __uint_as_float(raw[4 * i + 2]), __uint_as_float(raw[4 * i + 3])));
-        }
-      }
-    }
-    tc_fence_before();
-    cluster_sync_all();  // release / acquire: every block addressed to this CTA is written
-    tc_fence_after();
-  }
-
-  // ---------------- the epilogue's inputs, landed in shared memory ----------------
-  // The ring is idle once the accumulator is complete.  xin: the cs - 1 partial blocks
-  // addressed to this CTA ([j][bnc / 4][128 rows] float4, as in the scratch); dsm: the
-  // tile's delta rows ([128][bnc] fp32, 16-byte chunks XOR-swizzled by row & 7).  Both
-  // arrive by cp.async and are waited for once, so their latencies overlap instead of
-  // following one another chunk by chunk.
-  const bool delta_mode = a.ex.mode == kExpandDelta;
-  float4* xin = reinterpret_cast<float4*>(stage_base);
-  float* dsm = reinterpret_cast<float*>(stage_base + (size_t)(cs - 1) * nq * kBM * 16);
-  if (epi && cs > 1) {
-    for (int q = 0, j = 0; q < cs; ++q) {
-      if (q == z) continue;
-      const float4* src = xk_in + (size_t)q * nq * kBM;
-      float4* dst = xin + (size_t)j * nq * kBM + rt;
-      for (int c4 = 0; c4 < nq; ++c4) cp_async_16(dst + (size_t)c4 * kBM, src + (size_t)c4 * kBM);
-      ++j;
-    }
-  }
-  bool add_delta = false;  // delta mode: the row adds the low-rank term of the delta buffer
-  if (epi && delta_mode) {
-    // only now the low-rank kernel's results are needed: the main loop and the split-K
-    // exchange ran while it was still working
-    griddep_wait();
-    if (row < a.M) {
-      const int t = a.ex.token_slot[row];
-      add_delta = t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0;
-      // one CTA per row block reports ids outside [-1, S) or naming empty slots
-      if (nt_i == 0 && z == 0) {
-        if (t < -1 || t >= a.ex.S) atomicOr(a.err, LORA_ERRF_BAD_ID);
-        else if (t >= 0 && !add_delta) atomicOr(a.err, LORA_ERRF_EMPTY_SLOT);
-      }
-    }
-    // the tile's delta rows (the buffer holds the batch's rows, at most 512): consecutive
-    // threads fetch consecutive 16-byte chunks of a row
-    const int et = threadIdx.x - 64;
-    const int cfirst = n0 + z * bnc;  // first column this CTA finishes
-    for (int idx = et; idx < kBM * nq; idx += 128) {
-      const int r = idx / nq, ch = idx - r * nq;
-      const int gr = m0 + r, gc = cfirst + ch * 4;
-      if (gr < a.M && gc < a.N)
-        cp_async_16(dsm + (size_t)r * bnc + ((ch ^ (r & 7)) << 2),
-                    a.ex.delta + (size_t)gr * a.N + gc);
-    }
-  }
-  if (epi && (cs > 1 || delta_mode)) {
-    cp_async_wait_all();
-    named_barrier(1, 128);  // delta rows fetched by the other epilogue threads
-  }
-  if (epi) {
-    __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.y) + (size_t)row * a.N;
-    const int cbase = z * bnc;  // first accumulator column this CTA finishes
-    const float* drow = dsm + (size_t)rt * bnc;
-#pragma unroll 1
-    for (int c = 0; c < bnc; c += 32) {
-      const int nc = n0 + cbase + c;
-      uint32_t raw[32];
-      tmem_ld_32x32b_x32(tmem_row + cbase + c, raw);
-      tmem_ld_wait();
-      float acc[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(raw[i]);
-      for (int j = 0; j < cs - 1; ++j) {
-        const float4* blk = xin + (size_t)j * nq * kBM + rt;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 v = blk[(size_t)((c >> 2) + i) * kBM];
-          acc[i * 4 + 0] += v.x;
-          acc[i * 4 + 1] += v.y;
-          acc[i * 4 + 2] += v.z;
-          acc[i * 4 + 3] += v.w;
-        }
-      }
-      float4 d[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        d[q] = add_delta
-                   ? *reinterpret_cast<const float4*>(drow + ((((c >> 2) + q) ^ (rt & 7)) << 2))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      epilogue_chunk32(acc, a, row, nc, add_delta, d, yrow);
     }
   }
 
+  // split K: the producer and MMA warps meet the epilogue warps' cluster barrier
+  if (cs > 1 && warp < 2) {
+    cluster_arrive_release();
+    cluster_wait_acquire();
+  }
   tc_fence_before();
   __syncthreads();
   // pairs: the peer is done with this CTA's TMEM, shared memory and barriers
@@ -550,9 +623,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     if (PAIR)
-      tmem_dealloc_pair(tmem_base, BN);
+      tmem_dealloc_pair(tmem_base, 2 * BN);
     else
-      tmem_dealloc(tmem_base, BN);
+      tmem_dealloc(tmem_base, 2 * BN);
   }
 }
 
@@ -585,13 +658,20 @@ cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Raise (never lower) one kernel variant's dynamic shared-memory limit: one cache per
+// variant, shared by every caller.
+template <int BN, bool PAIR>
+static cudaError_t raise_smem_limit(int bytes) {
+  static int limit = 0;
+  return ensure_smem_limit(gemm_tc_kernel<BN, PAIR>, bytes, &limit);
+}
+
 // CTAs of this GEMM that can be resident at once in clusters of `csize` CTAs (every variant
 // holds one CTA per SM; a cluster must fit in one GPC, whose sizes differ).  Queried once.
 static int resident_ctas(int csize, int num_sms) {
   static int cache[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
   if (csize < 1 || csize > 8) return 0;
   if (cache[csize] == 0) {
-    static int limit = 0;
     const int smem = 200 * 1024;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -605,7 +685,7 @@ static int resident_ctas(int csize, int num_sms) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (ensure_smem_limit(gemm_tc_kernel<256, false>, smem, &limit) == cudaSuccess &&
+    if (raise_smem_limit<256, false>(smem) == cudaSuccess &&
         cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<256, false>, &cfg) == cudaSuccess &&
         n > 0) {
       cache[csize] = std::min(num_sms, n * csize);
@@ -618,13 +698,18 @@ static int resident_ctas(int csize, int num_sms) {
 }
 
 // Tile shape, K split and CTA pairs, by least estimated time (cycles).  Measured on this
-// kernel: a 64-wide K block costs ~550 cycles whatever the tile (4 MMA instructions at
-// ~124 cycles each below N = 256, 128 at N = 256, plus ~50 of barrier hand-off), unless
-// its operands arrive slower than ~100 B per cycle per SM; CTA pairs halve the W rows a
-// CTA loads.  Each wave adds ~3k cycles of prologue, pipeline fill and epilogue; a split
-// K adds the exchange of fp32 partials through L2 (written and read at ~50 B per cycle per
-// SM).  Large problems (no split allowed) weigh the same costs without the split.
-GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split) {
+// kernel: a 64-wide K block costs its 4 MMA instructions (~124 cycles each below N = 256,
+// 128 at N = 256) plus ~50 cycles of barrier hand-off, or its operand delivery at ~75 B
+// per cycle per SM when that is slower (a 128 x 256 tile's 48 KB per block; a CTA pair
+// halves the W rows each CTA loads, which made 256 x 256 pair tiles ~15% faster per block
+// than 128 x 256 single-CTA tiles).  Each wave adds ~3k cycles of prologue, pipeline fill
+// and epilogue; a split K adds the exchange of fp32 partials through L2 (written and read
+// at ~50 B per cycle per SM).  Large problems (no split allowed) weigh the same costs
+// without the split; their expand blocks (one per distinct slot of a tile) are not in
+// the estimate, but a pair runs the expand blocks of all its 256 rows on both CTAs, which
+// doubles them where slots change every few rows: pairs are taken there only when the
+// batch averages at least 128 rows per slot (`slots` = the layer's slot count, 0 = none).
+GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split, int slots) {
   const int mt = (M + kBM - 1) / kBM;
   const int nkb = (K + kBK - 1) / kBK;
   // every one of the cs K ranges of ceil(nkb / cs) blocks must be non-empty
@@ -632,15 +717,15 @@ GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split) {
   GemmPlan p{64, 1, 0};
   double best = 1e30;
   const int cand[3] = {256, 128, 64};
-  // single CTAs first: a pair is taken only where it is estimated faster (its epilogue ends
-  // on a cluster barrier, ~1 us slower per tile)
+  // single CTAs first: a pair is taken only where it is estimated faster
   for (int pair = 0; pair <= 1; ++pair) {
     if (pair && mt < 2) continue;  // a pair over one row tile would leave a CTA idle
+    if (pair && !allow_split && slots > 0 && (long long)M < 128LL * slots) continue;
     for (int i = 0; i < 3; ++i) {
       const int bn = cand[i];
       if (pair && bn < 128) continue;
       const double bytes = kABytes + (double)(pair ? bn / 2 : bn) * kBK * 2;
-      const double per_kb = std::max(bytes / 100.0, 4.0 * std::max(124.0, 0.5 * bn)) + 50.0;
+      const double per_kb = std::max(bytes / 75.0, 4.0 * std::max(124.0, 0.5 * bn)) + 50.0;
       const int ctas_m = pair ? 2 * ((mt + 1) / 2) : mt;
       const int tiles = ctas_m * ((N + bn - 1) / bn);
       // each CTA finishes bn / cs >= 32 columns (its epilogue and the split-K exchange work
@@ -676,7 +761,7 @@ static size_t exchange_floats(const GemmPlan& p, int M, int N) {
 }
 
 size_t gemm_tc_exchange_floats(int M, int N, int K, int num_sms) {
-  return exchange_floats(gemm_tc_plan(M, N, K, num_sms, true), M, N);
+  return exchange_floats(gemm_tc_plan(M, N, K, num_sms, true, 0), M, N);
 }
 
 size_t gemm_tc_plan_exchange_floats(const GemmPlan& p, int M, int N) {
@@ -687,7 +772,7 @@ int gemm_tc_tile_index(int BN) { return BN == 256 ? 0 : (BN == 128 ? 1 : 2); }
 
 static size_t tc_smem_bytes(int BN, bool pair, int stages, int xscr_bytes) {
   const size_t stage = (size_t)kABytes + (size_t)(pair ? BN / 2 : BN) * kBK * 2;
-  return 1024 + stages * stage + xscr_bytes + (2 * kBM + 6) * 4 + (4 * stages + 3) * 8;
+  return 1024 + stages * stage + xscr_bytes + (2 * kBM + 6) * 4 + (4 * stages + 6) * 8;
 }
 
 template <int BN, bool PAIR>
@@ -712,8 +797,7 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   const size_t stage = (size_t)kABytes + (size_t)(PAIR ? BN / 2 : BN) * kBK * 2;
   if ((cs > 1 || a.ex.mode == kExpandDelta) && (size_t)stages * stage < (size_t)kBM * BN * 4)
     return cudaErrorInvalidConfiguration;
-  static int limit = 0;
-  cudaError_t e = ensure_smem_limit(gemm_tc_kernel<BN, PAIR>, (int)smem, &limit);
+  cudaError_t e = raise_smem_limit<BN, PAIR>((int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -723,10 +807,18 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   attr[1].val.clusterDim.x = PAIR ? 2 : 1;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = cs;
-  // pairs: an even number of row tiles (a last CTA past M loads zeros and stores nothing)
+  // work units: (row tile, or pair of row tiles; column tile).  v mode: a persistent grid
+  // of at most the resident CTAs (pairs), each running units round-robin; delta mode (its
+  // epilogue reuses the idle ring): one unit per CTA.  A pair's last CTA may lie past M: it
+  // loads zeros and stores nothing.
   const int mt = (a.M + kBM - 1) / kBM;
-  const int mtp = PAIR ? (mt + 1) / 2 : mt;  // row tiles, or pairs of them
-  cfg.gridDim = dim3(PAIR ? 2 * mtp : mt, (a.N + BN - 1) / BN, cs);
+  const int mtp = PAIR ? (mt + 1) / 2 : mt;
+  const int nt = (a.N + BN - 1) / BN;
+  const int units = mtp * nt;
+  const int csize = (PAIR ? 2 : 1) * cs;
+  int G = units;
+  if (a.ex.mode == kExpandV) G = std::max(1, std::min(units, resident_ctas(csize, a.num_sms) / csize));
+  cfg.gridDim = dim3((PAIR ? 2 : 1) * G, 1, cs);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -737,13 +829,14 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   const int group_m =
       std::max(1, std::min(mtp, (int)((32u << 20) / ((size_t)a.K * band_rows * 2))));
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, PAIR>, tmap_x, tmap_w, tmap_bx, a, stages,
-                            xscr, group_m);
+                            xscr, group_m, mtp, nt);
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
                            const CUtensorMap* tmap_bx3, cudaStream_t stream) {
   if (a.ex.mode == kExpandV && !tmap_bx3) return cudaErrorInvalidValue;
-  GemmPlan plan = gemm_tc_plan(a.M, a.N, a.K, a.num_sms, a.ex.mode != kExpandV);
+  GemmPlan plan = gemm_tc_plan(a.M, a.N, a.K, a.num_sms, a.ex.mode != kExpandV,
+                               a.ex.mode == kExpandV ? a.ex.S : 0);
   if (a.force_bn != 0) {
     // v mode never splits K: its expand blocks run after the base ones in one accumulator
     plan = GemmPlan{a.force_bn, a.ex.mode == kExpandV ? 1 : a.force_cs, a.force_pair};

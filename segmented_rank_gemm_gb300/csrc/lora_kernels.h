@@ -128,6 +128,14 @@ __host__ __device__ inline ExpandLayout expand_layout(int R) {
   const int rx = R <= 64 ? 64 : 128;
   return ExpandLayout{rx, 2 * rx / 64, rx};
 }
+// The 16-column K chunks of a slot's expand block b (0 <= b < nbs) that hold rank columns
+// (bit kk set); the others are padding, zero in both halves of the product.
+__host__ __device__ inline unsigned expand_chunks(const ExpandLayout& xl, int R, int b) {
+  if (xl.nbs == 1) return R > 16 ? 0xFu : 0x5u;  // hi in columns [0, R), lo in [32, 32 + R)
+  const int sub = b % (xl.rx / 64);
+  const int real = R - 64 * sub < 64 ? R - 64 * sub : 64;
+  return (1u << ((real + 15) / 16)) - 1u;
+}
 
 // ---- base GEMM with the low-rank term added in its epilogue ----
 // kExpandV: y += [v^hi | v^lo] [B^T ; B^T] as extra tensor-core K blocks (large batches).
@@ -173,7 +181,7 @@ struct GemmPlan {
   int ksplit;   // K ranges per output tile, 1..4
   int pair;     // 1: CTA pairs (cta_group::2 MMAs, 256-row tiles, N tile 256 or 128)
 };
-GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split);
+GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split, int slots);
 // Floats of split-K exchange scratch the tcgen05 GEMM needs for an M-row batch with the
 // K split allowed (0 when its plan does not split K).
 size_t gemm_tc_exchange_floats(int M, int N, int K, int num_sms);
