@@ -507,12 +507,18 @@ __global__ void __maxnreg__(120)
   __shared__ float v_s[kStrGroup][32];
   constexpr int kIds = kSlotMaxT / kStrThreads;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (S + kStrThreads - 1) / kStrThreads;  // consecutive slots per thread
+  const int q_begin = min(S, tid * per), q_end = min(S, q_begin + per);
+  // the ids and this thread's slots' loaded flags are requested together (one round trip)
   int ids[kIds];
 #pragma unroll
   for (int u = 0; u < kIds; ++u) {
     const int i = tid * kIds + u;
     ids[u] = i < T ? token_slot[i] : -1;
   }
+  uint32_t loaded_bits = 0;  // bit q - q_begin: slot q holds an adapter (per <= 32)
+  for (int q = q_begin; q < q_end; ++q)
+    loaded_bits |= (loaded[q] != 0 ? 1u : 0u) << (q - q_begin);
   // ---- the item list: rows per slot, then groups per loaded slot, exclusive scan ----
   for (int q = tid; q <= S; q += kStrThreads) grp_off[q] = 0;
   __syncthreads();
@@ -520,11 +526,10 @@ __global__ void __maxnreg__(120)
   for (int u = 0; u < kIds; ++u)
     if (ids[u] >= 0 && ids[u] < S) atomicAdd(&grp_off[ids[u]], 1);
   __syncthreads();
-  const int per = (S + kStrThreads - 1) / kStrThreads;  // consecutive slots per thread
-  const int q_begin = min(S, tid * per), q_end = min(S, q_begin + per);
   int mine = 0;
   for (int q = q_begin; q < q_end; ++q) {
-    const int g = loaded[q] != 0 ? (grp_off[q] + kStrGroup - 1) / kStrGroup : 0;
+    const int g = (loaded_bits >> (q - q_begin)) & 1u ? (grp_off[q] + kStrGroup - 1) / kStrGroup
+                                                      : 0;
     grp_off[q] = g;
     mine += g;
   }
@@ -549,7 +554,6 @@ __global__ void __maxnreg__(120)
   if (tid == 0) grp_off[S] = n_items;
   __syncthreads();
 
-  const int kv = K / 8, nv = N / 8;  // 16-byte chunks of a row of x / 8-column chunks of N
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     // the item's slot: the last s with grp_off[s] <= it
     int lo = 0, hi = S - 1;
@@ -559,15 +563,21 @@ __global__ void __maxnreg__(120)
       else hi = mid - 1;
     }
     const int s = lo, g0 = (it - grp_off[s]) * kStrGroup;  // first row (in slot order)
-    // every 16-byte chunk of A_s and B_s this thread will read, requested into L2 now: the
-    // DRAM round trips overlap the row scan below, and the loads after it hit L2
-    const int rs = min(R, RMAX);
-    for (int e = tid; e < kv; e += kStrThreads)
-      for (int j = 0; j < rs; ++j)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(At_pool + ((size_t)s * R + j) * K + e * 8));
-    for (int e = tid; e < nv; e += kStrThreads)
-      for (int j = 0; j < rs; ++j)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(B_pool + ((size_t)s * R + j) * N + e * 8));
+    const int r = rank[s];  // requested now, needed after the row scan
+    const float sc = scale[s];
+    // the slot's A and B rows (two contiguous ranges) requested into L2 now, in 32 KB bulk
+    // prefetches from the lanes of warp 0: the DRAM round trips overlap the row scan
+    // below, and the loads after it hit L2
+    if (warp == 0) {
+      const int rs = min(r, min(R, RMAX));
+      const size_t a_bytes = (size_t)rs * K * 2, b_bytes = (size_t)rs * N * 2;
+      const char* a0 = reinterpret_cast<const char*>(At_pool + (size_t)s * R * K);
+      const char* b0 = reinterpret_cast<const char*>(B_pool + (size_t)s * R * N);
+      for (size_t off = (size_t)lane << 15; off < a_bytes; off += (size_t)32 << 15)
+        bulk_prefetch_l2(a0 + off, (uint32_t)min(a_bytes - off, (size_t)1 << 15));
+      for (size_t off = (size_t)lane << 15; off < b_bytes; off += (size_t)32 << 15)
+        bulk_prefetch_l2(b0 + off, (uint32_t)min(b_bytes - off, (size_t)1 << 15));
+    }
     // ---- the slot's rows g0 .. g0 + kStrGroup - 1, in row order ----
     int cnt = 0;
 #pragma unroll
@@ -593,8 +603,6 @@ __global__ void __maxnreg__(120)
       }
     __syncthreads();
     const int ng = min(kStrGroup, nrows - g0);
-    const int r = rank[s];
-    const float sc = scale[s];
     const __nv_bfloat16* At = At_pool + (size_t)s * R * K;
     const __nv_bfloat16* Bs = B_pool + (size_t)s * R * N;
     // shrink: v_s[0 .. ng), ROWS rows a pass (the last pass may take one)
