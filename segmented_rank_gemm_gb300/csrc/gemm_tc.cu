@@ -128,15 +128,42 @@ __device__ __forceinline__ void unit_tile(int u, int mtp, int nt, int group_m, i
   ntile = w / gm;
 }
 
-// Registers capped at 136: two warps of this kernel and two of the decode BGMV kernel
-// (120 registers) share each of an SM's four 16K-register files, so the two kernels run
-// side by side.
-template <int BN, bool PAIR>
-__global__ void __maxnreg__(136)
+// The work of CTA (pair) slot g of G: `full_rounds` whole tiles (units g, g + G, ...; fewer
+// where they run past U), then -- stream-K, when the units leave a last round of at most
+// half the slots busy -- those remaining tiles cut in two: slot g < sk_slots takes half
+// g & 1 of tile full_rounds G + g / 2, the head (K blocks from 0, and the tile's expand
+// blocks) on the even slot, which finishes the tile, the tail on the odd one, written as
+// an fp32 partial.  Both are their slot's last segment.  Segment k of slot g: unit u, K
+// blocks [k0, k1); false past the last one.
+__device__ __forceinline__ bool seg_at(int k, int g, int G, int U, int nkb, int full_rounds,
+                                       int sk_slots, int& u, int& k0, int& k1) {
+  const int nfull = min(full_rounds, (U - g + G - 1) / G);  // whole units g + j G < U
+  if (k < nfull) {
+    u = g + k * G;
+    k0 = 0;
+    k1 = nkb;
+    return true;
+  }
+  if (k > nfull || g >= sk_slots) return false;
+  u = full_rounds * G + (g >> 1);
+  const int half = nkb >> 1;  // the host splits only K ranges of >= 2 blocks
+  k0 = (g & 1) ? half : 0;
+  k1 = (g & 1) ? nkb : half;
+  return true;
+}
+
+// Delta mode (decode) caps registers at 136: two warps of this kernel and two of the
+// decode BGMV kernel (120 registers) share each of an SM's four 16K-register files, so the
+// two kernels run side by side.  VMODE is a template parameter so that the delta-mode
+// variants carry none of the expand-block and stream-K code; the v-mode variants share
+// their SMs with no other kernel and get more registers.
+template <int BN, bool PAIR, bool VMODE>
+__global__ void __maxnreg__(VMODE ? 168 : 136)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_bx, GemmArgs a, int stages,
-                   int xscr_bytes, int group_m, int mtp, int nt) {
+                   int xscr_bytes, int group_m, int mtp, int nt, int full_rounds,
+                   int sk_slots) {
   constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of the W (or B expand) tile this CTA loads
   constexpr int kBBytes = kBRows * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
@@ -182,7 +209,7 @@ __global__ void __maxnreg__(136)
   const int kb_begin = z * per;
   const int nkb = min(nkb_all, kb_begin + per) - kb_begin;
   const int bnc = BN / cs;  // columns this CTA finishes
-  const bool vmode = a.ex.mode == kExpandV;
+  constexpr bool vmode = VMODE;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -226,15 +253,20 @@ __global__ void __maxnreg__(136)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int u = g0, k = 0; ok && u < U; u += G, ++k) {
+      int hk = 0;  // head segments so far (v mode: one xinfo phase each)
+      for (int k = 0; ok; ++k) {
+        int u, k0, k1;
+        if (!seg_at(k, g0, G, U, nkb, full_rounds, sk_slots, u, k0, k1)) break;
         int pm_i, nt_i;
         unit_tile(u, mtp, nt, group_m, pm_i, nt_i);
         const int m0 = (PAIR ? 2 * pm_i + pr : pm_i) * kBM, n0 = nt_i * BN;
-        // each tile starts its K range at a rotated block (the same for both CTAs of a
-        // pair), so tiles sharing an x or W tile do not request the same lines at once
-        const int rot = (int)((pm_i + nt_i) % (unsigned)nkb);
-        for (int it = 0; it < nkb; ++it) {
-          const int kb = kb_begin + (rot + it) % nkb;
+        // a whole tile starts its K range at a rotated block (the same for both CTAs of a
+        // pair), so tiles sharing an x or W tile do not request the same lines at once;
+        // stream-K pieces run in order
+        const int nk = k1 - k0;
+        const int rot = nk == nkb ? (int)((pm_i + nt_i) % (unsigned)nkb) : 0;
+        for (int it = 0; it < nk; ++it) {
+          const int kb = kb_begin + k0 + (rot + it) % nk;
           if (!mbar_wait(&empty[s], ph ^ 1u, a.err)) {
             ok = false;
             break;
@@ -263,8 +295,9 @@ __global__ void __maxnreg__(136)
         // hands the stage to the epilogue warps for the A half.  Their waits are on xgrant:
         // two grants of one stage are separated by their own fill, so those waits are on
         // adjacent phases too.
-        if (!ok || !vmode) continue;
-        if (!mbar_wait(xinfo_bar, (uint32_t)k & 1u, a.err)) break;
+        if (!ok || !vmode || k0 != 0) continue;  // expand blocks go with a tile's head
+        if (!mbar_wait(xinfo_bar, (uint32_t)hk & 1u, a.err)) break;
+        ++hk;
         const int nx = *x_blocks;
         const ExpandLayout xl = expand_layout(a.ex.R);
         for (int e = 0; e < nx; ++e) {
@@ -324,7 +357,10 @@ __global__ void __maxnreg__(136)
         else
           tc_commit(&empty[stage]);
       };
-      for (int u = g0, k = 0; ok && u < U; u += G, ++k) {
+      int hk = 0;  // head segments so far (v mode: one xinfo phase each)
+      for (int k = 0; ok; ++k) {
+        int u, k0, k1;
+        if (!seg_at(k, g0, G, U, nkb, full_rounds, sk_slots, u, k0, k1)) break;
         const int b = k & 1;
         const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
         // the epilogue has drained this buffer's previous tile (tile k - 2); pairs: both
@@ -333,7 +369,7 @@ __global__ void __maxnreg__(136)
                    : mbar_wait(&tmem_empty[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, a.err)))
           break;
         tc_fence_after();
-        for (int it = 0; it < nkb; ++it) {
+        for (int it = 0; it < k1 - k0; ++it) {
           if (!mbar_wait(&full[s], ph, a.err)) {
             ok = false;
             break;
@@ -345,7 +381,9 @@ __global__ void __maxnreg__(136)
             ph ^= 1u;
           }
         }
-        if (ok && vmode && mbar_wait(xinfo_bar, (uint32_t)k & 1u, a.err)) {
+        const bool head = k0 == 0;
+        if (ok && vmode && head && !mbar_wait(xinfo_bar, (uint32_t)hk & 1u, a.err)) ok = false;
+        if (ok && vmode && head) {
           // the low-rank expand: blocks the epilogue warps write into the same ring; only
           // the K chunks that hold rank columns are multiplied
           const int nx = *x_blocks;
@@ -371,6 +409,7 @@ __global__ void __maxnreg__(136)
             }
           }
         }
+        if (vmode && head) ++hk;
         if (PAIR)
           tc_commit_pair_mc(&tmem_full[b], pair_mask);  // both CTAs' accumulators complete
         else
@@ -387,7 +426,15 @@ __global__ void __maxnreg__(136)
     uint32_t gpar = 0;  // bit s = parity of stage s's next xgrant phase
     int ring = 0;       // ring blocks (base and expand) of this CTA's earlier tiles
     if (vmode) griddep_wait();  // v and the checked slots come from earlier kernels
-    for (int u = g0, k = 0; u < U; u += G, ++k) {
+    // stream-K: flags carry the launch's epoch + 1 (the epoch advances when the last CTA of a
+    // launch exits, so no flag of an earlier launch matches)
+    const int32_t epoch =
+        VMODE && sk_slots > 0 ? *reinterpret_cast<volatile int32_t*>(a.sk_sync) : 0;
+    for (int k = 0;; ++k) {
+      int u, k0, k1;
+      if (!seg_at(k, g0, G, U, nkb, full_rounds, sk_slots, u, k0, k1)) break;
+      const bool head = k0 == 0;
+      const int nk = k1 - k0;
       int pm_i, nt_i;
       unit_tile(u, mtp, nt, group_m, pm_i, nt_i);
       const int mt_i = PAIR ? 2 * pm_i + pr : pm_i;
@@ -397,7 +444,7 @@ __global__ void __maxnreg__(136)
       const uint32_t tmem_row =
           tmem_base + (uint32_t)(b * BN) + (static_cast<uint32_t>(quad * 32) << 16);
       bool ok = true;
-      if (vmode) {
+      if (vmode && head) {
         // ---- v mode: write the low-rank expand as extra K blocks of the ring ----
         // y_tile += sum over the tile's distinct slots u of [v_u^hi | v_u^lo] [B_u^T ; B_u^T],
         // where v_u holds the v rows of slot u's rows and zeros elsewhere.  A block's 8
@@ -453,7 +500,7 @@ __global__ void __maxnreg__(136)
           }
         }
         for (int e = 0; e < nx; ++e) {
-          const int st = (ring + nkb + e) % stages;  // after the tile's base blocks
+          const int st = (ring + nk + e) % stages;  // after the tile's base blocks
           const uint32_t gp = (gpar >> st) & 1u;
           gpar ^= 1u << st;
           if (!mbar_wait(&xgrant[st], gp, a.err)) {
@@ -478,13 +525,44 @@ __global__ void __maxnreg__(136)
               mbar_arrive(&xa_full[st]);
           }
         }
-        ring += nkb + nx;
+        ring += nx;
       }
+      ring += nk;
       const bool full_ok = ok && mbar_wait(&tmem_full[b], (uint32_t)(k >> 1) & 1u, a.err);
       // a split K (one tile per CTA) must still meet its cluster barrier below, whatever
       // the error (the flag is set); otherwise stop here
       if (!full_ok && cs == 1) break;
       tc_fence_after();
+      if (VMODE && !head) {
+        // ---- stream-K tail: its fp32 partial, for the slot that finishes the tile ----
+        float4* part = reinterpret_cast<float4*>(a.sk_part) + (size_t)blockIdx.x * (BN / 4) * kBM + rt;
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(tmem_row + c, raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            __stcg(part + (size_t)((c >> 2) + i) * kBM,
+                   make_float4(__uint_as_float(raw[4 * i]), __uint_as_float(raw[4 * i + 1]),
+                               __uint_as_float(raw[4 * i + 2]), __uint_as_float(raw[4 * i + 3])));
+        }
+        __threadfence();  // the partial is visible device-wide before the flag
+        tc_fence_before();
+        named_barrier(1, 128);
+        if (et == 0) {
+          st_release_gpu(a.sk_sync + 2 + blockIdx.x, epoch + 1);
+          if (PAIR && pr != 0)
+            mbar_arrive_remote(dsmem_map(smem_u32(&tmem_empty[b]), lead_rank));
+          else
+            mbar_arrive(&tmem_empty[b]);
+        }
+        continue;
+      }
+      // stream-K head of a split tile: its tail's partial (slot g0 + 1) is added below
+      const int sk_src = VMODE && nk < nkb ? (PAIR ? 2 * (g0 + 1) + pr : g0 + 1) : -1;
+      if (sk_src >= 0 && et == 0 &&
+          !wait_flag_gpu(a.sk_sync + 2 + sk_src, epoch + 1, a.err))
+        ok = false;
 
       // ---------------- split K: exchange partial accumulators through L2 ----------------
       // (delta mode, one tile per CTA.)  Scratch of this output block: [d][z] blocks (CTA
@@ -526,6 +604,9 @@ __global__ void __maxnreg__(136)
       // as in the scratch); dsm: the tile's delta rows ([128][bnc] fp32, 16-byte chunks
       // XOR-swizzled by row & 7).  Both arrive by cp.async and are waited for once, so
       // their latencies overlap instead of following one another chunk by chunk.
+      // (A stream-K head is its slot's last segment, so the ring is idle for it too: its
+      // tail's partial lands there the same way, as the one extra block.)
+      const int n_extra = cs > 1 ? cs - 1 : (sk_src >= 0 ? 1 : 0);
       float4* xin = reinterpret_cast<float4*>(stage_base);
       float* dsm = reinterpret_cast<float*>(stage_base + (size_t)(cs - 1) * nq * kBM * 16);
       if (cs > 1) {
@@ -537,6 +618,11 @@ __global__ void __maxnreg__(136)
             cp_async_16(dst + (size_t)c4 * kBM, src + (size_t)c4 * kBM);
           ++j;
         }
+      } else if (sk_src >= 0) {
+        named_barrier(1, 128);  // the flag was seen by thread 0 of the epilogue
+        const float4* src = reinterpret_cast<const float4*>(a.sk_part) +
+                            (size_t)sk_src * (BN / 4) * kBM + rt;
+        for (int c4 = 0; c4 < nq; ++c4) cp_async_16(xin + (size_t)c4 * kBM + rt, src + (size_t)c4 * kBM);
       }
       bool add_delta = false;  // delta mode: the row adds the low-rank term of the delta buffer
       if (!vmode) {
@@ -563,7 +649,7 @@ __global__ void __maxnreg__(136)
                         a.ex.delta + (size_t)gr * a.N + gc);
         }
       }
-      if (cs > 1 || !vmode) {
+      if (n_extra > 0 || !vmode) {
         cp_async_wait_all();
         named_barrier(1, 128);  // delta rows fetched by the other epilogue threads
       }
@@ -579,7 +665,7 @@ __global__ void __maxnreg__(136)
         float acc[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(raw[i]);
-        for (int j = 0; j < cs - 1; ++j) {
+        for (int j = 0; j < n_extra; ++j) {
           const float4* blk = xin + (size_t)j * nq * kBM + rt;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -618,6 +704,15 @@ __global__ void __maxnreg__(136)
   }
   tc_fence_before();
   __syncthreads();
+  // stream-K: the last CTA to leave advances the epoch (every CTA read it at its start)
+  if (VMODE && sk_slots > 0 && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.sk_sync + 1, 1) == (int)(gridDim.x * gridDim.z) - 1) {
+      atomicExch(a.sk_sync + 1, 0);
+      __threadfence();
+      atomicAdd(a.sk_sync, 1);
+    }
+  }
   // pairs: the peer is done with this CTA's TMEM, shared memory and barriers
   if (PAIR) cluster_sync_all();
   if (warp == 1) {
@@ -660,10 +755,10 @@ cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K
 
 // Raise (never lower) one kernel variant's dynamic shared-memory limit: one cache per
 // variant, shared by every caller.
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, bool VMODE>
 static cudaError_t raise_smem_limit(int bytes) {
   static int limit = 0;
-  return ensure_smem_limit(gemm_tc_kernel<BN, PAIR>, bytes, &limit);
+  return ensure_smem_limit(gemm_tc_kernel<BN, PAIR, VMODE>, bytes, &limit);
 }
 
 // CTAs of this GEMM that can be resident at once in clusters of `csize` CTAs (every variant
@@ -685,8 +780,9 @@ static int resident_ctas(int csize, int num_sms) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (raise_smem_limit<256, false>(smem) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<256, false>, &cfg) == cudaSuccess &&
+    if (raise_smem_limit<256, false, true>(smem) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<256, false, true>, &cfg) ==
+            cudaSuccess &&
         n > 0) {
       cache[csize] = std::min(num_sms, n * csize);
     } else {
@@ -775,7 +871,7 @@ static size_t tc_smem_bytes(int BN, bool pair, int stages, int xscr_bytes) {
   return 1024 + stages * stage + xscr_bytes + (2 * kBM + 6) * 4 + (4 * stages + 6) * 8;
 }
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, bool VMODE>
 static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUtensorMap& tmap_x,
                              const CUtensorMap& tmap_w, const CUtensorMap& tmap_bx,
                              cudaStream_t stream) {
@@ -795,9 +891,10 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   if (smem > budget) return cudaErrorInvalidConfiguration;
   // the epilogue lands its split-K partials and delta rows (128 x BN fp32) in the ring
   const size_t stage = (size_t)kABytes + (size_t)(PAIR ? BN / 2 : BN) * kBK * 2;
-  if ((cs > 1 || a.ex.mode == kExpandDelta) && (size_t)stages * stage < (size_t)kBM * BN * 4)
+  if ((cs > 1 || a.ex.mode == kExpandDelta || a.sk_part) &&
+      (size_t)stages * stage < (size_t)kBM * BN * 4)
     return cudaErrorInvalidConfiguration;
-  cudaError_t e = raise_smem_limit<BN, PAIR>((int)smem);
+  cudaError_t e = raise_smem_limit<BN, PAIR, VMODE>((int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -818,6 +915,16 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   const int csize = (PAIR ? 2 : 1) * cs;
   int G = units;
   if (a.ex.mode == kExpandV) G = std::max(1, std::min(units, resident_ctas(csize, a.num_sms) / csize));
+  // stream-K: when the units leave a last round of at most half the slots busy, those
+  // tiles are cut in two (head and tail on two slots) instead
+  int full_rounds = (units + G - 1) / G, sk_slots = 0;
+  if (a.ex.mode == kExpandV && a.sk_part && a.sk_sync && units > G && (a.K + kBK - 1) / kBK >= 2) {
+    const int rem = units % G;
+    if (rem > 0 && 2 * rem <= G) {
+      full_rounds = units / G;
+      sk_slots = 2 * rem;
+    }
+  }
   cfg.gridDim = dim3((PAIR ? 2 : 1) * G, 1, cs);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
@@ -828,8 +935,25 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   const size_t band_rows = (size_t)kBM * (PAIR ? 2 : 1);
   const int group_m =
       std::max(1, std::min(mtp, (int)((32u << 20) / ((size_t)a.K * band_rows * 2))));
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, PAIR>, tmap_x, tmap_w, tmap_bx, a, stages,
-                            xscr, group_m, mtp, nt);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, PAIR, VMODE>, tmap_x, tmap_w, tmap_bx, a,
+                            stages,
+                            xscr, group_m, mtp, nt, full_rounds, sk_slots);
+}
+
+template <bool VMODE>
+static cudaError_t launch_variant(const GemmArgs& a, const GemmPlan& plan,
+                                  const CUtensorMap& tmap_x, const CUtensorMap& tw,
+                                  const CUtensorMap& tb, cudaStream_t stream) {
+  if (plan.pair) {
+    if (plan.block_n == 256) return launch_tc<256, true, VMODE>(a, plan, tmap_x, tw, tb, stream);
+    if (plan.block_n == 128) return launch_tc<128, true, VMODE>(a, plan, tmap_x, tw, tb, stream);
+    return cudaErrorInvalidConfiguration;
+  }
+  switch (plan.block_n) {
+    case 256: return launch_tc<256, false, VMODE>(a, plan, tmap_x, tw, tb, stream);
+    case 128: return launch_tc<128, false, VMODE>(a, plan, tmap_x, tw, tb, stream);
+    default: return launch_tc<64, false, VMODE>(a, plan, tmap_x, tw, tb, stream);
+  }
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
@@ -850,16 +974,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
   const int ti = gemm_tc_tile_index(plan.pair ? plan.block_n / 2 : plan.block_n);
   const CUtensorMap& tw = tmap_w3[ti];
   const CUtensorMap& tb = tmap_bx3 ? tmap_bx3[ti] : tw;  // unused in delta mode
-  if (plan.pair) {
-    if (plan.block_n == 256) return launch_tc<256, true>(a, plan, tmap_x, tw, tb, stream);
-    if (plan.block_n == 128) return launch_tc<128, true>(a, plan, tmap_x, tw, tb, stream);
-    return cudaErrorInvalidConfiguration;
-  }
-  switch (plan.block_n) {
-    case 256: return launch_tc<256, false>(a, plan, tmap_x, tw, tb, stream);
-    case 128: return launch_tc<128, false>(a, plan, tmap_x, tw, tb, stream);
-    default: return launch_tc<64, false>(a, plan, tmap_x, tw, tb, stream);
-  }
+  return a.ex.mode == kExpandV ? launch_variant<true>(a, plan, tmap_x, tw, tb, stream)
+                                : launch_variant<false>(a, plan, tmap_x, tw, tb, stream);
 }
 
 }  // namespace lora

@@ -356,6 +356,33 @@ __device__ __forceinline__ void bulk_commit_group() {
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// A flag word in global memory, released / acquired at GPU scope.
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int32_t v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Wait until *p == v.  Bounded like the mbarrier waits: false (and the timeout flag) after
+// LORA_WAIT_TIMEOUT_NS.
+__device__ __forceinline__ bool wait_flag_gpu(const int32_t* p, int32_t v, int32_t* err) {
+  if (ld_acquire_gpu(p) == v) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i) {
+      if (ld_acquire_gpu(p) == v) return true;
+      __nanosleep(64);
+    }
+    if (globaltimer_ns() - t0 > LORA_WAIT_TIMEOUT_NS) {
+      if (err) atomicOr(err, LORA_ERRF_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Request [p, p + bytes) into L2 without waiting (p and bytes multiples of 16).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),

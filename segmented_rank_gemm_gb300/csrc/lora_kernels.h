@@ -166,6 +166,10 @@ struct GemmArgs {
   float* xk;         // split K: scratch for the exchanged fp32 partials (L2-resident)
   size_t xk_floats;  // its capacity (gemm_tc_exchange_floats of the batch)
   int force_bn, force_cs, force_pair;  // tcgen05 tiling fixed by the caller (force_bn 0: auto)
+  // stream-K (large batches): fp32 partial per CTA [num_sms][128][256] and sync words
+  // {epoch, exit count, flag per CTA} (zeroed at allocation); null: no stream-K
+  float* sk_part;
+  int32_t* sk_sync;
 };
 // tcgen05 / TMEM / TMA kernel (gemm_tc.cu).  tmap_w3 holds the layer's cached maps of the
 // packed weight for N tiles of 256, 128 and 64 rows (in that order); tmap_bx3 the maps of

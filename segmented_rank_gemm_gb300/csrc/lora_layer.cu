@@ -64,6 +64,8 @@ struct lora_layer {
   int v_planes = 1;              // K-split partial planes of v (bf16: tensor-core shrink)
   float* delta = nullptr;        // [min(T_max, kDeltaMaxT)][N] fp32 (delta mode, bf16)
   float* xk = nullptr;           // split-K exchange scratch of the base GEMM (delta mode)
+  float* sk_part = nullptr;      // stream-K partials of the base GEMM (v mode)
+  int32_t* sk_sync = nullptr;    // stream-K epoch, exit count and flags (zeroed)
   size_t xk_floats = 0;
   GemmPlan gemm_plan{0, 0, 0};   // fixed by lora_set_gemm_plan (block_n 0: automatic)
   int max_tiles = 0;
@@ -118,8 +120,8 @@ cudaError_t dmalloc(T** p, size_t count) {
 void free_all(lora_layer* L) {
   void* ptrs[] = {L->Wp, L->A_pool, L->B_pool, L->Bx_pool, L->A_stage, L->scale, L->rank, L->loaded,
                   L->row_slot, L->perm, L->seg_offsets, L->seg_slot, L->tile_seg,
-                  L->tile_row0, L->meta, L->err, L->v, L->delta, L->xk, L->x_stage,
-                  L->ids_stage, L->y_stage};
+                  L->tile_row0, L->meta, L->err, L->v, L->delta, L->xk, L->sk_part,
+                  L->sk_sync, L->x_stage, L->ids_stage, L->y_stage};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (L->stage_free) cudaEventDestroy(L->stage_free);
@@ -213,6 +215,10 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
             (dtype != LORA_BF16 ||
              dmalloc(&L->delta, (size_t)std::min(max_tokens, kDeltaMaxT) * N) == cudaSuccess) &&
             (L->xk_floats == 0 || dmalloc(&L->xk, L->xk_floats) == cudaSuccess) &&
+            // v-mode batches (bf16, more than 512 rows) may cut the last tiles in two
+            (dtype != LORA_BF16 || max_tokens <= kDeltaMaxT ||
+             (dmalloc(&L->sk_part, (size_t)L->num_sms * 128 * 256) == cudaSuccess &&
+              dmalloc(&L->sk_sync, (size_t)L->num_sms + 2) == cudaSuccess)) &&
             cudaMalloc(&L->x_stage, (size_t)max_tokens * K * es) == cudaSuccess &&
             dmalloc(&L->ids_stage, max_tokens) == cudaSuccess &&
             cudaMalloc(&L->y_stage, (size_t)max_tokens * N * es) == cudaSuccess &&
@@ -237,7 +243,9 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
        cudaMemsetAsync(L->loaded, 0, S * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->meta, 0, 32, stream) == cudaSuccess &&
        cudaMemsetAsync(L->err, 0, 4, stream) == cudaSuccess &&
-       cudaMemsetAsync(L->v, 0, (size_t)L->v_planes * max_tokens * R * 4, stream) == cudaSuccess;
+       cudaMemsetAsync(L->v, 0, (size_t)L->v_planes * max_tokens * R * 4, stream) == cudaSuccess &&
+       (!L->sk_sync ||
+        cudaMemsetAsync(L->sk_sync, 0, ((size_t)L->num_sms + 2) * 4, stream) == cudaSuccess);
   if (!ok) return bail(LORA_ECUDA);
 
   if (dtype == LORA_BF16) {
@@ -487,6 +495,8 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.num_sms = L->num_sms;
   ga.xk = L->xk;
   ga.xk_floats = L->xk_floats;
+  ga.sk_part = L->sk_part;
+  ga.sk_sync = L->sk_sync;
   ga.force_bn = L->gemm_plan.block_n;
   ga.force_cs = L->gemm_plan.ksplit;
   ga.force_pair = L->gemm_plan.pair;

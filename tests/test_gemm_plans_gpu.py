@@ -56,6 +56,16 @@ def test_v_mode_every_plan():
     _sweep(wl, V_PLANS)
 
 
+def test_v_mode_stream_k_tail():
+    # more tiles than resident CTAs (pairs), with a short last round: on 152 SMs every
+    # tiling below leaves 12 to 64 tiles over, which are cut in two (head and tail on two
+    # CTAs, the tail added to the head's accumulator as an fp32 partial); 17 K blocks give
+    # halves of 8 and 9
+    wl = workloads.synthetic(4106, 2600, 1032, 2048, S=24, ranks=16, R=16, base_frac=0.1,
+                             layout="runs")
+    _sweep(wl, [(256, 1, 0), (128, 1, 0), (64, 1, 0), (256, 1, 1), (128, 1, 1)])
+
+
 def test_v_mode_wide_rank_pairs():
     # rank 64: two expand blocks per slot (hi and lo halves in separate blocks)
     wl = workloads.synthetic(4104, 900, 384, 512, S=10, ranks=[64, 40, 8, 64, 17, 64, 1, 33, 64, 2],
