@@ -462,15 +462,25 @@ def run_ours(args):
                 layers[i].forward_host(x_h[i], ids_h[i], y_h[i], stream)
         stream.synchronize()
         n_e2e = args.steps
+        # consecutive steps go to several streams (instance j always to stream j % n, so
+        # each layer object and its staging stay on one stream), as a serving loop would
+        # issue them: steps' host copies overlap other steps' kernels
+        n_st = max(1, min(args.e2e_streams, len(layers)))
+        streams = (stream,) + tuple(torch.cuda.Stream(device=dev) for _ in range(n_st - 1))
         barrier(world)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        with torch.cuda.stream(stream):
-            for i in range(n_e2e):
-                j = i % len(layers)
-                layers[j].forward_host(x_h[j], ids_h[j], y_h[j], stream)
+        for s_k in streams[1:]:
+            s_k.wait_event(e0)
+        for i in range(n_e2e):
+            j = i % len(layers)
+            s_j = streams[j % n_st]
+            with torch.cuda.stream(s_j):
+                layers[j].forward_host(x_h[j], ids_h[j], y_h[j], s_j)
+        for s_k in streams[1:]:
+            stream.wait_stream(s_k)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -479,6 +489,7 @@ def run_ours(args):
         e2e = {"value": aggregate(T, n_e2e, world, e_sec), "unit": UNIT,
                "h2d_bytes_per_step": T * K * es + T * 4, "d2h_bytes_per_step": T * N * es,
                "ms_per_step": e_sec * 1e3 / n_e2e,
+               "streams": n_st,
                "path": "lora_forward_host: pinned x/ids H2D, %s, y D2H" % (
                    "BGMV, GEMM" if work["mode"] == "delta" else "builder, SGMV shrink, GEMM")}
 
@@ -626,6 +637,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=4,
+                    help="streams the end-to-end steps rotate over (instance j on stream j %% n)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
