@@ -500,6 +500,18 @@ __global__ void __maxnreg__(120)
   // main loop reads x, which that kernel may have written)
   griddep_wait();
   griddep_launch_dependents();
+  // With at most one slot per CTA, CTA b requests slot b's A and B rows into L2 right away,
+  // before the ids are read: the DRAM traffic of every slot then overlaps the item-list
+  // setup below (the items' own prefetches find the lines present or in flight).
+  if (S <= (int)gridDim.x && (int)blockIdx.x < S && threadIdx.x < 32) {
+    const int rs = min(R, RMAX);
+    const size_t a_bytes = (size_t)rs * K * 2, b_bytes = (size_t)rs * N * 2;
+    const char* a0 = reinterpret_cast<const char*>(At_pool + (size_t)blockIdx.x * R * K);
+    const char* b0 = reinterpret_cast<const char*>(B_pool + (size_t)blockIdx.x * R * N);
+    const size_t off = (size_t)threadIdx.x << 15;
+    if (off < a_bytes) bulk_prefetch_l2(a0 + off, (uint32_t)min(a_bytes - off, (size_t)1 << 15));
+    if (off < b_bytes) bulk_prefetch_l2(b0 + off, (uint32_t)min(b_bytes - off, (size_t)1 << 15));
+  }
   extern __shared__ int grp_off[];  // [S + 1]: rows per slot, then first item of each slot
   __shared__ int rows_s[kStrGroup];
   __shared__ int warp_cnt[kStrThreads / 32];
