@@ -152,6 +152,33 @@ def test_host_buffer_entry_point():
     layer.close()
 
 
+def test_host_entry_point_concurrent_streams():
+    # four layers on four streams, each called several times in turn (as a serving loop
+    # rotating independent batches over streams): every call's copies and kernels overlap
+    # other layers' work, and every result must still be its own
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    cases = []
+    for i, (T, mode_rows) in enumerate([(200, 8), (700, 16), (64, 8), (1100, 16)]):
+        wl = workloads.synthetic(320 + i, T, 264, 392, S=6, ranks=mode_rows, R=16,
+                                 base_frac=0.1, layout="runs" if T > 512 else "random")
+        layer = build_layer(wl)
+        x_h = wl.x.clone().pin_memory()
+        ids_h = wl.token_slot.clone().pin_memory()
+        outs = [torch.empty(wl.T, wl.N, dtype=BF16).pin_memory() for _ in range(3)]
+        cases.append((wl, layer, x_h, ids_h, outs))
+    for rep in range(3):
+        for (wl, layer, x_h, ids_h, outs), st in zip(cases, streams):
+            with torch.cuda.stream(st):
+                layer.forward_host(x_h, ids_h, outs[rep], st)
+    torch.cuda.synchronize()
+    for wl, layer, x_h, ids_h, outs in cases:
+        assert layer.status() == 0
+        ref = oracle_rows(wl)
+        for y_h in outs:
+            assert_parity(y_h, ref, BF16, what="concurrent host entry T=%d" % wl.T)
+        layer.close()
+
+
 def test_argument_errors():
     from segmented_rank_gemm_gb300.lora import LoraError, LoraLayer
     wl = workloads.synthetic(310, 64, 64, 64, S=2, ranks=4, R=4)
