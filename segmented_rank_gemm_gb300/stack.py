@@ -8,7 +8,8 @@ k, v and u are computed (and kept) but do not feed forward: the projection shape
 its adapter slot through the whole stack.
 
 Orchestration only: every projection is one ``set_batch_segments`` + ``lora_forward`` of the
-C ABI; ``capture`` records the whole pass in one CUDA graph.
+C ABI; k, v and u run on a side stream beside the chain; ``capture`` records the whole pass
+(both streams) in one CUDA graph.
 """
 from __future__ import annotations
 
@@ -44,15 +45,51 @@ class LoraStack:
         K = {"h": 4096, "q": 4096, "k": 1024, "v": 1024, "o": 4096, "g": 14336, "u": 14336}
         self.buf = {n: torch.empty(T, k, dtype=torch.bfloat16, device=self.device)
                     for n, k in K.items()}
+        self.side = torch.cuda.Stream(device=self.device)
         self.graph = None
 
-    def step(self, stream=None):
-        """One chained pass: h <- h0, then every projection of every layer in order."""
-        self.buf["h"].copy_(self.h0)
+    def _run(self, layer, src, dst, stream):
+        layer.set_batch(self.ids, stream)
+        layer.forward(self.buf[src], self.buf[dst], stream)
+
+    def step(self, stream=None, concurrent=True):
+        """One chained pass: h <- h0, then every projection of every layer.
+
+        The projections whose outputs do not feed forward (k, v, u) run on a side stream,
+        beside the chain q -> o -> gate -> down on `stream`; events order the buffers they
+        share: k and v read this layer's h before down overwrites it, u reads o before the
+        next layer's o overwrites it.  The side stream joins `stream` at the end."""
+        stream = stream or torch.cuda.current_stream(self.device)
+        side = self.side if concurrent else stream  # concurrent=False: one stream, in order
+        with torch.cuda.stream(stream):
+            self.buf["h"].copy_(self.h0)
+        e_h = torch.cuda.Event()
+        e_h.record(stream)
+        e_u = None
         for row in self.layers:
-            for layer, (src, dst) in zip(row, CHAIN):
-                layer.set_batch(self.ids, stream)
-                layer.forward(self.buf[src], self.buf[dst], stream)
+            p_q, p_k, p_v, p_o, p_g, p_u, p_d = row
+            side.wait_event(e_h)                      # this layer's h is written
+            self._run(p_k, "h", "k", side)
+            self._run(p_v, "h", "v", side)
+            e_v = torch.cuda.Event()
+            e_v.record(side)
+            self._run(p_q, "h", "q", stream)
+            if e_u is not None:
+                stream.wait_event(e_u)                # the previous layer's u has read o
+            self._run(p_o, "q", "o", stream)
+            e_o = torch.cuda.Event()
+            e_o.record(stream)
+            side.wait_event(e_o)
+            self._run(p_u, "o", "u", side)
+            e_u = torch.cuda.Event()
+            e_u.record(side)
+            self._run(p_g, "o", "g", stream)
+            stream.wait_event(e_v)                    # k and v have read h
+            self._run(p_d, "g", "h", stream)
+            e_h = torch.cuda.Event()
+            e_h.record(stream)
+        if e_u is not None:
+            stream.wait_event(e_u)
         return self.buf["h"]
 
     def capture(self, stream):
