@@ -6,15 +6,24 @@
 // term differs by adapter.  "Serving LoRA adapters ..." (vLLM) Step 4: the expand multiplies
 // the fp32 rank buffer by B and adds it to the base output.
 //
-// One CTA computes a 128 x BN block of y over a range of K blocks (6 warps):
+// A CTA computes 128 x BN blocks of y (6 warps):
 //   warp 0      TMA producer: 64-wide K blocks of x [M,K] and of the packed weight W^T [N,K]
 //               (both K-major, 128-byte swizzle) into a ring of shared-memory stages.
-//   warp 1      allocates BN TMEM columns; one lane issues tcgen05.mma (M=128, N=BN, K=16,
-//               bf16 x bf16 -> fp32 in TMEM) and frees each stage with tcgen05.commit.
+//   warp 1      allocates 2 x BN TMEM columns (two accumulators); one lane issues
+//               tcgen05.mma (M=128, N=BN, K=16, bf16 x bf16 -> fp32 in TMEM) and frees each
+//               stage with tcgen05.commit.
 //   warps 2..5  epilogue: each thread owns one output row (one TMEM lane); it reads the
 //               accumulator 32 columns at a time (tcgen05.ld) and rounds to bf16 once.
 //               In delta mode it first adds the fp32 delta[row, n] the BGMV kernel
 //               expanded (rows with slot -1 store the base product only).
+// Large batches (v mode) run a persistent grid of at most the resident CTAs (pairs): each
+// walks its tiles round-robin in bands of row tiles (a wave then shares one band of x in
+// L2), the MMAs filling one accumulator while the epilogue drains the other.  When the
+// last round would keep at most half of them busy, its tiles are cut in two (stream-K):
+// one CTA takes the head K blocks and the tile's expand blocks and finishes the tile, the
+// next the tail, handed over as an fp32 partial through L2 with a flag tagged by a
+// per-launch epoch.  Small batches (delta mode) run one tile per CTA.  The mode is a
+// template parameter, so the delta-mode variants carry none of the v-mode code.
 // v mode (the expand on the tensor cores): while the main loop runs, the epilogue warps list
 // the tile's distinct slots u (ascending) and then write extra K blocks into the same ring,
 // after the base blocks: y_tile += sum_u [V_u^hi | V_u^lo] [B_u^T ; B_u^T], where V_u is v
@@ -38,7 +47,7 @@
 // A pair thereby moves the same operand bytes per SM as a 128 x BN/2 tile while every MMA
 // instruction does the work of a 128 x BN one (the issue rate, ~124 cycles per instruction
 // however narrow, bounds tiles below 256 columns).
-// Each CTA starts its K range at a rotated K block (and wraps around), so the CTAs that
+// A whole tile starts its K range at a rotated K block (and wraps around), so the CTAs that
 // share an x tile or a W tile do not all request the same lines from L2 at the same moment.
 // Launch: programmatic dependent launch after the low-rank kernel: the main loop and the
 // split-K exchange read only x, W and the accumulators, so they run while the low-rank
