@@ -495,17 +495,21 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
           *x_blocks = nx;
           mbar_arrive(xinfo_bar);
         }
-        // this row's hi and lo halves in the block layout (while the main loop runs)
+        // this row's hi and lo halves in the block layout (while the main loop runs), their
+        // 16-byte chunks already XOR-swizzled by row & 7 as in the ring, so the copy below
+        // moves chunk p to chunk p and neither side has bank conflicts
         uint8_t* mine = xscr + (size_t)et * xl.nbs * 128;
+        const int sw = et & 7;
         if (srow >= 0) {
           for (int j0 = 0; j0 < xl.rx; j0 += 8) {
             uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
             if (j0 < a.ex.R) v_hi_lo8(a.ex, m0 + et, j0, hi, lo);
             const int hb = xl.nbs == 1 ? 0 : j0 / 64;                // block of the hi part
             const int lb = xl.nbs == 1 ? 0 : xl.rx / 64 + j0 / 64;   // block of the lo part
-            const int off = xl.nbs == 1 ? j0 * 2 : (j0 % 64) * 2;     // byte in the block
-            *reinterpret_cast<uint4*>(mine + hb * 128 + off) = hi;
-            *reinterpret_cast<uint4*>(mine + lb * 128 + off + (xl.nbs == 1 ? 64 : 0)) = lo;
+            const int hc = xl.nbs == 1 ? j0 / 8 : (j0 % 64) / 8;     // chunk in the block
+            const int lc = hc + (xl.nbs == 1 ? 4 : 0);
+            *reinterpret_cast<uint4*>(mine + hb * 128 + ((hc ^ sw) << 4)) = hi;
+            *reinterpret_cast<uint4*>(mine + lb * 128 + ((lc ^ sw) << 4)) = lo;
           }
         }
         for (int e = 0; e < nx; ++e) {
@@ -521,9 +525,10 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
           uint8_t* sa = stage_base + (size_t)st * kStageBytes;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint4 val = own ? *reinterpret_cast<const uint4*>(mine + blk * 128 + c * 16)
+            const int p = (c ^ sw) << 4;  // the 8 rows of a quarter-warp cover all banks
+            const uint4 val = own ? *reinterpret_cast<const uint4*>(mine + blk * 128 + p)
                                   : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(sa + et * 128 + ((c ^ (et & 7)) << 4)) = val;
+            *reinterpret_cast<uint4*>(sa + et * 128 + p) = val;
           }
           fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async-proxy reads
           named_barrier(1, 128);
