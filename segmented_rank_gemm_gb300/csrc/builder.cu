@@ -18,8 +18,11 @@
 //                                           window_groups of its segments (tile_seg)
 //   meta = {n_seg, T_a, n_tiles}
 // Method (a counting sort that needs no atomics, so the order is unique):
+//   0. The slots' loaded flags are staged in shared memory.
 //   1. W "walker" warps each own a contiguous range of rows and count, per slot, the rows
-//      of their range (warp match_any groups equal slots within 32 rows).
+//      of their range (warp match_any groups equal slots within 32 rows).  A walker reads
+//      the ids of up to kWalkBatch x 32 rows in one batch and keeps their checked slots in
+//      registers for step 3, so its loads are not one dependent round trip per 32 rows.
 //   2. Per slot, an exclusive prefix over the walkers, then one block-wide exclusive scan
 //      over slots gives each slot's segment start, segment index and first tile.
 //   3. Each walker re-walks its range in row order and scatters row indices to
@@ -30,6 +33,7 @@
 namespace lora {
 
 static constexpr int kBuilderThreads = 1024;
+static constexpr int kWalkBatch = 8;  // 32-row groups a walker loads (and keeps) at once
 // windows per thread in window mode: 1024 * 8 windows of 128 rows cover 2^20 rows
 static constexpr int kMaxWinPerThread = 8;
 
@@ -63,6 +67,7 @@ __global__ void __launch_bounds__(kBuilderThreads, 1)
   extern __shared__ int32_t sm[];
   int32_t* hist = sm;                      // [n_walk][S]: counts, then cursors
   int32_t* total = sm + (size_t)n_walk * S;  // [S]
+  int32_t* loaded_s = total + S;             // [S]
   __shared__ Scan3 warp_tot[32];
   __shared__ Scan3 grand;
 
@@ -73,35 +78,57 @@ __global__ void __launch_bounds__(kBuilderThreads, 1)
   griddep_launch_dependents();
 
   for (int i = tid; i < n_walk * S; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
+  for (int q = tid; q < S; q += blockDim.x) loaded_s[q] = loaded[q];
 
   // rows [w*chunk, min(T, (w+1)*chunk)) belong to walker w
   const int chunk = (T + n_walk - 1) / n_walk;
   const int r_begin = warp * chunk;
   const int r_end = min(T, r_begin + chunk);
+  // a walker whose range fits one batch keeps its rows' checked slots for step 3
+  const bool kept = r_end - r_begin <= 32 * kWalkBatch;
+  int slot_kept[kWalkBatch];
+  // the first batch of ids is requested before the barrier, alongside the flags
+  int raw_b[kWalkBatch];
+#pragma unroll
+  for (int u = 0; u < kWalkBatch; ++u) {
+    const int i = r_begin + u * 32 + lane;
+    raw_b[u] = warp < n_walk && i < r_end ? token_slot[i] : -1;
+  }
+  __syncthreads();
 
   // ---- 1. validate ids and count per (walker, slot) ----
   if (warp < n_walk) {
     int32_t* my_hist = hist + (size_t)warp * S;
-    for (int base = r_begin; base < r_end; base += 32) {
-      const int i = base + lane;
-      const bool valid = i < r_end;
-      int s = -1;
-      if (valid) {
-        const int raw = token_slot[i];
-        if (raw < -1 || raw >= S) {
-          atomicOr(err, LORA_ERRF_BAD_ID);
-        } else if (raw >= 0 && loaded[raw] == 0) {
-          atomicOr(err, LORA_ERRF_EMPTY_SLOT);
-        } else {
-          s = raw;
+    for (int b0 = r_begin; b0 < r_end; b0 += 32 * kWalkBatch) {
+      if (b0 != r_begin) {
+#pragma unroll
+        for (int u = 0; u < kWalkBatch; ++u) {
+          const int i = b0 + u * 32 + lane;
+          raw_b[u] = i < r_end ? token_slot[i] : -1;
         }
-        row_slot[i] = s;
       }
-      const int key = valid ? s : -2;
-      const unsigned peers = __match_any_sync(0xffffffffu, key);
-      if (valid && s >= 0 && lane == __ffs(peers) - 1) my_hist[s] += __popc(peers);
-      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < kWalkBatch; ++u) {
+        const int i = b0 + u * 32 + lane;
+        const bool valid = i < r_end;
+        int s = -1;
+        if (valid) {
+          const int raw = raw_b[u];
+          if (raw < -1 || raw >= S) {
+            atomicOr(err, LORA_ERRF_BAD_ID);
+          } else if (raw >= 0 && loaded_s[raw] == 0) {
+            atomicOr(err, LORA_ERRF_EMPTY_SLOT);
+          } else {
+            s = raw;
+          }
+          row_slot[i] = s;
+        }
+        slot_kept[u] = s;
+        const int key = valid ? s : -2;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (valid && s >= 0 && lane == __ffs(peers) - 1) my_hist[s] += __popc(peers);
+        __syncwarp();
+      }
     }
   }
   __syncthreads();
@@ -225,10 +252,8 @@ __global__ void __launch_bounds__(kBuilderThreads, 1)
   // ---- 3. stable scatter: walkers re-walk their rows in order ----
   if (warp < n_walk) {
     int32_t* cursor = hist + (size_t)warp * S;
-    for (int base = r_begin; base < r_end; base += 32) {
-      const int i = base + lane;
+    auto scatter32 = [&](int i, int s) {
       const bool valid = i < r_end;
-      const int s = valid ? row_slot[i] : -1;
       const int key = valid ? s : -2;
       const unsigned peers = __match_any_sync(0xffffffffu, key);
       const int leader = __ffs(peers) - 1;
@@ -241,18 +266,28 @@ __global__ void __launch_bounds__(kBuilderThreads, 1)
         if (lane == leader) cursor[s] = b + __popc(peers);
       }
       __syncwarp();
+    };
+    if (kept) {
+#pragma unroll
+      for (int u = 0; u < kWalkBatch; ++u)
+        if (r_begin + u * 32 < r_end) scatter32(r_begin + u * 32 + lane, slot_kept[u]);
+    } else {
+      for (int base = r_begin; base < r_end; base += 32) {
+        const int i = base + lane;
+        scatter32(i, i < r_end ? row_slot[i] : -1);
+      }
     }
   }
 }
 
 int builder_smem_bytes(int S, int* n_walk_out) {
-  // walkers x slots counters must fit next to the per-slot totals in 200 KB
-  const int budget_ints = 200 * 1024 / 4 - S;
+  // walkers x slots counters must fit next to the per-slot totals and flags in 200 KB
+  const int budget_ints = 200 * 1024 / 4 - 2 * S;
   int n_walk = budget_ints / S;
   if (n_walk > kBuilderThreads / 32) n_walk = kBuilderThreads / 32;
   if (n_walk < 1) n_walk = 1;
   *n_walk_out = n_walk;
-  return (n_walk * S + S) * 4;
+  return (n_walk * S + 2 * S) * 4;
 }
 
 cudaError_t launch_segment_builder(const BuilderArgs& a, cudaStream_t stream) {
