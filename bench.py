@@ -625,6 +625,108 @@ def run_reference(args):
     print(json.dumps(out))
 
 
+def run_swap_in(args):
+    """Adapter residency on the 8B-class stack (224 projections, rank 16, ~80 MiB per
+    adapter): (1) the swap-in of one adapter from the cache's pinned host tier into a GPU
+    slot of every projection (one host-to-device copy + one scatter kernel), timed with
+    CUDA events on the cache's stream; (2) chained passes over the stack, each naming three
+    adapters, first with every adapter resident, then sliding one new adapter into every
+    batch by a prefetch issued while the previous pass computes -- the pages' claim that a
+    prefetched swap-in hides behind the running batch."""
+    from segmented_rank_gemm_gb300.lora import AdapterCache
+    from segmented_rank_gemm_gb300.stack import LoraStack
+    from segmented_rank_gemm_gb300.workloads import STACK_PROJECTIONS
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    S, H, r = 4, 8, 16
+    st = LoraStack(S=S, seed=CONFIGS["stack_8b"]["seed"], device=dev)
+    layers = [layer for row in st.layers for layer in row]
+    cache = AdapterCache(layers, S, H)
+    g = torch.Generator().manual_seed(7)
+    shapes = {}
+    for _, k, n in STACK_PROJECTIONS:  # one random (A, B) per shape; content is irrelevant
+        if (k, n) not in shapes:
+            shapes[(k, n)] = ((torch.randn(k, r, generator=g) * 0.02).to(torch.bfloat16),
+                              (torch.randn(r, n, generator=g) * 0.02).to(torch.bfloat16))
+    A_list = [shapes[(L.K, L.N)][0] for L in layers]
+    B_list = [shapes[(L.K, L.N)][1] for L in layers]
+    t0 = time.perf_counter()
+    for a in range(H):
+        cache.add(a, A_list, B_list, 2.0 * r)
+    add_ms = (time.perf_counter() - t0) * 1e3 / H
+    image = sum((L.max_rank + 7) // 8 * 8 * (L.K + L.N) * 2 for L in layers)
+    cs = torch.cuda.ExternalStream(cache.stream, device=dev)
+
+    # (1) swap-in latency: no batch in flight, each prefetch evicts the LRU adapter
+    order = [a % H for a in range(S, S + 4 * H)]
+    for a in order[:H]:
+        cache.prefetch([a])
+    cache.sync()
+    host_s = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cs)
+    for a in order[H:]:
+        t = time.perf_counter()
+        cache.prefetch([a])
+        host_s.append(time.perf_counter() - t)
+    e1.record(cs)
+    cache.sync()
+    n_swaps = len(order) - H
+    swap_ms = e0.elapsed_time(e1) / n_swaps
+
+    # (2) passes: resident adapters only, then one prefetched newcomer per batch
+    stream = torch.cuda.Stream(device=dev)
+    graph = st.capture(stream)
+    rng = np.random.default_rng(3)
+    T = st.T
+
+    def passes(n, sliding):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for k in range(n + 3):
+            if k == 3:
+                ev[0].record(stream)
+            base = k if sliding else 0
+            names = [(base + j) % H for j in range(3)]
+            ids = np.asarray(names)[rng.integers(0, 3, size=T)].astype(np.int64)
+            slots = cache.map_batch(ids, stream)
+            with torch.cuda.stream(stream):
+                st.ids.copy_(torch.from_numpy(slots.astype(np.int32)), non_blocking=True)
+                graph.replay()
+            if sliding:
+                cache.prefetch([(base + 3) % H])  # the next batch's newcomer
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / n
+
+    cache.prefetch([0, 1, 2])
+    n = max(args.steps, 8)
+    resident_ms = passes(n, False)
+    before = cache.stats()
+    sliding_ms = passes(n, True)
+    after = cache.stats()
+    cache.close()
+    st.close()
+    out = {
+        "metric": "adapter swap-in, host DRAM -> GPU slots (8B-class rank-16 adapter)",
+        "value": swap_ms, "unit": "ms per adapter", "higher_is_better": False, "n_gpus": 1,
+        "steps": n_swaps, "dtype": "bf16", "data": "synthetic (random-init adapters)",
+        "config": {"workload": "8B-class stack, 32 layers x 7 projections, rank 16, "
+                   "%d GPU slots, %d adapters in the pinned host tier" % (S, H),
+                   "image_bytes": image, "projections": len(layers)},
+        "swap_in": {"ms": swap_ms, "gbs": image / (swap_ms * 1e-3) / 1e9,
+                    "host_call_ms_median": statistics.median(host_s) * 1e3,
+                    "launches": 2, "add_ms_per_adapter": add_ms},
+        "overlap": {"passes": n, "ms_per_pass_resident": resident_ms,
+                    "ms_per_pass_one_prefetched_swap_in": sliding_ms,
+                    "swap_ins": after["prefetches"] - before["prefetches"],
+                    "misses": after["misses"] - before["misses"],
+                    "hidden_fraction": max(0.0, 1.0 - max(0.0, sliding_ms - resident_ms)
+                                           / swap_ms)},
+    }
+    print(json.dumps(out))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -640,10 +742,14 @@ def main(argv=None):
     ap.add_argument("--e2e-streams", type=int, default=4,
                     help="streams the end-to-end steps rotate over (instance j on stream j %% n)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--swap-in", action="store_true",
+                    help="measure adapter swap-ins through the adapter cache instead")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3  # at least 3 warm-up steps
-    if args.impl == "reference":
+    if args.swap_in:
+        run_swap_in(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -55,7 +55,9 @@ enum lora_status {
     LORA_ECUDA = -5,    /* a CUDA runtime call failed; lora_last_error has the message */
     LORA_ENOMEM = -6,   /* device or host allocation failed */
     LORA_ESTATE = -7,   /* call out of order: lora_forward without matching set_batch_segments */
-    LORA_ETIMEOUT = -8  /* (device) a pipeline wait inside a kernel gave up; results invalid */
+    LORA_ETIMEOUT = -8, /* (device) a pipeline wait inside a kernel gave up; results invalid */
+    LORA_ENOENT = -9,   /* (adapter cache) adapter id not held in the host tier */
+    LORA_ECAPACITY = -10 /* (adapter cache) more distinct adapters than GPU slots */
 };
 
 /*

@@ -26,6 +26,7 @@
 #include "lora_layer.h"
 #include "lora_common.cuh"
 #include "lora_kernels.h"
+#include "layer_state.h"
 
 using namespace lora;
 
@@ -37,58 +38,6 @@ constexpr int kMaxTokens = 1 << 20;
 constexpr int kDeltaMaxT = 512;  // largest batch computed in delta mode
 
 }  // namespace
-
-struct lora_layer {
-  int K = 0, N = 0, S = 0, T_max = 0, dtype = 0, device = 0, num_sms = 0;
-  int max_rank = 0;  // largest adapter rank a slot accepts
-  int R = 0;         // slot rank width: max_rank rounded up to a multiple of 8 (zero padded)
-  size_t esize = 0;
-  void* Wp = nullptr;      // packed base weight: bf16 [N][K], f32 [K][N]
-  void* A_pool = nullptr;  // [S][R][K]
-  void* B_pool = nullptr;  // [S][R][N]
-  void* Bx_pool = nullptr; // [S][N][wx] bf16, the B expand pool of the tensor-core expand
-  void* A_stage = nullptr; // [K][R] staging for the transposition of a loaded A
-  float* scale = nullptr;  // [S]
-  int32_t* rank = nullptr;    // [S]
-  int32_t* loaded = nullptr;  // [S]
-  // batch layout (segment builder outputs)
-  int32_t* row_slot = nullptr;   // [T_max]
-  int32_t* perm = nullptr;       // [T_max]
-  int32_t* seg_offsets = nullptr;// [S+1]
-  int32_t* seg_slot = nullptr;   // [S]
-  int32_t* tile_seg = nullptr;   // [max_tiles]
-  int32_t* tile_row0 = nullptr;  // [max_tiles]
-  int32_t* meta = nullptr;       // [8]: builder counts, shrink work counters
-  int32_t* err = nullptr;        // [1]
-  float* v = nullptr;            // [v_planes][T_max][R] fp32, scaled by alpha / r (v mode)
-  int v_planes = 1;              // K-split partial planes of v (bf16: tensor-core shrink)
-  float* delta = nullptr;        // [min(T_max, kDeltaMaxT)][N] fp32 (delta mode, bf16)
-  float* xk = nullptr;           // split-K exchange scratch of the base GEMM (delta mode)
-  float* sk_part = nullptr;      // stream-K partials of the base GEMM (v mode)
-  int32_t* sk_sync = nullptr;    // stream-K epoch, exit count and flags (zeroed)
-  size_t xk_floats = 0;
-  GemmPlan gemm_plan{0, 0, 0};   // fixed by lora_set_gemm_plan (block_n 0: automatic)
-  int max_tiles = 0;
-  int T_batch = -1;              // T of the last set_batch_segments, -1 = none
-  bool segments_pending = false;  // that batch's builder has not run yet (decode batches)
-  const int32_t* token_slot = nullptr;  // the caller's ids of that batch
-  // staging for lora_forward_host
-  void* x_stage = nullptr;
-  int32_t* ids_stage = nullptr;
-  void* y_stage = nullptr;
-  // ordering
-  cudaEvent_t stage_free = nullptr;    // recorded after a load's transposition
-  cudaEvent_t last_forward = nullptr;  // recorded after each forward (when not capturing)
-  bool have_forward = false;
-  std::vector<cudaEvent_t> pending;    // loads not yet waited on by a forward
-  std::vector<cudaEvent_t> spare;
-  CUtensorMap tmap_w[3];
-  CUtensorMap tmap_a;  // A pool [S*R rows][K] with a (64 x round_up(R, 16)) box (bf16)
-  CUtensorMap tmap_bx[3];  // B expand pool [S*N rows][wx], boxes of 256/128/64 rows
-  cudaEvent_t trace[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
-  bool tracing = false;
-  char last_error[512] = {0};
-};
 
 namespace {
 
@@ -154,6 +103,21 @@ cudaError_t wait_pending_loads(lora_layer* L, cudaStream_t stream) {
 }
 
 }  // namespace
+
+namespace lora {
+
+cudaEvent_t layer_take_event(lora_layer* L) {
+  if (!L->spare.empty()) {
+    cudaEvent_t e = L->spare.back();
+    L->spare.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+  return e;
+}
+
+}  // namespace lora
 
 extern "C" {
 
@@ -271,17 +235,6 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
   return LORA_OK;
 }
 
-static cudaEvent_t take_event(lora_layer* L) {
-  if (!L->spare.empty()) {
-    cudaEvent_t e = L->spare.back();
-    L->spare.pop_back();
-    return e;
-  }
-  cudaEvent_t e = nullptr;
-  if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
-  return e;
-}
-
 int load_adapter_slot(lora_layer_t* L, int slot, const void* A_src, const void* B_src, int r,
                       float alpha, void* side_) {
   if (!L) return LORA_EINVAL;
@@ -314,7 +267,7 @@ int load_adapter_slot(lora_layer_t* L, int slot, const void* A_src, const void* 
                                 (int)R, (int)N, side));
   LORA_CUDA(L, launch_slot_meta(L->scale, L->rank, L->loaded, slot, alpha / (float)r, r, 1,
                                 side));
-  cudaEvent_t ev = take_event(L);
+  cudaEvent_t ev = layer_take_event(L);
   if (!ev) return fail(L, LORA_ECUDA, "cudaEventCreate failed");
   LORA_CUDA(L, cudaEventRecord(ev, side));
   L->pending.push_back(ev);
@@ -327,7 +280,7 @@ int unload_adapter_slot(lora_layer_t* L, int slot, void* side_) {
   cudaStream_t side = static_cast<cudaStream_t>(side_);
   if (L->have_forward) LORA_CUDA(L, cudaStreamWaitEvent(side, L->last_forward, 0));
   LORA_CUDA(L, launch_slot_meta(L->scale, L->rank, L->loaded, slot, 0.f, 0, 0, side));
-  cudaEvent_t ev = take_event(L);
+  cudaEvent_t ev = layer_take_event(L);
   if (!ev) return fail(L, LORA_ECUDA, "cudaEventCreate failed");
   LORA_CUDA(L, cudaEventRecord(ev, side));
   L->pending.push_back(ev);

@@ -1,4 +1,5 @@
-"""ctypes binding of the layer's C ABI (``include/lora_layer.h``).
+"""ctypes binding of the layer's C ABI (``include/lora_layer.h``) and of the adapter cache
+over it (``include/lora_residency.h``).
 
 The functions below carry the C names and only marshal arguments: torch tensors become
 raw pointers, torch streams become ``cudaStream_t`` handles, and a negative status
@@ -19,15 +20,33 @@ from .build import LIB_PATH
 
 LORA_F32, LORA_BF16 = 0, 1
 STATUS = {0: "LORA_OK", -1: "LORA_EINVAL", -2: "LORA_ESLOT", -3: "LORA_ERANK", -4: "LORA_EID",
-          -5: "LORA_ECUDA", -6: "LORA_ENOMEM", -7: "LORA_ESTATE", -8: "LORA_ETIMEOUT"}
+          -5: "LORA_ECUDA", -6: "LORA_ENOMEM", -7: "LORA_ESTATE", -8: "LORA_ETIMEOUT",
+          -9: "LORA_ENOENT", -10: "LORA_ECAPACITY"}
 LORA_OK, LORA_EINVAL, LORA_ESLOT, LORA_ERANK, LORA_EID = 0, -1, -2, -3, -4
 LORA_ECUDA, LORA_ENOMEM, LORA_ESTATE, LORA_ETIMEOUT = -5, -6, -7, -8
+LORA_ENOENT, LORA_ECAPACITY = -9, -10
 
 # every entry point declared in include/lora_layer.h
 ABI_FUNCTIONS = ("lora_layer_create", "load_adapter_slot", "unload_adapter_slot",
                  "set_batch_segments", "lora_forward", "lora_forward_host", "lora_get_status",
                  "lora_get_segments", "lora_set_trace_events", "lora_set_gemm_plan",
                  "lora_last_error", "lora_layer_destroy", "lora_build_segments_static")
+# every entry point declared in include/lora_residency.h
+CACHE_FUNCTIONS = ("lora_cache_create", "lora_cache_add", "lora_cache_remove",
+                   "lora_cache_map_batch", "lora_cache_prefetch", "lora_cache_slot_of",
+                   "lora_cache_get_stats", "lora_cache_stream", "lora_cache_sync",
+                   "lora_cache_last_error", "lora_cache_destroy")
+
+
+class CacheStats(ctypes.Structure):
+    """lora_cache_stats_t."""
+    _fields_ = [("hits", ctypes.c_int64), ("misses", ctypes.c_int64),
+                ("prefetches", ctypes.c_int64), ("gpu_evictions", ctypes.c_int64),
+                ("host_evictions", ctypes.c_int64), ("bytes_swapped", ctypes.c_int64),
+                ("resident", ctypes.c_int32), ("registered", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {name: int(getattr(self, name)) for name, _ in self._fields_}
 
 
 class LoraError(RuntimeError):
@@ -60,6 +79,25 @@ def _load() -> ctypes.CDLL:
     for name in ABI_FUNCTIONS:
         if name not in ("lora_last_error", "lora_layer_destroy"):
             getattr(L, name).restype = i32
+    i64 = ctypes.c_int64
+    L.lora_cache_create.argtypes = [ctypes.POINTER(vp), vp, i32, i32, i32]
+    L.lora_cache_add.argtypes = [vp, i64, i32, f32, vp, vp]
+    L.lora_cache_remove.argtypes = [vp, i64]
+    L.lora_cache_map_batch.argtypes = [vp, vp, i32, vp, vp]
+    L.lora_cache_prefetch.argtypes = [vp, vp, i32]
+    L.lora_cache_slot_of.argtypes = [vp, i64]
+    L.lora_cache_get_stats.argtypes = [vp, ctypes.POINTER(CacheStats)]
+    L.lora_cache_stream.argtypes = [vp]
+    L.lora_cache_stream.restype = vp
+    L.lora_cache_sync.argtypes = [vp]
+    L.lora_cache_last_error.argtypes = [vp]
+    L.lora_cache_last_error.restype = ctypes.c_char_p
+    L.lora_cache_destroy.argtypes = [vp]
+    L.lora_cache_destroy.restype = None
+    for name in ("lora_cache_create", "lora_cache_add", "lora_cache_remove",
+                 "lora_cache_map_batch", "lora_cache_prefetch", "lora_cache_slot_of",
+                 "lora_cache_get_stats", "lora_cache_sync"):
+        getattr(L, name).restype = i32
     return L
 
 
@@ -258,6 +296,142 @@ class LoraLayer:
     def close(self):
         if getattr(self, "handle", None):
             lora_layer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ---------------------------------------------------------------------------------
+# adapter cache (include/lora_residency.h)
+# ---------------------------------------------------------------------------------
+
+def _check_cache(cache, rc: int) -> int:
+    if rc < 0:
+        msg = _lib.lora_cache_last_error(cache).decode() if cache else ""
+        raise LoraError(rc, msg)
+    return rc
+
+
+def lora_cache_create(layers, num_slots: int, host_capacity: int) -> int:
+    """``layers``: layer handles (ints) or ``LoraLayer`` objects; [] keeps only the books."""
+    hs = [l.handle if isinstance(l, LoraLayer) else l for l in layers]
+    arr = (ctypes.c_void_p * max(len(hs), 1))(*hs)
+    h = ctypes.c_void_p()
+    _check_cache(None, _lib.lora_cache_create(ctypes.byref(h), ctypes.cast(arr, ctypes.c_void_p)
+                                              if hs else None, len(hs), num_slots,
+                                              host_capacity))
+    return h.value
+
+
+def lora_cache_add(cache, adapter_id: int, r: int, alpha: float, A_host=(), B_host=()) -> None:
+    """``A_host`` / ``B_host``: per layer, contiguous CPU tensors [K, r] / [r, N]."""
+    n = len(A_host)
+    A = (ctypes.c_void_p * max(n, 1))(*[_ptr(a) for a in A_host])
+    B = (ctypes.c_void_p * max(n, 1))(*[_ptr(b) for b in B_host])
+    _check_cache(cache, _lib.lora_cache_add(cache, int(adapter_id), int(r), float(alpha),
+                                            ctypes.cast(A, ctypes.c_void_p) if n else None,
+                                            ctypes.cast(B, ctypes.c_void_p) if n else None))
+
+
+def lora_cache_remove(cache, adapter_id: int) -> None:
+    _check_cache(cache, _lib.lora_cache_remove(cache, int(adapter_id)))
+
+
+def lora_cache_map_batch(cache, token_adapter, stream=0):
+    """``token_adapter``: int64 numpy array (host); returns the int32 numpy slot ids.
+    ``stream``: the batches' stream (a torch stream, a handle, or None for torch's current
+    stream; the default 0 is the legacy default stream, as a cache without layers needs)."""
+    import numpy as np
+    ta = np.ascontiguousarray(token_adapter, dtype=np.int64)
+    out = np.empty(max(len(ta), 1), np.int32)
+    _check_cache(cache, _lib.lora_cache_map_batch(cache, ta.ctypes.data, len(ta),
+                                                  out.ctypes.data, _stream(stream)))
+    return out[:len(ta)]
+
+
+def lora_cache_prefetch(cache, ids) -> None:
+    import numpy as np
+    a = np.ascontiguousarray(ids, dtype=np.int64)
+    _check_cache(cache, _lib.lora_cache_prefetch(cache, a.ctypes.data if len(a) else None,
+                                                 len(a)))
+
+
+def lora_cache_slot_of(cache, adapter_id: int) -> int:
+    return _lib.lora_cache_slot_of(cache, int(adapter_id))
+
+
+def lora_cache_get_stats(cache) -> dict:
+    st = CacheStats()
+    _check_cache(cache, _lib.lora_cache_get_stats(cache, ctypes.byref(st)))
+    return st.as_dict()
+
+
+def lora_cache_stream(cache) -> int:
+    return _lib.lora_cache_stream(cache) or 0
+
+
+def lora_cache_sync(cache) -> None:
+    _check_cache(cache, _lib.lora_cache_sync(cache))
+
+
+def lora_cache_last_error(cache) -> str:
+    return _lib.lora_cache_last_error(cache).decode()
+
+
+def lora_cache_destroy(cache) -> None:
+    _lib.lora_cache_destroy(cache)
+
+
+class AdapterCache:
+    """Owns one adapter cache over ``layers`` (``LoraLayer`` objects, kept alive here)."""
+
+    def __init__(self, layers, num_slots: int, host_capacity: int):
+        self.layers = list(layers)
+        self.num_slots, self.host_capacity = num_slots, host_capacity
+        self.handle = lora_cache_create(self.layers, num_slots, host_capacity)
+
+    def add(self, adapter_id: int, A_list, B_list, alpha: float, r: int = None) -> None:
+        """Per layer: A [K, r] and B [r, N] in the layer dtype (moved to host memory)."""
+        A_list = [a.detach().to("cpu").contiguous() for a in A_list]
+        B_list = [b.detach().to("cpu").contiguous() for b in B_list]
+        for L, A, B in zip(self.layers, A_list, B_list):
+            if A.dtype != L.dtype or B.dtype != L.dtype:
+                raise ValueError("adapter dtype must match the layer dtype")
+            if A.shape[0] != L.K or B.shape[1] != L.N or A.shape[1] != B.shape[0]:
+                raise ValueError("A must be [K, r] and B [r, N]")
+        if r is None:
+            r = int(A_list[0].shape[1])
+        lora_cache_add(self.handle, adapter_id, r, alpha, A_list, B_list)
+
+    def remove(self, adapter_id: int) -> None:
+        lora_cache_remove(self.handle, adapter_id)
+
+    def map_batch(self, token_adapter, stream=None):
+        return lora_cache_map_batch(self.handle, token_adapter, stream)
+
+    def prefetch(self, ids) -> None:
+        lora_cache_prefetch(self.handle, ids)
+
+    def slot_of(self, adapter_id: int) -> int:
+        return lora_cache_slot_of(self.handle, adapter_id)
+
+    def stats(self) -> dict:
+        return lora_cache_get_stats(self.handle)
+
+    @property
+    def stream(self) -> int:
+        return lora_cache_stream(self.handle)
+
+    def sync(self) -> None:
+        lora_cache_sync(self.handle)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lora_cache_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
     so = ctypes.CDLL(lib.LIB_PATH)
     for name in header_functions():
         assert hasattr(so, name), name
-    assert set(lib.ABI_FUNCTIONS) == set(header_functions())
+    assert set(lib.ABI_FUNCTIONS) | set(lib.CACHE_FUNCTIONS) == set(header_functions())
 
 
 def test_create_rejects_bad_arguments(lib):

@@ -1,0 +1,180 @@
+"""The adapter cache on the GPU, through the C ABI: layers whose slots are filled only by
+swap-ins from the cache's host tier, checked against the oracle evaluated on the adapters
+by id (not by slot), so every eviction and reload must put the right weights in the right
+slot of every layer.
+
+Layers of three kinds share the cache: bf16 (delta mode up to 512 rows, tensor-core expand
+with the B expand pool above), a second bf16 shape, and fp32.  Batches alternate between
+200 and 600 rows, name at most as many adapters as there are slots, and are chosen so
+that most of them swap something in.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from segmented_rank_gemm_gb300 import workloads
+from gpu_helpers import assert_parity
+
+pytestmark = pytest.mark.gpu
+BF16, F32 = torch.bfloat16, torch.float32
+
+N_IDS, SLOTS = 9, 4
+RANKS = [1, 16, 8, 3, 12, 16, 2, 5, 9]
+SHAPES = [(256, 192, BF16), (128, 264, BF16), (72, 40, F32)]  # K, N, dtype
+T_MAX = 640
+
+
+def _universe():
+    """Per layer: W and the N_IDS adapters (index = adapter id)."""
+    return [workloads.synthetic(900 + i, 1, K, N, S=N_IDS, ranks=RANKS, R=16, dtype=dt,
+                                base_frac=0.0)
+            for i, (K, N, dt) in enumerate(SHAPES)]
+
+
+def _build(wls, slots=SLOTS, host=N_IDS):
+    from segmented_rank_gemm_gb300.lora import AdapterCache, LoraLayer
+    layers = [LoraLayer(wl.W.cuda(), slots + 2, 16, T_MAX) for wl in wls]
+    cache = AdapterCache(layers, slots, host)
+    for a in range(N_IDS):
+        cache.add(a, [wl.adapters[a][0] for wl in wls], [wl.adapters[a][1] for wl in wls],
+                  wls[0].adapters[a][2])
+    return layers, cache
+
+
+def _run_batch(layers, cache, wls, ids, seed, stream):
+    """Map, forward every layer on `stream`; returns the outputs and their inputs."""
+    slots = cache.map_batch(ids, stream)
+    g = torch.Generator().manual_seed(seed)
+    outs = []
+    with torch.cuda.stream(stream):  # every device buffer of the batch is made on `stream`
+        tok = torch.from_numpy(slots.astype(np.int32)).cuda()
+        for L, wl in zip(layers, wls):
+            x = torch.randn(len(ids), wl.K, generator=g).to(wl.dtype)
+            outs.append((x, L(x.cuda(), tok, stream=stream)))
+    return slots, outs
+
+
+def _check(wls, ids, outs, what):
+    for wl, (x, y) in zip(wls, outs):
+        table = oracle.SlotTable(wl.adapters, wl.K, wl.N)
+        ref = oracle.forward_rows(x, wl.W, table, torch.tensor(ids, dtype=torch.int32))
+        assert_parity(y, ref, wl.dtype, what="%s K=%d N=%d" % (what, wl.K, wl.N))
+
+
+def test_swaps_keep_parity_over_a_batch_sequence():
+    from segmented_rank_gemm_gb300.lora import LoraError
+    wls = _universe()
+    layers, cache = _build(wls)
+    stream = torch.cuda.Stream()
+    rng = np.random.default_rng(11)
+    pending = []
+    for step in range(10):
+        T = 200 if step % 2 == 0 else 600
+        names = rng.choice(N_IDS, size=int(rng.integers(1, SLOTS + 1)), replace=False)
+        ids = np.where(rng.random(T) < 0.1, -1, rng.choice(names, size=T)).astype(np.int64)
+        slots, outs = _run_batch(layers, cache, wls, ids, step, stream)
+        for a in set(ids.tolist()) - {-1}:
+            assert slots[ids == a][0] == cache.slot_of(a)
+        pending.append((ids, outs))
+        if step % 3 == 2:  # prefetch an adapter beside this batch, if a slot is free of it
+            try:
+                cache.prefetch(rng.choice(N_IDS, size=1))
+            except LoraError as e:
+                assert e.code == -10  # LORA_ECAPACITY: every slot serves the running batch
+    torch.cuda.synchronize()
+    for step, (ids, outs) in enumerate(pending):
+        _check(wls, ids, outs, "step %d" % step)
+    for L in layers:
+        assert L.status(stream) == 0
+    st = cache.stats()
+    assert st["misses"] >= 6 and st["gpu_evictions"] >= 3, st
+    image = sum(16 * (wl.K + wl.N) * (2 if wl.dtype == BF16 else 4) for wl in wls)
+    assert st["bytes_swapped"] >= (st["misses"] + st["prefetches"]) * image
+    cache.close()
+
+
+def test_one_slot_eviction_under_a_running_batch():
+    """One slot: each batch evicts the previous batch's adapter right after that batch's
+    forwards were enqueued (no host synchronisation), so the swap-in must wait for them."""
+    wls = _universe()
+    layers, cache = _build(wls, slots=1, host=N_IDS)
+    stream = torch.cuda.Stream()
+    runs = []
+    for step, a in enumerate([0, 5, 1, 5, 8, 2]):
+        ids = np.full(200 if step % 2 else 600, a, np.int64)
+        ids[::7] = -1
+        runs.append((ids, _run_batch(layers, cache, wls, ids, 100 + step, stream)[1]))
+    torch.cuda.synchronize()
+    for step, (ids, outs) in enumerate(runs):
+        _check(wls, ids, outs, "one-slot step %d" % step)
+    assert cache.stats()["gpu_evictions"] == 5
+    cache.close()
+
+
+def test_replace_and_remove():
+    wls = _universe()
+    layers, cache = _build(wls)
+    stream = torch.cuda.Stream()
+    ids = np.array([3, 4, -1, 3, 4] * 40, np.int64)
+    _run_batch(layers, cache, wls, ids, 1, stream)
+    # adapter 3 gets new weights under the same id (in place) while that batch may run
+    new3 = [workloads.synthetic(950 + i, 1, wl.K, wl.N, S=1, ranks=[7], R=16, dtype=wl.dtype)
+            .adapters[0] for i, wl in enumerate(wls)]
+    cache.add(3, [a[0] for a in new3], [a[1] for a in new3], new3[0][2])
+    for wl, a in zip(wls, new3):
+        wl.adapters[3] = a
+    _, outs = _run_batch(layers, cache, wls, ids, 2, stream)
+    torch.cuda.synchronize()
+    _check(wls, ids, outs, "after replacing adapter 3")
+    # removing adapter 4 empties its slot: a forged batch still naming that slot computes
+    # base only and raises the layers' id flag
+    slot4 = cache.slot_of(4)
+    cache.remove(4)
+    cache.map_batch(np.array([3], np.int64), stream)  # the next batch point empties it
+    base = torch.full((64,), -1, dtype=torch.int32)
+    with torch.cuda.stream(stream):
+        forged = torch.full((64,), slot4, dtype=torch.int32, device="cuda")
+        for L, wl in zip(layers, wls):
+            x = torch.randn(64, wl.K, generator=torch.Generator().manual_seed(5)).to(wl.dtype)
+            y = L(x.cuda(), forged, stream=stream)
+            torch.cuda.synchronize()
+            table = oracle.SlotTable(wl.adapters, wl.K, wl.N)
+            ref = oracle.forward_rows(x, wl.W, table, base)
+            assert_parity(y, ref, wl.dtype, what="removed slot, base only")
+            assert L.status(stream) == -4  # LORA_EID
+    with pytest.raises(Exception):
+        cache.map_batch(np.array([4], np.int64), stream)
+    cache.close()
+
+
+def test_swap_in_through_many_layers_and_capacity_errors():
+    """Twenty layers in one image (one copy + one scatter launch per swap-in), and the
+    batch-level capacity error of the pages (more adapters than slots)."""
+    from segmented_rank_gemm_gb300.lora import AdapterCache, LoraError, LoraLayer
+    wl = workloads.synthetic(990, 1, 128, 136, S=6, ranks=[4, 8, 16, 2, 9, 16], R=16,
+                             base_frac=0.0)
+    layers = [LoraLayer(wl.W.cuda(), 3, 16, 256) for _ in range(20)]
+    cache = AdapterCache(layers, 3, 6)
+    for a in range(6):
+        A, B, alpha = wl.adapters[a]
+        cache.add(a, [A] * 20, [B] * 20, alpha)
+    with pytest.raises(LoraError) as e:
+        cache.map_batch(np.array([0, 1, 2, 3], np.int64))
+    assert e.value.code == -10  # LORA_ECAPACITY
+    stream = torch.cuda.Stream()
+    rng = np.random.default_rng(3)
+    table = oracle.SlotTable(wl.adapters, wl.K, wl.N)
+    for step in range(6):
+        names = rng.choice(6, size=3, replace=False)
+        ids = rng.choice(names, size=256).astype(np.int64)
+        slots = cache.map_batch(ids, stream)
+        x = torch.randn(256, wl.K, dtype=BF16)
+        with torch.cuda.stream(stream):
+            tok = torch.from_numpy(slots.astype(np.int32)).cuda()
+            ys = [L(x.cuda(), tok, stream=stream) for L in layers]
+        torch.cuda.synchronize()
+        ref = oracle.forward_rows(x, wl.W, table, torch.tensor(ids, dtype=torch.int32))
+        for y in ys[::7]:
+            assert_parity(y, ref, BF16, what="20-layer image, step %d" % step)
+    cache.close()
