@@ -85,6 +85,7 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
  *              max_rank and kernels read only its first r rank columns.
  *   alpha      LoRA alpha; the slot's scale is alpha / r, computed in fp32 and applied in
  *              fp32 to the rank-r intermediate (it is not folded into B).
+ * (The same as load_adapter_slot_composed with one member of weight 1.)
  * Ordering: the copy waits for the most recent lora_forward of this layer, so an adapter
  * is never overwritten under a kernel still reading the slot; the next lora_forward waits
  * for the copy.  Loading into an occupied slot replaces its adapter.
@@ -92,6 +93,31 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
  */
 int load_adapter_slot(lora_layer_t* layer, int slot, const void* A_src, const void* B_src,
                       int r, float alpha, void* side_stream);
+
+/*
+ * Copy a composition of n adapters into slot `slot`: rows of this slot add
+ *     sum_i weight[i] * (alpha[i] / r[i]) * (x A_i) B_i
+ * to the base product.  "Multi-LoRA Serving 与 Adapter 隔离", section on adapter ownership
+ * in a continuous batch: a request may compose several LoRAs, which are added, and its
+ * identity is the ordered composition with its weights.
+ *   A_src[i]   [K, r[i]] row-major, B_src[i] [r[i], N] row-major, the layer's dtype, host or
+ *              device memory (as load_adapter_slot).
+ *   r[i] >= 1, sum_i r[i] <= max_rank.  alpha[i], weight[i]: any fp32 values.
+ * The members are stacked along the rank axis of the slot (member i takes the r[i] rank
+ * columns after those of members 0 .. i-1), each column with its own fp32 scale
+ * weight[i] * alpha[i] / r[i], applied to the rank-wide intermediate in fp32 (B is not
+ * rescaled, so the stored weights are not re-rounded).  Every kernel then serves the slot like one adapter of rank
+ * sum_i r[i].  load_adapter_slot is the case n = 1, weight 1.
+ * Ordering: as load_adapter_slot.  A layer whose slots all hold plain adapters runs a
+ * decode kernel that reads one scale per slot; the first composition with unequal column
+ * scales switches the layer's later forwards to the per-column variant, so a forward
+ * captured in a CUDA graph before that must be captured again.
+ * Errors: LORA_ESLOT, LORA_ERANK (a member's rank, or the sum, out of range), LORA_EINVAL
+ * (n < 1, null arrays or pointers), LORA_ECUDA.
+ */
+int load_adapter_slot_composed(lora_layer_t* layer, int slot, int n, const void* const* A_src,
+                               const void* const* B_src, const int* r, const float* alpha,
+                               const float* weight, void* side_stream);
 
 /*
  * Mark slot `slot` empty (rows naming it are then flagged and computed base only).

@@ -39,7 +39,8 @@
  * slot layout of every layer (A transposed and zero-padded to the slot width, B padded), in
  * one pinned host block.  A swap-in is one host-to-device copy of that block into a device
  * staging buffer and one kernel that scatters it into the slot of every layer and sets the
- * slots' scale (alpha / r), rank and loaded flag, both on the cache's own stream.
+ * slots' column scales (alpha / r), rank and loaded flag, both on the cache's own stream,
+ * created at the lowest priority.
  *
  * Ordering is per slot, so that a swap-in runs beside the batch in flight unless it
  * replaces one of that batch's adapters:

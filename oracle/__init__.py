@@ -198,3 +198,31 @@ def forward_merged(x, W, table: SlotTable, slot, _lib=None) -> np.ndarray:
                             _ptr(table.B), _ptr(table.rank), _ptr(table.alpha), _ptr(slot),
                             _ptr(y))
     return y
+
+
+def forward_composed(x, W, compositions, slot) -> np.ndarray:
+    """Rows whose slot holds a composition of adapters ("Multi-LoRA Serving 与 Adapter
+    隔离", adapter ownership in a continuous batch: a request may compose several LoRAs,
+    which are added, identified by the ordered members and their weights):
+
+        y[i] = x[i] W + sum_m weight_m * (alpha_m / r_m) * (x[i] A_m) B_m,   m in slot_i
+
+    ``compositions``: per slot ``None`` (empty) or a list of members
+    ``(A [K, r_m], B [r_m, N], alpha_m, weight_m)``.  Rows with slot -1, outside the list or
+    naming an empty slot are base only.  fp64 from the exact input values; numpy's matmul
+    serves as the dense product, nothing else is fused or reordered.
+    """
+    x, W, slot = _f64(x), _f64(W), _i32(slot)
+    y = x @ W
+    for s, comp in enumerate(compositions):
+        if not comp:
+            continue
+        rows = np.nonzero(slot == s)[0]
+        if rows.size == 0:
+            continue
+        xs = x[rows]
+        for A, B, alpha, weight in comp:
+            A, B = _f64(A), _f64(B)
+            r = A.shape[1]
+            y[rows] += float(weight) * (float(alpha) / r) * ((xs @ A) @ B)
+    return y

@@ -21,9 +21,11 @@ struct lora_layer {
   void* B_pool = nullptr;  // [S][R][N]
   void* Bx_pool = nullptr; // [S][N][wx] bf16, the B expand pool of the tensor-core expand
   void* A_stage = nullptr; // [K][R] staging for the transposition of a loaded A
-  float* scale = nullptr;  // [S]
+  float* scale = nullptr;  // [S][R] column scales (+ 32 padding entries)
   int32_t* rank = nullptr;    // [S]
   int32_t* loaded = nullptr;  // [S]
+  std::vector<char> percol;   // [S] host: the slot's columns carry different scales
+  int percol_slots = 0;       // slots with percol set
   // batch layout (segment builder outputs)
   int32_t* row_slot = nullptr;   // [T_max]
   int32_t* perm = nullptr;       // [T_max]
@@ -68,5 +70,9 @@ namespace lora {
 
 // An event from the layer's pool (created on demand).  nullptr if creation failed.
 cudaEvent_t layer_take_event(lora_layer* L);
+
+// Record whether slot `slot` now holds columns of different scales (a composition): the
+// decode BGMV kernel reads one scale per slot while no slot of the layer does.
+void layer_set_percol(lora_layer* L, int slot, bool varied);
 
 }  // namespace lora

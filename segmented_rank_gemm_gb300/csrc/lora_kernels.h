@@ -62,7 +62,7 @@ struct TileArgs {
   int K, N, R;
   const void* At_pool;  // [S][R][K] (transposed slot A, K contiguous)
   const void* B_pool;   // [S][R][N]
-  const float* scale;   // [S]
+  const float* scale;   // [S][R]: the scale of each rank column of a slot
   const int32_t* rank;  // [S]
   const int32_t* perm, *seg_offsets, *seg_slot, *tile_seg, *tile_row0, *meta;
   float* out;           // v [T_max][R] (v mode) or delta [T_max][N] (delta mode), fp32
@@ -77,7 +77,7 @@ struct ShrinkTcArgs {
   const void* x;  // [T,K] bf16
   int T, K, R;    // R: slot rank width (multiple of 8); v has R columns
   int Rt;         // MMA N: R rounded up to 16
-  const float* scale;  // [S]
+  const float* scale;  // [S][R]: the scale of each rank column of a slot
   const int32_t* perm, *seg_offsets, *seg_slot, *tile_seg, *tile_row0, *meta;
   int32_t* work;       // [2] item and exit counters, zero between launches (builder zeroes)
   float* v;            // [max_planes][T_max][R] fp32 partial sums over K ranges, scaled
@@ -104,10 +104,11 @@ struct BgmvArgs {
   int T, K, N, R, S;
   const void* At_pool;  // [S][R][K]
   const void* B_pool;   // [S][R][N]
-  const float* scale;   // [S]
+  const float* scale;   // [S][R]: the scale of each rank column of a slot
   const int32_t* rank;  // [S]
   float* delta;         // [T_max][N] fp32
   int num_sms;
+  bool per_column;      // some slot's columns carry different scales (a composition)
 };
 // Launched with programmatic stream serialization; it does not wait for the builder.
 cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream);
@@ -203,7 +204,14 @@ cudaError_t launch_transpose_pad(const void* A_kr, void* At_rk, int K, int r, in
 cudaError_t launch_pack_w_bf16(const void* W_kn, void* W_nk, int K, int N, cudaStream_t stream);
 // B expand pool row block of one slot: Bx[n][j] from B [R][N] (see expand_layout).
 cudaError_t launch_pack_bx(const void* B_rn, void* Bx_nw, int R, int N, cudaStream_t stream);
-cudaError_t launch_slot_meta(float* scale, int32_t* rank, int32_t* loaded, int slot, float s,
-                             int r, int is_loaded, cudaStream_t stream);
+// A slot's metadata: the scale of each of its R rank columns (an adapter's alpha / r on its
+// r columns; a composition's w_i alpha_i / r_i on the columns of member i; 0 beyond), its
+// rank and its loaded flag.
+constexpr int kMaxSlotRank = 128;
+struct SlotScales {
+  float v[kMaxSlotRank];
+};
+cudaError_t launch_slot_meta(float* scale, int R, int32_t* rank, int32_t* loaded, int slot,
+                             const SlotScales& cols, int r, int is_loaded, cudaStream_t stream);
 
 }  // namespace lora

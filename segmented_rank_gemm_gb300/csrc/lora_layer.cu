@@ -117,6 +117,11 @@ cudaEvent_t layer_take_event(lora_layer* L) {
   return e;
 }
 
+void layer_set_percol(lora_layer* L, int slot, bool varied) {
+  if ((L->percol[slot] != 0) != varied) L->percol_slots += varied ? 1 : -1;
+  L->percol[slot] = varied ? 1 : 0;
+}
+
 }  // namespace lora
 
 extern "C" {
@@ -156,6 +161,7 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
   const size_t es = L->esize;
   const size_t S = num_slots, R = L->R;
   L->max_tiles = (max_tokens + kTileRows - 1) / kTileRows + num_slots;
+  L->percol.assign(S, 0);
   // small batches split the shrink's K range over up to 8 planes of v; large ones need none
   L->v_planes = dtype == LORA_BF16 ? std::max(1, std::min(8, 65536 / max_tokens)) : 1;
   // the base GEMM of a delta-mode batch may split K: scratch for its largest exchange
@@ -166,7 +172,9 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
             cudaMalloc(&L->A_pool, S * R * K * es) == cudaSuccess &&
             cudaMalloc(&L->B_pool, S * R * N * es) == cudaSuccess &&
             cudaMalloc(&L->A_stage, (size_t)K * R * es) == cudaSuccess &&
-            dmalloc(&L->scale, S) == cudaSuccess && dmalloc(&L->rank, S) == cudaSuccess &&
+            // column scales [S][R], padded so that a read of 32 columns of any slot is in bounds
+            dmalloc(&L->scale, S * R + 32) == cudaSuccess &&
+            dmalloc(&L->rank, S) == cudaSuccess &&
             dmalloc(&L->loaded, S) == cudaSuccess &&
             dmalloc(&L->row_slot, max_tokens) == cudaSuccess &&
             dmalloc(&L->perm, max_tokens) == cudaSuccess &&
@@ -202,7 +210,7 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
        (!L->Bx_pool ||
         cudaMemsetAsync(L->Bx_pool, 0, S * expand_layout((int)R).wx * N * es, stream) ==
             cudaSuccess) &&
-       cudaMemsetAsync(L->scale, 0, S * 4, stream) == cudaSuccess &&
+       cudaMemsetAsync(L->scale, 0, (S * R + 32) * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->rank, 0, S * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->loaded, 0, S * 4, stream) == cudaSuccess &&
        cudaMemsetAsync(L->meta, 0, 32, stream) == cudaSuccess &&
@@ -235,13 +243,22 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
   return LORA_OK;
 }
 
-int load_adapter_slot(lora_layer_t* L, int slot, const void* A_src, const void* B_src, int r,
-                      float alpha, void* side_) {
+int load_adapter_slot_composed(lora_layer_t* L, int slot, int n, const void* const* A_src,
+                               const void* const* B_src, const int* r, const float* alpha,
+                               const float* weight, void* side_) {
   if (!L) return LORA_EINVAL;
   if (slot < 0 || slot >= L->S) return fail(L, LORA_ESLOT, "slot %d outside [0, %d)", slot, L->S);
-  if (r < 1 || r > L->max_rank)
-    return fail(L, LORA_ERANK, "rank %d outside [1, %d]", r, L->max_rank);
-  if (!A_src || !B_src) return fail(L, LORA_EINVAL, "null adapter pointer");
+  if (n < 1 || !A_src || !B_src || !r || !alpha || !weight)
+    return fail(L, LORA_EINVAL, "a composition needs n >= 1 members and their arrays");
+  int r_sum = 0;
+  for (int i = 0; i < n; ++i) {
+    if (r[i] < 1 || r[i] > L->max_rank)
+      return fail(L, LORA_ERANK, "member %d: rank %d outside [1, %d]", i, r[i], L->max_rank);
+    if (!A_src[i] || !B_src[i]) return fail(L, LORA_EINVAL, "member %d: null adapter pointer", i);
+    r_sum += r[i];
+  }
+  if (r_sum > L->max_rank)
+    return fail(L, LORA_ERANK, "composed rank %d above max_rank %d", r_sum, L->max_rank);
   cudaStream_t side = static_cast<cudaStream_t>(side_);
   const size_t es = L->esize;
   const size_t K = L->K, N = L->N, R = L->R;
@@ -249,24 +266,36 @@ int load_adapter_slot(lora_layer_t* L, int slot, const void* A_src, const void* 
   // never overwrite a slot under a forward still in flight, nor the staging buffer under
   // the previous load's transposition
   if (L->have_forward) LORA_CUDA(L, cudaStreamWaitEvent(side, L->last_forward, 0));
-  LORA_CUDA(L, cudaStreamWaitEvent(side, L->stage_free, 0));
-
-  LORA_CUDA(L, cudaMemcpyAsync(L->A_stage, A_src, K * r * es, cudaMemcpyDefault, side));
   char* At = static_cast<char*>(L->A_pool) + (size_t)slot * R * K * es;
-  LORA_CUDA(L, launch_transpose_pad(L->A_stage, At, (int)K, r, (int)R, L->dtype == LORA_BF16,
-                                    side));
-  LORA_CUDA(L, cudaEventRecord(L->stage_free, side));
   char* Bs = static_cast<char*>(L->B_pool) + (size_t)slot * R * N * es;
-  LORA_CUDA(L, cudaMemcpyAsync(Bs, B_src, (size_t)r * N * es, cudaMemcpyDefault, side));
-  if ((size_t)r < R)
-    LORA_CUDA(L, cudaMemsetAsync(Bs + (size_t)r * N * es, 0, (R - r) * N * es, side));
-  if (L->Bx_pool)  // the slot's rows of the B expand pool (rank rows >= r: the zeros just set)
+  SlotScales cols;
+  for (int j = 0; j < kMaxSlotRank; ++j) cols.v[j] = 0.f;
+  // member i occupies rank rows [o, o + r_i) of the slot: A_i^T in At, B_i in B
+  for (int i = 0, o = 0; i < n; o += r[i], ++i) {
+    LORA_CUDA(L, cudaStreamWaitEvent(side, L->stage_free, 0));
+    LORA_CUDA(L, cudaMemcpyAsync(L->A_stage, A_src[i], K * r[i] * es, cudaMemcpyDefault, side));
+    LORA_CUDA(L, launch_transpose_pad(L->A_stage, At + (size_t)o * K * es, (int)K, r[i], r[i],
+                                      L->dtype == LORA_BF16, side));
+    LORA_CUDA(L, cudaEventRecord(L->stage_free, side));
+    LORA_CUDA(L, cudaMemcpyAsync(Bs + (size_t)o * N * es, B_src[i], (size_t)r[i] * N * es,
+                                 cudaMemcpyDefault, side));
+    const float c = weight[i] * (alpha[i] / (float)r[i]);
+    for (int j = o; j < o + r[i]; ++j) cols.v[j] = c;
+  }
+  if ((size_t)r_sum < R) {
+    LORA_CUDA(L, cudaMemsetAsync(At + (size_t)r_sum * K * es, 0, (R - r_sum) * K * es, side));
+    LORA_CUDA(L, cudaMemsetAsync(Bs + (size_t)r_sum * N * es, 0, (R - r_sum) * N * es, side));
+  }
+  if (L->Bx_pool)  // the slot's rows of the B expand pool (rank rows >= r_sum: the zeros just set)
     LORA_CUDA(L, launch_pack_bx(Bs,
                                 static_cast<char*>(L->Bx_pool) +
                                     (size_t)slot * N * expand_layout((int)R).wx * es,
                                 (int)R, (int)N, side));
-  LORA_CUDA(L, launch_slot_meta(L->scale, L->rank, L->loaded, slot, alpha / (float)r, r, 1,
+  LORA_CUDA(L, launch_slot_meta(L->scale, (int)R, L->rank, L->loaded, slot, cols, r_sum, 1,
                                 side));
+  bool varied = false;
+  for (int j = 1; j < r_sum; ++j) varied |= cols.v[j] != cols.v[0];
+  layer_set_percol(L, slot, varied);
   cudaEvent_t ev = layer_take_event(L);
   if (!ev) return fail(L, LORA_ECUDA, "cudaEventCreate failed");
   LORA_CUDA(L, cudaEventRecord(ev, side));
@@ -274,12 +303,21 @@ int load_adapter_slot(lora_layer_t* L, int slot, const void* A_src, const void* 
   return LORA_OK;
 }
 
+int load_adapter_slot(lora_layer_t* L, int slot, const void* A_src, const void* B_src, int r,
+                      float alpha, void* side_) {
+  const float one = 1.f;
+  return load_adapter_slot_composed(L, slot, 1, &A_src, &B_src, &r, &alpha, &one, side_);
+}
+
 int unload_adapter_slot(lora_layer_t* L, int slot, void* side_) {
   if (!L) return LORA_EINVAL;
   if (slot < 0 || slot >= L->S) return fail(L, LORA_ESLOT, "slot %d outside [0, %d)", slot, L->S);
   cudaStream_t side = static_cast<cudaStream_t>(side_);
   if (L->have_forward) LORA_CUDA(L, cudaStreamWaitEvent(side, L->last_forward, 0));
-  LORA_CUDA(L, launch_slot_meta(L->scale, L->rank, L->loaded, slot, 0.f, 0, 0, side));
+  SlotScales none;
+  for (int j = 0; j < kMaxSlotRank; ++j) none.v[j] = 0.f;
+  LORA_CUDA(L, launch_slot_meta(L->scale, L->R, L->rank, L->loaded, slot, none, 0, 0, side));
+  layer_set_percol(L, slot, false);
   cudaEvent_t ev = layer_take_event(L);
   if (!ev) return fail(L, LORA_ECUDA, "cudaEventCreate failed");
   LORA_CUDA(L, cudaEventRecord(ev, side));
@@ -380,6 +418,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     ba.rank = L->rank;
     ba.delta = L->delta;
     ba.num_sms = L->num_sms;
+    ba.per_column = L->percol_slots > 0;
     LORA_CUDA(L, launch_bgmv_delta(ba, stream));
   } else if (bf16) {
     ShrinkTcArgs sa;

@@ -69,13 +69,14 @@ struct Scalar32 {
   __device__ __forceinline__ float operator[](int) const { return raw; }
 };
 
-// Shrink of one tile by one warp: v_s[q][j] = sc * sum_k x[row_q][k] * At[j][k] for the
+// Shrink of one tile by one warp: v_s[q][j] = sc[j] * sum_k x[row_q][k] * At[j][k] for the
 // warp's JW rank columns.  K is a multiple of the vector width (checked on the host).
 template <typename T, typename V, int JW>
 __device__ __forceinline__ void shrink_tile_warp(const T* __restrict__ x, int K,
                                                  const T* __restrict__ At, int r,
-                                                 const int* rows_s, int nr, float sc,
-                                                 float* v_s, int vstride, int warp, int lane) {
+                                                 const int* rows_s, int nr,
+                                                 const float* __restrict__ sc, float* v_s,
+                                                 int vstride, int warp, int lane) {
   constexpr int RB = (16 / JW) < 8 ? (16 / JW) : 8;  // rows per register block
   constexpr int VEC = V::N;
   const int j0 = warp * JW;
@@ -121,7 +122,8 @@ __device__ __forceinline__ void shrink_tile_warp(const T* __restrict__ x, int K,
       for (int qq = 0; qq < RB; ++qq)
 #pragma unroll
         for (int jj = 0; jj < JW; ++jj)
-          if (q0 + qq < nr && j0 + jj < r) v_s[(q0 + qq) * vstride + j0 + jj] = sc * acc[qq][jj];
+          if (q0 + qq < nr && j0 + jj < r)
+            v_s[(q0 + qq) * vstride + j0 + jj] = sc[j0 + jj] * acc[qq][jj];
     }
   }
 }
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     const int g = tile_seg[t];
     const int s = seg_slot[g];
     const int r = rank[s];
-    const float sc = scale[s];
+    const float* sc = scale + (size_t)s * R;  // the slot's column scales
     const int p0 = tile_row0[t];
     const int nr = min(kTileRows, seg_offsets[g + 1] - p0);
     if (tid < nr) rows_s[tid] = perm[p0 + tid];
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(kBgmvThreads, 8)  // <= 64 registers: 4 CTAs f
     const int s = token_slot[row];
     if (s < 0 || s >= S || loaded[s] == 0) continue;  // base only (same decision in all CTAs)
     const int r = rank[s];
-    const float sc = scale[s];
+    const float* sc = scale + (size_t)s * R;  // the slot's column scales
     const __nv_bfloat16* xr = x + (size_t)row * K;
     const __nv_bfloat16* At = At_pool + (size_t)s * R * K;
     float* vp = v_part[buf];
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(kBgmvThreads, 8)  // <= 64 registers: 4 CTAs f
       const uint32_t local = smem_u32(vp + tid);
       float sum = 0.f;
       for (uint32_t d = 0; d < csize; ++d) sum += dsmem_ld(dsmem_map(local, d));
-      v_s[tid] = sc * sum;
+      v_s[tid] = sc[tid] * sum;
     }
     __syncthreads();
 
@@ -367,12 +369,16 @@ static constexpr int kSlotMaxT = 512;  // largest decode batch (the delta buffer
 static constexpr int kStrThreads = 256;
 static constexpr int kStrRedMax = 64;  // rows x rank columns of one shrink pass
 
-// v of NQ rows (rank columns < RMAX) into vdst[q][j], scaled by sc; all threads of the CTA.
+// v of NQ rows (rank columns < RMAX) into vdst[q][j]; all threads of the CTA.  Thread
+// tid < NQ * RMAX finishes column j = tid % RMAX of row tid / RMAX and scales it by `sc`,
+// the scale of that column (a register: a shared-memory table here costs the kernel
+// registers it does not have).
 template <int RMAX, int NQ>
 __device__ __forceinline__ void stream_shrink(const __nv_bfloat16* __restrict__ x,
                                               const int* rows, int K, const __nv_bfloat16* At,
                                               int r, float sc, float (*red)[kStrRedMax],
                                               float (*vdst)[32]) {
+  static_assert(NQ * RMAX <= kStrThreads, "one finished column per thread");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float acc[NQ][RMAX];
 #pragma unroll
@@ -426,7 +432,7 @@ __device__ __forceinline__ void stream_shrink(const __nv_bfloat16* __restrict__ 
       if (lane == 0) red[warp][q * RMAX + j] = t;
     }
   __syncthreads();
-  for (int i = tid; i < NQ * RMAX; i += kStrThreads) {
+  for (int i = tid; i < NQ * RMAX; i += kStrThreads) {  // one pass: i == tid
     const int q = i / RMAX, j = i - q * RMAX;
     float sum = 0.f;
 #pragma unroll
@@ -488,7 +494,9 @@ static constexpr int kStrGroup = 2;
 // schedulers, each holding the registers of its own warps (16K), and a GEMM CTA's 6 warps
 // put 2 warps of ~136 registers on two of them; 2 warps of this kernel must fit beside
 // those for the two kernels to share the SM.
-template <int RMAX, int ROWS>
+// PERCOL: false when every slot's columns share one scale (plain adapters: the scale of
+// column 0 is the slot's), true when a slot holds a composition (one scale per column).
+template <int RMAX, int ROWS, bool PERCOL>
 __global__ void __maxnreg__(120)
     bgmv_stream_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ token_slot,
                        const int32_t* __restrict__ loaded, int T, int K, int N, int R, int S,
@@ -576,7 +584,12 @@ __global__ void __maxnreg__(120)
     }
     const int s = lo, g0 = (it - grp_off[s]) * kStrGroup;  // first row (in slot order)
     const int r = rank[s];  // requested now, needed after the row scan
-    const float sc = scale[s];
+    // the scale of rank column tid % RMAX, the one this thread finishes in the shrink
+    // (columns >= r are zeroed there, so a lane past column R - 1 may read any value: the
+    // scale table is padded by 32 entries, so the read stays inside it).  The per-column
+    // read costs this register-capped kernel a few spilled registers; layers of plain
+    // adapters read one scale per slot instead.
+    const float sc = scale[(size_t)s * R + (PERCOL ? (lane & (RMAX - 1)) : 0)];
     // the slot's A and B rows (two contiguous ranges) requested into L2 now, in 32 KB bulk
     // prefetches from the lanes of warp 0: the DRAM round trips overlap the row scan
     // below, and the loads after it hit L2
@@ -633,12 +646,12 @@ __global__ void __maxnreg__(120)
   }
 }
 
-static cudaError_t launch_bgmv_stream(const BgmvArgs& a, cudaStream_t stream) {
+template <int RMAX, int ROWS, bool PERCOL>
+static cudaError_t launch_bgmv_stream_t(const BgmvArgs& a, cudaStream_t stream) {
   // the SMs it runs on must keep the shared-memory split a GEMM CTA needs, or that CTA
   // waits for them to drain
-  static bool carveout16 = false, carveout32 = false;
-  cudaError_t e = a.R <= 16 ? prefer_max_smem_carveout(bgmv_stream_kernel<16, 2>, &carveout16)
-                            : prefer_max_smem_carveout(bgmv_stream_kernel<32, 1>, &carveout32);
+  static bool carveout = false;
+  cudaError_t e = prefer_max_smem_carveout(bgmv_stream_kernel<RMAX, ROWS, PERCOL>, &carveout);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -651,14 +664,19 @@ static cudaError_t launch_bgmv_stream(const BgmvArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
-  const __nv_bfloat16* At = static_cast<const __nv_bfloat16*>(a.At_pool);
-  const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(a.B_pool);
+  return cudaLaunchKernelEx(&cfg, bgmv_stream_kernel<RMAX, ROWS, PERCOL>,
+                            static_cast<const __nv_bfloat16*>(a.x), a.token_slot, a.loaded, a.T,
+                            a.K, a.N, a.R, a.S, static_cast<const __nv_bfloat16*>(a.At_pool),
+                            static_cast<const __nv_bfloat16*>(a.B_pool), a.scale, a.rank,
+                            a.delta);
+}
+
+static cudaError_t launch_bgmv_stream(const BgmvArgs& a, cudaStream_t stream) {
   if (a.R <= 16)
-    return cudaLaunchKernelEx(&cfg, bgmv_stream_kernel<16, 2>, x, a.token_slot, a.loaded, a.T,
-                              a.K, a.N, a.R, a.S, At, B, a.scale, a.rank, a.delta);
-  return cudaLaunchKernelEx(&cfg, bgmv_stream_kernel<32, 1>, x, a.token_slot, a.loaded, a.T, a.K,
-                            a.N, a.R, a.S, At, B, a.scale, a.rank, a.delta);
+    return a.per_column ? launch_bgmv_stream_t<16, 2, true>(a, stream)
+                        : launch_bgmv_stream_t<16, 2, false>(a, stream);
+  return a.per_column ? launch_bgmv_stream_t<32, 1, true>(a, stream)
+                      : launch_bgmv_stream_t<32, 1, false>(a, stream);
 }
 
 cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream) {

@@ -13,7 +13,11 @@
 // A swap-in moves one adapter image (every layer's slot blocks, already packed on the host
 // in the slot layout) with ONE host-to-device copy into a staging buffer, then ONE kernel
 // scatters it into the slot of every layer and writes the slots' metadata -- instead of
-// two copies and two small kernels per layer -- on the cache's own stream.
+// two copies and two small kernels per layer -- on the cache's own stream (the lowest
+// priority).  Measured beside a pass of the 8B stack (9.3 ms): a swap-in of 80 MiB takes
+// 0.44 ms and makes that pass ~0.3 ms longer; a variant with only the copy engines (two
+// copies per layer straight into the slots, no scatter kernel) took 1.4 ms, most of it
+// host time for the 448 copy calls, and lengthened the pass just as much.
 // Ordering is per slot, so that a swap-in overlaps the batch in flight unless it must
 // replace one of that batch's adapters:
 //   - lora_cache_map_batch(batch, stream) records a point on `stream`: everything enqueued
@@ -51,16 +55,18 @@ size_t align_up(size_t v) { return (v + kImageAlign - 1) / kImageAlign * kImageA
 struct SwapDesc {
   char* A_pool;  // [S][R][K] (A transposed, zero-padded)
   char* B_pool;  // [S][R][N]
-  float* scale;
+  float* scale;  // [S][R] column scales
   int32_t* rank;
   int32_t* loaded;
+  int R;         // the layer's slot width
   unsigned long long a_bytes, b_bytes;  // one slot's A and B block: R*K and R*N elements
   unsigned long long off_a, off_b;      // offsets of those blocks in the adapter image
 };
 
 // Slot `slot` of every layer (blockIdx.y) from the staged adapter image (copy != 0), and
-// the slot's scale, rank and loaded flag (copy == 0: only those, to empty the slot).  The
-// blocks are multiples of 16 bytes (R is a multiple of 8) and start 16-byte aligned.
+// the slot's column scales (s on the r columns of the adapter, 0 beyond), rank and loaded
+// flag (copy == 0: only those, to empty the slot).  The blocks are multiples of 16 bytes
+// (R is a multiple of 8) and start 16-byte aligned.
 __global__ void __launch_bounds__(kSwapThreads)
     swap_in_kernel(const SwapDesc* __restrict__ desc, const char* __restrict__ image, int slot,
                    int copy, float s, int r, int is_loaded) {
@@ -75,10 +81,13 @@ __global__ void __launch_bounds__(kSwapThreads)
     uint4* db = reinterpret_cast<uint4*>(d.B_pool + (size_t)slot * d.b_bytes);
     for (size_t i = first; i < d.b_bytes / 16; i += stride) db[i] = __ldg(sb + i);
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    d.scale[slot] = s;
-    d.rank[slot] = r;
-    d.loaded[slot] = is_loaded;
+  if (blockIdx.x == 0) {
+    for (int j = threadIdx.x; j < d.R; j += kSwapThreads)
+      d.scale[(size_t)slot * d.R + j] = j < r ? s : 0.f;
+    if (threadIdx.x == 0) {
+      d.rank[slot] = r;
+      d.loaded[slot] = is_loaded;
+    }
   }
 }
 
@@ -195,6 +204,7 @@ int swap_in(Cache* c, const Entry& e, int slot) {
     }
   CACHE_CUDA(c, cudaEventRecord(c->ready_ev[slot], c->stream));
   c->ready_pending[slot] = 1;
+  for (lora_layer* L : c->layers) lora::layer_set_percol(L, slot, false);
   c->stats.bytes_swapped += (int64_t)c->image_bytes;
   return LORA_OK;
 }
@@ -208,6 +218,7 @@ int empty_slot(Cache* c, int slot) {
   swap_in_kernel<<<dim3(1, (unsigned)c->layers.size()), kSwapThreads, 0, c->stream>>>(
       c->desc_dev, c->staging, slot, 0, 0.f, 0, 0);
   CACHE_CUDA(c, cudaGetLastError());
+  for (lora_layer* L : c->layers) lora::layer_set_percol(L, slot, false);
   CACHE_CUDA(c, cudaEventRecord(c->ready_ev[slot], c->stream));
   c->ready_pending[slot] = 1;
   return LORA_OK;
@@ -406,6 +417,7 @@ int lora_cache_create(lora_adapter_cache_t** out, lora_layer_t* const* layers, i
     d.scale = L->scale;
     d.rank = L->rank;
     d.loaded = L->loaded;
+    d.R = L->R;
     d.a_bytes = (unsigned long long)L->R * L->K * L->esize;
     d.b_bytes = (unsigned long long)L->R * L->N * L->esize;
     d.off_a = off;
@@ -437,7 +449,11 @@ int lora_cache_create(lora_adapter_cache_t** out, lora_layer_t* const* layers, i
       cudaGetLastError();
       return bail(LORA_ENOMEM);
     }
-    if (cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking) != cudaSuccess)
+    // swap-ins are background work: the lowest priority, so that the scatter's CTAs take
+    // SMs only after the forwards' pending CTAs
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&c->stream, cudaStreamNonBlocking, least) != cudaSuccess)
       return bail(LORA_ECUDA);
     for (int b = 0; b < host_capacity; ++b)
       if (cudaEventCreateWithFlags(&c->block_ev[b], cudaEventDisableTiming) != cudaSuccess)

@@ -34,7 +34,8 @@
 //               items, so an item's epilogue overlaps the next main loop.
 //   warps 2..5  epilogue: each thread owns one window row (TMEM lane): if the row belongs to
 //               one of the unit's segments, it multiplies that segment's Rt columns by the
-//               slot's alpha / r and stores the row's R fp32 values at v[kp][perm row].
+//               slot's column scales (alpha / r; w_i alpha_i / r_i on the columns of member
+//               i of a composition) and stores the row's R fp32 values at v[kp][perm row].
 // The x bytes dominate (every adapted row is read once per K range and unit of its
 // window); each A_s is read once per unit.
 // Launch: programmatic dependent launch after the segment builder; the kernel lets the base
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
       const int slot = ui.slot[g];
       mbar_arrive(&info_empty[ib]);
       const int grow = live ? a.perm[p] : 0;
-      const float sc = live ? a.scale[slot] : 0.f;
+      const float* sc = a.scale + (size_t)slot * a.R;  // the slot's column scales
       float* vrow = a.v + (size_t)kp * a.plane_stride + (size_t)grow * a.R;
       const int buf = item & 1;
       const uint32_t use = (uint32_t)(item >> 1);
@@ -279,10 +280,12 @@ __global__ void __launch_bounds__(kShThreads, 1)
         if (live && j >= 0 && j < Rt) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            if (j + 4 * q < a.R)
+            if (j + 4 * q < a.R) {
+              const float4 c = __ldg(reinterpret_cast<const float4*>(sc + j + 4 * q));
               *reinterpret_cast<float4*>(vrow + j + 4 * q) = make_float4(
-                  sc * __uint_as_float(raw[4 * q]), sc * __uint_as_float(raw[4 * q + 1]),
-                  sc * __uint_as_float(raw[4 * q + 2]), sc * __uint_as_float(raw[4 * q + 3]));
+                  c.x * __uint_as_float(raw[4 * q]), c.y * __uint_as_float(raw[4 * q + 1]),
+                  c.z * __uint_as_float(raw[4 * q + 2]), c.w * __uint_as_float(raw[4 * q + 3]));
+            }
         }
       }
       tc_fence_before();

@@ -91,16 +91,19 @@ cudaError_t launch_pack_bx(const void* B_rn, void* Bx_nw, int R, int N, cudaStre
   return cudaGetLastError();
 }
 
-__global__ void slot_meta_kernel(float* scale, int32_t* rank, int32_t* loaded, int slot, float s,
-                                 int r, int is_loaded) {
-  scale[slot] = s;
-  rank[slot] = r;
-  loaded[slot] = is_loaded;
+__global__ void slot_meta_kernel(float* scale, int R, int32_t* rank, int32_t* loaded, int slot,
+                                 SlotScales cols, int r, int is_loaded) {
+  for (int j = threadIdx.x; j < R; j += blockDim.x) scale[(size_t)slot * R + j] = cols.v[j];
+  if (threadIdx.x == 0) {
+    rank[slot] = r;
+    loaded[slot] = is_loaded;
+  }
 }
 
-cudaError_t launch_slot_meta(float* scale, int32_t* rank, int32_t* loaded, int slot, float s,
-                             int r, int is_loaded, cudaStream_t stream) {
-  slot_meta_kernel<<<1, 1, 0, stream>>>(scale, rank, loaded, slot, s, r, is_loaded);
+cudaError_t launch_slot_meta(float* scale, int R, int32_t* rank, int32_t* loaded, int slot,
+                             const SlotScales& cols, int r, int is_loaded, cudaStream_t stream) {
+  slot_meta_kernel<<<1, kMaxSlotRank, 0, stream>>>(scale, R, rank, loaded, slot, cols, r,
+                                                   is_loaded);
   return cudaGetLastError();
 }
 

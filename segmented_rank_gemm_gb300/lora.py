@@ -27,7 +27,8 @@ LORA_ECUDA, LORA_ENOMEM, LORA_ESTATE, LORA_ETIMEOUT = -5, -6, -7, -8
 LORA_ENOENT, LORA_ECAPACITY = -9, -10
 
 # every entry point declared in include/lora_layer.h
-ABI_FUNCTIONS = ("lora_layer_create", "load_adapter_slot", "unload_adapter_slot",
+ABI_FUNCTIONS = ("lora_layer_create", "load_adapter_slot", "load_adapter_slot_composed",
+                 "unload_adapter_slot",
                  "set_batch_segments", "lora_forward", "lora_forward_host", "lora_get_status",
                  "lora_get_segments", "lora_set_trace_events", "lora_set_gemm_plan",
                  "lora_last_error", "lora_layer_destroy", "lora_build_segments_static")
@@ -63,6 +64,7 @@ def _load() -> ctypes.CDLL:
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     L.lora_layer_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32, vp, vp]
     L.load_adapter_slot.argtypes = [vp, i32, vp, vp, i32, f32, vp]
+    L.load_adapter_slot_composed.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp]
     L.unload_adapter_slot.argtypes = [vp, i32, vp]
     L.set_batch_segments.argtypes = [vp, vp, i32, vp]
     L.lora_forward.argtypes = [vp, vp, vp, i32, vp]
@@ -156,6 +158,20 @@ def lora_layer_create(K, N, num_slots, max_rank, max_tokens, dtype, W, stream=No
 def load_adapter_slot(layer, slot, A, B, r, alpha, side_stream=None) -> None:
     _check(layer, _lib.load_adapter_slot(layer, slot, _ptr(A), _ptr(B), r, float(alpha),
                                          _stream(side_stream)))
+
+
+def load_adapter_slot_composed(layer, slot, members, side_stream=None) -> None:
+    """``members``: list of (A [K, r], B [r, N], alpha, weight) tensors/values."""
+    n = len(members)
+    A = (ctypes.c_void_p * n)(*[_ptr(m[0]) for m in members])
+    B = (ctypes.c_void_p * n)(*[_ptr(m[1]) for m in members])
+    r = (ctypes.c_int * n)(*[int(m[0].shape[1]) for m in members])
+    al = (ctypes.c_float * n)(*[float(m[2]) for m in members])
+    w = (ctypes.c_float * n)(*[float(m[3]) for m in members])
+    _check(layer, _lib.load_adapter_slot_composed(
+        layer, slot, n, ctypes.cast(A, ctypes.c_void_p), ctypes.cast(B, ctypes.c_void_p),
+        ctypes.cast(r, ctypes.c_void_p), ctypes.cast(al, ctypes.c_void_p),
+        ctypes.cast(w, ctypes.c_void_p), _stream(side_stream)))
 
 
 def unload_adapter_slot(layer, slot, side_stream=None) -> None:
@@ -257,6 +273,18 @@ class LoraLayer:
             raise ValueError("A must be [K, r] and B [r, N]")
         load_adapter_slot(self.handle, slot, A, B, r, alpha, side_stream)
         self._keep[slot] = (A, B)  # keep sources alive until the copy has run
+
+    def load_composed(self, slot: int, members, side_stream=None):
+        """``members``: list of (A [K, r_i], B [r_i, N], alpha_i, weight_i)."""
+        members = [(A.contiguous(), B.contiguous(), alpha, w) for A, B, alpha, w in members]
+        for A, B, _, _ in members:
+            if A.dtype != self.dtype or B.dtype != self.dtype:
+                raise ValueError("adapter dtype must match the layer dtype")
+            r = int(A.shape[1])
+            if tuple(A.shape) != (self.K, r) or tuple(B.shape) != (r, self.N):
+                raise ValueError("A must be [K, r] and B [r, N]")
+        load_adapter_slot_composed(self.handle, slot, members, side_stream)
+        self._keep[slot] = members  # keep sources alive until the copies have run
 
     def unload(self, slot: int, side_stream=None):
         unload_adapter_slot(self.handle, slot, side_stream)
