@@ -246,6 +246,18 @@ int lora_build_segments_static(const int32_t* token_slot_dev, int T, int num_slo
                                int32_t* seg_offsets_dev, int32_t* seg_slot_dev,
                                int32_t* counts_dev, void* stream);
 
+/*
+ * Self-test of the bounded waits that every pipeline kernel of this library uses (the pages
+ * have no counterpart).  Runs one kernel on `stream` whose wait nothing will complete --
+ * which = 0: a flag in global memory (as the stream-K hand-over), 1: an mbarrier phase (as
+ * the TMA / MMA / epilogue pipelines) -- and synchronises `stream`.  The wait gives up
+ * after its bound (2 s of global time), raises the timeout flag and returns, so the call
+ * takes ~2 s and returns LORA_ETIMEOUT, the expected result; the context stays usable.
+ * LORA_OK would mean the wait completed.  Allocates 8 bytes of device memory for the call.
+ * Errors: LORA_EINVAL (which), LORA_ENOMEM, LORA_ECUDA.
+ */
+int lora_wait_selftest(int which, void* stream);
+
 /* Text of the last error raised on this layer ("" if none).  Owned by the layer. */
 const char* lora_last_error(const lora_layer_t* layer);
 

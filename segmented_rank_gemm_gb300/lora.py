@@ -31,7 +31,8 @@ ABI_FUNCTIONS = ("lora_layer_create", "load_adapter_slot", "load_adapter_slot_co
                  "unload_adapter_slot",
                  "set_batch_segments", "lora_forward", "lora_forward_host", "lora_get_status",
                  "lora_get_segments", "lora_set_trace_events", "lora_set_gemm_plan",
-                 "lora_last_error", "lora_layer_destroy", "lora_build_segments_static")
+                 "lora_last_error", "lora_layer_destroy", "lora_build_segments_static",
+                 "lora_wait_selftest")
 # every entry point declared in include/lora_residency.h
 CACHE_FUNCTIONS = ("lora_cache_create", "lora_cache_add", "lora_cache_remove",
                    "lora_cache_map_batch", "lora_cache_prefetch", "lora_cache_slot_of",
@@ -74,6 +75,7 @@ def _load() -> ctypes.CDLL:
     L.lora_set_trace_events.argtypes = [vp, vp]
     L.lora_set_gemm_plan.argtypes = [vp, i32, i32, i32]
     L.lora_build_segments_static.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp]
+    L.lora_wait_selftest.argtypes = [i32, vp]
     L.lora_last_error.argtypes = [vp]
     L.lora_last_error.restype = ctypes.c_char_p
     L.lora_layer_destroy.argtypes = [vp]
@@ -236,6 +238,12 @@ def lora_build_segments_static(token_slot, T, num_slots, slot_loaded, perm, seg_
                                          _ptr(counts), _stream(stream))
     if rc < 0:
         raise LoraError(rc, "lora_build_segments_static")
+
+
+def lora_wait_selftest(which: int, stream=None) -> int:
+    """Run one bounded wait that nothing completes; returns the status (LORA_ETIMEOUT is
+    the expected result) without raising."""
+    return _lib.lora_wait_selftest(int(which), _stream(stream))
 
 
 def lora_last_error(layer) -> str:
