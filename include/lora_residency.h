@@ -117,6 +117,24 @@ int lora_cache_add(lora_adapter_cache_t* cache, int64_t id, int r, float alpha,
                    const void* const* A_host, const void* const* B_host);
 
 /*
+ * Put a composition of adapters already in the host tier into it under its own id
+ * ("Multi-LoRA Serving 与 Adapter 隔离", adapter ownership: a request may compose several
+ * LoRAs, which are added; its identity is the ordered members with their weights, so a
+ * composition is an adapter of its own here).  Rows naming `id` then add
+ *     sum_m weights[m] * (its own scaled delta of member_ids[m])
+ * -- the members stacked along the rank axis as load_adapter_slot_composed does, each
+ * column keeping its member's scale times the weight.  The image is packed from the
+ * members' host blocks at this call (later changes to a member do not reach it).
+ *   member_ids[0..n): ids in the host tier (not `id` itself); their ranks sum to at most
+ *   every layer's max_rank.
+ * Room is made as lora_cache_add does, never by dropping a member.
+ * Errors: LORA_EINVAL, LORA_ENOENT (a member), LORA_ERANK (the summed rank),
+ * LORA_ECAPACITY (the tier holds only members), LORA_ECUDA.
+ */
+int lora_cache_add_composed(lora_adapter_cache_t* cache, int64_t id, int n,
+                            const int64_t* member_ids, const float* weights);
+
+/*
  * Drop adapter `id` from both tiers.  Its GPU slot, if any, is emptied at once, or, if the
  * last mapped batch uses it, blocked until the next batch point (see "Ordering").
  * Errors: LORA_ENOENT, LORA_ECUDA.

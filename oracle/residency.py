@@ -87,6 +87,26 @@ class ResidencyModel:
         self.host.append(a)
         self._touch(a)
 
+    def add_composed(self, a, members):
+        """A composition of adapters in the host tier, held under its own id ``a``; room is
+        never made by dropping a member."""
+        if a < 0 or a in members:
+            raise ResidencyError("invalid")
+        if any(m not in self.host for m in members):
+            raise ResidencyError("unknown")
+        if a in self.host:
+            self._free_slot_of(a)
+            self._touch(a)
+            return
+        if len(self.host) == self.host_capacity:
+            cands = [b for b in self.recency if b in self.host and b not in members]
+            if not cands:
+                raise ResidencyError("capacity")
+            self.remove(cands[0])
+            self.stats["host_evictions"] += 1
+        self.host.append(a)
+        self._touch(a)
+
     def remove(self, a):
         if a not in self.host:
             raise ResidencyError("unknown")

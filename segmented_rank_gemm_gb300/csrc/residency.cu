@@ -64,12 +64,12 @@ struct SwapDesc {
 };
 
 // Slot `slot` of every layer (blockIdx.y) from the staged adapter image (copy != 0), and
-// the slot's column scales (s on the r columns of the adapter, 0 beyond), rank and loaded
-// flag (copy == 0: only those, to empty the slot).  The blocks are multiples of 16 bytes
-// (R is a multiple of 8) and start 16-byte aligned.
+// the slot's column scales (cols on the r columns of the adapter, 0 beyond), rank and
+// loaded flag (copy == 0: only those, to empty the slot).  The blocks are multiples of 16
+// bytes (R is a multiple of 8) and start 16-byte aligned.
 __global__ void __launch_bounds__(kSwapThreads)
     swap_in_kernel(const SwapDesc* __restrict__ desc, const char* __restrict__ image, int slot,
-                   int copy, float s, int r, int is_loaded) {
+                   int copy, lora::SlotScales cols, int r, int is_loaded) {
   const SwapDesc d = desc[blockIdx.y];
   if (copy) {
     const size_t stride = (size_t)gridDim.x * kSwapThreads;
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kSwapThreads)
   }
   if (blockIdx.x == 0) {
     for (int j = threadIdx.x; j < d.R; j += kSwapThreads)
-      d.scale[(size_t)slot * d.R + j] = j < r ? s : 0.f;
+      d.scale[(size_t)slot * d.R + j] = j < r ? cols.v[j] : 0.f;
     if (threadIdx.x == 0) {
       d.rank[slot] = r;
       d.loaded[slot] = is_loaded;
@@ -93,8 +93,9 @@ __global__ void __launch_bounds__(kSwapThreads)
 
 struct Entry {
   int block = -1;          // host block holding the packed image
-  int r = 0;
+  int r = 0;               // rank (a composition: the sum of its members' ranks)
   float alpha = 0.f;
+  std::vector<float> cols;  // a composition's column scales (empty: alpha / r on all r)
   int slot = -1;           // GPU slot, -1 = not resident
   unsigned long long last_use = 0;
   unsigned long long pin = 0;  // == the cache's pin generation: named by the current request
@@ -188,9 +189,14 @@ int swap_in(Cache* c, const Entry& e, int slot) {
                                 c->image_bytes, cudaMemcpyHostToDevice, c->stream));
   CACHE_CUDA(c, cudaEventRecord(c->block_ev[e.block], c->stream));
   c->block_ev_used[e.block] = 1;
+  lora::SlotScales cols;
+  bool varied = false;
+  for (int j = 0; j < lora::kMaxSlotRank; ++j)
+    cols.v[j] = j >= e.r ? 0.f : e.cols.empty() ? e.alpha / (float)e.r : e.cols[j];
+  for (int j = 1; j < e.r; ++j) varied |= cols.v[j] != cols.v[0];
   dim3 grid(swap_grid_x(c), (unsigned)c->layers.size());
-  swap_in_kernel<<<grid, kSwapThreads, 0, c->stream>>>(c->desc_dev, c->staging, slot, 1,
-                                                       e.alpha / (float)e.r, e.r, 1);
+  swap_in_kernel<<<grid, kSwapThreads, 0, c->stream>>>(c->desc_dev, c->staging, slot, 1, cols,
+                                                       e.r, 1);
   CACHE_CUDA(c, cudaGetLastError());
   // layers that expand v on the tensor cores keep a transposed copy of B per slot
   for (lora_layer* L : c->layers)
@@ -204,7 +210,7 @@ int swap_in(Cache* c, const Entry& e, int slot) {
     }
   CACHE_CUDA(c, cudaEventRecord(c->ready_ev[slot], c->stream));
   c->ready_pending[slot] = 1;
-  for (lora_layer* L : c->layers) lora::layer_set_percol(L, slot, false);
+  for (lora_layer* L : c->layers) lora::layer_set_percol(L, slot, varied);
   c->stats.bytes_swapped += (int64_t)c->image_bytes;
   return LORA_OK;
 }
@@ -215,8 +221,10 @@ int empty_slot(Cache* c, int slot) {
   if (c->layers.empty()) return LORA_OK;
   int rc = wait_slot_idle(c, slot);
   if (rc != LORA_OK) return rc;
+  lora::SlotScales none;
+  for (int j = 0; j < lora::kMaxSlotRank; ++j) none.v[j] = 0.f;
   swap_in_kernel<<<dim3(1, (unsigned)c->layers.size()), kSwapThreads, 0, c->stream>>>(
-      c->desc_dev, c->staging, slot, 0, 0.f, 0, 0);
+      c->desc_dev, c->staging, slot, 0, none, 0, 0);
   CACHE_CUDA(c, cudaGetLastError());
   for (lora_layer* L : c->layers) lora::layer_set_percol(L, slot, false);
   CACHE_CUDA(c, cudaEventRecord(c->ready_ev[slot], c->stream));
@@ -470,6 +478,50 @@ int lora_cache_create(lora_adapter_cache_t** out, lora_layer_t* const* layers, i
   return LORA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Take a host block for adapter `id` (its own block if it is held already: the adapter is
+// replaced in place and its slot emptied; else a free block, dropping the least recently
+// used adapter -- never one of `keep` -- if the tier is full) and wait until no swap-in
+// still reads it.  The caller has checked the adapter; only now is room made.
+int take_block(Cache* c, long long id, const std::vector<long long>& keep, int* block) {
+  auto it = c->entries.find(id);
+  if (it != c->entries.end()) {  // in-place replacement
+    *block = it->second.block;
+    if (it->second.slot >= 0) {
+      const int rc = release_slot(c, it->second.slot);
+      if (rc != LORA_OK) return rc;
+      it->second.slot = -1;
+    }
+  } else {
+    if (c->free_blocks.empty()) {
+      long long oldest = -1;
+      unsigned long long t = ~0ull;
+      for (const auto& kv : c->entries)
+        if (kv.second.last_use < t &&
+            std::find(keep.begin(), keep.end(), kv.first) == keep.end()) {
+          t = kv.second.last_use;
+          oldest = kv.first;
+        }
+      if (oldest < 0) return fail(c, LORA_ECAPACITY, "no host block can be freed");
+      const int rc = drop(c, oldest);
+      if (rc != LORA_OK) return rc;
+      ++c->stats.host_evictions;
+    }
+    *block = c->free_blocks.back();
+    c->free_blocks.pop_back();
+  }
+  if (!c->layers.empty() && c->block_ev_used[*block])
+    CACHE_CUDA(c, cudaEventSynchronize(c->block_ev[*block]));
+  return LORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int lora_cache_add(lora_adapter_cache_t* c, int64_t id, int r, float alpha,
                    const void* const* A_host, const void* const* B_host) {
   if (!c) return LORA_EINVAL;
@@ -485,39 +537,73 @@ int lora_cache_add(lora_adapter_cache_t* c, int64_t id, int r, float alpha,
     }
   }
   // the adapter is valid: only now make room for it
-  int block;
-  auto it = c->entries.find(id);
-  if (it != c->entries.end()) {  // in-place replacement
-    block = it->second.block;
-    if (it->second.slot >= 0) {
-      const int rc = release_slot(c, it->second.slot);
-      if (rc != LORA_OK) return rc;
-      it->second.slot = -1;
-    }
-  } else {
-    if (c->free_blocks.empty()) {
-      long long oldest = -1;
-      unsigned long long t = ~0ull;
-      for (const auto& kv : c->entries)
-        if (kv.second.last_use < t) {
-          t = kv.second.last_use;
-          oldest = kv.first;
-        }
-      const int rc = drop(c, oldest);
-      if (rc != LORA_OK) return rc;
-      ++c->stats.host_evictions;
-    }
-    block = c->free_blocks.back();
-    c->free_blocks.pop_back();
-  }
-  if (!c->layers.empty()) {
-    if (c->block_ev_used[block]) CACHE_CUDA(c, cudaEventSynchronize(c->block_ev[block]));
+  int block = -1;
+  const int rc = take_block(c, id, {}, &block);
+  if (rc != LORA_OK) return rc;
+  if (!c->layers.empty())
     pack_image(c, c->arena + (size_t)block * c->image_bytes, r, A_host, B_host);
-  }
   Entry& e = c->entries[id];
   e.block = block;
   e.r = r;
   e.alpha = alpha;
+  e.cols.clear();
+  e.slot = -1;
+  e.last_use = ++c->clock;
+  return LORA_OK;
+}
+
+int lora_cache_add_composed(lora_adapter_cache_t* c, int64_t id, int n,
+                            const int64_t* member_ids, const float* weights) {
+  if (!c) return LORA_EINVAL;
+  if (id < 0) return fail(c, LORA_EINVAL, "adapter id %lld < 0", (long long)id);
+  if (n < 1 || !member_ids || !weights) return fail(c, LORA_EINVAL, "bad composition");
+  int r_sum = 0;
+  std::vector<long long> members;
+  for (int m = 0; m < n; ++m)
+    if (member_ids[m] == id)
+      return fail(c, LORA_EINVAL, "a composition cannot name its own id");
+  for (int m = 0; m < n; ++m) {
+    auto it = c->entries.find(member_ids[m]);
+    if (it == c->entries.end())
+      return fail(c, LORA_ENOENT, "member %lld is not in the cache", (long long)member_ids[m]);
+    r_sum += it->second.r;
+    members.push_back(member_ids[m]);
+  }
+  if (r_sum > c->max_r)
+    return fail(c, LORA_ERANK, "composed rank %d above %d", r_sum, c->max_r);
+  // the members' column scales, weighted, in member order
+  std::vector<float> cols;
+  for (int m = 0; m < n; ++m) {
+    const Entry& me = c->entries[members[m]];
+    for (int j = 0; j < me.r; ++j)
+      cols.push_back(weights[m] * (me.cols.empty() ? me.alpha / (float)me.r : me.cols[j]));
+  }
+  int block = -1;
+  const int rc = take_block(c, id, members, &block);  // never drops a member
+  if (rc != LORA_OK) return rc;
+  if (!c->layers.empty()) {
+    // rank rows of member m follow those of members 0 .. m-1, in every layer's blocks
+    char* dst = c->arena + (size_t)block * c->image_bytes;
+    for (size_t l = 0; l < c->layers.size(); ++l) {
+      const lora_layer* L = c->layers[l];
+      const size_t es = L->esize, K = L->K, N = L->N, R = L->R;
+      size_t o = 0;
+      for (int m = 0; m < n; ++m) {
+        const Entry& me = c->entries[members[m]];
+        const char* src = c->arena + (size_t)me.block * c->image_bytes;
+        memmove(dst + c->desc[l].off_a + o * K * es, src + c->desc[l].off_a, me.r * K * es);
+        memmove(dst + c->desc[l].off_b + o * N * es, src + c->desc[l].off_b, me.r * N * es);
+        o += me.r;
+      }
+      memset(dst + c->desc[l].off_a + o * K * es, 0, (R - o) * K * es);
+      memset(dst + c->desc[l].off_b + o * N * es, 0, (R - o) * N * es);
+    }
+  }
+  Entry& e = c->entries[id];
+  e.block = block;
+  e.r = r_sum;
+  e.alpha = 0.f;
+  e.cols = cols;
   e.slot = -1;
   e.last_use = ++c->clock;
   return LORA_OK;

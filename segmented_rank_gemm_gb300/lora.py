@@ -34,7 +34,8 @@ ABI_FUNCTIONS = ("lora_layer_create", "load_adapter_slot", "load_adapter_slot_co
                  "lora_last_error", "lora_layer_destroy", "lora_build_segments_static",
                  "lora_wait_selftest")
 # every entry point declared in include/lora_residency.h
-CACHE_FUNCTIONS = ("lora_cache_create", "lora_cache_add", "lora_cache_remove",
+CACHE_FUNCTIONS = ("lora_cache_create", "lora_cache_add", "lora_cache_add_composed",
+                   "lora_cache_remove",
                    "lora_cache_map_batch", "lora_cache_prefetch", "lora_cache_slot_of",
                    "lora_cache_get_stats", "lora_cache_stream", "lora_cache_sync",
                    "lora_cache_last_error", "lora_cache_destroy")
@@ -86,6 +87,7 @@ def _load() -> ctypes.CDLL:
     i64 = ctypes.c_int64
     L.lora_cache_create.argtypes = [ctypes.POINTER(vp), vp, i32, i32, i32]
     L.lora_cache_add.argtypes = [vp, i64, i32, f32, vp, vp]
+    L.lora_cache_add_composed.argtypes = [vp, i64, i32, vp, vp]
     L.lora_cache_remove.argtypes = [vp, i64]
     L.lora_cache_map_batch.argtypes = [vp, vp, i32, vp, vp]
     L.lora_cache_prefetch.argtypes = [vp, vp, i32]
@@ -98,7 +100,8 @@ def _load() -> ctypes.CDLL:
     L.lora_cache_last_error.restype = ctypes.c_char_p
     L.lora_cache_destroy.argtypes = [vp]
     L.lora_cache_destroy.restype = None
-    for name in ("lora_cache_create", "lora_cache_add", "lora_cache_remove",
+    for name in ("lora_cache_create", "lora_cache_add", "lora_cache_add_composed",
+                 "lora_cache_remove",
                  "lora_cache_map_batch", "lora_cache_prefetch", "lora_cache_slot_of",
                  "lora_cache_get_stats", "lora_cache_sync"):
         getattr(L, name).restype = i32
@@ -373,6 +376,17 @@ def lora_cache_add(cache, adapter_id: int, r: int, alpha: float, A_host=(), B_ho
                                             ctypes.cast(B, ctypes.c_void_p) if n else None))
 
 
+def lora_cache_add_composed(cache, adapter_id: int, member_ids, weights) -> None:
+    import numpy as np
+    m = np.ascontiguousarray(member_ids, dtype=np.int64)
+    w = np.ascontiguousarray(weights, dtype=np.float32)
+    if m.shape != w.shape:
+        raise ValueError("one weight per member")
+    _check_cache(cache, _lib.lora_cache_add_composed(cache, int(adapter_id), len(m),
+                                                     m.ctypes.data if len(m) else None,
+                                                     w.ctypes.data if len(w) else None))
+
+
 def lora_cache_remove(cache, adapter_id: int) -> None:
     _check_cache(cache, _lib.lora_cache_remove(cache, int(adapter_id)))
 
@@ -442,6 +456,9 @@ class AdapterCache:
         if r is None:
             r = int(A_list[0].shape[1])
         lora_cache_add(self.handle, adapter_id, r, alpha, A_list, B_list)
+
+    def add_composed(self, adapter_id: int, member_ids, weights) -> None:
+        lora_cache_add_composed(self.handle, adapter_id, member_ids, weights)
 
     def remove(self, adapter_id: int) -> None:
         lora_cache_remove(self.handle, adapter_id)

@@ -195,8 +195,8 @@ def test_library_books_match_model(lib, seed, S, H, n_ids):
     model = ResidencyModel(S, H)
     try:
         for step in range(600):
-            op = rng.choice(["add", "add_bad", "remove", "batch", "prefetch"],
-                            p=[0.2, 0.03, 0.07, 0.55, 0.15])
+            op = rng.choice(["add", "add_bad", "compose", "remove", "batch", "prefetch"],
+                            p=[0.18, 0.03, 0.04, 0.07, 0.53, 0.15])
             if op == "add":
                 a = int(rng.integers(0, n_ids))
                 _, rc = _lib_call(lib, lib.lora_cache_add, cache, a, 4, 8.0)
@@ -206,6 +206,12 @@ def test_library_books_match_model(lib, seed, S, H, n_ids):
                 _, rc = _lib_call(lib, lib.lora_cache_add, cache, a, 0, 8.0)
                 _, rm = _model_call(model.add, a, False)
                 rc = -1 if rc == -3 else rc  # the library says which check failed
+            elif op == "compose":  # a composition of 1..3 ids (some maybe absent)
+                a = int(rng.integers(0, n_ids))
+                members = [int(v) for v in rng.choice(n_ids, size=int(rng.integers(1, 4)))]
+                _, rc = _lib_call(lib, lib.lora_cache_add_composed, cache, a, members,
+                                  [0.5] * len(members))
+                _, rm = _model_call(model.add_composed, a, members)
             elif op == "remove":
                 a = int(rng.integers(0, n_ids))
                 _, rc = _lib_call(lib, lib.lora_cache_remove, cache, a)

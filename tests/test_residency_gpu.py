@@ -178,3 +178,41 @@ def test_swap_in_through_many_layers_and_capacity_errors():
         for y in ys[::7]:
             assert_parity(y, ref, BF16, what="20-layer image, step %d" % step)
     cache.close()
+
+
+def test_composed_adapters_through_the_cache():
+    """Compositions held under their own ids beside plain adapters: packed from the members'
+    host blocks (so removing a member later leaves them intact), swapped in like any
+    adapter, rows naming them add their members' weighted deltas."""
+    wls = _universe()
+    layers, cache = _build(wls, host=N_IDS + 4)
+    compositions = {20: ([0, 3, 7], [0.5, -1.0, 2.0]), 21: ([2, 6], [1.0, 0.25]),
+                    22: ([2, 2], [0.5, 0.5])}
+    for cid, (members, weights) in compositions.items():
+        cache.add_composed(cid, members, weights)
+    cache.remove(7)  # the composition 20 keeps its own copy
+    per_layer = []
+    for wl in wls:
+        comps = {a: [(A, B, al, 1.0)] for a, (A, B, al) in enumerate(wl.adapters)}
+        for cid, (members, weights) in compositions.items():
+            comps[cid] = [(*wl.adapters[m], w) for m, w in zip(members, weights)]
+        per_layer.append(comps)
+    stream = torch.cuda.Stream()
+    rng = np.random.default_rng(21)
+    runs = []
+    for step, names in enumerate([[20, 1], [21, 22, 20], [0, 21, 5, 22], [20, 21]]):
+        T = 200 if step % 2 == 0 else 600
+        ids = np.where(rng.random(T) < 0.1, -1, rng.choice(names, size=T)).astype(np.int64)
+        runs.append((ids, _run_batch(layers, cache, wls, ids, 300 + step, stream)[1]))
+    torch.cuda.synchronize()
+    for step, (ids, outs) in enumerate(runs):
+        for wl, comps, (x, y) in zip(wls, per_layer, outs):
+            order = sorted(comps)
+            index = {a: i for i, a in enumerate(order)}
+            slot_ids = torch.tensor([index[int(a)] if a >= 0 else -1 for a in ids],
+                                    dtype=torch.int32)
+            ref = oracle.forward_composed(x, wl.W, [comps[a] for a in order], slot_ids)
+            assert_parity(y, ref, wl.dtype, what="composed ids, step %d K=%d" % (step, wl.K))
+    for L in layers:
+        assert L.status(stream) == 0
+    cache.close()
