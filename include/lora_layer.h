@@ -77,6 +77,32 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
                       int max_tokens, int dtype, const void* W_dev, void* stream);
 
 /*
+ * As lora_layer_create, with adapters stored at their true rank in a row pool instead of
+ * one max_rank-wide block per slot ("Multi-LoRA Serving: Architecture for Thousands of
+ * Adapters", sections on heterogeneous ranks and S-LoRA's kernels: a rank-8 and a rank-64
+ * adapter in one batch without padding every adapter to the maximum rank; the adapters are
+ * kept in a non-contiguous, ragged layout the kernels index per request).
+ *   pool_rows  rank rows of the pool, rounded up to 8: at least max_rank rounded up to 8, at
+ *              most num_slots times that.  The A pool takes pool_rows x K and the B pool
+ *              pool_rows x N elements (a plain layer: num_slots x max_rank rounded to 8).
+ * A load takes the adapter's rank rounded up to 8 consecutive rows, first fit, after
+ * returning the rows its slot held; an unload returns them.  A load that finds no such run
+ * of free rows fails with LORA_ENOMEM and leaves the slot as it was.  Every kernel reads a
+ * slot from its first row, so results equal those of a plain layer.  Adapter caches do
+ * not manage pooled layers.
+ * Errors: as lora_layer_create; LORA_EINVAL for pool_rows out of range.
+ */
+int lora_layer_create_pooled(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
+                             int max_tokens, int dtype, const void* W_dev, void* stream,
+                             int pool_rows);
+
+/*
+ * The layer's pool rows in use (held by loaded slots; a plain layer: all of them) and in
+ * total.  Host bookkeeping only, no synchronisation.  Errors: LORA_EINVAL (null).
+ */
+int lora_get_pool_usage(const lora_layer_t* layer, int* used_rows, int* pool_rows);
+
+/*
  * Copy one adapter into slot `slot` ("activation" in vLLM's Step 3).
  *   A_src      [K,r] row-major, B_src [r,N] row-major, the layer's dtype.  Host (pinned
  *              for a truly asynchronous copy) or device memory; it must stay valid and

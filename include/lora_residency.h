@@ -90,7 +90,8 @@ typedef struct lora_cache_stats {
 /*
  * Create a cache over `n_layers` layers (borrowed: they must outlive the cache) that share
  * the slot numbering [0, num_slots).
- *   layers         n_layers layer handles, all on the current device; n_layers = 0 gives a
+ *   layers         n_layers layer handles (not pooled: lora_layer_create), all on the
+ *                  current device; n_layers = 0 gives a
  *                  cache that only keeps the books (slot assignment, recency, statistics)
  *                  and touches no device: it needs no GPU.
  *   num_slots      1 <= num_slots <= every layer's num_slots (vLLM's max_loras).

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kSimtThreads)
       if (gn >= a.N) continue;
       float out = acc[i][j];
       if (s >= 0) {
-        const float* bcol = Bp + (size_t)s * R * a.N + gn;
+        const float* bcol = Bp + (size_t)ex.row_base[s] * a.N + gn;
         for (int jj = 0; jj < r; ++jj) out = fmaf(vs[m * (R + 1) + jj], bcol[(size_t)jj * a.N], out);
       }
       y[(size_t)gm * a.N + gn] = out;

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <map>
 #include <vector>
 
 #include "lora_kernels.h"
@@ -17,8 +18,13 @@ struct lora_layer {
   int R = 0;         // slot rank width: max_rank rounded up to a multiple of 8 (zero padded)
   size_t esize = 0;
   void* Wp = nullptr;      // packed base weight: bf16 [N][K], f32 [K][N]
-  void* A_pool = nullptr;  // [S][R][K]
-  void* B_pool = nullptr;  // [S][R][N]
+  void* A_pool = nullptr;  // [P][K] rank rows: slot s from row row_base[s]
+  void* B_pool = nullptr;  // [P][N] rank rows
+  int P = 0;               // pool rows: S * R, or the row budget of a pooled layer
+  bool pooled = false;     // slots placed by the row allocator (their true rank, rounded to 8)
+  int32_t* row_base = nullptr;      // [S] device: first pool row of each slot (-1: none)
+  std::vector<int> rb_h, rows_h;    // host: each slot's first row and row count
+  std::map<int, int> free_rows;     // pooled: free row ranges (first row -> count)
   void* Bx_pool = nullptr; // [S][N][wx] bf16, the B expand pool of the tensor-core expand
   void* A_stage = nullptr; // [K][R] staging for the transposition of a loaded A
   float* scale = nullptr;  // [S][R] column scales (+ 32 padding entries)

@@ -60,8 +60,9 @@ cudaError_t launch_segment_builder(const BuilderArgs& a, cudaStream_t stream);
 struct TileArgs {
   const void* x;  // [T,K] bf16 or f32
   int K, N, R;
-  const void* At_pool;  // [S][R][K] (transposed slot A, K contiguous)
-  const void* B_pool;   // [S][R][N]
+  const void* At_pool;  // [P][K] rank rows (transposed slot A, K contiguous)
+  const void* B_pool;   // [P][N] rank rows
+  const int32_t* row_base;  // [S] first pool row of each slot
   const float* scale;   // [S][R]: the scale of each rank column of a slot
   const int32_t* rank;  // [S]
   const int32_t* perm, *seg_offsets, *seg_slot, *tile_seg, *tile_row0, *meta;
@@ -78,6 +79,7 @@ struct ShrinkTcArgs {
   int T, K, R;    // R: slot rank width (multiple of 8); v has R columns
   int Rt;         // MMA N: R rounded up to 16
   const float* scale;  // [S][R]: the scale of each rank column of a slot
+  const int32_t* row_base;  // [S] first row of each slot in the A pool (the TMA row)
   const int32_t* perm, *seg_offsets, *seg_slot, *tile_seg, *tile_row0, *meta;
   int32_t* work;       // [2] item and exit counters, zero between launches (builder zeroes)
   float* v;            // [max_planes][T_max][R] fp32 partial sums over K ranges, scaled
@@ -91,7 +93,7 @@ int sgmv_shrink_tc_groups(int Rt);
 // The K split for a batch of T rows over S slots (the number of v planes the shrink writes),
 // at most max_planes.
 int sgmv_shrink_tc_split(int T, int K, int S, int num_sms, int max_planes);
-// tmap_a: the A pool [S*R rows][K] bf16 with a (64 x Rt) box.  Writes planes 0 .. ks - 1 of
+// tmap_a: the A pool [P rows][K] bf16 with a (64 x Rt) box.  Writes planes 0 .. ks - 1 of
 // v.  Launched with programmatic stream serialization (it waits for the builder itself).
 cudaError_t launch_sgmv_shrink_tc(const ShrinkTcArgs& a, const CUtensorMap& tmap_a,
                                   cudaStream_t stream);
@@ -102,8 +104,11 @@ struct BgmvArgs {
   const int32_t* token_slot;  // [T] as given by the caller
   const int32_t* loaded;      // [S]
   int T, K, N, R, S;
-  const void* At_pool;  // [S][R][K]
-  const void* B_pool;   // [S][R][N]
+  const void* At_pool;  // [P][K] rank rows
+  const void* B_pool;   // [P][N] rank rows
+  const int32_t* row_base;  // [S] first pool row of each slot (-1: none)
+  int pool_rows;        // P
+  bool pooled;          // slots placed by the row allocator (else slot s at row s * R)
   const float* scale;   // [S][R]: the scale of each rank column of a slot
   const int32_t* rank;  // [S]
   float* delta;         // [T_max][N] fp32
@@ -153,7 +158,8 @@ struct ExpandArgs {
   size_t v_plane_stride;    //   floats between planes
   const float* delta;       // [T_max][N] fp32                                (delta mode)
   int R;
-  const void* B_pool;   // [S][R][N]
+  const void* B_pool;   // [P][N] rank rows
+  const int32_t* row_base;  // [S] first pool row of each slot
   const int32_t* rank;  // [S]
 };
 struct GemmArgs {
@@ -202,8 +208,10 @@ cudaError_t launch_transpose_pad(const void* A_kr, void* At_rk, int K, int r, in
                                  cudaStream_t stream);
 // Wp[n][k] = W[k][n] (bf16 base weight packing).
 cudaError_t launch_pack_w_bf16(const void* W_kn, void* W_nk, int K, int N, cudaStream_t stream);
-// B expand pool row block of one slot: Bx[n][j] from B [R][N] (see expand_layout).
-cudaError_t launch_pack_bx(const void* B_rn, void* Bx_nw, int R, int N, cudaStream_t stream);
+// B expand pool row block of one slot: Bx[n][j] from B [R][N] (see expand_layout; the
+// layout is that of slot width R, rows of B at or beyond `rows` read as zero).
+cudaError_t launch_pack_bx(const void* B_rn, void* Bx_nw, int R, int rows, int N,
+                           cudaStream_t stream);
 // A slot's metadata: the scale of each of its R rank columns (an adapter's alpha / r on its
 // r columns; a composition's w_i alpha_i / r_i on the columns of member i; 0 beyond), its
 // rank and its loaded flag.
@@ -211,7 +219,9 @@ constexpr int kMaxSlotRank = 128;
 struct SlotScales {
   float v[kMaxSlotRank];
 };
+// Also sets row_base[slot] = rb when row_base is not null.
 cudaError_t launch_slot_meta(float* scale, int R, int32_t* rank, int32_t* loaded, int slot,
-                             const SlotScales& cols, int r, int is_loaded, cudaStream_t stream);
+                             const SlotScales& cols, int r, int is_loaded, int32_t* row_base,
+                             int rb, cudaStream_t stream);
 
 }  // namespace lora

@@ -70,7 +70,7 @@ void free_all(lora_layer* L) {
   void* ptrs[] = {L->Wp, L->A_pool, L->B_pool, L->Bx_pool, L->A_stage, L->scale, L->rank, L->loaded,
                   L->row_slot, L->perm, L->seg_offsets, L->seg_slot, L->tile_seg,
                   L->tile_row0, L->meta, L->err, L->v, L->delta, L->xk, L->sk_part,
-                  L->sk_sync, L->x_stage, L->ids_stage, L->y_stage};
+                  L->sk_sync, L->x_stage, L->ids_stage, L->y_stage, L->row_base};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (L->stage_free) cudaEventDestroy(L->stage_free);
@@ -126,8 +126,13 @@ void layer_set_percol(lora_layer* L, int slot, bool varied) {
 
 extern "C" {
 
-int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
-                      int max_tokens, int dtype, const void* W_dev, void* stream_) {
+}  // extern "C"
+
+// pool_rows 0: slot s owns rows [s R, s R + R) of the pools; > 0: a row pool of that many
+// rows (rounded up to 8) from which each load takes its rank rounded up to 8 rows.
+static int create_layer(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
+                        int max_tokens, int dtype, const void* W_dev, void* stream_,
+                        int pool_rows) {
   if (!out) return LORA_EINVAL;
   *out = nullptr;
   if (K < 1 || N < 1 || num_slots < 1 || num_slots > kMaxSlots || max_rank < 1 ||
@@ -135,6 +140,10 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
     return LORA_EINVAL;
   if (dtype != LORA_F32 && dtype != LORA_BF16) return LORA_EINVAL;
   if (dtype == LORA_BF16 && (K % 8 != 0 || N % 8 != 0)) return LORA_EINVAL;
+  const int R8 = (max_rank + 7) / 8 * 8;
+  if (pool_rows < 0 || (pool_rows > 0 && ((pool_rows + 7) / 8 * 8 < R8 ||
+                                           (long long)pool_rows > (long long)num_slots * R8)))
+    return LORA_EINVAL;
 
   lora_layer* L = new (std::nothrow) lora_layer();
   if (!L) return LORA_ENOMEM;
@@ -160,8 +169,21 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
 
   const size_t es = L->esize;
   const size_t S = num_slots, R = L->R;
+  L->pooled = pool_rows > 0;
+  L->P = L->pooled ? (pool_rows + 7) / 8 * 8 : (int)(S * R);
+  const size_t P = L->P;
   L->max_tiles = (max_tokens + kTileRows - 1) / kTileRows + num_slots;
   L->percol.assign(S, 0);
+  L->rb_h.assign(S, -1);
+  L->rows_h.assign(S, 0);
+  if (L->pooled) {
+    L->free_rows[0] = L->P;
+  } else {
+    for (size_t q = 0; q < S; ++q) {
+      L->rb_h[q] = (int)(q * R);
+      L->rows_h[q] = (int)R;
+    }
+  }
   // small batches split the shrink's K range over up to 8 planes of v; large ones need none
   L->v_planes = dtype == LORA_BF16 ? std::max(1, std::min(8, 65536 / max_tokens)) : 1;
   // the base GEMM of a delta-mode batch may split K: scratch for its largest exchange
@@ -169,8 +191,9 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
     for (int m = 1; m <= std::min(max_tokens, kDeltaMaxT); ++m)
       L->xk_floats = std::max(L->xk_floats, gemm_tc_exchange_floats(m, N, K, L->num_sms));
   bool ok = cudaMalloc(&L->Wp, (size_t)K * N * es) == cudaSuccess &&
-            cudaMalloc(&L->A_pool, S * R * K * es) == cudaSuccess &&
-            cudaMalloc(&L->B_pool, S * R * N * es) == cudaSuccess &&
+            cudaMalloc(&L->A_pool, P * K * es) == cudaSuccess &&
+            cudaMalloc(&L->B_pool, P * N * es) == cudaSuccess &&
+            dmalloc(&L->row_base, S) == cudaSuccess &&
             cudaMalloc(&L->A_stage, (size_t)K * R * es) == cudaSuccess &&
             // column scales [S][R], padded so that a read of 32 columns of any slot is in bounds
             dmalloc(&L->scale, S * R + 32) == cudaSuccess &&
@@ -205,8 +228,10 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
        cudaEventCreateWithFlags(&L->last_forward, cudaEventDisableTiming) == cudaSuccess;
   if (!ok) return bail(LORA_ECUDA);
 
-  ok = cudaMemsetAsync(L->A_pool, 0, S * R * K * es, stream) == cudaSuccess &&
-       cudaMemsetAsync(L->B_pool, 0, S * R * N * es, stream) == cudaSuccess &&
+  ok = cudaMemsetAsync(L->A_pool, 0, P * K * es, stream) == cudaSuccess &&
+       cudaMemsetAsync(L->B_pool, 0, P * N * es, stream) == cudaSuccess &&
+       cudaMemcpyAsync(L->row_base, L->rb_h.data(), S * sizeof(int32_t), cudaMemcpyHostToDevice,
+                       stream) == cudaSuccess &&
        (!L->Bx_pool ||
         cudaMemsetAsync(L->Bx_pool, 0, S * expand_layout((int)R).wx * N * es, stream) ==
             cudaSuccess) &&
@@ -225,7 +250,7 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
     for (int i = 0; i < 3; ++i)
       if (encode_tmap_bf16(&L->tmap_w[i], L->Wp, N, K, kTcTileN[i]) != cudaSuccess)
         return bail(LORA_ECUDA);
-    if (encode_tmap_bf16(&L->tmap_a, L->A_pool, (int)(S * R), K, (L->R + 15) / 16 * 16) !=
+    if (encode_tmap_bf16(&L->tmap_a, L->A_pool, (int)P, K, (L->R + 15) / 16 * 16) !=
         cudaSuccess)
       return bail(LORA_ECUDA);
     if (L->Bx_pool)
@@ -240,6 +265,74 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
   }
   if (cudaStreamSynchronize(stream) != cudaSuccess) return bail(LORA_ECUDA);
   *out = L;
+  return LORA_OK;
+}
+
+// First fit over the free row ranges: the first row of `rows` rows, or -1.
+static int pool_alloc(lora_layer* L, int rows) {
+  for (auto it = L->free_rows.begin(); it != L->free_rows.end(); ++it) {
+    if (it->second < rows) continue;
+    const int first = it->first, left = it->second - rows;
+    L->free_rows.erase(it);
+    if (left > 0) L->free_rows[first + rows] = left;
+    return first;
+  }
+  return -1;
+}
+
+// Take rows [first, first + rows), which lie inside one free range, or return -1.
+static int pool_alloc_at(lora_layer* L, int first, int rows) {
+  auto it = L->free_rows.upper_bound(first);
+  if (it == L->free_rows.begin()) return -1;
+  --it;
+  const int f = it->first, n = it->second;
+  if (first + rows > f + n) return -1;
+  L->free_rows.erase(it);
+  if (first > f) L->free_rows[f] = first - f;
+  if (f + n > first + rows) L->free_rows[first + rows] = f + n - (first + rows);
+  return first;
+}
+
+// Return rows [first, first + rows) to the free ranges, merging neighbours.
+static void pool_free(lora_layer* L, int first, int rows) {
+  auto next = L->free_rows.lower_bound(first);
+  if (next != L->free_rows.end() && next->first == first + rows) {
+    rows += next->second;
+    next = L->free_rows.erase(next);
+  }
+  if (next != L->free_rows.begin()) {
+    auto prev = std::prev(next);
+    if (prev->first + prev->second == first) {
+      prev->second += rows;
+      return;
+    }
+  }
+  L->free_rows[first] = rows;
+}
+
+extern "C" {
+
+int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
+                      int max_tokens, int dtype, const void* W_dev, void* stream_) {
+  return create_layer(out, K, N, num_slots, max_rank, max_tokens, dtype, W_dev, stream_, 0);
+}
+
+int lora_layer_create_pooled(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
+                             int max_tokens, int dtype, const void* W_dev, void* stream_,
+                             int pool_rows) {
+  if (pool_rows < 1) return LORA_EINVAL;
+  return create_layer(out, K, N, num_slots, max_rank, max_tokens, dtype, W_dev, stream_,
+                      pool_rows);
+}
+
+int lora_get_pool_usage(const lora_layer_t* L, int* used_rows, int* pool_rows) {
+  if (!L || !used_rows || !pool_rows) return LORA_EINVAL;
+  int free_total = 0;
+  for (const auto& kv : L->free_rows) free_total += kv.second;
+  int used = 0;
+  for (int q = 0; q < L->S; ++q) used += L->rows_h[q];
+  *used_rows = L->pooled ? L->P - free_total : used;
+  *pool_rows = L->P;
   return LORA_OK;
 }
 
@@ -262,12 +355,30 @@ int load_adapter_slot_composed(lora_layer_t* L, int slot, int n, const void* con
   cudaStream_t side = static_cast<cudaStream_t>(side_);
   const size_t es = L->esize;
   const size_t K = L->K, N = L->N, R = L->R;
+  // the slot's pool rows: fixed [slot R, slot R + R), or (pooled) its rank rounded up to 8
+  // rows from the row allocator -- the rows it held before are returned first
+  const int rows = L->pooled ? (r_sum + 7) / 8 * 8 : (int)R;
+  int rb = L->rb_h[slot];
+  if (L->pooled) {
+    const int old_rb = L->rb_h[slot], old_rows = L->rows_h[slot];
+    if (old_rows > 0) pool_free(L, old_rb, old_rows);
+    rb = pool_alloc(L, rows);
+    if (rb < 0) {
+      if (old_rows > 0) {  // the slot keeps its rows and its adapter
+        const int back = pool_alloc_at(L, old_rb, old_rows);
+        (void)back;
+      }
+      return fail(L, LORA_ENOMEM, "the row pool has no %d free consecutive rows", rows);
+    }
+    L->rb_h[slot] = rb;
+    L->rows_h[slot] = rows;
+  }
 
   // never overwrite a slot under a forward still in flight, nor the staging buffer under
   // the previous load's transposition
   if (L->have_forward) LORA_CUDA(L, cudaStreamWaitEvent(side, L->last_forward, 0));
-  char* At = static_cast<char*>(L->A_pool) + (size_t)slot * R * K * es;
-  char* Bs = static_cast<char*>(L->B_pool) + (size_t)slot * R * N * es;
+  char* At = static_cast<char*>(L->A_pool) + (size_t)rb * K * es;
+  char* Bs = static_cast<char*>(L->B_pool) + (size_t)rb * N * es;
   SlotScales cols;
   for (int j = 0; j < kMaxSlotRank; ++j) cols.v[j] = 0.f;
   // member i occupies rank rows [o, o + r_i) of the slot: A_i^T in At, B_i in B
@@ -282,17 +393,19 @@ int load_adapter_slot_composed(lora_layer_t* L, int slot, int n, const void* con
     const float c = weight[i] * (alpha[i] / (float)r[i]);
     for (int j = o; j < o + r[i]; ++j) cols.v[j] = c;
   }
-  if ((size_t)r_sum < R) {
-    LORA_CUDA(L, cudaMemsetAsync(At + (size_t)r_sum * K * es, 0, (R - r_sum) * K * es, side));
-    LORA_CUDA(L, cudaMemsetAsync(Bs + (size_t)r_sum * N * es, 0, (R - r_sum) * N * es, side));
+  if (r_sum < rows) {
+    LORA_CUDA(L, cudaMemsetAsync(At + (size_t)r_sum * K * es, 0, (size_t)(rows - r_sum) * K * es,
+                                 side));
+    LORA_CUDA(L, cudaMemsetAsync(Bs + (size_t)r_sum * N * es, 0, (size_t)(rows - r_sum) * N * es,
+                                 side));
   }
   if (L->Bx_pool)  // the slot's rows of the B expand pool (rank rows >= r_sum: the zeros just set)
     LORA_CUDA(L, launch_pack_bx(Bs,
                                 static_cast<char*>(L->Bx_pool) +
                                     (size_t)slot * N * expand_layout((int)R).wx * es,
-                                (int)R, (int)N, side));
+                                (int)R, rows, (int)N, side));
   LORA_CUDA(L, launch_slot_meta(L->scale, (int)R, L->rank, L->loaded, slot, cols, r_sum, 1,
-                                side));
+                                L->row_base, rb, side));
   bool varied = false;
   for (int j = 1; j < r_sum; ++j) varied |= cols.v[j] != cols.v[0];
   layer_set_percol(L, slot, varied);
@@ -316,7 +429,15 @@ int unload_adapter_slot(lora_layer_t* L, int slot, void* side_) {
   if (L->have_forward) LORA_CUDA(L, cudaStreamWaitEvent(side, L->last_forward, 0));
   SlotScales none;
   for (int j = 0; j < kMaxSlotRank; ++j) none.v[j] = 0.f;
-  LORA_CUDA(L, launch_slot_meta(L->scale, L->R, L->rank, L->loaded, slot, none, 0, 0, side));
+  // a pooled slot returns its rows (a later load reusing them waits for the last forward)
+  const bool had_rows = L->pooled && L->rows_h[slot] > 0;
+  if (had_rows) {
+    pool_free(L, L->rb_h[slot], L->rows_h[slot]);
+    L->rb_h[slot] = -1;
+    L->rows_h[slot] = 0;
+  }
+  LORA_CUDA(L, launch_slot_meta(L->scale, L->R, L->rank, L->loaded, slot, none, 0, 0,
+                                L->pooled ? L->row_base : nullptr, -1, side));
   layer_set_percol(L, slot, false);
   cudaEvent_t ev = layer_take_event(L);
   if (!ev) return fail(L, LORA_ECUDA, "cudaEventCreate failed");
@@ -414,6 +535,9 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     ba.S = L->S;
     ba.At_pool = L->A_pool;
     ba.B_pool = L->B_pool;
+    ba.row_base = L->row_base;
+    ba.pool_rows = L->P;
+    ba.pooled = L->pooled;
     ba.scale = L->scale;
     ba.rank = L->rank;
     ba.delta = L->delta;
@@ -428,6 +552,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     sa.R = L->R;
     sa.Rt = (L->R + 15) / 16 * 16;
     sa.scale = L->scale;
+    sa.row_base = L->row_base;
     sa.perm = L->perm;
     sa.seg_offsets = L->seg_offsets;
     sa.seg_slot = L->seg_slot;
@@ -449,6 +574,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     ta.R = L->R;
     ta.At_pool = L->A_pool;
     ta.B_pool = L->B_pool;
+    ta.row_base = L->row_base;
     ta.scale = L->scale;
     ta.rank = L->rank;
     ta.perm = L->perm;
@@ -482,6 +608,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.ex.delta = L->delta;
   ga.ex.R = L->R;
   ga.ex.B_pool = L->B_pool;
+  ga.ex.row_base = L->row_base;
   ga.ex.rank = L->rank;
   ga.err = L->err;
   ga.num_sms = L->num_sms;

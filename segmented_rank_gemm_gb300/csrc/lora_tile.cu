@@ -181,6 +181,7 @@ template <typename T, typename V, bool kDelta>
 __global__ void __launch_bounds__(kTileThreads, 2)
     lora_tile_kernel(const T* __restrict__ x, int K, int N, int R,
                      const T* __restrict__ At_pool, const T* __restrict__ B_pool,
+                     const int32_t* __restrict__ row_base,
                      const float* __restrict__ scale, const int32_t* __restrict__ rank,
                      const int32_t* __restrict__ perm, const int32_t* __restrict__ seg_offsets,
                      const int32_t* __restrict__ seg_slot, const int32_t* __restrict__ tile_seg,
@@ -203,7 +204,8 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     const int nr = min(kTileRows, seg_offsets[g + 1] - p0);
     if (tid < nr) rows_s[tid] = perm[p0 + tid];
     __syncthreads();
-    const T* At = At_pool + (size_t)s * R * K;
+    const int rb = row_base[s];  // the slot's first pool row
+    const T* At = At_pool + (size_t)rb * K;
     if (r <= 8)
       shrink_tile_warp<T, V, 1>(x, K, At, r, rows_s, nr, sc, v_s, vstride, warp, lane);
     else if (r <= 16)
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
       shrink_tile_warp<T, V, 16>(x, K, At, r, rows_s, nr, sc, v_s, vstride, warp, lane);
     __syncthreads();
     if constexpr (kDelta) {
-      expand_tile_delta(reinterpret_cast<const __nv_bfloat16*>(B_pool) + (size_t)s * R * N, N, r,
+      expand_tile_delta(reinterpret_cast<const __nv_bfloat16*>(B_pool) + (size_t)rb * N, N, r,
                         v_s, vstride, rows_s, nr, out, tid);
     } else {
       for (int i = tid; i < nr * r; i += kTileThreads) {
@@ -248,7 +250,8 @@ __global__ void __launch_bounds__(kBgmvThreads, 8)  // <= 64 registers: 4 CTAs f
     bgmv_delta_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ token_slot,
                       const int32_t* __restrict__ loaded, int T, int K, int N, int R, int S,
                       const __nv_bfloat16* __restrict__ At_pool,
-                      const __nv_bfloat16* __restrict__ B_pool, const float* __restrict__ scale,
+                      const __nv_bfloat16* __restrict__ B_pool,
+                      const int32_t* __restrict__ row_base, const float* __restrict__ scale,
                       const int32_t* __restrict__ rank, float* __restrict__ delta, int kchunk,
                       int nchunk) {
   griddep_wait();  // the previous kernel's writes (x, the delta it read) are settled
@@ -270,7 +273,8 @@ __global__ void __launch_bounds__(kBgmvThreads, 8)  // <= 64 registers: 4 CTAs f
     const int r = rank[s];
     const float* sc = scale + (size_t)s * R;  // the slot's column scales
     const __nv_bfloat16* xr = x + (size_t)row * K;
-    const __nv_bfloat16* At = At_pool + (size_t)s * R * K;
+    const int rb = row_base[s];  // the slot's first pool row
+    const __nv_bfloat16* At = At_pool + (size_t)rb * K;
     float* vp = v_part[buf];
     buf ^= 1;
 
@@ -316,7 +320,7 @@ __global__ void __launch_bounds__(kBgmvThreads, 8)  // <= 64 registers: 4 CTAs f
     __syncthreads();
 
     // ---- 3. delta over [nb0, nb1) ----
-    const __nv_bfloat16* Bs = B_pool + (size_t)s * R * N;
+    const __nv_bfloat16* Bs = B_pool + (size_t)rb * N;
     float* drow = delta + (size_t)row * N;
     for (int n = nb0 + tid * 8; n < nb1; n += kBgmvThreads * 8) {
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -496,12 +500,16 @@ static constexpr int kStrGroup = 2;
 // those for the two kernels to share the SM.
 // PERCOL: false when every slot's columns share one scale (plain adapters: the scale of
 // column 0 is the slot's), true when a slot holds a composition (one scale per column).
-template <int RMAX, int ROWS, bool PERCOL>
+// POOLED: false when slot s starts at pool row s * R, true when a row allocator placed it
+// (row_base[s]; the A and B rows of a slot then number its rank rounded up to 8).
+template <int RMAX, int ROWS, bool PERCOL, bool POOLED>
 __global__ void __maxnreg__(120)
     bgmv_stream_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ token_slot,
                        const int32_t* __restrict__ loaded, int T, int K, int N, int R, int S,
                        const __nv_bfloat16* __restrict__ At_pool,
-                       const __nv_bfloat16* __restrict__ B_pool, const float* __restrict__ scale,
+                       const __nv_bfloat16* __restrict__ B_pool,
+                       const int32_t* __restrict__ row_base, int pool_rows,
+                       const float* __restrict__ scale,
                        const int32_t* __restrict__ rank, float* __restrict__ delta) {
   // launched while the previous kernel (the previous forward's base GEMM) still runs: wait
   // for it before reading x or writing delta, and only then let the base GEMM start (its
@@ -512,10 +520,13 @@ __global__ void __maxnreg__(120)
   // before the ids are read: the DRAM traffic of every slot then overlaps the item-list
   // setup below (the items' own prefetches find the lines present or in flight).
   if (S <= (int)gridDim.x && (int)blockIdx.x < S && threadIdx.x < 32) {
-    const int rs = min(R, RMAX);
+    // (pooled: the rows from the slot's first row, as many as the pool still holds; an
+    // empty slot has no first row and requests nothing)
+    const int rb0 = POOLED ? row_base[blockIdx.x] : (int)blockIdx.x * R;
+    const int rs = POOLED ? (rb0 < 0 ? 0 : min(min(R, RMAX), pool_rows - rb0)) : min(R, RMAX);
     const size_t a_bytes = (size_t)rs * K * 2, b_bytes = (size_t)rs * N * 2;
-    const char* a0 = reinterpret_cast<const char*>(At_pool + (size_t)blockIdx.x * R * K);
-    const char* b0 = reinterpret_cast<const char*>(B_pool + (size_t)blockIdx.x * R * N);
+    const char* a0 = reinterpret_cast<const char*>(At_pool + (size_t)max(rb0, 0) * K);
+    const char* b0 = reinterpret_cast<const char*>(B_pool + (size_t)max(rb0, 0) * N);
     const size_t off = (size_t)threadIdx.x << 15;
     if (off < a_bytes) bulk_prefetch_l2(a0 + off, (uint32_t)min(a_bytes - off, (size_t)1 << 15));
     if (off < b_bytes) bulk_prefetch_l2(b0 + off, (uint32_t)min(b_bytes - off, (size_t)1 << 15));
@@ -525,6 +536,7 @@ __global__ void __maxnreg__(120)
   __shared__ int warp_cnt[kStrThreads / 32];
   __shared__ float red[kStrThreads / 32][kStrRedMax];
   __shared__ float v_s[kStrGroup][32];
+  __shared__ int rb_s;  // pooled: the item's slot's first pool row
   constexpr int kIds = kSlotMaxT / kStrThreads;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (S + kStrThreads - 1) / kStrThreads;  // consecutive slots per thread
@@ -594,10 +606,13 @@ __global__ void __maxnreg__(120)
     // prefetches from the lanes of warp 0: the DRAM round trips overlap the row scan
     // below, and the loads after it hit L2
     if (warp == 0) {
+      // (pooled: warp 0 reads the slot's first row and leaves it in shared memory)
+      const int rbw = POOLED ? row_base[s] : s * R;
+      if (POOLED && lane == 0) rb_s = rbw;
       const int rs = min(r, min(R, RMAX));
       const size_t a_bytes = (size_t)rs * K * 2, b_bytes = (size_t)rs * N * 2;
-      const char* a0 = reinterpret_cast<const char*>(At_pool + (size_t)s * R * K);
-      const char* b0 = reinterpret_cast<const char*>(B_pool + (size_t)s * R * N);
+      const char* a0 = reinterpret_cast<const char*>(At_pool + (size_t)rbw * K);
+      const char* b0 = reinterpret_cast<const char*>(B_pool + (size_t)rbw * N);
       for (size_t off = (size_t)lane << 15; off < a_bytes; off += (size_t)32 << 15)
         bulk_prefetch_l2(a0 + off, (uint32_t)min(a_bytes - off, (size_t)1 << 15));
       for (size_t off = (size_t)lane << 15; off < b_bytes; off += (size_t)32 << 15)
@@ -628,8 +643,9 @@ __global__ void __maxnreg__(120)
       }
     __syncthreads();
     const int ng = min(kStrGroup, nrows - g0);
-    const __nv_bfloat16* At = At_pool + (size_t)s * R * K;
-    const __nv_bfloat16* Bs = B_pool + (size_t)s * R * N;
+    const int rbi = POOLED ? rb_s : s * R;  // the slot's first pool row
+    const __nv_bfloat16* At = At_pool + (size_t)rbi * K;
+    const __nv_bfloat16* Bs = B_pool + (size_t)rbi * N;
     // shrink: v_s[0 .. ng), ROWS rows a pass (the last pass may take one)
     for (int q0 = 0; q0 < ng; q0 += ROWS) {
       if (ng - q0 >= ROWS)
@@ -646,12 +662,13 @@ __global__ void __maxnreg__(120)
   }
 }
 
-template <int RMAX, int ROWS, bool PERCOL>
+template <int RMAX, int ROWS, bool PERCOL, bool POOLED>
 static cudaError_t launch_bgmv_stream_t(const BgmvArgs& a, cudaStream_t stream) {
   // the SMs it runs on must keep the shared-memory split a GEMM CTA needs, or that CTA
   // waits for them to drain
   static bool carveout = false;
-  cudaError_t e = prefer_max_smem_carveout(bgmv_stream_kernel<RMAX, ROWS, PERCOL>, &carveout);
+  cudaError_t e =
+      prefer_max_smem_carveout(bgmv_stream_kernel<RMAX, ROWS, PERCOL, POOLED>, &carveout);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -664,19 +681,25 @@ static cudaError_t launch_bgmv_stream_t(const BgmvArgs& a, cudaStream_t stream) 
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bgmv_stream_kernel<RMAX, ROWS, PERCOL>,
+  return cudaLaunchKernelEx(&cfg, bgmv_stream_kernel<RMAX, ROWS, PERCOL, POOLED>,
                             static_cast<const __nv_bfloat16*>(a.x), a.token_slot, a.loaded, a.T,
                             a.K, a.N, a.R, a.S, static_cast<const __nv_bfloat16*>(a.At_pool),
-                            static_cast<const __nv_bfloat16*>(a.B_pool), a.scale, a.rank,
-                            a.delta);
+                            static_cast<const __nv_bfloat16*>(a.B_pool), a.row_base,
+                            a.pool_rows, a.scale, a.rank, a.delta);
+}
+
+template <int RMAX, int ROWS>
+static cudaError_t launch_bgmv_stream_r(const BgmvArgs& a, cudaStream_t stream) {
+  if (a.pooled)
+    return a.per_column ? launch_bgmv_stream_t<RMAX, ROWS, true, true>(a, stream)
+                        : launch_bgmv_stream_t<RMAX, ROWS, false, true>(a, stream);
+  return a.per_column ? launch_bgmv_stream_t<RMAX, ROWS, true, false>(a, stream)
+                      : launch_bgmv_stream_t<RMAX, ROWS, false, false>(a, stream);
 }
 
 static cudaError_t launch_bgmv_stream(const BgmvArgs& a, cudaStream_t stream) {
-  if (a.R <= 16)
-    return a.per_column ? launch_bgmv_stream_t<16, 2, true>(a, stream)
-                        : launch_bgmv_stream_t<16, 2, false>(a, stream);
-  return a.per_column ? launch_bgmv_stream_t<32, 1, true>(a, stream)
-                      : launch_bgmv_stream_t<32, 1, false>(a, stream);
+  return a.R <= 16 ? launch_bgmv_stream_r<16, 2>(a, stream)
+                   : launch_bgmv_stream_r<32, 1>(a, stream);
 }
 
 cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream) {
@@ -712,8 +735,8 @@ cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, bgmv_delta_kernel, static_cast<const __nv_bfloat16*>(a.x),
                             a.token_slot, a.loaded, a.T, a.K, a.N, a.R, a.S,
                             static_cast<const __nv_bfloat16*>(a.At_pool),
-                            static_cast<const __nv_bfloat16*>(a.B_pool), a.scale, a.rank, a.delta,
-                            kchunk, nchunk);
+                            static_cast<const __nv_bfloat16*>(a.B_pool), a.row_base, a.scale,
+                            a.rank, a.delta, kchunk, nchunk);
 }
 
 cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStream_t stream) {
@@ -746,7 +769,7 @@ cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStrea
     const T* B = static_cast<const T*>(a.B_pool);
     if (delta) return cudaErrorInvalidValue;  // delta mode runs bgmv_delta_kernel
     return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, V, false>, x, a.K, a.N, a.R, At, B,
-                              a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
+                              a.row_base, a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
                               a.tile_row0, a.meta, a.out);
   }
   if (delta) return cudaErrorInvalidValue;  // delta mode is a bf16 path
@@ -757,10 +780,10 @@ cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStrea
   const bool vec4 = a.K % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0;
   if (vec4)
     return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, Vec16<T>, false>, x, a.K, a.N, a.R, At, B,
-                              a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
+                              a.row_base, a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
                               a.tile_row0, a.meta, a.out);
   return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, Scalar32, false>, x, a.K, a.N, a.R, At, B,
-                            a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
+                            a.row_base, a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
                             a.tile_row0, a.meta, a.out);
 }
 

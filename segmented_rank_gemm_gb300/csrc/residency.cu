@@ -206,7 +206,7 @@ int swap_in(Cache* c, const Entry& e, int slot) {
                         static_cast<char*>(L->B_pool) + (size_t)slot * L->R * L->N * es,
                         static_cast<char*>(L->Bx_pool) +
                             (size_t)slot * L->N * lora::expand_layout(L->R).wx * es,
-                        L->R, L->N, c->stream));
+                        L->R, L->R, L->N, c->stream));
     }
   CACHE_CUDA(c, cudaEventRecord(c->ready_ev[slot], c->stream));
   c->ready_pending[slot] = 1;
@@ -415,7 +415,8 @@ int lora_cache_create(lora_adapter_cache_t** out, lora_layer_t* const* layers, i
   size_t off = 0;
   for (int l = 0; l < n_layers; ++l) {
     lora_layer* L = layers[l];
-    if (!L || num_slots > L->S) return bail(LORA_EINVAL);
+    // (a pooled layer places its slots by its own row allocator: not served here)
+    if (!L || num_slots > L->S || L->pooled) return bail(LORA_EINVAL);
     if (l > 0 && L->device != c->layers[0]->device) return bail(LORA_EINVAL);
     c->layers.push_back(L);
     c->max_r = std::min(c->max_r, L->max_rank);

@@ -27,7 +27,10 @@
 //               read by the other warps.  Per 64-wide K block it gathers the window's 128 x
 //               rows (perm[p0 + i]) with 16-byte cp.async copies into the 128-byte-swizzled
 //               K-major layout the MMA reads (positions past the window end are
-//               zero-filled), and lane 0 loads the G A blocks with TMA.  The stage's
+//               zero-filled), and lane 0 loads the G A blocks with TMA (Rt rows from
+//               each slot's first pool row: rows past the slot's own rank belong to
+//               other slots or lie past the pool (zero-filled); their columns carry a
+//               zero scale, so only the slot's rank columns reach v).  The stage's
 //               mbarrier counts the 32 lanes' cp.async completions and the TMA bytes.
 //   warp 1      one lane issues tcgen05.mma (M=128, N=G*Rt, K=16; bf16 x bf16 -> fp32) and
 //               frees each stage with tcgen05.commit.  Two accumulators alternate between
@@ -64,6 +67,7 @@ struct UnitInfo {
   int G, kp;                    // segments in the unit, K range of this item
   int off[kShMaxGroups + 1];    // segment g covers positions [off[g], off[g + 1])
   int slot[kShMaxGroups];
+  int rowb[kShMaxGroups];       // the slot's first row in the A pool
 };
 
 int sgmv_shrink_tc_groups(int Rt) { return std::max(1, std::min(kShMaxGroups, kShNmax / Rt)); }
@@ -150,7 +154,9 @@ __global__ void __launch_bounds__(kShThreads, 1)
       const int G = __popc(__ballot_sync(0xffffffffu, in));
       if (in) {
         ui.off[lane] = max(o, p0);
-        ui.slot[lane] = a.seg_slot[gs + lane];
+        const int sl = a.seg_slot[gs + lane];
+        ui.slot[lane] = sl;
+        ui.rowb[lane] = a.row_base[sl];
       }
       if (lane == G) ui.off[G] = min(o, p1);
       if (lane == 0) {
@@ -177,7 +183,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
           mbar_arrive_expect_tx(&full[s], (uint32_t)(G * Rt * 128));
           for (int g = 0; g < G; ++g)
             tma_load_2d(sx + kShXBytes + g * Rt * 128, &tmap_a, &full[s], kb * kShBK,
-                        ui.slot[g] * a.R);
+                        ui.rowb[g]);
         }
         const int k = kb * kShBK + c * 8;
 #pragma unroll
@@ -281,10 +287,14 @@ __global__ void __launch_bounds__(kShThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             if (j + 4 * q < a.R) {
+              // columns past the slot's rank have scale 0; select rather than multiply,
+              // so that whatever the pool holds past the slot's rows cannot leak in
               const float4 c = __ldg(reinterpret_cast<const float4*>(sc + j + 4 * q));
               *reinterpret_cast<float4*>(vrow + j + 4 * q) = make_float4(
-                  c.x * __uint_as_float(raw[4 * q]), c.y * __uint_as_float(raw[4 * q + 1]),
-                  c.z * __uint_as_float(raw[4 * q + 2]), c.w * __uint_as_float(raw[4 * q + 3]));
+                  c.x != 0.f ? c.x * __uint_as_float(raw[4 * q]) : 0.f,
+                  c.y != 0.f ? c.y * __uint_as_float(raw[4 * q + 1]) : 0.f,
+                  c.z != 0.f ? c.z * __uint_as_float(raw[4 * q + 2]) : 0.f,
+                  c.w != 0.f ? c.w * __uint_as_float(raw[4 * q + 3]) : 0.f);
             }
         }
       }

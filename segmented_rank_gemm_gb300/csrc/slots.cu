@@ -3,9 +3,9 @@
 //
 // "Serving LoRA adapters: from the model name to the wrapped layer" (vLLM), Step 3: the
 // activation copies each module's A and B into stacked buffers at the slot index; buffers
-// are sized for the maximum rank.  Here A [K,r] is stored transposed and zero-padded as
-// At [R][K] (K contiguous: the shrink streams it with coalesced vector loads) and B [r,N]
-// is copied as rows 0..r-1 of the slot's [R][N] block, rows r..R-1 zeroed.
+// are sized for the maximum rank.  Here A [K,r] is stored transposed as rank rows of At
+// (K contiguous: the shrink streams it with coalesced vector loads) and B [r,N] as rank
+// rows of B, both from the slot's first pool row; rows past r that the slot owns are zero.
 #include "lora_common.cuh"
 #include "lora_kernels.h"
 
@@ -66,7 +66,8 @@ cudaError_t launch_pack_w_bf16(const void* W_kn, void* W_nk, int K, int N, cudaS
 __global__ void pack_bx_kernel(const __nv_bfloat16* __restrict__ B, __nv_bfloat16* __restrict__ Bx,
                                int R, int N, int wx, int half) {
   // Bx[n][j] = B[j mod half][n] for j < wx (half = wx / 2 when both halves repeat B^T,
-  // else half = wx), 0 where that rank index is >= R.  32x32 tiles through shared memory.
+  // else half = wx), 0 where that rank index is >= R (here: the rows the slot owns).
+  // 32x32 tiles through shared memory.
   __shared__ __nv_bfloat16 tile[32][33];
   const int n0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
   for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
@@ -82,28 +83,32 @@ __global__ void pack_bx_kernel(const __nv_bfloat16* __restrict__ B, __nv_bfloat1
   }
 }
 
-cudaError_t launch_pack_bx(const void* B_rn, void* Bx_nw, int R, int N, cudaStream_t stream) {
+cudaError_t launch_pack_bx(const void* B_rn, void* Bx_nw, int R, int rows, int N,
+                           cudaStream_t stream) {
   const ExpandLayout L = expand_layout(R);
   dim3 block(32, 8), grid((N + 31) / 32, (L.wx + 31) / 32);
   pack_bx_kernel<<<grid, block, 0, stream>>>(static_cast<const __nv_bfloat16*>(B_rn),
-                                             static_cast<__nv_bfloat16*>(Bx_nw), R, N, L.wx,
-                                             L.nbs == 1 ? L.wx / 2 : L.wx);
+                                             static_cast<__nv_bfloat16*>(Bx_nw), min(R, rows), N,
+                                             L.wx, L.nbs == 1 ? L.wx / 2 : L.wx);
   return cudaGetLastError();
 }
 
 __global__ void slot_meta_kernel(float* scale, int R, int32_t* rank, int32_t* loaded, int slot,
-                                 SlotScales cols, int r, int is_loaded) {
+                                 SlotScales cols, int r, int is_loaded, int32_t* row_base,
+                                 int rb) {
   for (int j = threadIdx.x; j < R; j += blockDim.x) scale[(size_t)slot * R + j] = cols.v[j];
   if (threadIdx.x == 0) {
     rank[slot] = r;
     loaded[slot] = is_loaded;
+    if (row_base) row_base[slot] = rb;
   }
 }
 
 cudaError_t launch_slot_meta(float* scale, int R, int32_t* rank, int32_t* loaded, int slot,
-                             const SlotScales& cols, int r, int is_loaded, cudaStream_t stream) {
+                             const SlotScales& cols, int r, int is_loaded, int32_t* row_base,
+                             int rb, cudaStream_t stream) {
   slot_meta_kernel<<<1, kMaxSlotRank, 0, stream>>>(scale, R, rank, loaded, slot, cols, r,
-                                                   is_loaded);
+                                                   is_loaded, row_base, rb);
   return cudaGetLastError();
 }
 

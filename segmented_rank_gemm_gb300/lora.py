@@ -27,7 +27,8 @@ LORA_ECUDA, LORA_ENOMEM, LORA_ESTATE, LORA_ETIMEOUT = -5, -6, -7, -8
 LORA_ENOENT, LORA_ECAPACITY = -9, -10
 
 # every entry point declared in include/lora_layer.h
-ABI_FUNCTIONS = ("lora_layer_create", "load_adapter_slot", "load_adapter_slot_composed",
+ABI_FUNCTIONS = ("lora_layer_create", "lora_layer_create_pooled", "lora_get_pool_usage",
+                 "load_adapter_slot", "load_adapter_slot_composed",
                  "unload_adapter_slot",
                  "set_batch_segments", "lora_forward", "lora_forward_host", "lora_get_status",
                  "lora_get_segments", "lora_set_trace_events", "lora_set_gemm_plan",
@@ -65,6 +66,9 @@ def _load() -> ctypes.CDLL:
     L = ctypes.CDLL(LIB_PATH)
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     L.lora_layer_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32, vp, vp]
+    L.lora_layer_create_pooled.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32, vp,
+                                           vp, i32]
+    L.lora_get_pool_usage.argtypes = [vp, vp, vp]
     L.load_adapter_slot.argtypes = [vp, i32, vp, vp, i32, f32, vp]
     L.load_adapter_slot_composed.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp]
     L.unload_adapter_slot.argtypes = [vp, i32, vp]
@@ -158,6 +162,23 @@ def lora_layer_create(K, N, num_slots, max_rank, max_tokens, dtype, W, stream=No
     _check(None, _lib.lora_layer_create(ctypes.byref(h), K, N, num_slots, max_rank, max_tokens,
                                         code, _ptr(W), _stream(stream)))
     return h.value
+
+
+def lora_layer_create_pooled(K, N, num_slots, max_rank, max_tokens, dtype, W, pool_rows,
+                             stream=None) -> int:
+    h = ctypes.c_void_p()
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    _check(None, _lib.lora_layer_create_pooled(ctypes.byref(h), K, N, num_slots, max_rank,
+                                               max_tokens, code, _ptr(W), _stream(stream),
+                                               int(pool_rows)))
+    return h.value
+
+
+def lora_get_pool_usage(layer):
+    """(rows in use, rows in the pool)."""
+    used, total = ctypes.c_int(), ctypes.c_int()
+    _check(layer, _lib.lora_get_pool_usage(layer, ctypes.byref(used), ctypes.byref(total)))
+    return used.value, total.value
 
 
 def load_adapter_slot(layer, slot, A, B, r, alpha, side_stream=None) -> None:
@@ -265,14 +286,21 @@ class LoraLayer:
     """Owns one C layer.  ``W`` [K, N] is a CUDA tensor (bf16 or fp32)."""
 
     def __init__(self, W: torch.Tensor, num_slots: int, max_rank: int, max_tokens: int,
-                 stream=None):
+                 stream=None, pool_rows: int = 0):
+        """``pool_rows`` > 0: adapters stored at their true rank in a row pool of that many
+        rank rows (lora_layer_create_pooled)."""
         if not W.is_cuda:
             raise ValueError("W must be a CUDA tensor")
         self.K, self.N = int(W.shape[0]), int(W.shape[1])
         self.num_slots, self.max_rank, self.max_tokens = num_slots, max_rank, max_tokens
         self.dtype = W.dtype
-        self.handle = lora_layer_create(self.K, self.N, num_slots, max_rank, max_tokens,
-                                        W.dtype, W.contiguous(), stream)
+        if pool_rows:
+            self.handle = lora_layer_create_pooled(self.K, self.N, num_slots, max_rank,
+                                                   max_tokens, W.dtype, W.contiguous(),
+                                                   pool_rows, stream)
+        else:
+            self.handle = lora_layer_create(self.K, self.N, num_slots, max_rank, max_tokens,
+                                            W.dtype, W.contiguous(), stream)
         self._keep = {}
 
     def load(self, slot: int, A: torch.Tensor, B: torch.Tensor, alpha: float, side_stream=None):
@@ -328,6 +356,10 @@ class LoraLayer:
 
     def segments(self, stream=None):
         return lora_get_segments(self.handle, self.max_tokens, self.num_slots, stream)
+
+    def pool_usage(self):
+        """(rank rows in use, rank rows in the pool)."""
+        return lora_get_pool_usage(self.handle)
 
     def set_gemm_plan(self, block_n: int, k_split: int = 1, cta_pair: int = 0):
         lora_set_gemm_plan(self.handle, block_n, k_split, cta_pair)

@@ -64,6 +64,11 @@ def test_create_rejects_bad_arguments(lib):
         assert not h.value
     assert L.lora_layer_create(ctypes.byref(h), 8, 8, 4, 16, 8, lib.LORA_BF16, None, None) == lib.LORA_EINVAL
     assert L.lora_layer_create(None, 8, 8, 4, 16, 8, lib.LORA_BF16, dummy, None) == lib.LORA_EINVAL
+    # a row pool below one slot of max_rank rows (16) or above num_slots of them (64)
+    for rows in (0, 8, 65):
+        assert L.lora_layer_create_pooled(ctypes.byref(h), 8, 8, 4, 16, 8, lib.LORA_BF16, dummy,
+                                          None, rows) == lib.LORA_EINVAL
+        assert not h.value
 
 
 def test_null_layer_calls_are_rejected(lib):
