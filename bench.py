@@ -72,10 +72,12 @@ def peaks():
 # algorithmic work per step (what the method must move / compute)
 # ------------------------------------------------------------------------------------
 
-def algorithmic(wl, delta_mode=None):
+def algorithmic(wl, delta_mode=None, fp8=False):
     """Bytes and FLOPs per step: x, W, y once; each distinct adapter slice used in the
     batch once at its true rank; ids; the fp32 intermediate of the low-rank term once
-    (v [T_a, r] in v mode; delta [T_a, N] in delta mode, batches of <= 512 bf16 rows)."""
+    (v [T_a, r] in v mode; delta [T_a, N] in delta mode, batches of <= 512 bf16 rows).
+    fp8 (e4m3 base): W one byte an element, and the quantised x (one byte an element)
+    written once and read by the GEMM instead of x."""
     T, K, N = wl.T, wl.K, wl.N
     es = 2 if wl.dtype == torch.bfloat16 else 4
     if delta_mode is None:
@@ -91,8 +93,11 @@ def algorithmic(wl, delta_mode=None):
     d_bytes = n_ad * N * 4
     base = {"x": T * K * es, "W": K * N * es, "y": T * N * es, "ids": T * 4}
     lora_flops = 2 * sum(ranks[int(s)] * (K + N) for s in ids[adapted])
+    if fp8:
+        base["W"] = K * N
+        base["xq"] = 2 * T * K  # written by the quantiser, read by the GEMM
     if delta_mode:  # low-rank kernel: x, A, B -> delta; GEMM: x, W, delta -> y
-        gemm = base["x"] + base["W"] + base["y"] + d_bytes + base["ids"]
+        gemm = (T * K if fp8 else base["x"]) + base["W"] + base["y"] + d_bytes + base["ids"]
         lowrank = base["x"] + a_bytes + b_bytes + d_bytes + base["ids"]
     else:  # tile kernel: x, A -> v; GEMM: x, W, v, B -> y
         gemm = base["x"] + base["W"] + base["y"] + b_bytes + v_bytes + base["ids"]
@@ -327,7 +332,7 @@ def run_ours(args):
     for i in range(args.layers):
         seed = cfg["seed"] + 7919 * i + 104729 * rank
         wl = make_workload(args.config, seed, "cpu" if i == 0 else dev)
-        layer = LoraLayer(wl.W.to(dev), wl.S, wl.R, wl.T)
+        layer = LoraLayer(wl.W.to(dev), wl.S, wl.R, wl.T, fp8_base=args.fp8)
         for s, ad in enumerate(wl.adapters):
             if ad is not None:
                 layer.load(s, ad[0].to(dev), ad[1].to(dev), ad[2])
@@ -342,7 +347,7 @@ def run_ours(args):
             del wl
     torch.cuda.synchronize()
     T, K, N = wl0.T, wl0.K, wl0.N
-    work = algorithmic(wl0)
+    work = algorithmic(wl0, fp8=args.fp8)
 
     stream = torch.cuda.Stream(device=dev)
 
@@ -500,10 +505,11 @@ def run_ours(args):
     gemm_s = kern_us["gemm"] * 1e-6
     achieved = work["gemm_bytes"] / gemm_s / 1e9
     kernel_src = os.path.join(ROOT, "segmented_rank_gemm_gb300", "csrc", "gemm_tc.cu")
-    roofline = {"kernel": "gemm_tc_kernel (base GEMM + fused expand)", "bound": "hbm",
+    roofline = {"kernel": "gemm_tc_kernel (base GEMM%s + fused expand)"
+                          % (", e4m3" if args.fp8 else ""), "bound": "hbm",
                 "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"],
-                "traffic": traffic_from_profile(kernel_src, args.config),
+                "traffic": None if args.fp8 else traffic_from_profile(kernel_src, args.config),
                 "peak_source": pk["source"], "algorithmic_bytes_per_launch": work["gemm_bytes"],
                 "avg_launch_us": kern_us["gemm"]}
     if args.config != "decode_bgmv":
@@ -521,9 +527,13 @@ def run_ours(args):
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl0.dtype == torch.bfloat16
-        else "f32", "data": "synthetic (seeded, shapes of the pages' 8B-class workloads)",
-        "config": {"workload": cfg["desc"], "T": T, "K": K, "N": N, "slots": wl0.S,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": ("e4m3 base, bf16 low-rank" if args.fp8 else "bf16")
+        if wl0.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded, shapes of the pages' 8B-class workloads)",
+        "config": {"workload": cfg["desc"] + (", base in e4m3 (x per row, W per column)"
+                                              if args.fp8 else ""),
+                   "T": T, "K": K, "N": N, "slots": wl0.S,
                    "slot_rank_width": wl0.R, "distinct_slots": work["distinct_slots"],
                    "adapted_rows": work["adapted_rows"], "parallelism": "replicas x%d" % world,
                    "l2": "rotating %d independent layer instances (~%d MB of weights and slots)"
@@ -540,7 +550,7 @@ def run_ours(args):
                            "achieved_gbs": work["lowrank_bytes"] / (kern_us["shrink"] * 1e-6) / 1e9,
                            "mode": work["mode"]},
         # decode batches (bf16, <= 512 rows): BGMV + GEMM; larger: builder + shrink + GEMM
-        "gpu_launches": (2 if work["mode"] == "delta" else 3) * args.steps,
+        "gpu_launches": ((3 if args.fp8 else 2) if work["mode"] == "delta" else 3) * args.steps,
         "clocks": clocks,
         "e2e": e2e,
         "wall_s_timed": t_wall1 - t_wall0,
@@ -742,6 +752,8 @@ def main(argv=None):
     ap.add_argument("--e2e-streams", type=int, default=4,
                     help="streams the end-to-end steps rotate over (instance j on stream j %% n)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="decode workload with the base in e4m3 (lora_layer_create_fp8)")
     ap.add_argument("--swap-in", action="store_true",
                     help="measure adapter swap-ins through the adapter cache instead")
     args = ap.parse_args(argv)

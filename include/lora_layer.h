@@ -77,6 +77,26 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
                       int max_tokens, int dtype, const void* W_dev, void* stream);
 
 /*
+ * As lora_layer_create for bf16 activations and adapters, with the base product in e4m3
+ * ("Multi-LoRA Serving 与 Adapter 隔离", section on quantisation: an FP8 base with an FP16
+ * LoRA is the usual mixed precision; the quantised product and the LoRA term meet in the
+ * kernel's accumulator and epilogue, and the float delta is never added to the packed
+ * quantised weights).  For every row i and column n:
+ *     y[i,n] = bf16( sx[i] sw[n] sum_k xq[i,k] wq[k,n]  +  low-rank term of x[i] )
+ *   - W_dev [K,N] bf16 is quantised once here, per column: sw[n] = max_k |W[k,n]| / 448
+ *     (1 for a zero column), wq = e4m3(W / sw), round to nearest even, saturating;
+ *   - each forward quantises x per row the same way (sx[i] = max_k |x[i,k]| / 448) in a
+ *     kernel of its own before the low-rank kernel; scales and divisions are fp32;
+ *   - the low-rank term is computed from the bf16 x as in a plain layer;
+ *   - the base runs as e4m3 x e4m3 tcgen05 MMAs (kind::f8f6f4) with fp32 accumulation.
+ * Limits: K a multiple of 16; max_tokens <= 512 (decode batches: the layer holds no
+ * prefill path).  The packed weight takes K x N bytes.
+ * Errors: as lora_layer_create.
+ */
+int lora_layer_create_fp8(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
+                          int max_tokens, const void* W_dev, void* stream);
+
+/*
  * As lora_layer_create, with adapters stored at their true rank in a row pool instead of
  * one max_rank-wide block per slot ("Multi-LoRA Serving: Architecture for Thousands of
  * Adapters", sections on heterogeneous ranks and S-LoRA's kernels: a rank-8 and a rank-64

@@ -166,16 +166,21 @@ __device__ __forceinline__ bool seg_at(int k, int g, int G, int U, int nkb, int 
 // two kernels run side by side.  VMODE is a template parameter so that the delta-mode
 // variants carry none of the expand-block and stream-K code; the v-mode variants share
 // their SMs with no other kernel and get more registers.
-template <int BN, bool PAIR, bool VMODE>
+// FP8: the base operands are e4m3 (x quantised per row, W per column; delta mode only): a
+// 128-byte K block then holds 128 elements instead of 64, the MMAs are kind::f8f6f4, and
+// the epilogue scales the accumulator by sx[row] sw[col] before it adds the delta.
+template <int BN, bool PAIR, bool VMODE, bool FP8 = false>
 __global__ void __maxnreg__(VMODE ? 168 : 136)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_bx, GemmArgs a, int stages,
                    int xscr_bytes, int group_m, int mtp, int nt, int full_rounds,
                    int sk_slots) {
+  static_assert(!(FP8 && VMODE), "the e4m3 base runs in delta mode only");
   constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of the W (or B expand) tile this CTA loads
   constexpr int kBBytes = kBRows * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
+  constexpr int kKE = FP8 ? 2 * kBK : kBK;  // K elements per block (128 bytes of a row)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -213,7 +218,7 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
   const uint16_t pair_mask = (uint16_t)(3u << lead_rank);
   // split K: this CTA's range of K blocks (the host keeps every range non-empty)
   const int cs = gridDim.z, z = blockIdx.z;
-  const int nkb_all = (a.K + kBK - 1) / kBK;
+  const int nkb_all = (a.K + kKE - 1) / kKE;
   const int per = (nkb_all + cs - 1) / cs;
   const int kb_begin = z * per;
   const int nkb = min(nkb_all, kb_begin + per) - kb_begin;
@@ -286,12 +291,12 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
             // are counted on the even CTA's barrier, which its MMA lane waits on
             if (pr == 0) mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
             const uint32_t fb = dsmem_map(smem_u32(&full[s]), lead_rank);
-            tma_load_2d_pair(sa, &tmap_x, fb, kb * kBK, m0);
-            tma_load_2d_pair(sa + kABytes, &tmap_w, fb, kb * kBK, n0 + pr * kBRows);
+            tma_load_2d_pair(sa, &tmap_x, fb, kb * kKE, m0);
+            tma_load_2d_pair(sa + kABytes, &tmap_w, fb, kb * kKE, n0 + pr * kBRows);
           } else {
             mbar_arrive_expect_tx(&full[s], kStageBytes);
-            tma_load_2d(sa, &tmap_x, &full[s], kb * kBK, m0);
-            tma_load_2d(sa + kABytes, &tmap_w, &full[s], kb * kBK, n0);
+            tma_load_2d(sa, &tmap_x, &full[s], kb * kKE, m0);
+            tma_load_2d(sa + kABytes, &tmap_w, &full[s], kb * kKE, n0);
           }
           if (++s == stages) {
             s = 0;
@@ -338,7 +343,8 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
   } else if (warp == 1) {
     // ---------------- MMA issuer (pairs: the even CTA's lane, for both CTAs) ----------------
     if (lane == 0 && pr == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN);
+      constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(PAIR ? 2 * kBM : kBM, BN)
+                                     : idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN);
       // descriptors built once: the start-address field counts 16-byte units, so a stage
       // is + s * kStageBytes / 16 and a 16-wide K step inside the 128-byte row is + 2
       const uint64_t a_desc0 = smem_desc_sw128(smem_u32(stage_base));
@@ -354,7 +360,14 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
         for (int kk = 0; kk < kBK / 16; ++kk) {
           if (!((chunks >> kk) & 1u)) continue;
           const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-          if (PAIR)
+          // (a 32-byte step of the row either way: 16 bf16 or 32 e4m3 elements of K)
+          if (FP8 && PAIR)
+            tc_mma_f8_pair(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
+                           idesc, acc);
+          else if (FP8)
+            tc_mma_f8(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2), idesc,
+                      acc);
+          else if (PAIR)
             tc_mma_bf16_pair(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
                              idesc, acc);
           else
@@ -690,6 +703,18 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
             acc[i * 4 + 3] += v.w;
           }
         }
+        if (FP8) {  // the e4m3 product back to the x and W scales (sw is padded past N)
+          const float sxr = row < a.M ? __ldg(a.sx + row) : 0.f;
+          const float4* swp = reinterpret_cast<const float4*>(a.sw + nc);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 w = __ldg(swp + i);
+            acc[i * 4 + 0] *= sxr * w.x;
+            acc[i * 4 + 1] *= sxr * w.y;
+            acc[i * 4 + 2] *= sxr * w.z;
+            acc[i * 4 + 3] *= sxr * w.w;
+          }
+        }
         float4 d[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q)
@@ -767,12 +792,26 @@ cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t encode_tmap_u8(CUtensorMap* map, const void* base, int rows, int K, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  if (K % 16 != 0) return cudaErrorInvalidValue;  // rows start on 16-byte boundaries
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(2 * kBK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Raise (never lower) one kernel variant's dynamic shared-memory limit: one cache per
 // variant, shared by every caller.
-template <int BN, bool PAIR, bool VMODE>
+template <int BN, bool PAIR, bool VMODE, bool FP8 = false>
 static cudaError_t raise_smem_limit(int bytes) {
   static int limit = 0;
-  return ensure_smem_limit(gemm_tc_kernel<BN, PAIR, VMODE>, bytes, &limit);
+  return ensure_smem_limit(gemm_tc_kernel<BN, PAIR, VMODE, FP8>, bytes, &limit);
 }
 
 // CTAs of this GEMM that can be resident at once in clusters of `csize` CTAs (every variant
@@ -885,7 +924,7 @@ static size_t tc_smem_bytes(int BN, bool pair, int stages, int xscr_bytes) {
   return 1024 + stages * stage + xscr_bytes + (2 * kBM + 6) * 4 + (4 * stages + 6) * 8;
 }
 
-template <int BN, bool PAIR, bool VMODE>
+template <int BN, bool PAIR, bool VMODE, bool FP8 = false>
 static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUtensorMap& tmap_x,
                              const CUtensorMap& tmap_w, const CUtensorMap& tmap_bx,
                              cudaStream_t stream) {
@@ -908,7 +947,7 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   if ((cs > 1 || a.ex.mode == kExpandDelta || a.sk_part) &&
       (size_t)stages * stage < (size_t)kBM * BN * 4)
     return cudaErrorInvalidConfiguration;
-  cudaError_t e = raise_smem_limit<BN, PAIR, VMODE>((int)smem);
+  cudaError_t e = raise_smem_limit<BN, PAIR, VMODE, FP8>((int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -949,9 +988,23 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   const size_t band_rows = (size_t)kBM * (PAIR ? 2 : 1);
   const int group_m =
       std::max(1, std::min(mtp, (int)((32u << 20) / ((size_t)a.K * band_rows * 2))));
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, PAIR, VMODE>, tmap_x, tmap_w, tmap_bx, a,
-                            stages,
-                            xscr, group_m, mtp, nt, full_rounds, sk_slots);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, PAIR, VMODE, FP8>, tmap_x, tmap_w, tmap_bx,
+                            a, stages, xscr, group_m, mtp, nt, full_rounds, sk_slots);
+}
+
+static cudaError_t launch_variant_fp8(const GemmArgs& a, const GemmPlan& plan,
+                                      const CUtensorMap& tmap_x, const CUtensorMap& tw,
+                                      cudaStream_t stream) {
+  if (plan.pair) {
+    if (plan.block_n == 256) return launch_tc<256, true, false, true>(a, plan, tmap_x, tw, tw, stream);
+    if (plan.block_n == 128) return launch_tc<128, true, false, true>(a, plan, tmap_x, tw, tw, stream);
+    return cudaErrorInvalidConfiguration;
+  }
+  switch (plan.block_n) {
+    case 256: return launch_tc<256, false, false, true>(a, plan, tmap_x, tw, tw, stream);
+    case 128: return launch_tc<128, false, false, true>(a, plan, tmap_x, tw, tw, stream);
+    default: return launch_tc<64, false, false, true>(a, plan, tmap_x, tw, tw, stream);
+  }
 }
 
 template <bool VMODE>
@@ -973,13 +1026,21 @@ static cudaError_t launch_variant(const GemmArgs& a, const GemmPlan& plan,
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
                            const CUtensorMap* tmap_bx3, cudaStream_t stream) {
   if (a.ex.mode == kExpandV && !tmap_bx3) return cudaErrorInvalidValue;
-  GemmPlan plan = gemm_tc_plan(a.M, a.N, a.K, a.num_sms, a.ex.mode != kExpandV,
+  if (a.fp8 && (a.ex.mode != kExpandDelta || !a.tmap_xq || !a.sx || !a.sw || a.K % 16 != 0))
+    return cudaErrorInvalidValue;
+  // the plan counts K blocks of 128 bytes: an e4m3 row of K elements is K / 2 bf16 wide
+  const int k_bytes2 = a.fp8 ? (a.K + 1) / 2 : a.K;
+  GemmPlan plan = gemm_tc_plan(a.M, a.N, k_bytes2, a.num_sms, a.ex.mode != kExpandV,
                                a.ex.mode == kExpandV ? a.ex.S : 0);
   if (a.force_bn != 0) {
     // v mode never splits K: its expand blocks run after the base ones in one accumulator
     plan = GemmPlan{a.force_bn, a.ex.mode == kExpandV ? 1 : a.force_cs, a.force_pair};
-    const int nkb = (a.K + kBK - 1) / kBK, c = plan.ksplit;
+    const int nkb = (k_bytes2 + kBK - 1) / kBK, c = plan.ksplit;
     if (c > 1 && (c - 1) * ((nkb + c - 1) / c) >= nkb) return cudaErrorInvalidConfiguration;
+  }
+  if (a.fp8) {
+    const int ti = gemm_tc_tile_index(plan.pair ? plan.block_n / 2 : plan.block_n);
+    return launch_variant_fp8(a, plan, *a.tmap_xq, tmap_w3[ti], stream);
   }
   CUtensorMap tmap_x;
   cudaError_t e = encode_tmap_bf16(&tmap_x, a.x, a.M, a.K, kBM);

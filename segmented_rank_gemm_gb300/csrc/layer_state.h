@@ -17,7 +17,12 @@ struct lora_layer {
   int max_rank = 0;  // largest adapter rank a slot accepts
   int R = 0;         // slot rank width: max_rank rounded up to a multiple of 8 (zero padded)
   size_t esize = 0;
-  void* Wp = nullptr;      // packed base weight: bf16 [N][K], f32 [K][N]
+  void* Wp = nullptr;      // packed base weight: bf16 [N][K], f32 [K][N], e4m3 [N][K]
+  bool fp8 = false;        // e4m3 base (x quantised per row each forward, W per column)
+  uint8_t* xq = nullptr;   // fp8: [T_max][K] quantised x
+  float* sx = nullptr;     // fp8: [T_max] row scales
+  float* sw = nullptr;     // fp8: [N rounded up to 256] column scales, zero past N
+  CUtensorMap tmap_xq;     // fp8: xq with (128 x 128) boxes
   void* A_pool = nullptr;  // [P][K] rank rows: slot s from row row_base[s]
   void* B_pool = nullptr;  // [P][N] rank rows
   int P = 0;               // pool rows: S * R, or the row budget of a pooled layer

@@ -177,6 +177,12 @@ struct GemmArgs {
   // {epoch, exit count, flag per CTA} (zeroed at allocation); null: no stream-K
   float* sk_part;
   int32_t* sk_sync;
+  // e4m3 base (delta mode only): x quantised per row (tmap_xq: [M rows][K] bytes, (128 x
+  // 128) box), W per column (tmap_w3: [N rows][K] bytes); y = sx[row] sw[col] (xq wq) + delta
+  bool fp8 = false;
+  const CUtensorMap* tmap_xq = nullptr;
+  const float* sx = nullptr;  // [M]
+  const float* sw = nullptr;  // [N rounded up to 256], zero past N
 };
 // tcgen05 / TMEM / TMA kernel (gemm_tc.cu).  tmap_w3 holds the layer's cached maps of the
 // packed weight for N tiles of 256, 128 and 64 rows (in that order); tmap_bx3 the maps of
@@ -185,6 +191,18 @@ struct GemmArgs {
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
                            const CUtensorMap* tmap_bx3, cudaStream_t stream);
 constexpr int kTcTileN[3] = {256, 128, 64};
+
+// ---- e4m3 base (fp8.cu) ----
+// 2-D tensor map over [rows][K] bytes (K-major, K a multiple of 16) with a (128 x box_rows)
+// box and the 128-byte swizzle.
+cudaError_t encode_tmap_u8(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
+// x [T][K] bf16 -> xq [T][K] e4m3 and sx [T]: sx = max |x[row]| / 448 (1 for a zero row),
+// xq = e4m3(x / sx), round to nearest even, saturating.  One CTA per row; a plain launch.
+cudaError_t launch_quant_rows_e4m3(const void* x, int T, int K, uint8_t* xq, float* sx,
+                                   cudaStream_t stream);
+// W [K][N] bf16 -> Wq [N][K] e4m3 (transposed, K-major) and sw [N]: per column as above.
+cudaError_t launch_quant_cols_e4m3(const void* W, int K, int N, uint8_t* Wq, float* sw,
+                                   cudaStream_t stream);
 // Encode a 2-D bf16 tensor map for a K-major [rows, K] matrix with a (64 x box_rows) box.
 cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
 struct GemmPlan {

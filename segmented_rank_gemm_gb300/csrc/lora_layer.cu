@@ -70,7 +70,8 @@ void free_all(lora_layer* L) {
   void* ptrs[] = {L->Wp, L->A_pool, L->B_pool, L->Bx_pool, L->A_stage, L->scale, L->rank, L->loaded,
                   L->row_slot, L->perm, L->seg_offsets, L->seg_slot, L->tile_seg,
                   L->tile_row0, L->meta, L->err, L->v, L->delta, L->xk, L->sk_part,
-                  L->sk_sync, L->x_stage, L->ids_stage, L->y_stage, L->row_base};
+                  L->sk_sync, L->x_stage, L->ids_stage, L->y_stage, L->row_base,
+                  L->xq, L->sx, L->sw};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (L->stage_free) cudaEventDestroy(L->stage_free);
@@ -132,7 +133,7 @@ extern "C" {
 // rows (rounded up to 8) from which each load takes its rank rounded up to 8 rows.
 static int create_layer(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
                         int max_tokens, int dtype, const void* W_dev, void* stream_,
-                        int pool_rows) {
+                        int pool_rows, bool fp8 = false) {
   if (!out) return LORA_EINVAL;
   *out = nullptr;
   if (K < 1 || N < 1 || num_slots < 1 || num_slots > kMaxSlots || max_rank < 1 ||
@@ -140,6 +141,8 @@ static int create_layer(lora_layer_t** out, int K, int N, int num_slots, int max
     return LORA_EINVAL;
   if (dtype != LORA_F32 && dtype != LORA_BF16) return LORA_EINVAL;
   if (dtype == LORA_BF16 && (K % 8 != 0 || N % 8 != 0)) return LORA_EINVAL;
+  // an e4m3 base: bf16 activations, K a multiple of 16 (16-byte rows), decode batches only
+  if (fp8 && (dtype != LORA_BF16 || K % 16 != 0 || max_tokens > kDeltaMaxT)) return LORA_EINVAL;
   const int R8 = (max_rank + 7) / 8 * 8;
   if (pool_rows < 0 || (pool_rows > 0 && ((pool_rows + 7) / 8 * 8 < R8 ||
                                            (long long)pool_rows > (long long)num_slots * R8)))
@@ -169,6 +172,7 @@ static int create_layer(lora_layer_t** out, int K, int N, int num_slots, int max
 
   const size_t es = L->esize;
   const size_t S = num_slots, R = L->R;
+  L->fp8 = fp8;
   L->pooled = pool_rows > 0;
   L->P = L->pooled ? (pool_rows + 7) / 8 * 8 : (int)(S * R);
   const size_t P = L->P;
@@ -189,8 +193,14 @@ static int create_layer(lora_layer_t** out, int K, int N, int num_slots, int max
   // the base GEMM of a delta-mode batch may split K: scratch for its largest exchange
   if (dtype == LORA_BF16)
     for (int m = 1; m <= std::min(max_tokens, kDeltaMaxT); ++m)
-      L->xk_floats = std::max(L->xk_floats, gemm_tc_exchange_floats(m, N, K, L->num_sms));
-  bool ok = cudaMalloc(&L->Wp, (size_t)K * N * es) == cudaSuccess &&
+      L->xk_floats =  // (an e4m3 row of K elements has the bytes of K / 2 bf16)
+          std::max(L->xk_floats, gemm_tc_exchange_floats(m, N, fp8 ? K / 2 : K, L->num_sms));
+  const size_t n256 = ((size_t)N + 255) / 256 * 256;
+  bool ok = cudaMalloc(&L->Wp, (size_t)K * N * (fp8 ? 1 : es)) == cudaSuccess &&
+            (!fp8 || (cudaMalloc(reinterpret_cast<void**>(&L->xq), (size_t)max_tokens * K) ==
+                          cudaSuccess &&
+                      dmalloc(&L->sx, max_tokens) == cudaSuccess &&
+                      dmalloc(&L->sw, n256) == cudaSuccess)) &&
             cudaMalloc(&L->A_pool, P * K * es) == cudaSuccess &&
             cudaMalloc(&L->B_pool, P * N * es) == cudaSuccess &&
             dmalloc(&L->row_base, S) == cudaSuccess &&
@@ -245,7 +255,20 @@ static int create_layer(lora_layer_t** out, int K, int N, int num_slots, int max
         cudaMemsetAsync(L->sk_sync, 0, ((size_t)L->num_sms + 2) * 4, stream) == cudaSuccess);
   if (!ok) return bail(LORA_ECUDA);
 
-  if (dtype == LORA_BF16) {
+  if (fp8) {  // W quantised per column into [N][K] e4m3; x's map over the layer's xq
+    if (cudaMemsetAsync(L->sw, 0, n256 * sizeof(float), stream) != cudaSuccess ||
+        launch_quant_cols_e4m3(W_dev, K, N, static_cast<uint8_t*>(L->Wp), L->sw, stream) !=
+            cudaSuccess)
+      return bail(LORA_ECUDA);
+    for (int i = 0; i < 3; ++i)
+      if (encode_tmap_u8(&L->tmap_w[i], L->Wp, N, K, kTcTileN[i]) != cudaSuccess)
+        return bail(LORA_ECUDA);
+    if (encode_tmap_u8(&L->tmap_xq, L->xq, max_tokens, K, kTcTileRows) != cudaSuccess)
+      return bail(LORA_ECUDA);
+    if (encode_tmap_bf16(&L->tmap_a, L->A_pool, (int)P, K, (L->R + 15) / 16 * 16) !=
+        cudaSuccess)
+      return bail(LORA_ECUDA);
+  } else if (dtype == LORA_BF16) {
     if (launch_pack_w_bf16(W_dev, L->Wp, K, N, stream) != cudaSuccess) return bail(LORA_ECUDA);
     for (int i = 0; i < 3; ++i)
       if (encode_tmap_bf16(&L->tmap_w[i], L->Wp, N, K, kTcTileN[i]) != cudaSuccess)
@@ -315,6 +338,12 @@ extern "C" {
 int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
                       int max_tokens, int dtype, const void* W_dev, void* stream_) {
   return create_layer(out, K, N, num_slots, max_rank, max_tokens, dtype, W_dev, stream_, 0);
+}
+
+int lora_layer_create_fp8(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
+                          int max_tokens, const void* W_dev, void* stream_) {
+  return create_layer(out, K, N, num_slots, max_rank, max_tokens, LORA_BF16, W_dev, stream_, 0,
+                      true);
 }
 
 int lora_layer_create_pooled(lora_layer_t** out, int K, int N, int num_slots, int max_rank,
@@ -543,6 +572,9 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     ba.delta = L->delta;
     ba.num_sms = L->num_sms;
     ba.per_column = L->percol_slots > 0;
+    // e4m3 base: x quantised first (a plain launch after the previous forward); the BGMV
+    // waits for it, and the GEMM launches only once the BGMV has
+    if (L->fp8) LORA_CUDA(L, launch_quant_rows_e4m3(x_dev, T, L->K, L->xq, L->sx, stream));
     LORA_CUDA(L, launch_bgmv_delta(ba, stream));
   } else if (bf16) {
     ShrinkTcArgs sa;
@@ -619,6 +651,10 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.force_bn = L->gemm_plan.block_n;
   ga.force_cs = L->gemm_plan.ksplit;
   ga.force_pair = L->gemm_plan.pair;
+  ga.fp8 = L->fp8;
+  ga.tmap_xq = L->fp8 ? &L->tmap_xq : nullptr;
+  ga.sx = L->sx;
+  ga.sw = L->sw;
   LORA_CUDA(L, trace_mark(L, 4, stream));
   if (bf16)
     LORA_CUDA(L, launch_gemm_tc(ga, L->tmap_w, L->Bx_pool ? L->tmap_bx : nullptr, stream));

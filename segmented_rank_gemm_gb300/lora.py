@@ -27,7 +27,8 @@ LORA_ECUDA, LORA_ENOMEM, LORA_ESTATE, LORA_ETIMEOUT = -5, -6, -7, -8
 LORA_ENOENT, LORA_ECAPACITY = -9, -10
 
 # every entry point declared in include/lora_layer.h
-ABI_FUNCTIONS = ("lora_layer_create", "lora_layer_create_pooled", "lora_get_pool_usage",
+ABI_FUNCTIONS = ("lora_layer_create", "lora_layer_create_pooled", "lora_layer_create_fp8",
+                 "lora_get_pool_usage",
                  "load_adapter_slot", "load_adapter_slot_composed",
                  "unload_adapter_slot",
                  "set_batch_segments", "lora_forward", "lora_forward_host", "lora_get_status",
@@ -69,6 +70,7 @@ def _load() -> ctypes.CDLL:
     L.lora_layer_create_pooled.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32, vp,
                                            vp, i32]
     L.lora_get_pool_usage.argtypes = [vp, vp, vp]
+    L.lora_layer_create_fp8.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, vp, vp]
     L.load_adapter_slot.argtypes = [vp, i32, vp, vp, i32, f32, vp]
     L.load_adapter_slot_composed.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp]
     L.unload_adapter_slot.argtypes = [vp, i32, vp]
@@ -171,6 +173,13 @@ def lora_layer_create_pooled(K, N, num_slots, max_rank, max_tokens, dtype, W, po
     _check(None, _lib.lora_layer_create_pooled(ctypes.byref(h), K, N, num_slots, max_rank,
                                                max_tokens, code, _ptr(W), _stream(stream),
                                                int(pool_rows)))
+    return h.value
+
+
+def lora_layer_create_fp8(K, N, num_slots, max_rank, max_tokens, W, stream=None) -> int:
+    h = ctypes.c_void_p()
+    _check(None, _lib.lora_layer_create_fp8(ctypes.byref(h), K, N, num_slots, max_rank,
+                                            max_tokens, _ptr(W), _stream(stream)))
     return h.value
 
 
@@ -286,15 +295,21 @@ class LoraLayer:
     """Owns one C layer.  ``W`` [K, N] is a CUDA tensor (bf16 or fp32)."""
 
     def __init__(self, W: torch.Tensor, num_slots: int, max_rank: int, max_tokens: int,
-                 stream=None, pool_rows: int = 0):
+                 stream=None, pool_rows: int = 0, fp8_base: bool = False):
         """``pool_rows`` > 0: adapters stored at their true rank in a row pool of that many
-        rank rows (lora_layer_create_pooled)."""
+        rank rows (lora_layer_create_pooled); ``fp8_base``: the base product in e4m3
+        (lora_layer_create_fp8; W bf16)."""
         if not W.is_cuda:
             raise ValueError("W must be a CUDA tensor")
         self.K, self.N = int(W.shape[0]), int(W.shape[1])
         self.num_slots, self.max_rank, self.max_tokens = num_slots, max_rank, max_tokens
         self.dtype = W.dtype
-        if pool_rows:
+        if fp8_base:
+            if pool_rows or W.dtype != torch.bfloat16:
+                raise ValueError("an e4m3 base layer takes a bf16 W and no row pool")
+            self.handle = lora_layer_create_fp8(self.K, self.N, num_slots, max_rank, max_tokens,
+                                                W.contiguous(), stream)
+        elif pool_rows:
             self.handle = lora_layer_create_pooled(self.K, self.N, num_slots, max_rank,
                                                    max_tokens, W.dtype, W.contiguous(),
                                                    pool_rows, stream)

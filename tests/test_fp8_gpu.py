@@ -1,0 +1,111 @@
+"""The e4m3-base layer (lora_layer_create_fp8) on the GPU against the oracle's definition:
+y = sx sw (xq wq) + the low-rank term of the bf16 x, with the quantisation of x (per row,
+every forward) and W (per column, at creation) decided exactly as the oracle decides it.
+Ragged shapes, inputs already on the e4m3 grid (quantisation is the identity: the plain
+product), every tiling of the decode-mode GEMM, and the decode workload's full shape.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import fp8
+from segmented_rank_gemm_gb300 import workloads
+from gpu_helpers import assert_parity
+
+pytestmark = pytest.mark.gpu
+BF16 = torch.bfloat16
+
+
+def _ref(wl, rows=None):
+    x = wl.x.float().numpy()
+    table = oracle.SlotTable(wl.adapters, wl.K, wl.N)
+    delta = oracle.forward_rows(wl.x, torch.zeros(wl.K, wl.N, dtype=torch.float64), table,
+                                wl.token_slot, rows=rows)
+    base = fp8.base_w8a8(x if rows is None else x[rows], wl.W.float().numpy())
+    return base + delta
+
+
+def _layer(wl):
+    from segmented_rank_gemm_gb300.lora import LoraLayer
+    layer = LoraLayer(wl.W.cuda(), wl.S, wl.R, max(wl.T, 1), fp8_base=True)
+    for s, ad in enumerate(wl.adapters):
+        if ad is not None:
+            layer.load(s, ad[0].cuda(), ad[1].cuda(), ad[2])
+    return layer
+
+
+@pytest.mark.parametrize("T,K,N", [(256, 512, 320), (300, 1024, 264), (1, 64, 72),
+                                   (129, 256, 1040)])
+def test_fp8_base_parity(T, K, N):
+    wl = workloads.synthetic(700 + T, T, K, N, S=6, ranks=[1, 16, 8, 3, 12, 2], R=16,
+                             base_frac=0.15, empty_slots=(4,))
+    layer = _layer(wl)
+    y = layer(wl.x.cuda(), wl.token_slot.cuda())
+    torch.cuda.synchronize()
+    assert layer.status() == (-4 if (wl.token_slot == 4).any() else 0)
+    assert_parity(y, _ref(wl), BF16, what="fp8 base T=%d K=%d N=%d" % (T, K, N))
+    layer.close()
+
+
+def test_fp8_on_grid_inputs_equal_the_plain_product():
+    rng = np.random.default_rng(3)
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F])
+    grid = np.unique([float(fp8.e4m3_round(v)) for v in
+                      [(-1) ** (c >> 7) * (2.0 ** ((c >> 3 & 15) - 7) * (1 + (c & 7) / 8)
+                                           if (c >> 3 & 15) else (c & 7) * 2.0 ** -9)
+                       for c in codes]])
+    T, K, N = 64, 128, 96
+    x = rng.choice(grid, size=(T, K)) / 64.0  # on the grid, row max set to 448 / 64 below
+    x[:, 5] = 448.0 / 64.0
+    W = rng.choice(grid, size=(K, N)) / 4096.0
+    W[7, :] = 448.0 / 4096.0
+    wl = workloads.synthetic(720, T, K, N, S=2, ranks=[4, 8], R=8, base_frac=0.3)
+    wl.x = torch.tensor(x, dtype=BF16)
+    wl.W = torch.tensor(W, dtype=BF16)
+    assert np.array_equal(wl.x.double().numpy(), x) and np.array_equal(wl.W.double().numpy(), W)
+    layer = _layer(wl)
+    y = layer(wl.x.cuda(), wl.token_slot.cuda())
+    torch.cuda.synchronize()
+    plain = oracle.forward_rows(wl.x, wl.W, oracle.SlotTable(wl.adapters, K, N), wl.token_slot)
+    assert np.allclose(_ref(wl), plain, rtol=0, atol=1e-12)  # quantisation is the identity
+    assert_parity(y, plain, BF16, what="fp8 base, inputs on the e4m3 grid")
+    layer.close()
+
+
+def test_fp8_every_decode_plan():
+    wl = workloads.synthetic(730, 300, 1024, 520, S=5, ranks=16, R=16, base_frac=0.1)
+    ref = _ref(wl)
+    layer = _layer(wl)
+    for bn in (64, 128, 256):
+        for ks in (1, 2, 4):
+            for pair in (0, 1):
+                if bn // ks < 32 or (pair and bn < 128):
+                    continue
+                layer.set_gemm_plan(bn, ks, pair)
+                y = layer(wl.x.cuda(), wl.token_slot.cuda())
+                torch.cuda.synchronize()
+                assert layer.status() == 0
+                assert_parity(y, ref, BF16, what="fp8 plan (%d, %d, %d)" % (bn, ks, pair))
+    layer.close()
+
+
+def test_fp8_decode_workload_full_shape():
+    wl = workloads.decode_bgmv(seed=1002, device="cpu")
+    layer = _layer(wl)
+    y = layer(wl.x.cuda(), wl.token_slot.cuda())
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    rows = np.arange(0, wl.T, 5)
+    assert_parity(y[rows], _ref(wl, rows), BF16, what="fp8 base, decode workload")
+    layer.close()
+
+
+def test_fp8_limits():
+    from segmented_rank_gemm_gb300.lora import LoraError, LoraLayer
+    W = torch.zeros(72, 64, dtype=BF16, device="cuda")  # K = 72: not a multiple of 16
+    with pytest.raises(LoraError):
+        LoraLayer(W, 2, 8, 16, fp8_base=True)
+    W = torch.zeros(64, 64, dtype=BF16, device="cuda")
+    with pytest.raises(LoraError):
+        LoraLayer(W, 2, 8, 513, fp8_base=True)  # prefill batches: not served
