@@ -24,7 +24,8 @@ CHAIN = (("h", "q"), ("h", "k"), ("h", "v"), ("q", "o"), ("o", "g"), ("o", "u"),
 
 class LoraStack:
     def __init__(self, n_layers: int = 32, T: int = 512, S: int = 100, r: int = 16,
-                 seed: int = 1005, device="cuda"):
+                 seed: int = 1005, device="cuda", fp8_base: bool = False):
+        """``fp8_base``: every projection's base product in e4m3 (lora_layer_create_fp8)."""
         self.n_layers, self.T, self.S, self.device = n_layers, T, S, torch.device(device)
         self.h0, ids = workloads.stack_tokens(seed=seed, T=T, S=S, device=self.device)
         self.ids = ids.to(self.device)
@@ -34,7 +35,7 @@ class LoraStack:
             for p in range(len(workloads.STACK_PROJECTIONS)):
                 W, adapters = workloads.stack_projection(l, p, seed=seed, S=S, r=r,
                                                          device=self.device)
-                layer = LoraLayer(W, S, r, T)
+                layer = LoraLayer(W, S, r, T, fp8_base=fp8_base)
                 for s, (A, B, alpha) in enumerate(adapters):
                     layer.load(s, A, B, alpha)
                 torch.cuda.synchronize()
