@@ -21,20 +21,36 @@ __device__ __forceinline__ uint8_t to_e4m3(float v, float s) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(v, s), __NV_SATFINITE, __NV_E4M3));
 }
 
-// One CTA per row; K a multiple of 16.
+// One CTA per row; K a multiple of 16.  Each thread's 16-byte chunks of the row (at most
+// kQHold of them: K <= 8 * kQThreads * kQHold = 16384) are loaded once, together, held in
+// registers through the max reduction and converted from there: one round trip to memory.
+// Chunks past that (longer rows) are read again for the conversion.
+static constexpr int kQHold = 8;
 __global__ void __launch_bounds__(kQThreads)
     quant_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ x, int K, uint8_t* __restrict__ xq,
                            float* __restrict__ sx) {
   __shared__ float wmax[kQThreads / 32];
   const int row = blockIdx.x, tid = threadIdx.x;
+  const int nv = K / 8;  // 16-byte chunks of the row
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * K);
+  uint4 hold[kQHold];
+#pragma unroll
+  for (int i = 0; i < kQHold; ++i) {
+    const int e = tid + i * kQThreads;
+    hold[i] = e < nv ? __ldg(xr + e) : make_uint4(0u, 0u, 0u, 0u);
+  }
   float m = 0.f;
-  for (int e = tid; e < K / 8; e += kQThreads) {
+#pragma unroll
+  for (int i = 0; i < kQHold; ++i) {
+    const uint32_t w[4] = {hold[i].x, hold[i].y, hold[i].z, hold[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  }
+  for (int e = tid + kQHold * kQThreads; e < nv; e += kQThreads) {
     const uint4 v = __ldg(xr + e);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -46,8 +62,7 @@ __global__ void __launch_bounds__(kQThreads)
   const float s = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f;
   if (tid == 0) sx[row] = s;
   uint2* qr = reinterpret_cast<uint2*>(xq + (size_t)row * K);
-  for (int e = tid; e < K / 8; e += kQThreads) {
-    const uint4 v = __ldg(xr + e);
+  auto convert = [&](const uint4& v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t q[2] = {0u, 0u};
 #pragma unroll
@@ -55,8 +70,14 @@ __global__ void __launch_bounds__(kQThreads)
       const uint32_t lo = to_e4m3(bf16_lo(w[i]), s), hi = to_e4m3(bf16_hi(w[i]), s);
       q[i >> 1] |= (lo | (hi << 8)) << (16 * (i & 1));
     }
-    qr[e] = make_uint2(q[0], q[1]);
+    return make_uint2(q[0], q[1]);
+  };
+#pragma unroll
+  for (int i = 0; i < kQHold; ++i) {
+    const int e = tid + i * kQThreads;
+    if (e < nv) qr[e] = convert(hold[i]);
   }
+  for (int e = tid + kQHold * kQThreads; e < nv; e += kQThreads) qr[e] = convert(__ldg(xr + e));
 }
 
 cudaError_t launch_quant_rows_e4m3(const void* x, int T, int K, uint8_t* xq, float* sx,
