@@ -331,6 +331,19 @@ int make_resident(Cache* c, const std::vector<long long>& ids, bool batch) {
   return LORA_OK;
 }
 
+// dst[j][k] = src[k][j] for j < r, k < K, in blocks of 64 k so that the r source rows of a
+// block stay in the cache while its r destination rows are written.
+template <typename E>
+void transpose_rows(E* dst, const E* src, size_t K, int r) {
+  for (size_t k0 = 0; k0 < K; k0 += 64) {
+    const size_t k1 = std::min(K, k0 + 64);
+    for (int j = 0; j < r; ++j) {
+      E* d = dst + (size_t)j * K;
+      for (size_t k = k0; k < k1; ++k) d[k] = src[k * r + j];
+    }
+  }
+}
+
 // Pack adapter (A_l [K,r], B_l [r,N] per layer) into the host block: At [R][K] with rows
 // >= r zero, B [R][N] with rows >= r zero, at the layer's offsets.
 void pack_image(const Cache* c, char* blk, int r, const void* const* A_host,
@@ -340,14 +353,12 @@ void pack_image(const Cache* c, char* blk, int r, const void* const* A_host,
     const size_t es = L->esize, K = L->K, N = L->N, R = L->R;
     char* at = blk + c->desc[l].off_a;
     const char* A = static_cast<const char*>(A_host[l]);
-    for (size_t j = 0; j < R; ++j) {
-      char* row = at + j * K * es;
-      if ((int)j >= r) {
-        memset(row, 0, K * es);
-        continue;
-      }
-      for (size_t k = 0; k < K; ++k) memcpy(row + k * es, A + (k * r + j) * es, es);
-    }
+    // At[j][k] = A[k][j]: typed element copies (a memcpy call per element would dominate)
+    if (es == 2)
+      transpose_rows(reinterpret_cast<uint16_t*>(at), reinterpret_cast<const uint16_t*>(A), K, r);
+    else
+      transpose_rows(reinterpret_cast<uint32_t*>(at), reinterpret_cast<const uint32_t*>(A), K, r);
+    memset(at + (size_t)r * K * es, 0, (R - r) * K * es);
     char* b = blk + c->desc[l].off_b;
     memcpy(b, B_host[l], (size_t)r * N * es);
     memset(b + (size_t)r * N * es, 0, (R - r) * N * es);
