@@ -260,8 +260,7 @@ def run_stack(args):
         for _ in range(max(args.warmup, 3)):
             g.replay()
     stream.synchronize()
-    sampler = ClockSampler(os.path.join(ROOT, "gpurun_out", "clocks_bench_stack.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    sampler = ClockSampler(args.clocks_csv)
     sampler.start()
     t_soak = time.time()
     while time.time() - t_soak < args.soak_seconds:
@@ -410,8 +409,7 @@ def run_ours(args):
                     step(i + offset)
 
     # clocks: sample through a short soak and the timed region
-    sampler = ClockSampler(os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    sampler = ClockSampler(args.clocks_csv)
     sampler.start()
     t_soak = time.time()
     with torch.cuda.stream(stream):
@@ -760,6 +758,8 @@ def main(argv=None):
     ap.add_argument("--e2e-streams", type=int, default=4,
                     help="streams the end-to-end steps rotate over (instance j on stream j %% n)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="also write the nvidia-smi clock samples to this CSV file")
     ap.add_argument("--fp8", action="store_true",
                     help="decode workload with the base in e4m3 (lora_layer_create_fp8)")
     ap.add_argument("--swap-in", action="store_true",
