@@ -339,10 +339,16 @@ def run_ours(args):
     for i in range(args.layers):
         seed = cfg["seed"] + 7919 * i + 104729 * rank
         wl = make_workload(args.config, seed, "cpu" if i == 0 else dev)
-        layer = LoraLayer(wl.W.to(dev), wl.S, wl.R, wl.T, fp8_base=args.fp8)
+        pool_rows = 0
+        if args.pooled:  # adapters at their true rank (rounded up to 8) in a row pool
+            pool_rows = sum((int(ad[0].shape[1]) + 7) // 8 * 8 for ad in wl.adapters
+                            if ad is not None)
+        layer = LoraLayer(wl.W.to(dev), wl.S, wl.R, wl.T, fp8_base=args.fp8, pool_rows=pool_rows)
         for s, ad in enumerate(wl.adapters):
             if ad is not None:
                 layer.load(s, ad[0].to(dev), ad[1].to(dev), ad[2])
+        if i == 0:
+            pool_usage = layer.pool_usage()  # after the loads
         x = wl.x.to(dev)
         ids = wl.token_slot.to(dev)
         y = torch.empty(wl.T, wl.N, dtype=wl.dtype, device=dev)
@@ -547,6 +553,8 @@ def run_ours(args):
                    "graphs": ("one graph per rotation of %d steps (one per instance)" % len(layers))
                              if not args.no_graph else False},
         "roofline": roofline,
+        "slot_pool": {"pooled": bool(args.pooled), "rows_used": pool_usage[0],
+                      "rows": pool_usage[1], "padded_rows": wl0.S * ((wl0.R + 7) // 8 * 8)},
         "step_hbm": {"algorithmic_bytes": work["step_bytes"],
                      "achieved_gbs": work["step_bytes"] / (ms_per_step * 1e-3) / 1e9,
                      "frac_of_measured": work["step_bytes"] / (ms_per_step * 1e-3) / 1e9 / pk["hbm_gbs"],
@@ -760,6 +768,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-csv", default=None,
                     help="also write the nvidia-smi clock samples to this CSV file")
+    ap.add_argument("--pooled", action="store_true",
+                    help="adapters at their true rank in a row pool (lora_layer_create_pooled)")
     ap.add_argument("--fp8", action="store_true",
                     help="decode workload with the base in e4m3 (lora_layer_create_fp8)")
     ap.add_argument("--swap-in", action="store_true",
