@@ -297,10 +297,10 @@ cudaError_t launch_segment_builder(const BuilderArgs& a, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   int n_walk = 1;
   const int smem = builder_smem_bytes(a.S, &n_walk);
-  static int limit = 0;
-  static bool carveout = false;
-  cudaError_t e = ensure_smem_limit(segment_builder_kernel, smem, &limit);
-  if (e == cudaSuccess) e = prefer_max_smem_carveout(segment_builder_kernel, &carveout);
+  static int limit[kAttrDevices] = {};
+  static bool carveout[kAttrDevices] = {};
+  cudaError_t e = ensure_smem_limit(segment_builder_kernel, smem, limit);
+  if (e == cudaSuccess) e = prefer_max_smem_carveout(segment_builder_kernel, carveout);
   if (e != cudaSuccess) return e;
   segment_builder_kernel<<<1, kBuilderThreads, smem, stream>>>(
       a.token_slot, a.T, a.S, a.loaded, n_walk, a.rows_per_tile, a.window_rows,

@@ -93,8 +93,8 @@ __global__ void __launch_bounds__(kSimtThreads)
 
 cudaError_t launch_gemm_simt_f32(const GemmArgs& a, cudaStream_t stream) {
   const size_t smem = (size_t)kSimtTile * (a.ex.R + 1) * sizeof(float);
-  static int limit = 0;
-  cudaError_t e = ensure_smem_limit(gemm_simt_f32_kernel, (int)smem, &limit);
+  static int limit[kAttrDevices] = {};
+  cudaError_t e = ensure_smem_limit(gemm_simt_f32_kernel, (int)smem, limit);
   if (e != cudaSuccess) return e;
   dim3 grid((a.M + kSimtTile - 1) / kSimtTile, (a.N + kSimtTile - 1) / kSimtTile);
   gemm_simt_f32_kernel<<<grid, kSimtThreads, smem, stream>>>(a);

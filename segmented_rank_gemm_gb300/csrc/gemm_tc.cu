@@ -810,16 +810,24 @@ cudaError_t encode_tmap_u8(CUtensorMap* map, const void* base, int rows, int K, 
 // variant, shared by every caller.
 template <int BN, bool PAIR, bool VMODE, bool FP8 = false>
 static cudaError_t raise_smem_limit(int bytes) {
-  static int limit = 0;
-  return ensure_smem_limit(gemm_tc_kernel<BN, PAIR, VMODE, FP8>, bytes, &limit);
+  static int limit[kAttrDevices] = {};
+  return ensure_smem_limit(gemm_tc_kernel<BN, PAIR, VMODE, FP8>, bytes, limit);
 }
 
 // CTAs of this GEMM that can be resident at once in clusters of `csize` CTAs (every variant
-// holds one CTA per SM; a cluster must fit in one GPC, whose sizes differ).  Queried once.
+// holds one CTA per SM; a cluster must fit in one GPC, whose sizes differ).  Queried once
+// per device.
 static int resident_ctas(int csize, int num_sms) {
-  static int cache[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+  static int cache_all[kAttrDevices][9] = {};
+  static int scratch[9] = {};
   if (csize < 1 || csize > 8) return 0;
-  if (cache[csize] == 0) {
+  const int dev = attr_device();
+  int* cache = dev >= 0 ? cache_all[dev] : scratch;
+  {
+    std::lock_guard<std::mutex> lock(attr_mutex());
+    if (cache[csize] != 0) return cache[csize];
+  }
+  {
     const int smem = 200 * 1024;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -832,18 +840,20 @@ static int resident_ctas(int csize, int num_sms) {
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int n = 0;
+    int n = 0, v = 0;
     if (raise_smem_limit<256, false, true>(smem) == cudaSuccess &&
         cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<256, false, true>, &cfg) ==
             cudaSuccess &&
         n > 0) {
-      cache[csize] = std::min(num_sms, n * csize);
+      v = std::min(num_sms, n * csize);
     } else {
       cudaGetLastError();
-      cache[csize] = csize == 1 ? num_sms : 8 * (num_sms / 8 / csize) * csize;
+      v = csize == 1 ? num_sms : 8 * (num_sms / 8 / csize) * csize;
     }
+    std::lock_guard<std::mutex> lock(attr_mutex());
+    cache[csize] = v;
+    return v;
   }
-  return cache[csize];
 }
 
 // Tile shape, K split and CTA pairs, by least estimated time (cycles).  Measured on this

@@ -5,31 +5,54 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace lora {
 
 constexpr int kTileRows = 16;     // rows per segment tile of the CUDA-core tile kernel
 constexpr int kTcTileRows = 128;  // rows per segment tile of the tensor-core shrink (MMA M)
 
+// Function attributes are set per device, so the caches below that remember which were
+// already set hold one entry per device ordinal (kAttrDevices of them) and are guarded by
+// one process-wide mutex (several host threads may launch at once).
+constexpr int kAttrDevices = 64;
+inline std::mutex& attr_mutex() {
+  static std::mutex m;
+  return m;
+}
+// The current device's ordinal, or -1 if it cannot be read or is beyond kAttrDevices (the
+// attribute is then set on every call: correct, only slower).
+inline int attr_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kAttrDevices) return -1;
+  return d;
+}
+
 // Kernels that run beside the base GEMM prefer the largest shared-memory carveout: an SM can
 // only take a GEMM CTA (~200 KB of shared memory) while it holds CTAs of other kernels if
-// its L1/shared split is already the one the GEMM needs.  Set once per kernel, outside
-// stream capture.
+// its L1/shared split is already the one the GEMM needs.  Set once per kernel and device,
+// outside stream capture.
 template <typename Kernel>
-inline cudaError_t prefer_max_smem_carveout(Kernel k, bool* done) {
-  if (*done) return cudaSuccess;
+inline cudaError_t prefer_max_smem_carveout(Kernel k, bool (&done)[kAttrDevices]) {
+  const int d = attr_device();
+  std::lock_guard<std::mutex> lock(attr_mutex());
+  if (d >= 0 && done[d]) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess) *done = true;
+  if (e == cudaSuccess && d >= 0) done[d] = true;
   return e;
 }
 
 // Raise a kernel's dynamic shared-memory limit only when a launch needs more than any
-// earlier launch in this process (so launches under stream capture set no attribute).
+// earlier launch on this device in this process (so launches under stream capture set no
+// attribute).
 template <typename Kernel>
-inline cudaError_t ensure_smem_limit(Kernel k, int bytes, int* cached) {
-  if (bytes <= *cached) return cudaSuccess;
+inline cudaError_t ensure_smem_limit(Kernel k, int bytes, int (&cached)[kAttrDevices]) {
+  const int d = attr_device();
+  std::lock_guard<std::mutex> lock(attr_mutex());
+  if (d >= 0 && bytes <= cached[d]) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) *cached = bytes;
+  if (e == cudaSuccess && d >= 0) cached[d] = bytes;
   return e;
 }
 

@@ -666,9 +666,9 @@ template <int RMAX, int ROWS, bool PERCOL, bool POOLED>
 static cudaError_t launch_bgmv_stream_t(const BgmvArgs& a, cudaStream_t stream) {
   // the SMs it runs on must keep the shared-memory split a GEMM CTA needs, or that CTA
   // waits for them to drain
-  static bool carveout = false;
+  static bool carveout[kAttrDevices] = {};
   cudaError_t e =
-      prefer_max_smem_carveout(bgmv_stream_kernel<RMAX, ROWS, PERCOL, POOLED>, &carveout);
+      prefer_max_smem_carveout(bgmv_stream_kernel<RMAX, ROWS, PERCOL, POOLED>, carveout);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -716,8 +716,8 @@ cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream) {
   const int cap = a.num_sms * 4 / cs;
   if (clusters > cap) clusters = cap;
   if (clusters < 1) clusters = 1;
-  static bool carveout = false;
-  cudaError_t e = prefer_max_smem_carveout(bgmv_delta_kernel, &carveout);
+  static bool carveout[kAttrDevices] = {};
+  cudaError_t e = prefer_max_smem_carveout(bgmv_delta_kernel, carveout);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -753,13 +753,13 @@ cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStrea
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  static bool carveout[3] = {false, false, false};
-  cudaError_t e = bf16 ? prefer_max_smem_carveout(lora_tile_kernel<__nv_bfloat16, Vec16<__nv_bfloat16>, false>, &carveout[0])
+  static bool carveout[3][kAttrDevices] = {};
+  cudaError_t e = bf16 ? prefer_max_smem_carveout(lora_tile_kernel<__nv_bfloat16, Vec16<__nv_bfloat16>, false>, carveout[0])
                        : cudaSuccess;
   if (e == cudaSuccess && !bf16)
-    e = prefer_max_smem_carveout(lora_tile_kernel<float, Vec16<float>, false>, &carveout[1]);
+    e = prefer_max_smem_carveout(lora_tile_kernel<float, Vec16<float>, false>, carveout[1]);
   if (e == cudaSuccess && !bf16)
-    e = prefer_max_smem_carveout(lora_tile_kernel<float, Scalar32, false>, &carveout[2]);
+    e = prefer_max_smem_carveout(lora_tile_kernel<float, Scalar32, false>, carveout[2]);
   if (e != cudaSuccess) return e;
   if (bf16) {
     using T = __nv_bfloat16;

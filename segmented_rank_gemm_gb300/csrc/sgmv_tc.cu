@@ -348,11 +348,11 @@ cudaError_t launch_sgmv_shrink_tc(const ShrinkTcArgs& a, const CUtensorMap& tmap
   int stages = 10;
   while (stages > 2 && fixed + (size_t)stages * stage_bytes > budget) --stages;
   const size_t smem = fixed + (size_t)stages * stage_bytes;
-  static int limit = 0;
-  static bool carveout = false;
-  cudaError_t e = ensure_smem_limit(sgmv_shrink_tc_kernel, (int)smem, &limit);
+  static int limit[kAttrDevices] = {};
+  static bool carveout[kAttrDevices] = {};
+  cudaError_t e = ensure_smem_limit(sgmv_shrink_tc_kernel, (int)smem, limit);
   if (e != cudaSuccess) return e;
-  e = prefer_max_smem_carveout(sgmv_shrink_tc_kernel, &carveout);
+  e = prefer_max_smem_carveout(sgmv_shrink_tc_kernel, carveout);
   if (e != cudaSuccess) return e;
   const int units = (a.T + kTcTileRows - 1) / kTcTileRows;  // at least (one per window)
   const int grid = std::max(1, std::min(units * ks, a.num_sms));

@@ -265,7 +265,24 @@ def lora_set_gemm_plan(layer, block_n: int, k_split: int = 1, cta_pair: int = 0)
 def lora_build_segments_static(token_slot, T, num_slots, slot_loaded, perm, seg_offsets,
                                seg_slot, counts, stream=None) -> None:
     """Segment builder without any device allocation (scratch in a static device array);
-    all tensors are caller-owned CUDA int32 tensors, ``slot_loaded`` may be None."""
+    all tensors are caller-owned CUDA int32 tensors, ``slot_loaded`` may be None.
+
+    The C entry point cannot see buffer sizes, so an undersized tensor here would become
+    an out-of-bounds device write: each tensor is checked first (int32, on a CUDA device,
+    contiguous, at least perm >= T, seg_offsets >= num_slots + 1, seg_slot >= num_slots,
+    counts >= 3, token_slot >= T, slot_loaded >= num_slots) and LORA_EINVAL is raised
+    otherwise."""
+    T, num_slots = int(T), int(num_slots)
+    need = {"token_slot": (token_slot, T), "perm": (perm, T),
+            "seg_offsets": (seg_offsets, num_slots + 1), "seg_slot": (seg_slot, num_slots),
+            "counts": (counts, 3)}
+    if slot_loaded is not None:
+        need["slot_loaded"] = (slot_loaded, num_slots)
+    for name, (t, n) in need.items():
+        if (not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or not t.is_cuda
+                or not t.is_contiguous() or t.numel() < max(n, 0)):
+            raise LoraError(LORA_EINVAL, "lora_build_segments_static: %s must be a contiguous "
+                            "CUDA int32 tensor of at least %d elements" % (name, n))
     rc = _lib.lora_build_segments_static(_ptr(token_slot), T, num_slots, _ptr(slot_loaded),
                                          _ptr(perm), _ptr(seg_offsets), _ptr(seg_slot),
                                          _ptr(counts), _stream(stream))

@@ -3,10 +3,9 @@
 
 Parity is taken per projection, at the stack's full sizes, against the oracle: every
 projection gets an input of its own from the seeded generator (the oracle never receives
-an output of the CUDA path), and sampled rows are compared element by element.  The
+an output of the CUDA path), and all 512 rows are compared element by element.  The
 chained pass itself is checked for what holds at any size: the graph-captured chain gives
 bit for bit the same result as the same calls issued one by one, and it stays finite."""
-import numpy as np
 import pytest
 import torch
 
@@ -31,10 +30,9 @@ def test_stack_projection_parity(layer_idx, proj):
     y = layer(x, ids.to(dev))
     torch.cuda.synchronize()
     assert layer.status() == 0
-    rows = np.random.default_rng(100 * layer_idx + proj).choice(x.shape[0], 24, replace=False)
     table = oracle.SlotTable([(A.cpu(), B.cpu(), a) for A, B, a in adapters], W.shape[0], W.shape[1])
-    ref = oracle.forward_rows(x.cpu(), W.cpu(), table, ids.cpu(), rows=rows)
-    assert_parity(y[torch.from_numpy(rows).to(dev)], ref, torch.bfloat16,
+    ref = oracle.forward_rows(x.cpu(), W.cpu(), table, ids.cpu())
+    assert_parity(y, ref, torch.bfloat16,
                   what="layer %d %s" % (layer_idx, workloads.STACK_PROJECTIONS[proj][0]))
     layer.close()
 
