@@ -1,17 +1,20 @@
 #!/usr/bin/env python
 """Throughput of the mixed-adapter LoRA linear layer on GB300.
 
-One step = one pass of the whole hot path over one batch: the device segment builder
-(set_batch_segments) and the layer forward (shrink + tensor-core base GEMM with the
-fused expand), through the library's C ABI.  The default workload is the decode BGMV
-batch: T=256 tokens (one per request), K=N=4096, rank 16, 128 resident adapter slots,
-each token's slot uniform with 10% base-only rows, bf16 with fp32 accumulation.
+The default workload is the largest single-GPU one: the 8B-class LoRA stack (32 layers x 7
+projections -- q/o 4096->4096, k/v 4096->1024, gate/up 4096->14336, down 14336->4096 --
+rank 16 on all 7, 100 resident adapter slots, 512 decode tokens with uniform slot ids,
+layer outputs chained).  One step = one chained pass: every projection is one
+set_batch_segments + lora_forward of the library's C ABI (BGMV shrink + expand, then the
+tcgen05 base GEMM that adds the low-rank term in its epilogue), the whole pass replayed
+from one CUDA graph.  Each pass streams ~22 GB of weights and slots, far beyond L2.
+
+--config selects a single-layer workload instead (decode BGMV, prefill SGMV, continuous
+batch): one step = set_batch_segments + lora_forward on one batch, rotating over
+independent layer instances so that consecutive steps never find their data in L2.
 
 Timing: warm-up steps, then exactly --steps steps bracketed by a barrier and a device
-synchronize, CUDA events on the launching stream, max over ranks.  Each step uses the
-next of L independent layer instances (weights, slot table, inputs), so consecutive
-steps never find their data in L2 (L x ~66 MB >> 129 MB).  Steps are replayed from
-CUDA graphs captured once per instance.
+synchronize, CUDA events on the launching stream, max over ranks.
 
 Prints one JSON line.  --impl reference times the CPU oracle instead (rank 0 only).
 """
@@ -241,9 +244,67 @@ def traffic_from_profile(kernel_src: str, config: str):
     return entry.get("dram_bytes_per_launch")
 
 
+def _stack_flops_bytes(T, n_layers, S, fp8=False):
+    """Algorithmic work of one chained pass: every projection's base FLOPs 2 T K N; bytes
+    W once (e4m3: one byte an element), each distinct adapter slice once (rank 16), the
+    projection's input and output once."""
+    from segmented_rank_gemm_gb300.workloads import STACK_PROJECTIONS
+    flops = sum(2 * T * k * n for _, k, n in STACK_PROJECTIONS) * n_layers
+    base_bytes = sum(k * n * (1 if fp8 else 2) for _, k, n in STACK_PROJECTIONS) * n_layers
+    ad_bytes = sum(16 * (k + n) * 2 for _, k, n in STACK_PROJECTIONS) * n_layers * S
+    act_bytes = sum(T * (k + n) * 2 for _, k, n in STACK_PROJECTIONS) * n_layers
+    return flops, base_bytes, ad_bytes, act_bytes
+
+
+def _stack_oracle_layer(seed, S, T):
+    """Layer 0 of the stack drawn on the host (same recipe and seed; the host generator's
+    values), as fp64 arrays for the oracle: per projection (x [T,K], W [K,N], slot table),
+    with x the projection's generator input; and the slot ids."""
+    import oracle
+    from segmented_rank_gemm_gb300 import workloads
+    _, ids = workloads.stack_tokens(seed=seed, T=T, S=S, device="cpu")
+    projs = []
+    for p in range(len(workloads.STACK_PROJECTIONS)):
+        W, adapters = workloads.stack_projection(0, p, seed=seed, S=S, device="cpu")
+        x = workloads.stack_input(p, T=T, seed=seed, device="cpu")
+        table = oracle.SlotTable(adapters, W.shape[0], W.shape[1])
+        projs.append((x.double().numpy(), W.double().numpy(), table))
+        del W, adapters
+    return oracle, projs, ids.numpy().astype(np.int32)
+
+
+def _stack_oracle_rows(oracle, projs, ids, rows):
+    """The oracle on `rows` through the 7 projections of one layer (seconds)."""
+    t0 = time.time()
+    for x, W, table in projs:
+        oracle.forward_rows(x, W, table, ids, rows=rows)
+    return time.time() - t0
+
+
+def stack_cpu_baseline(seed, S, T, n_layers, seconds):
+    """The oracle (plain C fp64, OpenMP over rows) on this host's cores, on a bounded
+    sample of the stack: one thread's worth of rows per round through the 7 projections of
+    layer 0, repeated for ``seconds``; tokens/s for the whole stack is rows / (n_layers x
+    the time per layer)."""
+    oracle, projs, ids = _stack_oracle_layer(seed, S, T)
+    threads = oracle.num_threads()
+    rng = np.random.default_rng(11)
+    rows_done, t = 0, 0.0
+    while t < seconds:
+        rows = np.sort(rng.choice(T, size=min(threads, T), replace=False)).astype(np.int64)
+        t += _stack_oracle_rows(oracle, projs, ids, rows)
+        rows_done += rows.shape[0]
+    return {"value": rows_done / (t * n_layers), "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": "%d rows (%d per round, seeded) through the 7 projections of layer 0 in "
+                      "%.1f s, scaled to the %d-layer stack (per-row work is the same in every "
+                      "layer)" % (rows_done, min(threads, T), t, n_layers)}
+
+
 def run_stack(args):
     """The 8B-class stack: one step = one chained pass over its 224 projections (captured
     in one CUDA graph); every pass streams ~22 GB of weights and slots, far beyond L2."""
+    from segmented_rank_gemm_gb300.lora import lora_set_trace_events, LORA_OK
     from segmented_rank_gemm_gb300.stack import LoraStack
     from segmented_rank_gemm_gb300.workloads import STACK_PROJECTIONS
 
@@ -252,14 +313,16 @@ def run_stack(args):
         torch.distributed.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    t_setup = time.time()
     st = LoraStack(seed=CONFIGS["stack_8b"]["seed"] + 104729 * rank, device=dev,
-                   fp8_base=args.fp8)
+                   fp8_base=args.fp8, n_layers=args.stack_layers)
     stream = torch.cuda.Stream(device=dev)
     g = st.capture(stream)
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
             g.replay()
     stream.synchronize()
+    setup_s = time.time() - t_setup
     sampler = ClockSampler(args.clocks_csv)
     sampler.start()
     t_soak = time.time()
@@ -269,6 +332,7 @@ def run_stack(args):
         stream.synchronize()
     barrier(world)
     torch.cuda.synchronize()
+    t_wall0 = time.time()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
@@ -277,21 +341,91 @@ def run_stack(args):
         ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    sampler.stop()
-    clocks = sampler.summary(t_soak, time.time())
+    t_wall1 = time.time()
     seconds = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
     T = st.T
-    flops = sum(2 * T * k * n for _, k, n in STACK_PROJECTIONS) * st.n_layers
-    base_bytes = sum(k * n * (1 if args.fp8 else 2) for _, k, n in STACK_PROJECTIONS) * st.n_layers
-    ad_bytes = sum(16 * (k + n) * 2 for _, k, n in STACK_PROJECTIONS) * st.n_layers * st.S
     step_s = seconds / args.steps
+
+    # ---- per-kernel durations: one eager pass on one stream with the trace events of
+    # every projection (each GEMM then runs alone; the pass itself is not the timed one) ----
+    n_proj = len(STACK_PROJECTIONS)
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_proj)]
+           for _ in st.layers]
+    for l, row in enumerate(st.layers):
+        for p, layer in enumerate(row):
+            lora_set_trace_events(layer.handle, evs[l][p])
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(4e6))  # keeps the GPU behind the host while it enqueues
+        st.step(stream, concurrent=False)
+    torch.cuda.synchronize()
+    for row in st.layers:
+        for layer in row:
+            lora_set_trace_events(layer.handle, None)
+    gemm_us = [[evs[l][p][4].elapsed_time(evs[l][p][5]) * 1e3 for p in range(n_proj)]
+               for l in range(len(st.layers))]
+    bgmv_us = [[evs[l][p][2].elapsed_time(evs[l][p][3]) * 1e3 for p in range(n_proj)]
+               for l in range(len(st.layers))]
+    t_clock_end = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_soak, t_clock_end)
+
+    # ---- end to end: h0 and the ids from pinned host memory, the chained pass through the
+    # C ABI (the captured graph of its 448 calls), h back to pinned host memory ----
+    e2e = None
+    if not args.no_e2e:
+        h0_h = st.h0.cpu().pin_memory()
+        ids_h = st.ids.cpu().pin_memory()
+        out_h = torch.empty(T, st.buf["h"].shape[1], dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                st.h0.copy_(h0_h, non_blocking=True)
+                st.ids.copy_(ids_h, non_blocking=True)
+                g.replay()
+                out_h.copy_(st.buf["h"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e_sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+        e2e = {"value": aggregate(T, args.steps, world, e_sec), "unit": UNIT,
+               "h2d_bytes_per_step": h0_h.numel() * 2 + ids_h.numel() * 4,
+               "d2h_bytes_per_step": out_h.numel() * 2,
+               "ms_per_step": e_sec * 1e3 / args.steps,
+               "path": "pinned h0 and ids H2D, the chained pass (224 x set_batch_segments + "
+                       "lora_forward, one CUDA graph), h D2H"}
+    for row in st.layers:
+        for layer in row:
+            assert layer.status(stream) == LORA_OK
+
+    flops, base_bytes, ad_bytes, act_bytes = _stack_flops_bytes(T, st.n_layers, st.S, args.fp8)
     pk = peaks()
-    tf = flops / step_s / 1e12
+    tf_step = flops / step_s / 1e12
     peak = pk["bf16_tflops_sustained"] or pk["bf16_tflops"]
-    peak_note = pk["source"] + " sustained"
+    peak_note = pk["source"] + " sustained bf16"
     if args.fp8:  # e4m3 contractions: the measured bf16 peak x the nominal ratio 4.5 / 2.25
         peak *= 2.0
-        peak_note += " bf16 x 2 (nominal e4m3 / bf16 ratio)"
+        peak_note += " x 2 (nominal e4m3 / bf16 ratio)"
+    gemm_total_s = sum(sum(r) for r in gemm_us) * 1e-6
+    n_gemm = len(st.layers) * n_proj
+    gemm_tf = flops / gemm_total_s / 1e12
+    per_shape = {}
+    for p, (name, k, n) in enumerate(STACK_PROJECTIONS):
+        us = statistics.mean(gemm_us[l][p] for l in range(len(st.layers)))
+        per_shape[name] = {"K": k, "N": n, "gemm_us": us,
+                           "gemm_tflops": 2 * T * k * n / (us * 1e-6) / 1e12,
+                           "bgmv_us": statistics.mean(bgmv_us[l][p] for l in range(len(st.layers)))}
+    kernel_src = os.path.join(ROOT, "segmented_rank_gemm_gb300", "csrc", "gemm_tc.cu")
     out = {
         "metric": METRIC, "value": aggregate(T, args.steps, world, seconds), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -301,22 +435,38 @@ def run_stack(args):
         "config": {"workload": CONFIGS["stack_8b"]["desc"] + (", base in e4m3 (x per row, W "
                                                              "per column)" if args.fp8 else ""),
                    "T": T, "layers": st.n_layers,
-                   "projections": 7 * st.n_layers, "slots": st.S, "graphs": True,
+                   "projections": n_proj * st.n_layers, "slots": st.S,
+                   "graphs": "one graph per chained pass",
                    "parallelism": "replicas x%d" % world,
-                   "l2": "each pass streams %.1f GB" % ((base_bytes + ad_bytes) / 1e9)},
-        "roofline": {"kernel": "whole chained pass (224 x builder + BGMV + tcgen05 GEMM)",
-                     "bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tf / peak, "traffic": None, "peak_source": peak_note,
-                     "algorithmic_flops_per_step": flops},
-        "step_hbm": {"algorithmic_bytes": base_bytes + ad_bytes,
-                     "achieved_gbs": (base_bytes + ad_bytes) / step_s / 1e9},
+                   "l2": "inputs larger than L2: each pass streams %.1f GB of weights and "
+                         "slots" % ((base_bytes + ad_bytes) / 1e9)},
+        "roofline": {"kernel": "gemm_tc_kernel (base GEMM + fused delta add), all %d launches "
+                               "of a pass" % n_gemm,
+                     "bound": "tensor", "achieved": gemm_tf, "peak": peak, "unit": "TFLOP/s",
+                     "frac": gemm_tf / peak,
+                     "traffic": None if args.fp8 else traffic_from_profile(kernel_src, "stack_8b"),
+                     "peak_source": peak_note,
+                     "frac_of_burst_peak": gemm_tf / (pk["bf16_tflops"] * (2 if args.fp8 else 1)),
+                     "algorithmic_flops_per_launch": flops / n_gemm,
+                     "avg_launch_us": gemm_total_s * 1e6 / n_gemm},
+        "step_tensor": {"achieved_tflops": tf_step, "frac_of_peak": tf_step / peak,
+                        "algorithmic_flops": flops},
+        "step_hbm": {"algorithmic_bytes": base_bytes + ad_bytes + act_bytes,
+                     "achieved_gbs": (base_bytes + ad_bytes + act_bytes) / step_s / 1e9},
+        "per_projection": per_shape,
         # per projection: BGMV + GEMM (decode batch: no segment builder)
-        "gpu_launches": 2 * 7 * st.n_layers * args.steps,
+        "gpu_launches": 2 * n_proj * st.n_layers * args.steps,
         "clocks": clocks,
+        "e2e": e2e,
+        "setup_s": setup_s,
+        "wall_s_timed": t_wall1 - t_wall0,
     }
+    st.close()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = stack_cpu_baseline(CONFIGS["stack_8b"]["seed"], st.S, T,
+                                                 st.n_layers, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(out))
-    st.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -610,10 +760,47 @@ def cpu_baseline(wl, seconds: float):
             % (reps, wl.T, dt)}
 
 
+def run_reference_stack(args):
+    """The oracle on the stack's workload: each step a seeded sample of rows (one per host
+    thread) through the 7 projections of layer 0; tokens/s for the whole stack is rows /
+    (layers x the time per layer)."""
+    seed, S, T, n_layers = CONFIGS["stack_8b"]["seed"], 100, 512, args.stack_layers
+    oracle, projs, ids = _stack_oracle_layer(seed, S, T)
+    threads = oracle.num_threads()
+    n_rows = min(threads, T)
+    rng = np.random.default_rng(0)
+    samples = [np.sort(rng.choice(T, size=n_rows, replace=False)).astype(np.int64)
+               for _ in range(args.steps + args.warmup)]
+    for i in range(args.warmup):
+        _stack_oracle_rows(oracle, projs, ids, samples[i])
+    t = 0.0
+    for i in range(args.steps):
+        t += _stack_oracle_rows(oracle, projs, ids, samples[args.warmup + i])
+    step_s = t * n_layers / args.steps  # one step: the sampled rows through the whole stack
+    value = n_rows / (step_s)
+    sample = ("%d of %d rows per step (seeded) through the 7 projections of layer 0, scaled "
+              "to %d layers, %d steps" % (n_rows, T, n_layers, args.steps))
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": CONFIGS["stack_8b"]["desc"], "T": T, "layers": n_layers,
+                   "projections": 7 * n_layers, "slots": S,
+                   "parallelism": "host cores, rank 0"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return  # the oracle runs on rank 0's host cores only
+    if args.config == "stack_8b":
+        return run_reference_stack(args)
     cfg = CONFIGS[args.config]
     wl = make_workload(args.config, cfg["seed"], "cpu")
     oracle, table, x, W, ids = _oracle_inputs(wl)
@@ -754,10 +941,13 @@ def run_swap_in(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 40 for the stack, 400 for the single layers)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=sorted(CONFIGS), default="decode_bgmv")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default="stack_8b")
+    ap.add_argument("--stack-layers", type=int, default=32,
+                    help="layers of the 8B-class stack (32 is the workload; fewer for profiling)")
     ap.add_argument("--layers", type=int, default=8, help="independent instances rotated")
     ap.add_argument("--soak-seconds", type=float, default=1.5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -775,6 +965,8 @@ def main(argv=None):
     ap.add_argument("--swap-in", action="store_true",
                     help="measure adapter swap-ins through the adapter cache instead")
     args = ap.parse_args(argv)
+    if args.steps is None:
+        args.steps = 40 if args.config == "stack_8b" else 400
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3  # at least 3 warm-up steps
     if args.swap_in:

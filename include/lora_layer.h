@@ -57,7 +57,9 @@ enum lora_status {
     LORA_ESTATE = -7,   /* call out of order: lora_forward without matching set_batch_segments */
     LORA_ETIMEOUT = -8, /* (device) a pipeline wait inside a kernel gave up; results invalid */
     LORA_ENOENT = -9,   /* (adapter cache) adapter id not held in the host tier */
-    LORA_ECAPACITY = -10 /* (adapter cache) more distinct adapters than GPU slots */
+    LORA_ECAPACITY = -10, /* (adapter cache) more distinct adapters than GPU slots */
+    LORA_EBOUNDS = -11  /* (device, debug flavour only) a kernel index fell outside its
+                           buffer; the access was skipped and the results are invalid */
 };
 
 /*

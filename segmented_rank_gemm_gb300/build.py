@@ -3,6 +3,13 @@
 Each ``csrc/*.cu`` file is compiled by nvcc for sm_103a only (in parallel), then linked
 into one shared library with the C ABI of ``include/lora_layer.h``.  Run as
 ``python -m segmented_rank_gemm_gb300.build`` or through ``__graft_entry__.build()``.
+
+``build(debug=True)`` (``--debug``) builds the debug flavour, ``liblora_layer_debug.so``,
+compiled with ``-DLORA_DEBUG``: the kernels check the indices they take from data (slot rows
+of the adapter pools, rows of the delta and v buffers, K-split planes) and, instead of
+accessing memory outside a buffer, skip the access and raise a device flag that
+``lora_get_status`` reports as LORA_EBOUNDS.  The binding loads it when the environment
+variable ``LORA_LAYER_LIBRARY`` is ``debug``.
 """
 from __future__ import annotations
 
@@ -18,6 +25,16 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "liblora_layer.so")
+DEBUG_BUILD_DIR = os.path.join(PKG, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(PKG, "liblora_layer_debug.so")
+
+
+def library_path() -> str:
+    """The flavour the binding loads: the debug one if LORA_LAYER_LIBRARY=debug."""
+    flavour = os.environ.get("LORA_LAYER_LIBRARY", "")
+    if flavour not in ("", "release", "debug"):
+        raise ValueError("LORA_LAYER_LIBRARY must be 'release' or 'debug', not %r" % flavour)
+    return DEBUG_LIB_PATH if flavour == "debug" else LIB_PATH
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -41,22 +58,26 @@ def _deps():
                                       os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    if debug:
+        extra_flags = ("-DLORA_DEBUG", *extra_flags)
+    if not force and up_to_date(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nv = nvcc()
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nv, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,14 +88,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB_PATH + ".%d.tmp" % os.getpid()
+    tmp = lib_path + ".%d.tmp" % os.getpid()
     cmd = [nv, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-lrt", "-lpthread", "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

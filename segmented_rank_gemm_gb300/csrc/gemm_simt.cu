@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(kSimtThreads)
   for (int e = tid; e < kSimtTile * R; e += kSimtThreads) {
     const int m = e / R, j = e % R;
     const int s = rs[m];
-    if (s >= 0 && j < ex.rank[s]) vs[m * (R + 1) + j] = ex.v[(size_t)(m0 + m) * R + j];
+    if (s >= 0 && j < ex.rank[s] && LORA_IN_BOUNDS(m0 + m < ex.v_rows, a.err))
+      vs[m * (R + 1) + j] = ex.v[(size_t)(m0 + m) * R + j];
   }
   __syncthreads();
 
@@ -82,7 +83,8 @@ __global__ void __launch_bounds__(kSimtThreads)
       const int gn = n0 + tx + 16 * j;
       if (gn >= a.N) continue;
       float out = acc[i][j];
-      if (s >= 0) {
+      if (s >= 0 && LORA_IN_BOUNDS(ex.row_base[s] >= 0 && ex.row_base[s] + r <= ex.pool_rows,
+                                   a.err)) {
         const float* bcol = Bp + (size_t)ex.row_base[s] * a.N + gn;
         for (int jj = 0; jj < r; ++jj) out = fmaf(vs[m * (R + 1) + jj], bcol[(size_t)jj * a.N], out);
       }

@@ -322,7 +322,9 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
           const int uu = e / xl.nbs, b = e - uu * xl.nbs;
           const int col = xl.nbs == 1 ? 0 : (b % (xl.rx / 64)) * 64;
           uint8_t* sa = stage_base + (size_t)s * kStageBytes;
-          const int brow = uslot[uu] * a.N + n0 + pr * kBRows;
+          // (a slot outside the table: the rows of slot 0 are loaded instead, and flagged)
+          const int us = LORA_IN_BOUNDS(uslot[uu] >= 0 && uslot[uu] < a.ex.S, a.err) ? uslot[uu] : 0;
+          const int brow = us * a.N + n0 + pr * kBRows;
           if (PAIR) {
             if (pr == 0) mbar_arrive_expect_tx(&full[s], 2 * kBBytes);
             tma_load_2d_pair(sa + kABytes, &tmap_bx, dsmem_map(smem_u32(&full[s]), lead_rank),
@@ -513,7 +515,7 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
         // moves chunk p to chunk p and neither side has bank conflicts
         uint8_t* mine = xscr + (size_t)et * xl.nbs * 128;
         const int sw = et & 7;
-        if (srow >= 0) {
+        if (srow >= 0 && LORA_IN_BOUNDS(m0 + et < a.ex.v_rows, a.err)) {
           for (int j0 = 0; j0 < xl.rx; j0 += 8) {
             uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
             if (j0 < a.ex.R) v_hi_lo8(a.ex, m0 + et, j0, hi, lo);
@@ -665,13 +667,15 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
             else if (t >= 0 && !add_delta) atomicOr(a.err, LORA_ERRF_EMPTY_SLOT);
           }
         }
+        if (add_delta && !LORA_IN_BOUNDS(row < a.ex.delta_rows, a.err)) add_delta = false;
         // the tile's delta rows (the buffer holds the batch's rows, at most 512):
         // consecutive threads fetch consecutive 16-byte chunks of a row
         const int cfirst = n0 + z * bnc;  // first column this CTA finishes
+        const int dr_end = min(a.M, a.ex.delta_rows);
         for (int idx = et; idx < kBM * nq; idx += 128) {
           const int r = idx / nq, ch = idx - r * nq;
           const int gr = m0 + r, gc = cfirst + ch * 4;
-          if (gr < a.M && gc < a.N)
+          if (gr < dr_end && gc < a.N)
             cp_async_16(dsm + (size_t)r * bnc + ((ch ^ (r & 7)) << 2),
                         a.ex.delta + (size_t)gr * a.N + gc);
         }

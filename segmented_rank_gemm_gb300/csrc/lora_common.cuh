@@ -14,12 +14,28 @@
 #define LORA_ERRF_BAD_ID 1       // a token id outside [-1, num_slots)
 #define LORA_ERRF_EMPTY_SLOT 2   // a token naming a slot that holds no adapter
 #define LORA_ERRF_TIMEOUT 4      // a pipeline wait gave up
+#define LORA_ERRF_BOUNDS 8       // (LORA_DEBUG builds) an index outside its buffer, access skipped
+
+// Device bounds checks of the debug flavour (compiled with -DLORA_DEBUG): LORA_IN_BOUNDS(c, err)
+// is c, and when c is false it also raises LORA_ERRF_BOUNDS on the layer's flag word, so the
+// caller skips the access instead of faulting.  In the release build it is `true` and the
+// check costs nothing.  The checks cover the indices that come from data the kernels read
+// (slot rows of the adapter pools, rows of the delta and v buffers, K-split planes).
+#ifdef LORA_DEBUG
+#define LORA_IN_BOUNDS(cond, err) ((cond) ? true : (::lora::raise_bounds(err), false))
+#else
+#define LORA_IN_BOUNDS(cond, err) true
+#endif
 
 #ifndef LORA_WAIT_TIMEOUT_NS
 #define LORA_WAIT_TIMEOUT_NS 2000000000ull  // 2 s: far beyond any legitimate wait
 #endif
 
 namespace lora {
+
+__device__ __forceinline__ void raise_bounds(int32_t* err) {
+  if (err) atomicOr(err, LORA_ERRF_BOUNDS);
+}
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

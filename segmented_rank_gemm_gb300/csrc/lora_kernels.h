@@ -89,7 +89,10 @@ struct TileArgs {
   const float* scale;   // [S][R]: the scale of each rank column of a slot
   const int32_t* rank;  // [S]
   const int32_t* perm, *seg_offsets, *seg_slot, *tile_seg, *tile_row0, *meta;
-  float* out;           // v [T_max][R] (v mode) or delta [T_max][N] (delta mode), fp32
+  float* out;           // v [out_rows][R] fp32
+  int out_rows;         // rows of out (T_max)
+  int pool_rows;        // P: rows of the A and B pools
+  int32_t* err;         // the layer's device flags (debug-flavour bounds checks)
   int max_tiles;        // upper bound of the builder's tile count (grid sizing)
   int num_sms;
 };
@@ -108,6 +111,8 @@ struct ShrinkTcArgs {
   float* v;            // [max_planes][T_max][R] fp32 partial sums over K ranges, scaled
   size_t plane_stride; // floats between planes (T_max * R)
   int ks;              // K split (planes written), from sgmv_shrink_tc_split
+  int pool_rows;       // P: rows of the A pool (debug-flavour bounds checks)
+  int v_rows;          // rows of a plane of v (T_max)
   int32_t* err;
   int num_sms;
 };
@@ -134,7 +139,9 @@ struct BgmvArgs {
   bool pooled;          // slots placed by the row allocator (else slot s at row s * R)
   const float* scale;   // [S][R]: the scale of each rank column of a slot
   const int32_t* rank;  // [S]
-  float* delta;         // [T_max][N] fp32
+  float* delta;         // [delta_rows][N] fp32
+  int delta_rows;       // rows of the delta buffer
+  int32_t* err;         // the layer's device flags (debug-flavour bounds checks)
   int num_sms;
   bool per_column;      // some slot's columns carry different scales (a composition)
 };
@@ -179,7 +186,10 @@ struct ExpandArgs {
   const float* v;           // [planes][T_max][R] fp32, scaled by alpha / r   (v mode):
   int v_planes;             //   v of a row = the sum of its planes, in plane order
   size_t v_plane_stride;    //   floats between planes
-  const float* delta;       // [T_max][N] fp32                                (delta mode)
+  const float* delta;       // [delta_rows][N] fp32                          (delta mode)
+  int delta_rows;           // rows of the delta buffer
+  int v_rows;               // rows of a plane of v (T_max)
+  int pool_rows;            // P: rows of the B pool
   int R;
   const void* B_pool;   // [P][N] rank rows
   const int32_t* row_base;  // [S] first pool row of each slot

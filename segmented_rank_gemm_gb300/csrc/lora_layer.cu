@@ -570,6 +570,8 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     ba.scale = L->scale;
     ba.rank = L->rank;
     ba.delta = L->delta;
+    ba.delta_rows = std::min(L->T_max, kDeltaMaxT);
+    ba.err = L->err;
     ba.num_sms = L->num_sms;
     ba.per_column = L->percol_slots > 0;
     // e4m3 base: x quantised first (a plain launch after the previous forward); the BGMV
@@ -595,6 +597,8 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     sa.v = L->v;
     sa.plane_stride = (size_t)L->T_max * L->R;
     sa.ks = v_split;
+    sa.pool_rows = L->P;
+    sa.v_rows = L->T_max;
     sa.err = L->err;
     sa.num_sms = L->num_sms;
     LORA_CUDA(L, launch_sgmv_shrink_tc(sa, L->tmap_a, stream));
@@ -616,6 +620,9 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     ta.tile_row0 = L->tile_row0;
     ta.meta = L->meta;
     ta.out = L->v;
+    ta.out_rows = L->T_max;
+    ta.pool_rows = L->P;
+    ta.err = L->err;
     ta.max_tiles = (T + kTileRows - 1) / kTileRows + std::min(T, L->S);
     ta.num_sms = L->num_sms;
     LORA_CUDA(L, launch_lora_tile(ta, bf16, false, stream));
@@ -638,6 +645,9 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.ex.v_planes = v_split;
   ga.ex.v_plane_stride = (size_t)L->T_max * L->R;
   ga.ex.delta = L->delta;
+  ga.ex.delta_rows = std::min(L->T_max, kDeltaMaxT);
+  ga.ex.v_rows = L->T_max;
+  ga.ex.pool_rows = L->P;
   ga.ex.R = L->R;
   ga.ex.B_pool = L->B_pool;
   ga.ex.row_base = L->row_base;
@@ -701,6 +711,8 @@ int lora_get_status(lora_layer_t* L, void* stream_) {
   LORA_CUDA(L, cudaStreamSynchronize(stream));
   LORA_CUDA(L, cudaMemcpy(&flags, L->err, 4, cudaMemcpyDeviceToHost));
   LORA_CUDA(L, cudaMemset(L->err, 0, 4));
+  if (flags & LORA_ERRF_BOUNDS)
+    return fail(L, LORA_EBOUNDS, "a device bounds check failed (flags=%d)", flags);
   if (flags & LORA_ERRF_TIMEOUT)
     return fail(L, LORA_ETIMEOUT, "a kernel pipeline wait timed out (flags=%d)", flags);
   if (flags & (LORA_ERRF_BAD_ID | LORA_ERRF_EMPTY_SLOT))

@@ -1,5 +1,6 @@
-// lora_tile.cu -- the low-rank half of the layer per segment tile: shrink v = x A_slot and,
-// in delta mode, expand delta = scale * v B_slot.
+// lora_tile.cu -- the low-rank half of the layer: per segment tile, the shrink v = x A_slot
+// (fp32 layers); for decode batches, BGMV shrink + expand into the fp32 delta [rows][N] =
+// scale * v B_slot, rows of delta_rows.
 //
 // "Serving multiple LoRAs: segmented matrix multiplies and adapter scheduling", section
 // "Not merging the weights, computing in batches": SGMV groups the tokens of one adapter
@@ -15,10 +16,8 @@
 //            registers, so each A vector is loaded once per RB rows and each lane keeps
 //            RB + JW independent 16-byte loads in flight; a butterfly shuffle sums the
 //            lanes.  v (fp32, already multiplied by alpha / r) goes to shared memory.
-//   v mode   v is written to global memory [row][j]; the base GEMM's epilogue expands it.
-//   delta    each thread owns 8 consecutive output columns, loads up to 16 rank rows of
-//   mode     B_slot at once, and writes delta[row][n] = sum_j v[row][j] B[j][n] in fp32;
-//            the base GEMM's epilogue adds it before its single rounding of y.
+//   v is written to global memory [row][j]; the base GEMM's epilogue expands it.  (Decode
+//   batches run the BGMV kernels further below, which expand into an fp32 delta.)
 // Only the true rank r of the slot is read: the zero padding of the slot never is.
 //
 // Launch: programmatic dependent launch.  The kernel lets the next kernel (the base GEMM,
@@ -128,56 +127,9 @@ __device__ __forceinline__ void shrink_tile_warp(const T* __restrict__ x, int K,
   }
 }
 
-// Expand of one tile: delta[row_q][n..n+8) = sum_j v_s[q][j] * B[j][n..n+8), fp32 out.
-__device__ __forceinline__ void expand_tile_delta(const __nv_bfloat16* __restrict__ Bs, int N,
-                                                  int r, const float* v_s, int vstride,
-                                                  const int* rows_s, int nr,
-                                                  float* __restrict__ delta, int tid) {
-  for (int n = tid * 8; n < N; n += kTileThreads * 8) {
-    for (int q0 = 0; q0 < nr; q0 += 4) {
-      float acc[4][8];
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[qq][e] = 0.f;
-      for (int j0 = 0; j0 < r; j0 += 16) {
-        uint4 b[16];
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
-          b[jj] = (j0 + jj < r) ? __ldg(reinterpret_cast<const uint4*>(Bs + (size_t)(j0 + jj) * N + n))
-                                : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const int q = min(q0 + qq, nr - 1);
-            const float vj = (j0 + jj < r) ? v_s[q * vstride + j0 + jj] : 0.f;
-            acc[qq][0] = fmaf(vj, bf16_lo(b[jj].x), acc[qq][0]);
-            acc[qq][1] = fmaf(vj, bf16_hi(b[jj].x), acc[qq][1]);
-            acc[qq][2] = fmaf(vj, bf16_lo(b[jj].y), acc[qq][2]);
-            acc[qq][3] = fmaf(vj, bf16_hi(b[jj].y), acc[qq][3]);
-            acc[qq][4] = fmaf(vj, bf16_lo(b[jj].z), acc[qq][4]);
-            acc[qq][5] = fmaf(vj, bf16_hi(b[jj].z), acc[qq][5]);
-            acc[qq][6] = fmaf(vj, bf16_lo(b[jj].w), acc[qq][6]);
-            acc[qq][7] = fmaf(vj, bf16_hi(b[jj].w), acc[qq][7]);
-          }
-        }
-      }
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
-        if (q0 + qq < nr) {
-          float4* d = reinterpret_cast<float4*>(delta + (size_t)rows_s[q0 + qq] * N + n);
-          d[0] = make_float4(acc[qq][0], acc[qq][1], acc[qq][2], acc[qq][3]);
-          d[1] = make_float4(acc[qq][4], acc[qq][5], acc[qq][6], acc[qq][7]);
-        }
-      }
-    }
-  }
-}
-
 // <= 128 registers a thread: two CTAs of this kernel, or one beside a base-GEMM CTA, fit
 // on an SM, so the GEMM launched after it can start while it runs.
-template <typename T, typename V, bool kDelta>
+template <typename T, typename V>
 __global__ void __launch_bounds__(kTileThreads, 2)
     lora_tile_kernel(const T* __restrict__ x, int K, int N, int R,
                      const T* __restrict__ At_pool, const T* __restrict__ B_pool,
@@ -186,7 +138,8 @@ __global__ void __launch_bounds__(kTileThreads, 2)
                      const int32_t* __restrict__ perm, const int32_t* __restrict__ seg_offsets,
                      const int32_t* __restrict__ seg_slot, const int32_t* __restrict__ tile_seg,
                      const int32_t* __restrict__ tile_row0, const int32_t* __restrict__ meta,
-                     float* __restrict__ out /* v [T][R] or delta [T][N] */) {
+                     float* __restrict__ out /* v [out_rows][R] */, int out_rows, int pool_rows,
+                     int32_t* __restrict__ err) {
   griddep_wait();
   griddep_launch_dependents();
   __shared__ int rows_s[kTileRows];
@@ -205,6 +158,10 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     if (tid < nr) rows_s[tid] = perm[p0 + tid];
     __syncthreads();
     const int rb = row_base[s];  // the slot's first pool row
+    if (!LORA_IN_BOUNDS(rb >= 0 && rb + r <= pool_rows, err)) {
+      __syncthreads();  // rows_s is rewritten by the next tile
+      continue;
+    }
     const T* At = At_pool + (size_t)rb * K;
     if (r <= 8)
       shrink_tile_warp<T, V, 1>(x, K, At, r, rows_s, nr, sc, v_s, vstride, warp, lane);
@@ -217,14 +174,10 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     else
       shrink_tile_warp<T, V, 16>(x, K, At, r, rows_s, nr, sc, v_s, vstride, warp, lane);
     __syncthreads();
-    if constexpr (kDelta) {
-      expand_tile_delta(reinterpret_cast<const __nv_bfloat16*>(B_pool) + (size_t)rb * N, N, r,
-                        v_s, vstride, rows_s, nr, out, tid);
-    } else {
-      for (int i = tid; i < nr * r; i += kTileThreads) {
-        const int q = i / r, j = i - q * r;
+    for (int i = tid; i < nr * r; i += kTileThreads) {
+      const int q = i / r, j = i - q * r;
+      if (LORA_IN_BOUNDS(rows_s[q] >= 0 && rows_s[q] < out_rows, err))
         out[(size_t)rows_s[q] * R + j] = v_s[q * vstride + j];
-      }
     }
     __syncthreads();
   }
@@ -252,7 +205,8 @@ __global__ void __launch_bounds__(kBgmvThreads, 8)  // <= 64 registers: 4 CTAs f
                       const __nv_bfloat16* __restrict__ At_pool,
                       const __nv_bfloat16* __restrict__ B_pool,
                       const int32_t* __restrict__ row_base, const float* __restrict__ scale,
-                      const int32_t* __restrict__ rank, float* __restrict__ delta, int kchunk,
+                      const int32_t* __restrict__ rank, float* __restrict__ delta,
+                      int delta_rows, int pool_rows, int32_t* __restrict__ err, int kchunk,
                       int nchunk) {
   griddep_wait();  // the previous kernel's writes (x, the delta it read) are settled
   griddep_launch_dependents();  // the base GEMM's main loop may start now
@@ -274,6 +228,8 @@ __global__ void __launch_bounds__(kBgmvThreads, 8)  // <= 64 registers: 4 CTAs f
     const float* sc = scale + (size_t)s * R;  // the slot's column scales
     const __nv_bfloat16* xr = x + (size_t)row * K;
     const int rb = row_base[s];  // the slot's first pool row
+    // (the same decision in all CTAs of the cluster: they read the same rb and r)
+    if (!LORA_IN_BOUNDS(rb >= 0 && rb + r <= pool_rows && row < delta_rows, err)) continue;
     const __nv_bfloat16* At = At_pool + (size_t)rb * K;
     float* vp = v_part[buf];
     buf ^= 1;
@@ -450,7 +406,8 @@ __device__ __forceinline__ void stream_shrink(const __nv_bfloat16* __restrict__ 
 template <int RMAX, int NG>
 __device__ __forceinline__ void stream_expand(const __nv_bfloat16* __restrict__ Bs, int N, int r,
                                               const float (*v_s)[32], const int* rows,
-                                              float* __restrict__ delta) {
+                                              float* __restrict__ delta, int delta_rows,
+                                              int32_t* __restrict__ err) {
   for (int e = threadIdx.x; e < N / 8; e += kStrThreads) {
     float o[NG][8];
 #pragma unroll
@@ -481,6 +438,7 @@ __device__ __forceinline__ void stream_expand(const __nv_bfloat16* __restrict__ 
     }
 #pragma unroll
     for (int q = 0; q < NG; ++q) {
+      if (!LORA_IN_BOUNDS(rows[q] >= 0 && rows[q] < delta_rows, err)) continue;
       float4* d = reinterpret_cast<float4*>(delta + (size_t)rows[q] * N + e * 8);
       d[0] = make_float4(o[q][0], o[q][1], o[q][2], o[q][3]);
       d[1] = make_float4(o[q][4], o[q][5], o[q][6], o[q][7]);
@@ -510,7 +468,8 @@ __global__ void __maxnreg__(120)
                        const __nv_bfloat16* __restrict__ B_pool,
                        const int32_t* __restrict__ row_base, int pool_rows,
                        const float* __restrict__ scale,
-                       const int32_t* __restrict__ rank, float* __restrict__ delta) {
+                       const int32_t* __restrict__ rank, float* __restrict__ delta,
+                       int delta_rows, int32_t* __restrict__ err) {
   // launched while the previous kernel (the previous forward's base GEMM) still runs: wait
   // for it before reading x or writing delta, and only then let the base GEMM start (its
   // main loop reads x, which that kernel may have written)
@@ -644,6 +603,11 @@ __global__ void __maxnreg__(120)
     __syncthreads();
     const int ng = min(kStrGroup, nrows - g0);
     const int rbi = POOLED ? rb_s : s * R;  // the slot's first pool row
+    // (rbi and r are the same in every thread: the whole CTA skips the item)
+    if (!LORA_IN_BOUNDS(rbi >= 0 && rbi + min(r, min(R, RMAX)) <= pool_rows, err)) {
+      __syncthreads();  // rows_s and v_s are rewritten by the next item
+      continue;
+    }
     const __nv_bfloat16* At = At_pool + (size_t)rbi * K;
     const __nv_bfloat16* Bs = B_pool + (size_t)rbi * N;
     // shrink: v_s[0 .. ng), ROWS rows a pass (the last pass may take one)
@@ -655,9 +619,9 @@ __global__ void __maxnreg__(120)
     }
     // expand: the group's delta rows
     if (ng == 1)
-      stream_expand<RMAX, 1>(Bs, N, r, v_s, rows_s, delta);
+      stream_expand<RMAX, 1>(Bs, N, r, v_s, rows_s, delta, delta_rows, err);
     else
-      stream_expand<RMAX, kStrGroup>(Bs, N, r, v_s, rows_s, delta);
+      stream_expand<RMAX, kStrGroup>(Bs, N, r, v_s, rows_s, delta, delta_rows, err);
     __syncthreads();  // rows_s and v_s are rewritten by the next item
   }
 }
@@ -685,7 +649,7 @@ static cudaError_t launch_bgmv_stream_t(const BgmvArgs& a, cudaStream_t stream) 
                             static_cast<const __nv_bfloat16*>(a.x), a.token_slot, a.loaded, a.T,
                             a.K, a.N, a.R, a.S, static_cast<const __nv_bfloat16*>(a.At_pool),
                             static_cast<const __nv_bfloat16*>(a.B_pool), a.row_base,
-                            a.pool_rows, a.scale, a.rank, a.delta);
+                            a.pool_rows, a.scale, a.rank, a.delta, a.delta_rows, a.err);
 }
 
 template <int RMAX, int ROWS>
@@ -736,7 +700,7 @@ cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream) {
                             a.token_slot, a.loaded, a.T, a.K, a.N, a.R, a.S,
                             static_cast<const __nv_bfloat16*>(a.At_pool),
                             static_cast<const __nv_bfloat16*>(a.B_pool), a.row_base, a.scale,
-                            a.rank, a.delta, kchunk, nchunk);
+                            a.rank, a.delta, a.delta_rows, a.pool_rows, a.err, kchunk, nchunk);
 }
 
 cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStream_t stream) {
@@ -754,12 +718,12 @@ cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStrea
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   static bool carveout[3][kAttrDevices] = {};
-  cudaError_t e = bf16 ? prefer_max_smem_carveout(lora_tile_kernel<__nv_bfloat16, Vec16<__nv_bfloat16>, false>, carveout[0])
+  cudaError_t e = bf16 ? prefer_max_smem_carveout(lora_tile_kernel<__nv_bfloat16, Vec16<__nv_bfloat16>>, carveout[0])
                        : cudaSuccess;
   if (e == cudaSuccess && !bf16)
-    e = prefer_max_smem_carveout(lora_tile_kernel<float, Vec16<float>, false>, carveout[1]);
+    e = prefer_max_smem_carveout(lora_tile_kernel<float, Vec16<float>>, carveout[1]);
   if (e == cudaSuccess && !bf16)
-    e = prefer_max_smem_carveout(lora_tile_kernel<float, Scalar32, false>, carveout[2]);
+    e = prefer_max_smem_carveout(lora_tile_kernel<float, Scalar32>, carveout[2]);
   if (e != cudaSuccess) return e;
   if (bf16) {
     using T = __nv_bfloat16;
@@ -768,9 +732,9 @@ cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStrea
     const T* At = static_cast<const T*>(a.At_pool);
     const T* B = static_cast<const T*>(a.B_pool);
     if (delta) return cudaErrorInvalidValue;  // delta mode runs bgmv_delta_kernel
-    return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, V, false>, x, a.K, a.N, a.R, At, B,
+    return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, V>, x, a.K, a.N, a.R, At, B,
                               a.row_base, a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
-                              a.tile_row0, a.meta, a.out);
+                              a.tile_row0, a.meta, a.out, a.out_rows, a.pool_rows, a.err);
   }
   if (delta) return cudaErrorInvalidValue;  // delta mode is a bf16 path
   using T = float;
@@ -779,12 +743,12 @@ cudaError_t launch_lora_tile(const TileArgs& a, bool bf16, bool delta, cudaStrea
   const T* B = static_cast<const T*>(a.B_pool);
   const bool vec4 = a.K % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0;
   if (vec4)
-    return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, Vec16<T>, false>, x, a.K, a.N, a.R, At, B,
+    return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, Vec16<T>>, x, a.K, a.N, a.R, At, B,
                               a.row_base, a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
-                              a.tile_row0, a.meta, a.out);
-  return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, Scalar32, false>, x, a.K, a.N, a.R, At, B,
+                              a.tile_row0, a.meta, a.out, a.out_rows, a.pool_rows, a.err);
+  return cudaLaunchKernelEx(&cfg, lora_tile_kernel<T, Scalar32>, x, a.K, a.N, a.R, At, B,
                             a.row_base, a.scale, a.rank, a.perm, a.seg_offsets, a.seg_slot, a.tile_seg,
-                            a.tile_row0, a.meta, a.out);
+                            a.tile_row0, a.meta, a.out, a.out_rows, a.pool_rows, a.err);
 }
 
 }  // namespace lora

@@ -156,7 +156,9 @@ __global__ void __launch_bounds__(kShThreads, 1)
         ui.off[lane] = max(o, p0);
         const int sl = a.seg_slot[gs + lane];
         ui.slot[lane] = sl;
-        ui.rowb[lane] = a.row_base[sl];
+        const int rb = a.row_base[sl];
+        // (a row outside the pool: its A blocks are taken from row 0, and flagged)
+        ui.rowb[lane] = LORA_IN_BOUNDS(rb >= 0 && rb < a.pool_rows, a.err) ? rb : 0;
       }
       if (lane == G) ui.off[G] = min(o, p1);
       if (lane == 0) {
@@ -272,6 +274,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
       mbar_arrive(&info_empty[ib]);
       const int grow = live ? a.perm[p] : 0;
       const float* sc = a.scale + (size_t)slot * a.R;  // the slot's column scales
+      const bool vrow_ok = !live || LORA_IN_BOUNDS(grow >= 0 && grow < a.v_rows && kp < a.ks, a.err);
       float* vrow = a.v + (size_t)kp * a.plane_stride + (size_t)grow * a.R;
       const int buf = item & 1;
       const uint32_t use = (uint32_t)(item >> 1);
@@ -283,7 +286,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
         tmem_ld_32x32b_x16(tmem_row + (uint32_t)(buf * kShNmax + j0), raw);
         tmem_ld_wait();
         const int j = j0 - col0;  // rank index of raw[0]
-        if (live && j >= 0 && j < Rt) {
+        if (live && vrow_ok && j >= 0 && j < Rt) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             if (j + 4 * q < a.R) {

@@ -16,15 +16,17 @@ import os
 
 import torch
 
-from .build import LIB_PATH
+from .build import library_path
+
+LIB_PATH = library_path()  # the release library, or the debug flavour (LORA_LAYER_LIBRARY=debug)
 
 LORA_F32, LORA_BF16 = 0, 1
 STATUS = {0: "LORA_OK", -1: "LORA_EINVAL", -2: "LORA_ESLOT", -3: "LORA_ERANK", -4: "LORA_EID",
           -5: "LORA_ECUDA", -6: "LORA_ENOMEM", -7: "LORA_ESTATE", -8: "LORA_ETIMEOUT",
-          -9: "LORA_ENOENT", -10: "LORA_ECAPACITY"}
+          -9: "LORA_ENOENT", -10: "LORA_ECAPACITY", -11: "LORA_EBOUNDS"}
 LORA_OK, LORA_EINVAL, LORA_ESLOT, LORA_ERANK, LORA_EID = 0, -1, -2, -3, -4
 LORA_ECUDA, LORA_ENOMEM, LORA_ESTATE, LORA_ETIMEOUT = -5, -6, -7, -8
-LORA_ENOENT, LORA_ECAPACITY = -9, -10
+LORA_ENOENT, LORA_ECAPACITY, LORA_EBOUNDS = -9, -10, -11
 
 # every entry point declared in include/lora_layer.h
 ABI_FUNCTIONS = ("lora_layer_create", "lora_layer_create_pooled", "lora_layer_create_fp8",
@@ -62,8 +64,9 @@ class LoraError(RuntimeError):
 
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
-        raise ImportError("liblora_layer.so is not built (run __graft_entry__.build() or "
-                          "python -m segmented_rank_gemm_gb300.build); no fallback exists")
+        raise ImportError("%s is not built (run __graft_entry__.build() or python -m "
+                          "segmented_rank_gemm_gb300.build [--debug]); no fallback exists"
+                          % os.path.basename(LIB_PATH))
     L = ctypes.CDLL(LIB_PATH)
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     L.lora_layer_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32, vp, vp]
