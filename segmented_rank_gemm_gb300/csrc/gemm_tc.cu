@@ -204,6 +204,9 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * stages + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the first launch of a split batch lets the second one start while it runs (it waits for
+  // this one before its epilogue reads anything this one's predecessor wrote)
+  if (a.trigger_next) griddep_launch_dependents();
   // Work units: output tiles, one per CTA (pair) slot and round: slot g runs units
   // g, g + G, g + 2 G, ... (delta mode: G is the number of units, one each).  CTA pairs:
   // the two CTAs of a pair are neighbours in x and cover 256 consecutive rows, CTA pr of
@@ -273,7 +276,7 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
         if (!seg_at(k, g0, G, U, nkb, full_rounds, sk_slots, u, k0, k1)) break;
         int pm_i, nt_i;
         unit_tile(u, mtp, nt, group_m, pm_i, nt_i);
-        const int m0 = (PAIR ? 2 * pm_i + pr : pm_i) * kBM, n0 = nt_i * BN;
+        const int m0 = (PAIR ? 2 * pm_i + pr : pm_i) * kBM, n0 = a.n_begin + nt_i * BN;
         // a whole tile starts its K range at a rotated block (the same for both CTAs of a
         // pair), so tiles sharing an x or W tile do not request the same lines at once;
         // stream-K pieces run in order
@@ -462,7 +465,7 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
       int pm_i, nt_i;
       unit_tile(u, mtp, nt, group_m, pm_i, nt_i);
       const int mt_i = PAIR ? 2 * pm_i + pr : pm_i;
-      const int m0 = mt_i * kBM, n0 = nt_i * BN;
+      const int m0 = mt_i * kBM, n0 = a.n_begin + nt_i * BN;
       const int row = m0 + rt;
       const int b = k & 1;
       const uint32_t tmem_row =
@@ -923,8 +926,30 @@ static size_t exchange_floats(const GemmPlan& p, int M, int N) {
   return gx * gy * p.ksplit * p.block_n * kBM;
 }
 
+// A delta-mode batch whose no-split plan leaves a last round of tiles at most half full
+// runs as two launches: the column tiles of the whole rounds without a K split, then the
+// remaining column tiles with a 2-way K split (their 2 x csize-CTA clusters fit in one
+// round), so the last round takes half the time.  Returns the column tiles of the first
+// launch, or 0 for no split.
+static int delta_split_tiles(const GemmPlan& p, int M, int N, int nkb, int num_sms) {
+  if (p.ksplit != 1 || nkb < 2) return 0;
+  const int csize = p.pair ? 2 : 1;
+  const int mt = (M + kBM - 1) / kBM, mtp = p.pair ? (mt + 1) / 2 : mt;
+  const int nt = (N + p.block_n - 1) / p.block_n, units = mtp * nt;
+  const int G = resident_ctas(csize, num_sms) / csize;
+  if (G < 1 || units <= G || units % G == 0 || 2 * (units % G) > G) return 0;
+  const int ntA = (units / G) * G / mtp, ntB = nt - ntA;
+  if (ntA < 1 || ntB < 1 || 2 * csize * mtp * ntB > resident_ctas(2 * csize, num_sms)) return 0;
+  if (p.block_n / 2 < 32) return 0;
+  return ntA;
+}
+
 size_t gemm_tc_exchange_floats(int M, int N, int K, int num_sms) {
-  return exchange_floats(gemm_tc_plan(M, N, K, num_sms, true, 0), M, N);
+  const GemmPlan p = gemm_tc_plan(M, N, K, num_sms, true, 0);
+  const int ntA = delta_split_tiles(p, M, N, (K + kBK - 1) / kBK, num_sms);
+  if (ntA > 0)  // the second launch: the remaining columns with a 2-way split
+    return exchange_floats(GemmPlan{p.block_n, 2, p.pair}, M, N - ntA * p.block_n);
+  return exchange_floats(p, M, N);
 }
 
 size_t gemm_tc_plan_exchange_floats(const GemmPlan& p, int M, int N) {
@@ -950,7 +975,7 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   if (a.ex.mode == kExpandV && (cs != 1 || a.ex.R % 8 != 0 || a.ex.R > 128 || a.ex.S > 32 * kBM))
     return cudaErrorInvalidValue;
   const int xscr = a.ex.mode == kExpandV ? kBM * expand_layout(a.ex.R).nbs * 128 : 0;
-  if (cs > 1 && (!a.xk || a.xk_floats < exchange_floats(plan, a.M, a.N)))
+  if (cs > 1 && (!a.xk || a.xk_floats < exchange_floats(plan, a.M, a.n_end - a.n_begin)))
     return cudaErrorInvalidValue;
   int stages = 8;
   while (stages > 2 && tc_smem_bytes(BN, PAIR, stages, xscr) > budget) --stages;
@@ -977,7 +1002,7 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   // loads zeros and stores nothing.
   const int mt = (a.M + kBM - 1) / kBM;
   const int mtp = PAIR ? (mt + 1) / 2 : mt;
-  const int nt = (a.N + BN - 1) / BN;
+  const int nt = (a.n_end - a.n_begin + BN - 1) / BN;
   const int units = mtp * nt;
   const int csize = (PAIR ? 2 : 1) * cs;
   int G = units;
@@ -1037,6 +1062,10 @@ static cudaError_t launch_variant(const GemmArgs& a, const GemmPlan& plan,
   }
 }
 
+static cudaError_t launch_one(const GemmArgs& a, const GemmPlan& plan,
+                              const CUtensorMap* tmap_w3, const CUtensorMap* tmap_bx3,
+                              cudaStream_t stream);
+
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
                            const CUtensorMap* tmap_bx3, cudaStream_t stream) {
   if (a.ex.mode == kExpandV && !tmap_bx3) return cudaErrorInvalidValue;
@@ -1052,6 +1081,30 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
     const int nkb = (k_bytes2 + kBK - 1) / kBK, c = plan.ksplit;
     if (c > 1 && (c - 1) * ((nkb + c - 1) / c) >= nkb) return cudaErrorInvalidConfiguration;
   }
+  GemmArgs whole = a;
+  whole.n_begin = 0;
+  whole.n_end = a.N;
+  whole.trigger_next = false;
+  // a last round at most half full: two launches (see delta_split_tiles)
+  const int ntA = a.ex.mode == kExpandDelta && a.force_bn == 0
+                      ? delta_split_tiles(plan, a.M, a.N, (k_bytes2 + kBK - 1) / kBK, a.num_sms)
+                      : 0;
+  if (ntA > 0) {
+    GemmArgs first = whole, second = whole;
+    first.n_end = ntA * plan.block_n;
+    first.trigger_next = true;
+    second.n_begin = first.n_end;
+    const GemmPlan plan2{plan.block_n, 2, plan.pair};
+    cudaError_t e = launch_one(first, plan, tmap_w3, tmap_bx3, stream);
+    if (e != cudaSuccess) return e;
+    return launch_one(second, plan2, tmap_w3, tmap_bx3, stream);
+  }
+  return launch_one(whole, plan, tmap_w3, tmap_bx3, stream);
+}
+
+// One launch of the tcgen05 GEMM with the given plan (columns a.n_begin .. a.n_end).
+static cudaError_t launch_one(const GemmArgs& a, const GemmPlan& plan, const CUtensorMap* tmap_w3,
+                              const CUtensorMap* tmap_bx3, cudaStream_t stream) {
   if (a.fp8) {
     const int ti = gemm_tc_tile_index(plan.pair ? plan.block_n / 2 : plan.block_n);
     return launch_variant_fp8(a, plan, *a.tmap_xq, tmap_w3[ti], stream);

@@ -206,6 +206,11 @@ struct GemmArgs {
   float* xk;         // split K: scratch for the exchanged fp32 partials (L2-resident)
   size_t xk_floats;  // its capacity (gemm_tc_exchange_floats of the batch)
   int force_bn, force_cs, force_pair;  // tcgen05 tiling fixed by the caller (force_bn 0: auto)
+  // columns [n_begin, n_end) of y computed by this launch (0, N for the whole product; the
+  // launcher sets them when it splits a batch over two launches), and whether the launch
+  // lets the next kernel on its stream start at once (the second launch of such a split)
+  int n_begin = 0, n_end = 0;
+  bool trigger_next = false;
   // stream-K (large batches): fp32 partial per CTA [num_sms][128][256] and sync words
   // {epoch, exit count, flag per CTA} (zeroed at allocation); null: no stream-K
   float* sk_part;

@@ -48,6 +48,23 @@ def test_delta_mode_one_row_pairs():
     _sweep(wl, [(128, 2, 1), (256, 4, 1), (128, 1, 0)])
 
 
+@pytest.mark.parametrize("T,K,N", [(512, 4096, 14336), (400, 1032, 14328), (300, 520, 10240)])
+def test_delta_mode_automatic_plan_wide_n(T, K, N):
+    # wide outputs on the automatic plan: where one tile per CTA (pair) would leave a last
+    # round at most half full, the batch runs as two launches (the whole rounds' column
+    # tiles, then the rest with a 2-way K split); ragged rows, K blocks and last tile
+    wl = workloads.synthetic(4120 + T, T, K, N, S=7, ranks=[16, 4, 8, 16, 1, 12, 16], R=16,
+                             base_frac=0.1)
+    layer = build_layer(wl)
+    try:
+        for rep in range(2):
+            y = run_layer(layer, wl)
+            assert layer.status() == 0
+            assert_parity(y, oracle_rows(wl), wl.dtype, what="%s automatic plan, launch %d" % (wl.name, rep))
+    finally:
+        layer.close()
+
+
 def test_v_mode_every_plan():
     # 700 rows in 5.5 row tiles (pairs: 3 pairs, the last CTA partial), 9 K blocks,
     # N = 1000; many slots per tile so every tile runs several expand blocks
