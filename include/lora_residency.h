@@ -90,10 +90,18 @@ typedef struct lora_cache_stats {
 /*
  * Create a cache over `n_layers` layers (borrowed: they must outlive the cache) that share
  * the slot numbering [0, num_slots).
- *   layers         n_layers layer handles (not pooled: lora_layer_create), all on the
- *                  current device; n_layers = 0 gives a
+ *   layers         n_layers layer handles, all on the current device; n_layers = 0 gives a
  *                  cache that only keeps the books (slot assignment, recency, statistics)
- *                  and touches no device: it needs no GPU.
+ *                  and touches no device: it needs no GPU.  Pooled layers
+ *                  (lora_layer_create_pooled: adapters at their true rank) are served: a
+ *                  swap-in gives back the rows its slot held and takes the adapter's rank
+ *                  rounded up to 8 consecutive rows, first fit, from each pooled layer's
+ *                  row pool.  All pooled layers of a cache must have the same pool_rows and
+ *                  hold no adapter when the cache is created, and from then on their slots
+ *                  change only through the cache (the cache moves their allocators in
+ *                  step).  A swap-in that finds no run of free rows fails with LORA_ENOMEM
+ *                  and leaves its slot empty (size the pool for the slots' ranks with room
+ *                  for fragmentation).
  *   num_slots      1 <= num_slots <= every layer's num_slots (vLLM's max_loras).
  *   host_capacity  adapters the host tier holds (vLLM's max_cpu_loras), >= num_slots.
  * Allocates host_capacity pinned host blocks of the adapter image size (the sum over the
@@ -156,7 +164,8 @@ int lora_cache_remove(lora_adapter_cache_t* cache, int64_t id);
  * name, and is swapped in (enqueued, not waited for).  Finally `stream` waits for the
  * batch's swap-ins.  The returned slots stay valid until the next lora_cache_map_batch,
  * lora_cache_add or lora_cache_remove.
- * Errors: as above, LORA_ECUDA.
+ * Errors: as above, LORA_ENOMEM (a pooled layer has no run of free rows for an adapter:
+ * that adapter's slot is left empty and the batch is not mapped), LORA_ECUDA.
  */
 int lora_cache_map_batch(lora_adapter_cache_t* cache, const int64_t* token_adapter, int T,
                          int32_t* token_slot, void* stream);

@@ -86,4 +86,11 @@ cudaEvent_t layer_take_event(lora_layer* L);
 // decode BGMV kernel reads one scale per slot while no slot of the layer does.
 void layer_set_percol(lora_layer* L, int slot, bool varied);
 
+// Pooled layers: return the rows slot `slot` holds to the row pool (its first row and row
+// count before, through *first / *rows; 0 rows if it held none).  Host bookkeeping only.
+void layer_release_rows(lora_layer* L, int slot, int* first, int* rows);
+// Pooled layers: give slot `slot` (holding no rows) `rows` consecutive rows of the pool,
+// first fit; returns the first row, or -1 if no run of free rows is that long.
+int layer_take_rows(lora_layer* L, int slot, int rows);
+
 }  // namespace lora

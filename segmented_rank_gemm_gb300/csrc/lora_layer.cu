@@ -333,6 +333,29 @@ static void pool_free(lora_layer* L, int first, int rows) {
   L->free_rows[first] = rows;
 }
 
+namespace lora {
+
+void layer_release_rows(lora_layer* L, int slot, int* first, int* rows) {
+  *first = L->rb_h[slot];
+  *rows = L->rows_h[slot];
+  if (L->pooled && *rows > 0) pool_free(L, *first, *rows);
+  if (L->pooled) {
+    L->rb_h[slot] = -1;
+    L->rows_h[slot] = 0;
+  }
+}
+
+int layer_take_rows(lora_layer* L, int slot, int rows) {
+  const int rb = pool_alloc(L, rows);
+  if (rb >= 0) {
+    L->rb_h[slot] = rb;
+    L->rows_h[slot] = rows;
+  }
+  return rb;
+}
+
+}  // namespace lora
+
 extern "C" {
 
 int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_rank,

@@ -28,6 +28,14 @@
 //   - until the next point, the previous batch's slots are in flight: a prefetch never
 //     takes them, and an adapter removed from them leaves its slot blocked (emptied at the
 //     next point) instead of rewriting it under a running kernel.
+// Pooled layers (lora_layer_create_pooled: adapters at their true rank in a row pool) are
+// served too.  A swap-in frees the rows its slot held and takes the adapter's rank rounded
+// up to 8 rows, first fit, from each pooled layer's allocator (the cache makes the same
+// moves in every pooled layer, so they all place the slot at the same row); the scatter
+// copies those rows only and sets the slot's first row.  Rows freed from one slot may be
+// reused by another slot while an earlier batch still reads them, so the cache remembers
+// per pool row the batch point of its last user, and a swap-in into rows waits for those
+// points as it waits for its slot's own.
 
 #include <cuda_runtime.h>
 
@@ -61,25 +69,36 @@ struct SwapDesc {
   int R;         // the layer's slot width
   unsigned long long a_bytes, b_bytes;  // one slot's A and B block: R*K and R*N elements
   unsigned long long off_a, off_b;      // offsets of those blocks in the adapter image
+  // pooled layers: the slot's rows start at the row the swap-in took (its first row table,
+  // null for a plain layer) and number rows (the rank rounded up to 8); bytes of a row
+  int32_t* row_base;
+  unsigned long long a_row, b_row;
 };
 
 // Slot `slot` of every layer (blockIdx.y) from the staged adapter image (copy != 0), and
 // the slot's column scales (cols on the r columns of the adapter, 0 beyond), rank and
 // loaded flag (copy == 0: only those, to empty the slot).  The blocks are multiples of 16
 // bytes (R is a multiple of 8) and start 16-byte aligned.
+// Pooled layers: rows `rows` from pool row `rb` (the same in every pooled layer); a plain
+// layer ignores both.  The image's blocks hold R rows; a pooled layer takes the first rows.
 __global__ void __launch_bounds__(kSwapThreads)
     swap_in_kernel(const SwapDesc* __restrict__ desc, const char* __restrict__ image, int slot,
-                   int copy, lora::SlotScales cols, int r, int is_loaded) {
+                   int copy, lora::SlotScales cols, int r, int is_loaded, int rb, int rows) {
   const SwapDesc d = desc[blockIdx.y];
+  const bool pooled = d.row_base != nullptr;
   if (copy) {
     const size_t stride = (size_t)gridDim.x * kSwapThreads;
     const size_t first = (size_t)blockIdx.x * kSwapThreads + threadIdx.x;
+    const size_t a_bytes = pooled ? (size_t)rows * d.a_row : d.a_bytes;
+    const size_t b_bytes = pooled ? (size_t)rows * d.b_row : d.b_bytes;
     const uint4* sa = reinterpret_cast<const uint4*>(image + d.off_a);
-    uint4* da = reinterpret_cast<uint4*>(d.A_pool + (size_t)slot * d.a_bytes);
-    for (size_t i = first; i < d.a_bytes / 16; i += stride) da[i] = __ldg(sa + i);
+    uint4* da = reinterpret_cast<uint4*>(
+        d.A_pool + (pooled ? (size_t)rb * d.a_row : (size_t)slot * d.a_bytes));
+    for (size_t i = first; i < a_bytes / 16; i += stride) da[i] = __ldg(sa + i);
     const uint4* sb = reinterpret_cast<const uint4*>(image + d.off_b);
-    uint4* db = reinterpret_cast<uint4*>(d.B_pool + (size_t)slot * d.b_bytes);
-    for (size_t i = first; i < d.b_bytes / 16; i += stride) db[i] = __ldg(sb + i);
+    uint4* db = reinterpret_cast<uint4*>(
+        d.B_pool + (pooled ? (size_t)rb * d.b_row : (size_t)slot * d.b_bytes));
+    for (size_t i = first; i < b_bytes / 16; i += stride) db[i] = __ldg(sb + i);
   }
   if (blockIdx.x == 0) {
     for (int j = threadIdx.x; j < d.R; j += kSwapThreads)
@@ -87,6 +106,7 @@ __global__ void __launch_bounds__(kSwapThreads)
     if (threadIdx.x == 0) {
       d.rank[slot] = r;
       d.loaded[slot] = is_loaded;
+      if (pooled) d.row_base[slot] = is_loaded ? rb : -1;
     }
   }
 }
@@ -128,6 +148,11 @@ struct lora_adapter_cache {
   std::vector<int> point_refs;
   std::vector<int> last_slots;          // slots of the last mapped batch (maybe in flight)
   std::vector<long long> last_names;    // its adapters
+  // pooled layers (all with the same row pool, moved in step): per pool row, the batch point
+  // of the last slot that held it and gave it back (-1: none pending); each entry holds a
+  // reference on that point
+  bool any_pooled = false;
+  std::vector<int> row_point;
   unsigned long long clock = 0, pin_gen = 0;
   lora_cache_stats_t stats{};
   char last_error[512] = {0};
@@ -180,11 +205,77 @@ int swap_grid_x(const Cache* c) {
   return std::max(1, std::min(1024, (4 * c->num_sms + n - 1) / n));
 }
 
-// Copy adapter e's image into `slot` of every layer.
+// Pooled layers: `slot` gives back the rows it holds (in every pooled layer, where they are
+// the same rows); until a swap-in takes them again they remember the slot's last use.
+void give_back_rows(Cache* c, int slot) {
+  if (!c->any_pooled) return;
+  int first = -1, rows = 0;
+  for (lora_layer* L : c->layers)
+    if (L->pooled) lora::layer_release_rows(L, slot, &first, &rows);
+  const int p = c->busy_point[slot];
+  for (int i = 0; i < rows; ++i) {
+    int& rp = c->row_point[first + i];
+    if (rp >= 0) --c->point_refs[rp];
+    rp = p;
+    if (p >= 0) ++c->point_refs[p];
+  }
+}
+
+// Pooled layers: `rows` rows for `slot` (holding none) in every pooled layer, and the
+// cache's stream made to wait for the last users of those rows.  *first: the first row.
+int take_rows(Cache* c, int slot, int rows, int* first) {
+  *first = 0;
+  if (!c->any_pooled) return LORA_OK;
+  int rb = -2;
+  for (lora_layer* L : c->layers) {
+    if (!L->pooled) continue;
+    const int got = lora::layer_take_rows(L, slot, rows);
+    if (got < 0 || (rb != -2 && got != rb)) {  // no run of free rows (or pools out of step)
+      for (lora_layer* M : c->layers) {
+        int f = 0, n = 0;
+        if (M->pooled) lora::layer_release_rows(M, slot, &f, &n);
+      }
+      return fail(c, LORA_ENOMEM, "the row pools have no %d free consecutive rows", rows);
+    }
+    rb = got;
+  }
+  std::vector<int> waited;
+  for (int i = 0; i < rows; ++i) {
+    int& rp = c->row_point[rb + i];
+    if (rp < 0) continue;
+    if (std::find(waited.begin(), waited.end(), rp) == waited.end()) {
+      CACHE_CUDA(c, cudaStreamWaitEvent(c->stream, c->point_ev[rp], 0));
+      waited.push_back(rp);
+    }
+    --c->point_refs[rp];
+    rp = -1;
+  }
+  *first = rb;
+  return LORA_OK;
+}
+
+// Copy adapter e's image into `slot` of every layer.  LORA_ENOMEM: a pooled layer has no
+// run of rows for it; the slot is then left empty.
 int swap_in(Cache* c, const Entry& e, int slot) {
   if (c->layers.empty()) return LORA_OK;
   int rc = wait_slot_idle(c, slot);
   if (rc != LORA_OK) return rc;
+  // pooled layers: the rows of the slot's previous adapter go back, the new adapter's rank
+  // rounded up to 8 rows are taken
+  const int rows = (e.r + 7) / 8 * 8;
+  int rb = 0;
+  if (c->any_pooled) {
+    give_back_rows(c, slot);
+    rc = take_rows(c, slot, rows, &rb);
+    if (rc != LORA_OK) {  // the slot holds no rows now: empty it in every layer
+      lora::SlotScales none;
+      for (int j = 0; j < lora::kMaxSlotRank; ++j) none.v[j] = 0.f;
+      swap_in_kernel<<<dim3(1, (unsigned)c->layers.size()), kSwapThreads, 0, c->stream>>>(
+          c->desc_dev, c->staging, slot, 0, none, 0, 0, 0, 0);
+      for (lora_layer* L : c->layers) lora::layer_set_percol(L, slot, false);
+      return rc;
+    }
+  }
   CACHE_CUDA(c, cudaMemcpyAsync(c->staging, c->arena + (size_t)e.block * c->image_bytes,
                                 c->image_bytes, cudaMemcpyHostToDevice, c->stream));
   CACHE_CUDA(c, cudaEventRecord(c->block_ev[e.block], c->stream));
@@ -196,17 +287,18 @@ int swap_in(Cache* c, const Entry& e, int slot) {
   for (int j = 1; j < e.r; ++j) varied |= cols.v[j] != cols.v[0];
   dim3 grid(swap_grid_x(c), (unsigned)c->layers.size());
   swap_in_kernel<<<grid, kSwapThreads, 0, c->stream>>>(c->desc_dev, c->staging, slot, 1, cols,
-                                                       e.r, 1);
+                                                       e.r, 1, rb, rows);
   CACHE_CUDA(c, cudaGetLastError());
   // layers that expand v on the tensor cores keep a transposed copy of B per slot
   for (lora_layer* L : c->layers)
     if (L->Bx_pool) {
       const size_t es = L->esize;
+      const size_t first_row = L->pooled ? (size_t)rb : (size_t)slot * L->R;
       CACHE_CUDA(c, lora::launch_pack_bx(
-                        static_cast<char*>(L->B_pool) + (size_t)slot * L->R * L->N * es,
+                        static_cast<char*>(L->B_pool) + first_row * L->N * es,
                         static_cast<char*>(L->Bx_pool) +
                             (size_t)slot * L->N * lora::expand_layout(L->R).wx * es,
-                        L->R, L->R, L->N, c->stream));
+                        L->R, L->pooled ? rows : L->R, L->N, c->stream));
     }
   CACHE_CUDA(c, cudaEventRecord(c->ready_ev[slot], c->stream));
   c->ready_pending[slot] = 1;
@@ -224,9 +316,10 @@ int empty_slot(Cache* c, int slot) {
   lora::SlotScales none;
   for (int j = 0; j < lora::kMaxSlotRank; ++j) none.v[j] = 0.f;
   swap_in_kernel<<<dim3(1, (unsigned)c->layers.size()), kSwapThreads, 0, c->stream>>>(
-      c->desc_dev, c->staging, slot, 0, none, 0, 0);
+      c->desc_dev, c->staging, slot, 0, none, 0, 0, 0, 0);
   CACHE_CUDA(c, cudaGetLastError());
   for (lora_layer* L : c->layers) lora::layer_set_percol(L, slot, false);
+  give_back_rows(c, slot);  // pooled layers: after the slot's last use
   CACHE_CUDA(c, cudaEventRecord(c->ready_ev[slot], c->stream));
   c->ready_pending[slot] = 1;
   return LORA_OK;
@@ -326,7 +419,13 @@ int make_resident(Cache* c, const std::vector<long long>& ids, bool batch) {
     if (batch) ++c->stats.misses;
     else ++c->stats.prefetches;
     const int rc = swap_in(c, e, slot);
-    if (rc != LORA_OK) return rc;
+    if (rc != LORA_OK) {
+      if (rc == LORA_ENOMEM) {  // the slot was left empty
+        c->slot_owner[slot] = kFree;
+        e.slot = -1;
+      }
+      return rc;
+    }
   }
   return LORA_OK;
 }
@@ -426,9 +525,16 @@ int lora_cache_create(lora_adapter_cache_t** out, lora_layer_t* const* layers, i
   size_t off = 0;
   for (int l = 0; l < n_layers; ++l) {
     lora_layer* L = layers[l];
-    // (a pooled layer places its slots by its own row allocator: not served here)
-    if (!L || num_slots > L->S || L->pooled) return bail(LORA_EINVAL);
+    if (!L || num_slots > L->S) return bail(LORA_EINVAL);
     if (l > 0 && L->device != c->layers[0]->device) return bail(LORA_EINVAL);
+    if (L->pooled) {
+      // pooled layers move in step: the same row pool, and no slot holding rows yet
+      for (int q = 0; q < L->S; ++q)
+        if (L->rows_h[q] > 0) return bail(LORA_EINVAL);
+      if (c->any_pooled && (int)c->row_point.size() != L->P) return bail(LORA_EINVAL);
+      c->any_pooled = true;
+      c->row_point.assign(L->P, -1);
+    }
     c->layers.push_back(L);
     c->max_r = std::min(c->max_r, L->max_rank);
     SwapDesc d;
@@ -444,6 +550,9 @@ int lora_cache_create(lora_adapter_cache_t** out, lora_layer_t* const* layers, i
     off = align_up(off + d.a_bytes);
     d.off_b = off;
     off = align_up(off + d.b_bytes);
+    d.row_base = L->pooled ? L->row_base : nullptr;
+    d.a_row = (unsigned long long)L->K * L->esize;
+    d.b_row = (unsigned long long)L->N * L->esize;
     c->desc.push_back(d);
   }
   if (n_layers == 0) c->max_r = 1 << 30;

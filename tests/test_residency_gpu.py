@@ -6,7 +6,10 @@ slot of every layer.
 Layers of three kinds share the cache: bf16 (delta mode up to 512 rows, tensor-core expand
 with the B expand pool above), a second bf16 shape, and fp32.  Batches alternate between
 200 and 600 rows, name at most as many adapters as there are slots, and are chosen so
-that most of them swap something in.
+that most of them swap something in.  The tests run over plain layers (slot s at rows
+s R .. s R + R) and over pooled ones (each adapter at its rank rounded up to 8 rows, placed
+by the pool's first-fit allocator at every swap-in: ranks 1 .. 16 in this universe move
+slots between runs of 8 and 16 rows, so rows are freed and taken again all the time).
 """
 import numpy as np
 import pytest
@@ -32,9 +35,11 @@ def _universe():
             for i, (K, N, dt) in enumerate(SHAPES)]
 
 
-def _build(wls, slots=SLOTS, host=N_IDS):
+def _build(wls, slots=SLOTS, host=N_IDS, pooled=False):
     from segmented_rank_gemm_gb300.lora import AdapterCache, LoraLayer
-    layers = [LoraLayer(wl.W.cuda(), slots + 2, 16, T_MAX) for wl in wls]
+    # pooled: room for every slot at rank 16 plus two spare runs (fragmentation)
+    pool = 16 * (slots + 2) if pooled else 0
+    layers = [LoraLayer(wl.W.cuda(), slots + 2, 16, T_MAX, pool_rows=pool) for wl in wls]
     cache = AdapterCache(layers, slots, host)
     for a in range(N_IDS):
         cache.add(a, [wl.adapters[a][0] for wl in wls], [wl.adapters[a][1] for wl in wls],
@@ -62,10 +67,11 @@ def _check(wls, ids, outs, what):
         assert_parity(y, ref, wl.dtype, what="%s K=%d N=%d" % (what, wl.K, wl.N))
 
 
-def test_swaps_keep_parity_over_a_batch_sequence():
+@pytest.mark.parametrize("pooled", [False, True], ids=["plain", "pooled"])
+def test_swaps_keep_parity_over_a_batch_sequence(pooled):
     from segmented_rank_gemm_gb300.lora import LoraError
     wls = _universe()
-    layers, cache = _build(wls)
+    layers, cache = _build(wls, pooled=pooled)
     stream = torch.cuda.Stream()
     rng = np.random.default_rng(11)
     pending = []
@@ -91,14 +97,20 @@ def test_swaps_keep_parity_over_a_batch_sequence():
     assert st["misses"] >= 6 and st["gpu_evictions"] >= 3, st
     image = sum(16 * (wl.K + wl.N) * (2 if wl.dtype == BF16 else 4) for wl in wls)
     assert st["bytes_swapped"] >= (st["misses"] + st["prefetches"]) * image
+    if pooled:  # the resident adapters hold exactly their ranks rounded up to 8 rows
+        want = sum((RANKS[a] + 7) // 8 * 8 for a in range(N_IDS) if cache.slot_of(a) >= 0)
+        for L in layers:
+            assert L.pool_usage()[0] == want
     cache.close()
 
 
-def test_one_slot_eviction_under_a_running_batch():
+@pytest.mark.parametrize("pooled", [False, True], ids=["plain", "pooled"])
+def test_one_slot_eviction_under_a_running_batch(pooled):
     """One slot: each batch evicts the previous batch's adapter right after that batch's
-    forwards were enqueued (no host synchronisation), so the swap-in must wait for them."""
+    forwards were enqueued (no host synchronisation), so the swap-in must wait for them
+    (pooled: the new adapter reuses rows the running batch reads)."""
     wls = _universe()
-    layers, cache = _build(wls, slots=1, host=N_IDS)
+    layers, cache = _build(wls, slots=1, host=N_IDS, pooled=pooled)
     stream = torch.cuda.Stream()
     runs = []
     for step, a in enumerate([0, 5, 1, 5, 8, 2]):
@@ -112,9 +124,10 @@ def test_one_slot_eviction_under_a_running_batch():
     cache.close()
 
 
-def test_replace_and_remove():
+@pytest.mark.parametrize("pooled", [False, True], ids=["plain", "pooled"])
+def test_replace_and_remove(pooled):
     wls = _universe()
-    layers, cache = _build(wls)
+    layers, cache = _build(wls, pooled=pooled)
     stream = torch.cuda.Stream()
     ids = np.array([3, 4, -1, 3, 4] * 40, np.int64)
     _run_batch(layers, cache, wls, ids, 1, stream)
@@ -180,12 +193,13 @@ def test_swap_in_through_many_layers_and_capacity_errors():
     cache.close()
 
 
-def test_composed_adapters_through_the_cache():
+@pytest.mark.parametrize("pooled", [False, True], ids=["plain", "pooled"])
+def test_composed_adapters_through_the_cache(pooled):
     """Compositions held under their own ids beside plain adapters: packed from the members'
     host blocks (so removing a member later leaves them intact), swapped in like any
     adapter, rows naming them add their members' weighted deltas."""
     wls = _universe()
-    layers, cache = _build(wls, host=N_IDS + 4)
+    layers, cache = _build(wls, host=N_IDS + 4, pooled=pooled)
     compositions = {20: ([0, 3, 7], [0.5, -1.0, 2.0]), 21: ([2, 6], [1.0, 0.25]),
                     22: ([2, 2], [0.5, 0.5])}
     for cid, (members, weights) in compositions.items():
@@ -213,6 +227,39 @@ def test_composed_adapters_through_the_cache():
                                     dtype=torch.int32)
             ref = oracle.forward_composed(x, wl.W, [comps[a] for a in order], slot_ids)
             assert_parity(y, ref, wl.dtype, what="composed ids, step %d K=%d" % (step, wl.K))
+    for L in layers:
+        assert L.status(stream) == 0
+    cache.close()
+
+
+def test_pooled_rows_exhausted_leaves_the_slot_empty():
+    """A pool too small for the adapter a batch needs: map_batch fails with LORA_ENOMEM, the
+    slot is left empty in every layer, and the cache keeps serving what fits."""
+    from segmented_rank_gemm_gb300.lora import AdapterCache, LoraError, LoraLayer
+    wls = _universe()[:2]
+    # 24 rows: adapter 1 (rank 16: 16 rows) and adapter 0 (rank 1: 8 rows) fit together;
+    # adapter 5 (rank 16) then needs 16 free rows while 8 are left
+    layers = [LoraLayer(wl.W.cuda(), 4, 16, T_MAX, pool_rows=24) for wl in wls]
+    cache = AdapterCache(layers, 3, N_IDS)
+    for a in range(N_IDS):
+        cache.add(a, [wl.adapters[a][0] for wl in wls], [wl.adapters[a][1] for wl in wls],
+                  wls[0].adapters[a][2])
+    stream = torch.cuda.Stream()
+    ids = np.array([1, 0, -1, 1] * 50, np.int64)
+    _, outs = _run_batch(layers, cache, wls, ids, 7, stream)
+    torch.cuda.synchronize()
+    _check(wls, ids, outs, "pool of 24 rows, adapters 1 and 0")
+    with pytest.raises(LoraError) as e:
+        cache.map_batch(np.array([1, 0, 5], np.int64), stream)
+    assert e.value.code == -6  # LORA_ENOMEM
+    assert cache.slot_of(5) == -1 and cache.slot_of(1) >= 0 and cache.slot_of(0) >= 0
+    for L in layers:
+        assert L.pool_usage()[0] == 24
+    # the adapters that fit are still served correctly
+    ids = np.array([0, 1, 1, -1] * 40, np.int64)
+    _, outs = _run_batch(layers, cache, wls, ids, 8, stream)
+    torch.cuda.synchronize()
+    _check(wls, ids, outs, "after a refused swap-in")
     for L in layers:
         assert L.status(stream) == 0
     cache.close()
