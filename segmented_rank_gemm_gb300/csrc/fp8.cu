@@ -9,84 +9,53 @@
 // e4m3 rounding to nearest even, saturating at +-448.
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
+#include "e4m3_row.cuh"
 #include "lora_common.cuh"
 #include "lora_kernels.h"
 
 namespace lora {
 
 static constexpr int kQThreads = 256;
-static constexpr float kE4m3Max = 448.f;
+static constexpr int kQHold = 8;  // 16-byte chunks a thread holds between the max and the conversion
 
-__device__ __forceinline__ uint8_t to_e4m3(float v, float s) {
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(v, s), __NV_SATFINITE, __NV_E4M3));
-}
-
-// One CTA per row; K a multiple of 16.  Each thread's 16-byte chunks of the row (at most
-// kQHold of them: K <= 8 * kQThreads * kQHold = 16384) are loaded once, together, held in
-// registers through the max reduction and converted from there: one round trip to memory.
-// Chunks past that (longer rows) are read again for the conversion.
-static constexpr int kQHold = 8;
+// The decode step's row quantiser (see launch_quant_rows_e4m3 and quantize_rows_e4m3_cta).
 __global__ void __launch_bounds__(kQThreads)
-    quant_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ x, int K, uint8_t* __restrict__ xq,
-                           float* __restrict__ sx) {
+    quant_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ x, int T, int K,
+                           uint8_t* __restrict__ xq, float* __restrict__ sx,
+                           int32_t* __restrict__ q_ready) {
   __shared__ float wmax[kQThreads / 32];
-  const int row = blockIdx.x, tid = threadIdx.x;
-  const int nv = K / 8;  // 16-byte chunks of the row
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * K);
-  uint4 hold[kQHold];
-#pragma unroll
-  for (int i = 0; i < kQHold; ++i) {
-    const int e = tid + i * kQThreads;
-    hold[i] = e < nv ? __ldg(xr + e) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  float m = 0.f;
-#pragma unroll
-  for (int i = 0; i < kQHold; ++i) {
-    const uint32_t w[4] = {hold[i].x, hold[i].y, hold[i].z, hold[i].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
-  }
-  for (int e = tid + kQHold * kQThreads; e < nv; e += kQThreads) {
-    const uint4 v = __ldg(xr + e);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  if ((tid & 31) == 0) wmax[tid >> 5] = m;
-  __syncthreads();
-  float amax = 0.f;
-#pragma unroll
-  for (int w = 0; w < kQThreads / 32; ++w) amax = fmaxf(amax, wmax[w]);
-  const float s = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f;
-  if (tid == 0) sx[row] = s;
-  uint2* qr = reinterpret_cast<uint2*>(xq + (size_t)row * K);
-  auto convert = [&](const uint4& v) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t q[2] = {0u, 0u};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = to_e4m3(bf16_lo(w[i]), s), hi = to_e4m3(bf16_hi(w[i]), s);
-      q[i >> 1] |= (lo | (hi << 8)) << (16 * (i & 1));
-    }
-    return make_uint2(q[0], q[1]);
-  };
-#pragma unroll
-  for (int i = 0; i < kQHold; ++i) {
-    const int e = tid + i * kQThreads;
-    if (e < nv) qr[e] = convert(hold[i]);
-  }
-  for (int e = tid + kQHold * kQThreads; e < nv; e += kQThreads) qr[e] = convert(__ldg(xr + e));
+  // the previous forward's base GEMM may still read xq, and the previous kernel may have
+  // written x: wait for it; the low-rank kernel may then start at once (it relies on this
+  // wait for the previous GEMM, and the base GEMM waits for the rows counted on q_ready)
+  griddep_wait();
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows = quantize_rows_e4m3_cta<kQThreads, kQHold>(x, T, K, xq, sx, wmax, warp, lane);
+  if (q_ready) publish_rows(q_ready, rows);
 }
 
 cudaError_t launch_quant_rows_e4m3(const void* x, int T, int K, uint8_t* xq, float* sx,
-                                   cudaStream_t stream) {
+                                   int32_t* q_ready, int num_sms, cudaStream_t stream) {
   if (T < 1) return cudaSuccess;
   if (K % 16 != 0) return cudaErrorInvalidValue;
-  quant_rows_e4m3_kernel<<<T, kQThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), K,
-                                                       xq, sx);
-  return cudaGetLastError();
+  // it shares SMs with the low-rank kernel and the base GEMM launched behind it: the SMs
+  // must keep the shared-memory split a GEMM CTA needs, or that CTA waits for them to drain
+  static bool carveout[kAttrDevices] = {};
+  cudaError_t e = prefer_max_smem_carveout(quant_rows_e4m3_kernel, carveout);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(std::max(1, std::min(T, num_sms)));
+  cfg.blockDim = dim3(kQThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quant_rows_e4m3_kernel, static_cast<const __nv_bfloat16*>(x), T,
+                            K, xq, sx, q_ready);
 }
 
 // max |W[k][n]| over the rows [k0, k1) of each column, into amax[n] (float bits as int:

@@ -205,8 +205,10 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the first launch of a split batch lets the second one start while it runs (it waits for
-  // this one before its epilogue reads anything this one's predecessor wrote)
-  if (a.trigger_next) griddep_launch_dependents();
+  // this one before its epilogue reads anything this one's predecessor wrote); e4m3 base:
+  // only once this CTA has seen every row of xq (below), so that the second launch, which
+  // resets the row count, starts after every CTA of this one has read it
+  if (a.trigger_next && !FP8) griddep_launch_dependents();
   // Work units: output tiles, one per CTA (pair) slot and round: slot g runs units
   // g, g + G, g + 2 G, ... (delta mode: G is the number of units, one each).  CTA pairs:
   // the two CTAs of a pair are neighbours in x and cover 256 consecutive rows, CTA pr of
@@ -243,6 +245,18 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
       mbar_init(&xa_full[s], PAIR ? 2 : 1);  // pairs: one arrival from each CTA's epilogue
     }
     fence_mbar_init();
+    if (FP8 && a.q_ready) {
+      // the rows of xq come from the low-rank kernel running beside this one: wait until
+      // all M are counted (bounded: on a timeout the error flag is set and the loads go
+      // ahead), then order this thread's TMA loads after the writes seen
+      wait_flag_gpu(a.q_ready, a.M, a.err);
+      fence_proxy_async_global();
+      if (a.q_reset &&
+          atomicAdd(a.q_ready + 1, 1) == (int)(gridDim.x * gridDim.y * gridDim.z) - 1) {
+        atomicExch(a.q_ready, 0);  // every CTA of the batch's launches has seen the count
+        atomicExch(a.q_ready + 1, 0);
+      }
+    }
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_x);
@@ -259,6 +273,7 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
   }
   tc_fence_before();
   __syncthreads();
+  if (a.trigger_next && FP8) griddep_launch_dependents();
   // pairs: the peer's barriers are initialised before this CTA's loads and MMAs signal them
   if (PAIR) cluster_sync_all();
   tc_fence_after();
@@ -657,6 +672,15 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
         for (int c4 = 0; c4 < nq; ++c4) cp_async_16(xin + (size_t)c4 * kBM + rt, src + (size_t)c4 * kBM);
       }
       bool add_delta = false;  // delta mode: the row adds the low-rank term of the delta buffer
+      // e4m3 base: the row's scale (written by the row quantiser this kernel's producer
+      // waited for: read through L2) and the scales of this CTA's columns, staged in the
+      // v-mode slot tables (idle here), all requested before the wait below
+      float sxr = 0.f;
+      float* sw_s = reinterpret_cast<float*>(slot_bits);  // [bnc <= 2 * kBM]
+      if (FP8) {
+        sxr = row < a.M ? __ldcg(a.sx + row) : 0.f;
+        for (int i = et; i < bnc; i += 128) sw_s[i] = __ldg(a.sw + n0 + z * bnc + i);
+      }
       if (!vmode) {
         // only now the low-rank kernel's results are needed: the main loop and the split-K
         // exchange ran while it was still working
@@ -711,11 +735,10 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
           }
         }
         if (FP8) {  // the e4m3 product back to the x and W scales (sw is padded past N)
-          const float sxr = row < a.M ? __ldg(a.sx + row) : 0.f;
-          const float4* swp = reinterpret_cast<const float4*>(a.sw + nc);
+          const float4* swp = reinterpret_cast<const float4*>(sw_s + c);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float4 w = __ldg(swp + i);
+            const float4 w = swp[i];
             acc[i * 4 + 0] *= sxr * w.x;
             acc[i * 4 + 1] *= sxr * w.y;
             acc[i * 4 + 2] *= sxr * w.z;
@@ -1085,6 +1108,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
   whole.n_begin = 0;
   whole.n_end = a.N;
   whole.trigger_next = false;
+  whole.q_reset = true;  // the last launch of the batch resets the e4m3 row count
   // a last round at most half full: two launches (see delta_split_tiles)
   const int ntA = a.ex.mode == kExpandDelta && a.force_bn == 0
                       ? delta_split_tiles(plan, a.M, a.N, (k_bytes2 + kBK - 1) / kBK, a.num_sms)
@@ -1093,6 +1117,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
     GemmArgs first = whole, second = whole;
     first.n_end = ntA * plan.block_n;
     first.trigger_next = true;
+    first.q_reset = false;
     second.n_begin = first.n_end;
     const GemmPlan plan2{plan.block_n, 2, plan.pair};
     cudaError_t e = launch_one(first, plan, tmap_w3, tmap_bx3, stream);

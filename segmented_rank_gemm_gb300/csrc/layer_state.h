@@ -23,6 +23,8 @@ struct lora_layer {
   float* sx = nullptr;     // fp8: [T_max] row scales
   float* sw = nullptr;     // fp8: [N rounded up to 256] column scales, zero past N
   CUtensorMap tmap_xq;     // fp8: xq with (128 x 128) boxes
+  int32_t* q_ready = nullptr;  // fp8: {rows of xq written, GEMM CTAs that saw them} (zeroed)
+  bool q_dirty = false;    // fp8: a forward stopped between the BGMV and the GEMM launches
   void* A_pool = nullptr;  // [P][K] rank rows: slot s from row row_base[s]
   void* B_pool = nullptr;  // [P][N] rank rows
   int P = 0;               // pool rows: S * R, or the row budget of a pooled layer

@@ -440,6 +440,12 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) 
                : "memory");
 }
 
+// Order this thread's later async-proxy (TMA) accesses of global memory after the
+// generic-proxy writes it has observed (e.g. through an acquire load of a flag).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

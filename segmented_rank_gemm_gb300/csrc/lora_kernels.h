@@ -144,6 +144,11 @@ struct BgmvArgs {
   int32_t* err;         // the layer's device flags (debug-flavour bounds checks)
   int num_sms;
   bool per_column;      // some slot's columns carry different scales (a composition)
+  // e4m3 base: x [T][K] is also quantised per row into xq / sx by a launch of the row
+  // quantiser ahead of the BGMV kernel, which counts the rows on q_ready[0]; null: bf16
+  uint8_t* xq = nullptr;
+  float* sx = nullptr;
+  int32_t* q_ready = nullptr;
 };
 // Launched with programmatic stream serialization; it does not wait for the builder.
 cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream);
@@ -221,6 +226,12 @@ struct GemmArgs {
   const CUtensorMap* tmap_xq = nullptr;
   const float* sx = nullptr;  // [M]
   const float* sw = nullptr;  // [N rounded up to 256], zero past N
+  // xq and sx are written by the low-rank kernel running beside this one: q_ready[0] counts
+  // the rows made visible, and every CTA's producer waits (bounded) for it to reach M
+  // before its first load of xq.  The last launch of a batch (q_reset) also counts its CTAs
+  // on q_ready[1], and the last of them sets both words back to 0 for the next batch.
+  int32_t* q_ready = nullptr;
+  bool q_reset = false;
 };
 // tcgen05 / TMEM / TMA kernel (gemm_tc.cu).  tmap_w3 holds the layer's cached maps of the
 // packed weight for N tiles of 256, 128 and 64 rows (in that order); tmap_bx3 the maps of
@@ -235,9 +246,12 @@ constexpr int kTcTileN[3] = {256, 128, 64};
 // box and the 128-byte swizzle.
 cudaError_t encode_tmap_u8(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
 // x [T][K] bf16 -> xq [T][K] e4m3 and sx [T]: sx = max |x[row]| / 448 (1 for a zero row),
-// xq = e4m3(x / sx), round to nearest even, saturating.  One CTA per row; a plain launch.
+// xq = e4m3(x / sx), round to nearest even, saturating.  min(T, num_sms) CTAs, CTA b the
+// rows b, b + gridDim.x, ...; each CTA counts its rows on q_ready once their stores are
+// visible.  Programmatic dependent launch: it waits for the previous kernel on the stream
+// (which may read xq or write x) and then at once lets the next one launch.
 cudaError_t launch_quant_rows_e4m3(const void* x, int T, int K, uint8_t* xq, float* sx,
-                                   cudaStream_t stream);
+                                   int32_t* q_ready, int num_sms, cudaStream_t stream);
 // W [K][N] bf16 -> Wq [N][K] e4m3 (transposed, K-major) and sw [N]: per column as above.
 cudaError_t launch_quant_cols_e4m3(const void* W, int K, int N, uint8_t* Wq, float* sw,
                                    cudaStream_t stream);

@@ -71,7 +71,7 @@ void free_all(lora_layer* L) {
                   L->row_slot, L->perm, L->seg_offsets, L->seg_slot, L->tile_seg,
                   L->tile_row0, L->meta, L->err, L->v, L->delta, L->xk, L->sk_part,
                   L->sk_sync, L->x_stage, L->ids_stage, L->y_stage, L->row_base,
-                  L->xq, L->sx, L->sw};
+                  L->xq, L->sx, L->sw, L->q_ready};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (L->stage_free) cudaEventDestroy(L->stage_free);
@@ -200,7 +200,8 @@ static int create_layer(lora_layer_t** out, int K, int N, int num_slots, int max
             (!fp8 || (cudaMalloc(reinterpret_cast<void**>(&L->xq), (size_t)max_tokens * K) ==
                           cudaSuccess &&
                       dmalloc(&L->sx, max_tokens) == cudaSuccess &&
-                      dmalloc(&L->sw, n256) == cudaSuccess)) &&
+                      dmalloc(&L->sw, n256) == cudaSuccess &&
+                      dmalloc(&L->q_ready, 2) == cudaSuccess)) &&
             cudaMalloc(&L->A_pool, P * K * es) == cudaSuccess &&
             cudaMalloc(&L->B_pool, P * N * es) == cudaSuccess &&
             dmalloc(&L->row_base, S) == cudaSuccess &&
@@ -257,6 +258,7 @@ static int create_layer(lora_layer_t** out, int K, int N, int num_slots, int max
 
   if (fp8) {  // W quantised per column into [N][K] e4m3; x's map over the layer's xq
     if (cudaMemsetAsync(L->sw, 0, n256 * sizeof(float), stream) != cudaSuccess ||
+        cudaMemsetAsync(L->q_ready, 0, 2 * sizeof(int32_t), stream) != cudaSuccess ||
         launch_quant_cols_e4m3(W_dev, K, N, static_cast<uint8_t*>(L->Wp), L->sw, stream) !=
             cudaSuccess)
       return bail(LORA_ECUDA);
@@ -597,9 +599,16 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     ba.err = L->err;
     ba.num_sms = L->num_sms;
     ba.per_column = L->percol_slots > 0;
-    // e4m3 base: x quantised first (a plain launch after the previous forward); the BGMV
-    // waits for it, and the GEMM launches only once the BGMV has
-    if (L->fp8) LORA_CUDA(L, launch_quant_rows_e4m3(x_dev, T, L->K, L->xq, L->sx, stream));
+    if (L->fp8) {
+      // e4m3 base: the BGMV kernel quantises x's rows as it starts and counts them on
+      // q_ready, which the GEMM's loads wait for and its last CTA resets.  A forward that
+      // stopped between the two launches left the count set: clear it first.
+      if (L->q_dirty) LORA_CUDA(L, cudaMemsetAsync(L->q_ready, 0, 2 * sizeof(int32_t), stream));
+      L->q_dirty = true;
+      ba.xq = L->xq;
+      ba.sx = L->sx;
+      ba.q_ready = L->q_ready;
+    }
     LORA_CUDA(L, launch_bgmv_delta(ba, stream));
   } else if (bf16) {
     ShrinkTcArgs sa;
@@ -688,11 +697,13 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.tmap_xq = L->fp8 ? &L->tmap_xq : nullptr;
   ga.sx = L->sx;
   ga.sw = L->sw;
+  ga.q_ready = L->fp8 ? L->q_ready : nullptr;
   LORA_CUDA(L, trace_mark(L, 4, stream));
   if (bf16)
     LORA_CUDA(L, launch_gemm_tc(ga, L->tmap_w, L->Bx_pool ? L->tmap_bx : nullptr, stream));
   else
     LORA_CUDA(L, launch_gemm_simt_f32(ga, stream));
+  L->q_dirty = false;
   LORA_CUDA(L, trace_mark(L, 5, stream));
 
   if (!is_capturing(stream)) {

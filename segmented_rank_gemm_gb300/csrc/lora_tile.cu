@@ -346,11 +346,13 @@ __device__ __forceinline__ void stream_shrink(const __nv_bfloat16* __restrict__ 
 #pragma unroll
     for (int j = 0; j < RMAX; ++j) acc[q][j] = 0.f;
   for (int e = tid; e < K / 8; e += kStrThreads) {
-    // the loads of a chunk go out together: the rows' x, then a batch of 16 rank rows of A
+    // the loads of a chunk go out together: the rows' x (through L2: after the e4m3 row
+    // quantiser this kernel does not wait for the kernel that may have written x), then a
+    // batch of 16 rank rows of A
     uint4 xv[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q)
-      xv[q] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)rows[q] * K + e * 8));
+      xv[q] = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)rows[q] * K + e * 8));
 #pragma unroll
     for (int j0 = 0; j0 < RMAX; j0 += 16) {
       if (j0 >= r) break;
@@ -469,27 +471,14 @@ __global__ void __maxnreg__(120)
                        const int32_t* __restrict__ row_base, int pool_rows,
                        const float* __restrict__ scale,
                        const int32_t* __restrict__ rank, float* __restrict__ delta,
-                       int delta_rows, int32_t* __restrict__ err) {
+                       int delta_rows, int32_t* __restrict__ err, int wait_prev) {
   // launched while the previous kernel (the previous forward's base GEMM) still runs: wait
   // for it before reading x or writing delta, and only then let the base GEMM start (its
-  // main loop reads x, which that kernel may have written)
-  griddep_wait();
+  // main loop reads x, which that kernel may have written).  After the e4m3 row quantiser
+  // (wait_prev 0) there is nothing to wait for: that kernel waited for the previous GEMM
+  // before it let this one launch, and x is read through L2 below.
+  if (wait_prev) griddep_wait();
   griddep_launch_dependents();
-  // With at most one slot per CTA, CTA b requests slot b's A and B rows into L2 right away,
-  // before the ids are read: the DRAM traffic of every slot then overlaps the item-list
-  // setup below (the items' own prefetches find the lines present or in flight).
-  if (S <= (int)gridDim.x && (int)blockIdx.x < S && threadIdx.x < 32) {
-    // (pooled: the rows from the slot's first row, as many as the pool still holds; an
-    // empty slot has no first row and requests nothing)
-    const int rb0 = POOLED ? row_base[blockIdx.x] : (int)blockIdx.x * R;
-    const int rs = POOLED ? (rb0 < 0 ? 0 : min(min(R, RMAX), pool_rows - rb0)) : min(R, RMAX);
-    const size_t a_bytes = (size_t)rs * K * 2, b_bytes = (size_t)rs * N * 2;
-    const char* a0 = reinterpret_cast<const char*>(At_pool + (size_t)max(rb0, 0) * K);
-    const char* b0 = reinterpret_cast<const char*>(B_pool + (size_t)max(rb0, 0) * N);
-    const size_t off = (size_t)threadIdx.x << 15;
-    if (off < a_bytes) bulk_prefetch_l2(a0 + off, (uint32_t)min(a_bytes - off, (size_t)1 << 15));
-    if (off < b_bytes) bulk_prefetch_l2(b0 + off, (uint32_t)min(b_bytes - off, (size_t)1 << 15));
-  }
   extern __shared__ int grp_off[];  // [S + 1]: rows per slot, then first item of each slot
   __shared__ int rows_s[kStrGroup];
   __shared__ int warp_cnt[kStrThreads / 32];
@@ -500,6 +489,23 @@ __global__ void __maxnreg__(120)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (S + kStrThreads - 1) / kStrThreads;  // consecutive slots per thread
   const int q_begin = min(S, tid * per), q_end = min(S, q_begin + per);
+  // With at most one slot per CTA, CTA b requests slot b's A and B rows into L2 right away,
+  // before the ids are read: the DRAM traffic of every slot then overlaps the item-list
+  // setup below (the items' own prefetches find the lines present or in flight).  Measured:
+  // requesting only the slots the batch names, once the ids are counted, costs the decode
+  // step more (~1 us later) than the unused slots' reads do.
+  if (S <= (int)gridDim.x && (int)blockIdx.x < S && warp == 0) {
+    // (pooled: the rows from the slot's first row, as many as the pool still holds; an
+    // empty slot has no first row and requests nothing)
+    const int rb0 = POOLED ? row_base[blockIdx.x] : (int)blockIdx.x * R;
+    const int rs = POOLED ? (rb0 < 0 ? 0 : min(min(R, RMAX), pool_rows - rb0)) : min(R, RMAX);
+    const size_t a_bytes = (size_t)rs * K * 2, b_bytes = (size_t)rs * N * 2;
+    const char* a0 = reinterpret_cast<const char*>(At_pool + (size_t)max(rb0, 0) * K);
+    const char* b0 = reinterpret_cast<const char*>(B_pool + (size_t)max(rb0, 0) * N);
+    const size_t off = (size_t)lane << 15;
+    if (off < a_bytes) bulk_prefetch_l2(a0 + off, (uint32_t)min(a_bytes - off, (size_t)1 << 15));
+    if (off < b_bytes) bulk_prefetch_l2(b0 + off, (uint32_t)min(b_bytes - off, (size_t)1 << 15));
+  }
   // the ids and this thread's slots' loaded flags are requested together (one round trip)
   int ids[kIds];
 #pragma unroll
@@ -649,7 +655,8 @@ static cudaError_t launch_bgmv_stream_t(const BgmvArgs& a, cudaStream_t stream) 
                             static_cast<const __nv_bfloat16*>(a.x), a.token_slot, a.loaded, a.T,
                             a.K, a.N, a.R, a.S, static_cast<const __nv_bfloat16*>(a.At_pool),
                             static_cast<const __nv_bfloat16*>(a.B_pool), a.row_base,
-                            a.pool_rows, a.scale, a.rank, a.delta, a.delta_rows, a.err);
+                            a.pool_rows, a.scale, a.rank, a.delta, a.delta_rows, a.err,
+                            a.xq ? 0 : 1);
 }
 
 template <int RMAX, int ROWS>
@@ -667,6 +674,11 @@ static cudaError_t launch_bgmv_stream(const BgmvArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream) {
+  if (a.xq) {  // e4m3 base: the row quantiser first (it lets this kernel launch at once)
+    const cudaError_t e =
+        launch_quant_rows_e4m3(a.x, a.T, a.K, a.xq, a.sx, a.q_ready, a.num_sms, stream);
+    if (e != cudaSuccess) return e;
+  }
   if (a.R <= 32 && a.T <= kSlotMaxT && a.K % 8 == 0 && a.N % 8 == 0)
     return launch_bgmv_stream(a, stream);  // slot-major, registers only
   // row-major: cluster of cs CTAs per row: 4 normally, fewer when K or N is small

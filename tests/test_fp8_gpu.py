@@ -109,3 +109,61 @@ def test_fp8_limits():
     W = torch.zeros(64, 64, dtype=BF16, device="cuda")
     with pytest.raises(LoraError):
         LoraLayer(W, 2, 8, 513, fp8_base=True)  # prefill batches: not served
+
+
+def test_fp8_back_to_back_forwards_and_split_batches():
+    # The BGMV kernel quantises x's rows as it starts and counts them; the GEMM's loads wait
+    # for the count, and the last CTA of the batch's last GEMM launch resets it.  Several
+    # forwards in a row on one stream, each with new x, on shapes whose automatic plan runs
+    # the GEMM as one launch and as two (a last round at most half full: N = 14336).
+    for T, K, N in [(512, 4096, 14336), (300, 1024, 4104), (37, 512, 264)]:
+        wl = workloads.synthetic(740 + T, T, K, N, S=7, ranks=[16, 4, 8, 16, 1, 12, 16], R=16,
+                                 base_frac=0.1)
+        layer = _layer(wl)
+        rows = np.arange(0, T, 7)
+        try:
+            for rep in range(3):
+                g = torch.Generator().manual_seed(9000 + 31 * T + rep)
+                wl.x = (torch.randn(T, K, generator=g) * (0.5 + rep)).to(BF16)
+                y = layer(wl.x.cuda(), wl.token_slot.cuda())
+                torch.cuda.synchronize()
+                assert layer.status() == 0, (T, K, N, rep)
+                assert_parity(y[rows], _ref(wl, rows), BF16,
+                              what="fp8 T=%d K=%d N=%d forward %d" % (T, K, N, rep))
+        finally:
+            layer.close()
+
+
+def test_fp8_wide_rank_quantises_in_its_own_launch():
+    # rank width 64: the decode BGMV runs row-major, and x is quantised by a launch of its
+    # own before it (counted the same way)
+    wl = workloads.synthetic(760, 200, 1024, 520, S=5, ranks=[64, 33, 8, 64, 1], R=64,
+                             base_frac=0.1)
+    layer = _layer(wl)
+    try:
+        for rep in range(2):
+            y = layer(wl.x.cuda(), wl.token_slot.cuda())
+            torch.cuda.synchronize()
+            assert layer.status() == 0
+            assert_parity(y, _ref(wl), BF16, what="fp8 rank width 64, forward %d" % rep)
+    finally:
+        layer.close()
+
+
+def test_fp8_forward_after_a_failed_launch():
+    # a GEMM plan refused at launch time (an empty K range) fails the forward after the BGMV
+    # kernel counted its rows; the next forward clears the count and is exact
+    from segmented_rank_gemm_gb300.lora import LoraError
+    wl = workloads.synthetic(770, 64, 128, 200, S=3, ranks=[8, 4, 16], R=16, base_frac=0.2)
+    layer = _layer(wl)
+    try:
+        layer.set_gemm_plan(128, 4, 0)  # K = 128 e4m3 elements: one K block, no 4-way split
+        with pytest.raises(LoraError):
+            layer(wl.x.cuda(), wl.token_slot.cuda())
+        layer.set_gemm_plan(0)
+        y = layer(wl.x.cuda(), wl.token_slot.cuda())
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        assert_parity(y, _ref(wl), BF16, what="fp8 forward after a refused plan")
+    finally:
+        layer.close()
