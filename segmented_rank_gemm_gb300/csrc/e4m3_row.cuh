@@ -20,14 +20,34 @@ __device__ __forceinline__ uint8_t to_e4m3(float v, float s) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(v, s), __NV_SATFINITE, __NV_E4M3));
 }
 
-// e4m3 codes of a / s (low byte) and b / s (high byte): each quotient correctly rounded in
-// fp32, then one conversion instruction for the pair (round to nearest even, saturating at
-// +-448: the same decisions as to_e4m3).
-__device__ __forceinline__ uint32_t to_e4m3x2(float a, float b, float s) {
-  const float qa = __fdiv_rn(a, s), qb = __fdiv_rn(b, s);
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(qb), "f"(qa));
-  return r;
+// Row scales whose quotients take the fast path below.
+__device__ __forceinline__ bool fast_scale(float s) { return s >= 0x1p-110f && s <= 0x1p110f; }
+
+// v / s for an element v of a row whose scale is s (|v| <= 448 s), given r = RN(1 / s).
+// Fast path (fast_scale(s)): Markstein's correction (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): q0 = RN(v r), the remainder v - q0 s exactly by one FMA, then q0 + rem r rounded
+// once.  Over every bf16 v and every scale s = RN(a / 448) of a bf16 a >= |v| in that
+// range, the e4m3 value of this quotient equals the e4m3 value of the correctly rounded
+// one (checked exhaustively on the host); the quotients themselves differ only for
+// subnormal v, whose quotients are far below e4m3's smallest step.  Otherwise the
+// correctly rounded division.
+__device__ __forceinline__ float row_quotient(float v, float s, float r, bool fast) {
+  if (fast) {
+    const float q0 = __fmul_rn(v, r);
+    const float rem = __fmaf_rn(-q0, s, v);
+    return __fmaf_rn(rem, r, q0);
+  }
+  return __fdiv_rn(v, s);
+}
+
+// e4m3 codes of a / s (low byte) and b / s (high byte) (row_quotient), one conversion
+// instruction for the pair: round to nearest even, saturating at +-448, as to_e4m3.
+__device__ __forceinline__ uint32_t to_e4m3x2(float a, float b, float s, float r, bool fast) {
+  const float qa = row_quotient(a, s, r, fast), qb = row_quotient(b, s, r, fast);
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(qb), "f"(qa));
+  return c;
 }
 
 // The rows blockIdx.x, blockIdx.x + gridDim.x, ... (< T) quantised by the calling CTA of NT
@@ -87,6 +107,8 @@ __device__ __forceinline__ int quantize_rows_e4m3_cta(const __nv_bfloat16* __res
     float amax = 0.f;
     for (int w = warp - sub; w < warp - sub + wpr; ++w) amax = fmaxf(amax, wmax[w]);
     const float s = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f;
+    const bool fast = fast_scale(s);
+    const float rcp = fast ? __frcp_rn(s) : 0.f;
     if (active) {
       if (t == 0) sx[row] = s;
       uint2* qr = reinterpret_cast<uint2*>(xq + (size_t)row * K);
@@ -95,7 +117,7 @@ __device__ __forceinline__ int quantize_rows_e4m3_cta(const __nv_bfloat16* __res
         uint32_t qq[2] = {0u, 0u};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          qq[i >> 1] |= to_e4m3x2(bf16_lo(w[i]), bf16_hi(w[i]), s) << (16 * (i & 1));
+          qq[i >> 1] |= to_e4m3x2(bf16_lo(w[i]), bf16_hi(w[i]), s, rcp, fast) << (16 * (i & 1));
         return make_uint2(qq[0], qq[1]);
       };
 #pragma unroll
