@@ -70,18 +70,45 @@ static constexpr int kABytes = kBM * kBK * 2;
 
 // Add the row's delta (delta mode, adapted rows) to 32 accumulator columns starting at
 // global column n and store them as bf16.
-__device__ __forceinline__ void epilogue_chunk32(float (&acc)[32], const GemmArgs& a, int row,
-                                                 int n, bool add_delta, const float4* d,
-                                                 __nv_bfloat16* yrow) {
-  if (add_delta) {
+// The 32 accumulator columns at TMEM address taddr (this thread's lane) as floats.
+__device__ __forceinline__ void tmem_acc32(uint32_t taddr, float (&acc)[32]) {
+  uint32_t raw[32];
+  tmem_ld_32x32b_x32(taddr, raw);
+  tmem_ld_wait();
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      acc[q * 4 + 0] += d[q].x;
-      acc[q * 4 + 1] += d[q].y;
-      acc[q * 4 + 2] += d[q].z;
-      acc[q * 4 + 3] += d[q].w;
-    }
+  for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(raw[i]);
+}
+
+// acc += columns c .. c + 31 of a partial block ([bnc / 4][128 rows] float4; blk points at
+// this thread's row of chunk 0).
+__device__ __forceinline__ void add_block32(float (&acc)[32], const float4* blk, int c) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 v = blk[(size_t)((c >> 2) + i) * 128];
+    acc[i * 4 + 0] += v.x;
+    acc[i * 4 + 1] += v.y;
+    acc[i * 4 + 2] += v.z;
+    acc[i * 4 + 3] += v.w;
   }
+}
+
+// The e4m3 product back to the x and W scales: acc[i] *= sx * sw[i] (sw: 32 column scales).
+__device__ __forceinline__ void scale32(float (&acc)[32], float sxr, const float* sw) {
+  const float4* swp = reinterpret_cast<const float4*>(sw);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 w = swp[i];
+    acc[i * 4 + 0] *= sxr * w.x;
+    acc[i * 4 + 1] *= sxr * w.y;
+    acc[i * 4 + 2] *= sxr * w.z;
+    acc[i * 4 + 3] *= sxr * w.w;
+  }
+}
+
+// Columns n .. n + 31 of row `row` of y (bf16, 16-byte stores; rows >= M and columns >= N
+// are not written).
+__device__ __forceinline__ void store_y32(const float (&acc)[32], const GemmArgs& a, int row,
+                                          int n, __nv_bfloat16* yrow) {
   if (row < a.M) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -173,7 +200,8 @@ template <int BN, bool PAIR, bool VMODE, bool FP8 = false>
 __global__ void __maxnreg__(VMODE ? 168 : 136)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_w,
-                   const __grid_constant__ CUtensorMap tmap_bx, GemmArgs a, int stages,
+                   const __grid_constant__ CUtensorMap tmap_bx,
+                   const __grid_constant__ CUtensorMap tmap_delta, GemmArgs a, int stages,
                    int xscr_bytes, int group_m, int mtp, int nt, int full_rounds,
                    int sk_slots) {
   static_assert(!(FP8 && VMODE), "the e4m3 base runs in delta mode only");
@@ -242,7 +270,9 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
     mbar_init(xinfo_bar, 1);
     for (int s = 0; s < stages; ++s) {
       mbar_init(&xgrant[s], 1);
-      mbar_init(&xa_full[s], PAIR ? 2 : 1);  // pairs: one arrival from each CTA's epilogue
+      // v-mode pairs: one arrival from each CTA's epilogue; delta mode counts one arrival
+      // (the epilogue's delta-tile loads may use it)
+      mbar_init(&xa_full[s], PAIR && vmode ? 2 : 1);
     }
     fence_mbar_init();
     if (FP8 && a.q_ready) {
@@ -620,7 +650,7 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
       if (cs > 1) {
         float4* xk_tile =
             reinterpret_cast<float4*>(a.xk) + (size_t)(mt_i * nt + nt_i) * cs * cs * nq * kBM;
-        xk_in = xk_tile + (size_t)z * cs * nq * kBM + rt;
+        xk_in = xk_tile + (size_t)z * cs * nq * kBM;
         for (int d = 0; d < cs; ++d) {
           if (d == z) continue;
           float4* blk = xk_tile + (size_t)(d * cs + z) * nq * kBM + rt;
@@ -646,45 +676,68 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
       }
 
       // ---------------- the epilogue's inputs, landed in shared memory ----------------
-      // (delta mode, one tile per CTA: the ring is idle once the accumulator is complete.)
-      // xin: the cs - 1 partial blocks addressed to this CTA ([j][bnc / 4][128 rows] float4,
-      // as in the scratch); dsm: the tile's delta rows ([128][bnc] fp32, 16-byte chunks
-      // XOR-swizzled by row & 7).  Both arrive by cp.async and are waited for once, so
-      // their latencies overlap instead of following one another chunk by chunk.
-      // (A stream-K head is its slot's last segment, so the ring is idle for it too: its
-      // tail's partial lands there the same way, as the one extra block.)
+      // (Delta mode has one tile per CTA, and a stream-K head is its slot's last segment: the
+      // ring is idle once the accumulator is complete, and holds these.)
       const int n_extra = cs > 1 ? cs - 1 : (sk_src >= 0 ? 1 : 0);
       float4* xin = reinterpret_cast<float4*>(stage_base);
-      float* dsm = reinterpret_cast<float*>(stage_base + (size_t)(cs - 1) * nq * kBM * 16);
-      if (cs > 1) {
-        for (int q = 0, j = 0; q < cs; ++q) {
-          if (q == z) continue;
-          const float4* src = xk_in + (size_t)q * nq * kBM;
-          float4* dst = xin + (size_t)j * nq * kBM + rt;
-          for (int c4 = 0; c4 < nq; ++c4)
-            cp_async_16(dst + (size_t)c4 * kBM, src + (size_t)c4 * kBM);
-          ++j;
-        }
-      } else if (sk_src >= 0) {
-        named_barrier(1, 128);  // the flag was seen by thread 0 of the epilogue
-        const float4* src = reinterpret_cast<const float4*>(a.sk_part) +
-                            (size_t)sk_src * (BN / 4) * kBM + rt;
-        for (int c4 = 0; c4 < nq; ++c4) cp_async_16(xin + (size_t)c4 * kBM + rt, src + (size_t)c4 * kBM);
-      }
-      bool add_delta = false;  // delta mode: the row adds the low-rank term of the delta buffer
-      // e4m3 base: the row's scale (written by the row quantiser this kernel's producer
-      // waited for: read through L2) and the scales of this CTA's columns, staged in the
-      // v-mode slot tables (idle here), all requested before the wait below
-      float sxr = 0.f;
-      float* sw_s = reinterpret_cast<float*>(slot_bits);  // [bnc <= 2 * kBM]
-      if (FP8) {
-        sxr = row < a.M ? __ldcg(a.sx + row) : 0.f;
-        for (int i = et; i < bnc; i += 128) sw_s[i] = __ldg(a.sw + n0 + z * bnc + i);
-      }
+      __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.y) + (size_t)row * a.N;
+      const int cbase = z * bnc;  // first accumulator column this CTA finishes
       if (!vmode) {
-        // only now the low-rank kernel's results are needed: the main loop and the split-K
-        // exchange ran while it was still working
+        // ---- delta mode ----
+        // xin: the cs - 1 partial blocks addressed to this CTA ([j][bnc / 4][128 rows]
+        // float4, as in the scratch), a bulk copy each; dsm: the tile's delta rows as
+        // [bnc / 32][128 rows][32] fp32 (16-byte chunk q of row r at chunk q ^ (r & 7): the
+        // 128-byte swizzle of a TMA box), a tensor load per 32 columns, each counted on its
+        // own barrier (the v-mode stage barriers xgrant and xa_full, idle here), so that the
+        // first columns are finished while the rest land.  (y leaves by 16-byte stores of
+        // each thread's row: staging it for TMA stores measured no faster.)
+        const uint32_t blk_bytes = (uint32_t)nq * kBM * 16;
+        const int nbox = bnc / 32;
+        float* dsm = reinterpret_cast<float*>(stage_base + (size_t)(cs - 1) * blk_bytes);
+        uint64_t* dbar = xgrant;  // [nbox <= 2 * stages]
+        if (cs > 1 && et == 0) {
+          // the peers' blocks were stored by generic-proxy writes seen through the cluster
+          // barrier: order the bulk copies (async proxy) after them
+          fence_proxy_async_global();
+          mbar_arrive_expect_tx(xinfo_bar, (uint32_t)(cs - 1) * blk_bytes);
+          for (int q = 0, j = 0; q < cs; ++q) {
+            if (q == z) continue;
+            bulk_load_g2s(xin + (size_t)j * nq * kBM, xk_in + (size_t)q * nq * kBM, blk_bytes,
+                          xinfo_bar);
+            ++j;
+          }
+        }
+        // e4m3 base: the row's scale (written by the row quantiser this kernel's producer
+        // waited for: read through L2) and this CTA's column scales, staged in the v-mode
+        // slot tables (idle here)
+        float sxr = 0.f;
+        float* sw_s = reinterpret_cast<float*>(slot_bits);  // [bnc <= 2 * kBM]
+        if (FP8) {
+          sxr = row < a.M ? __ldcg(a.sx + row) : 0.f;
+          for (int i = et; i < bnc; i += 128) sw_s[i] = __ldg(a.sw + n0 + cbase + i);
+        }
+        // (one tile per CTA: every barrier below is in its first phase)
+        if (cs > 1 && !mbar_wait(xinfo_bar, 0u, a.err)) ok = false;
+        named_barrier(1, 128);  // the column scales staged
+        // While the low-rank kernel may still run: this CTA's columns of the product, the
+        // peers' partials added and (e4m3) scaled, back into block 0 (row rt's own entries)
+        if (cs > 1) {
+#pragma unroll 1
+          for (int c = 0; c < bnc; c += 32) {
+            float acc[32];
+            tmem_acc32(tmem_row + cbase + c, acc);
+            for (int j = 0; j < cs - 1; ++j) add_block32(acc, xin + (size_t)j * nq * kBM + rt, c);
+            if (FP8) scale32(acc, sxr, sw_s + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              xin[(size_t)((c >> 2) + i) * kBM + rt] =
+                  make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+          }
+        }
+        // only now the low-rank kernel's results are needed: the main loop, the split-K
+        // exchange and the partial sums ran while it was still working
         griddep_wait();
+        bool add_delta = false;  // the row adds the low-rank term of the delta buffer
         if (row < a.M) {
           const int t = a.ex.token_slot[row];
           add_delta = t >= 0 && t < a.ex.S && a.ex.loaded[t] != 0;
@@ -695,63 +748,64 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
           }
         }
         if (add_delta && !LORA_IN_BOUNDS(row < a.ex.delta_rows, a.err)) add_delta = false;
-        // the tile's delta rows (the buffer holds the batch's rows, at most 512):
-        // consecutive threads fetch consecutive 16-byte chunks of a row
-        const int cfirst = n0 + z * bnc;  // first column this CTA finishes
-        const int dr_end = min(a.M, a.ex.delta_rows);
-        for (int idx = et; idx < kBM * nq; idx += 128) {
-          const int r = idx / nq, ch = idx - r * nq;
-          const int gr = m0 + r, gc = cfirst + ch * 4;
-          if (gr < dr_end && gc < a.N)
-            cp_async_16(dsm + (size_t)r * bnc + ((ch ^ (r & 7)) << 2),
-                        a.ex.delta + (size_t)gr * a.N + gc);
+        // the tile's delta rows (the buffer holds the batch's rows, at most 512; the map
+        // fills zeros past its rows and past N)
+        const int cfirst = n0 + cbase;  // first column this CTA finishes
+        if (et == 0) {
+          fence_proxy_async_global();  // written by the low-rank kernel (waited for above)
+          for (int h = 0; h < nbox; ++h) {
+            mbar_arrive_expect_tx(&dbar[h], (uint32_t)kBM * 32 * 4);
+            tma_load_2d(dsm + (size_t)h * kBM * 32, &tmap_delta, &dbar[h], cfirst + 32 * h, m0);
+          }
         }
-      }
-      if (n_extra > 0 || !vmode) {
-        cp_async_wait_all();
-        named_barrier(1, 128);  // delta rows fetched by the other epilogue threads
-      }
-      __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(a.y) + (size_t)row * a.N;
-      const int cbase = z * bnc;  // first accumulator column this CTA finishes
-      const float* drow = dsm + (size_t)rt * bnc;
 #pragma unroll 1
-      for (int c = 0; c < bnc; c += 32) {
-        const int nc = n0 + cbase + c;
-        uint32_t raw[32];
-        tmem_ld_32x32b_x32(tmem_row + cbase + c, raw);
-        tmem_ld_wait();
-        float acc[32];
+        for (int c = 0; c < bnc; c += 32) {
+          float acc[32];
+          if (cs > 1) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(raw[i]);
-        for (int j = 0; j < n_extra; ++j) {
-          const float4* blk = xin + (size_t)j * nq * kBM + rt;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 v = blk[(size_t)((c >> 2) + i) * kBM];
-            acc[i * 4 + 0] += v.x;
-            acc[i * 4 + 1] += v.y;
-            acc[i * 4 + 2] += v.z;
-            acc[i * 4 + 3] += v.w;
+            for (int i = 0; i < 8; ++i) {
+              const float4 v = xin[(size_t)((c >> 2) + i) * kBM + rt];
+              acc[4 * i] = v.x;
+              acc[4 * i + 1] = v.y;
+              acc[4 * i + 2] = v.z;
+              acc[4 * i + 3] = v.w;
+            }
+          } else {
+            tmem_acc32(tmem_row + cbase + c, acc);
+            if (FP8) scale32(acc, sxr, sw_s + c);
           }
-        }
-        if (FP8) {  // the e4m3 product back to the x and W scales (sw is padded past N)
-          const float4* swp = reinterpret_cast<const float4*>(sw_s + c);
+          if (!mbar_wait(&dbar[c >> 5], 0u, a.err)) ok = false;
+          if (add_delta) {
+            const float* dbox = dsm + (size_t)(c >> 5) * kBM * 32 + (size_t)rt * 32;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 w = swp[i];
-            acc[i * 4 + 0] *= sxr * w.x;
-            acc[i * 4 + 1] *= sxr * w.y;
-            acc[i * 4 + 2] *= sxr * w.z;
-            acc[i * 4 + 3] *= sxr * w.w;
+            for (int q = 0; q < 8; ++q) {
+              const float4 d = *reinterpret_cast<const float4*>(dbox + ((q ^ (rt & 7)) << 2));
+              acc[4 * q] += d.x;
+              acc[4 * q + 1] += d.y;
+              acc[4 * q + 2] += d.z;
+              acc[4 * q + 3] += d.w;
+            }
           }
+          store_y32(acc, a, row, cfirst + c, yrow);
         }
-        float4 d[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          d[q] = add_delta
-                     ? *reinterpret_cast<const float4*>(drow + ((((c >> 2) + q) ^ (rt & 7)) << 2))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        epilogue_chunk32(acc, a, row, nc, add_delta, d, yrow);
+      } else {
+        // ---- v mode: a stream-K head adds its tail's partial (one block) ----
+        if (sk_src >= 0) {
+          named_barrier(1, 128);  // the flag was seen by thread 0 of the epilogue
+          const float4* src = reinterpret_cast<const float4*>(a.sk_part) +
+                              (size_t)sk_src * (BN / 4) * kBM + rt;
+          for (int c4 = 0; c4 < nq; ++c4)
+            cp_async_16(xin + (size_t)c4 * kBM + rt, src + (size_t)c4 * kBM);
+          cp_async_wait_all();
+          named_barrier(1, 128);
+        }
+#pragma unroll 1
+        for (int c = 0; c < bnc; c += 32) {
+          float acc[32];
+          tmem_acc32(tmem_row + cbase + c, acc);
+          for (int j = 0; j < n_extra; ++j) add_block32(acc, xin + (size_t)j * nq * kBM + rt, c);
+          store_y32(acc, a, row, n0 + cbase + c, yrow);
+        }
       }
       // this buffer is drained: the MMAs may fill it with tile k + 2 (pairs: both CTAs'
       // epilogues arrive on the even CTA's barrier)
@@ -817,6 +871,20 @@ cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_tmap_delta(CUtensorMap* map, const float* base, int rows, int N) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  if (N % 4 != 0 || rows < 1) return cudaErrorInvalidValue;  // rows start on 16-byte boundaries
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
+  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kBM)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -1004,7 +1072,9 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   while (stages > 2 && tc_smem_bytes(BN, PAIR, stages, xscr) > budget) --stages;
   const size_t smem = tc_smem_bytes(BN, PAIR, stages, xscr);
   if (smem > budget) return cudaErrorInvalidConfiguration;
-  // the epilogue lands its split-K partials and delta rows (128 x BN fp32) in the ring
+  // the epilogue lands its split-K partials and delta rows (128 x BN fp32) in the ring, and
+  // counts each 32-column delta box on one of the 2 * stages v-mode stage barriers
+  if (a.ex.mode == kExpandDelta && 2 * stages < BN / cs / 32) return cudaErrorInvalidConfiguration;
   const size_t stage = (size_t)kABytes + (size_t)(PAIR ? BN / 2 : BN) * kBK * 2;
   if ((cs > 1 || a.ex.mode == kExpandDelta || a.sk_part) &&
       (size_t)stages * stage < (size_t)kBM * BN * 4)
@@ -1050,8 +1120,11 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   const size_t band_rows = (size_t)kBM * (PAIR ? 2 : 1);
   const int group_m =
       std::max(1, std::min(mtp, (int)((32u << 20) / ((size_t)a.K * band_rows * 2))));
+  // delta mode: the delta tile arrives through the delta buffer's map
+  if (!VMODE && !a.tmap_delta) return cudaErrorInvalidValue;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, PAIR, VMODE, FP8>, tmap_x, tmap_w, tmap_bx,
-                            a, stages, xscr, group_m, mtp, nt, full_rounds, sk_slots);
+                            VMODE ? tmap_w : *a.tmap_delta, a, stages, xscr, group_m, mtp, nt,
+                            full_rounds, sk_slots);
 }
 
 static cudaError_t launch_variant_fp8(const GemmArgs& a, const GemmPlan& plan,

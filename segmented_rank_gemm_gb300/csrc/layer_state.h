@@ -51,6 +51,7 @@ struct lora_layer {
   float* v = nullptr;            // [v_planes][T_max][R] fp32, scaled by alpha / r (v mode)
   int v_planes = 1;              // K-split partial planes of v (bf16: tensor-core shrink)
   float* delta = nullptr;        // [min(T_max, kDeltaMaxT)][N] fp32 (delta mode, bf16)
+  CUtensorMap tmap_delta;        // delta with (32 x 128) boxes (valid when delta is set)
   float* xk = nullptr;           // split-K exchange scratch of the base GEMM (delta mode)
   float* sk_part = nullptr;      // stream-K partials of the base GEMM (v mode)
   int32_t* sk_sync = nullptr;    // stream-K epoch, exit count and flags (zeroed)

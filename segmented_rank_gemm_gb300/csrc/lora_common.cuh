@@ -152,6 +152,17 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, ui
       : "memory");
 }
 
+// Contiguous global -> shared copy of `bytes` (multiple of 16; both addresses 16-byte
+// aligned) by the TMA unit, counted on `bar`.
+__device__ __forceinline__ void bulk_load_g2s(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Pair form: the data lands in this CTA's shared memory, the completed bytes are counted on
 // `bar_cluster` (a shared::cluster address, here the even CTA's barrier of the pair).
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tmap,

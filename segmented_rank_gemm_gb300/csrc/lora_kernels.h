@@ -232,6 +232,9 @@ struct GemmArgs {
   // on q_ready[1], and the last of them sets both words back to 0 for the next batch.
   int32_t* q_ready = nullptr;
   bool q_reset = false;
+  // delta mode (required there): the map of the delta buffer (encode_tmap_delta), through
+  // which the epilogue's delta tile arrives by TMA
+  const CUtensorMap* tmap_delta = nullptr;
 };
 // tcgen05 / TMEM / TMA kernel (gemm_tc.cu).  tmap_w3 holds the layer's cached maps of the
 // packed weight for N tiles of 256, 128 and 64 rows (in that order); tmap_bx3 the maps of
@@ -257,6 +260,10 @@ cudaError_t launch_quant_cols_e4m3(const void* W, int K, int N, uint8_t* Wq, flo
                                    cudaStream_t stream);
 // Encode a 2-D bf16 tensor map for a K-major [rows, K] matrix with a (64 x box_rows) box.
 cudaError_t encode_tmap_bf16(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
+// Encode the map of an fp32 delta buffer [rows][N] (N a multiple of 4) with (32 x 128)
+// boxes and the 128-byte swizzle: a box lands as 128 rows of 128 bytes, 16-byte chunk q of
+// row r at chunk q ^ (r & 7); reads past the buffer fill zeros.
+cudaError_t encode_tmap_delta(CUtensorMap* map, const float* base, int rows, int N);
 struct GemmPlan {
   int block_n;  // N tile: 256, 128 or 64
   int ksplit;   // K ranges per output tile, 1..4

@@ -288,6 +288,10 @@ static int create_layer(lora_layer_t** out, int K, int N, int num_slots, int max
         cudaSuccess)
       return bail(LORA_ECUDA);
   }
+  // the decode GEMM's epilogue reads its delta tile through this map
+  if (L->delta && encode_tmap_delta(&L->tmap_delta, L->delta, std::min(max_tokens, kDeltaMaxT),
+                                    N) != cudaSuccess)
+    return bail(LORA_ECUDA);
   if (cudaStreamSynchronize(stream) != cudaSuccess) return bail(LORA_ECUDA);
   *out = L;
   return LORA_OK;
@@ -698,6 +702,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.sx = L->sx;
   ga.sw = L->sw;
   ga.q_ready = L->fp8 ? L->q_ready : nullptr;
+  ga.tmap_delta = L->delta ? &L->tmap_delta : nullptr;
   LORA_CUDA(L, trace_mark(L, 4, stream));
   if (bf16)
     LORA_CUDA(L, launch_gemm_tc(ga, L->tmap_w, L->Bx_pool ? L->tmap_bx : nullptr, stream));
