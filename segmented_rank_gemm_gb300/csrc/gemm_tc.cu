@@ -204,7 +204,11 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
                    const __grid_constant__ CUtensorMap tmap_delta, GemmArgs a, int stages,
                    int xscr_bytes, int group_m, int mtp, int nt, int full_rounds,
                    int sk_slots) {
-  static_assert(!(FP8 && VMODE), "the e4m3 base runs in delta mode only");
+  // e4m3 base in v mode: the low-rank expand blocks (bf16) accumulate apart from the base
+  // (e4m3) blocks, in a second accumulator of BN columns beside each buffer's, so that the
+  // epilogue scales the base product alone: TMEM holds 2 x 2 x BN columns, BN <= 128
+  static_assert(!(FP8 && VMODE) || BN <= 128, "e4m3 v mode: tiles of at most 128 columns");
+  constexpr int kAccCols = FP8 && VMODE ? 2 * BN : BN;  // TMEM columns of one buffer
   constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of the W (or B expand) tile this CTA loads
   constexpr int kBBytes = kBRows * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
@@ -221,7 +225,10 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
   int* uslot = reinterpret_cast<int*>(slot_bits + kBM);  // [128]
   int* wsum = uslot + kBM;                               // [4] per epilogue warp
   int* x_blocks = wsum + 4;                              // expand blocks of this tile
-  uint64_t* bars = reinterpret_cast<uint64_t*>(x_blocks + 2);
+  // e4m3: [BN] column scales, read as float4 (16-byte aligned: slot_bits is, and the four
+  // words from x_blocks on round the tables to a multiple of 16 bytes)
+  float* sw_tile = reinterpret_cast<float*>(x_blocks + 4);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sw_tile + (FP8 ? BN : 0));
   uint64_t* full = bars;
   uint64_t* empty = bars + stages;
   uint64_t* tmem_full = bars + 2 * stages;       // [2] accumulator buffer complete
@@ -297,9 +304,9 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
   // other with the next tile
   if (warp == 1) {
     if (PAIR)
-      tmem_alloc_pair(tmem_holder, 2 * BN);
+      tmem_alloc_pair(tmem_holder, 2 * kAccCols);
     else
-      tmem_alloc(tmem_holder, 2 * BN);
+      tmem_alloc(tmem_holder, 2 * kAccCols);
   }
   tc_fence_before();
   __syncthreads();
@@ -395,6 +402,7 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
     if (lane == 0 && pr == 0) {
       constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(PAIR ? 2 * kBM : kBM, BN)
                                      : idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN);
+      constexpr uint32_t idesc_x = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN);  // expand blocks
       // descriptors built once: the start-address field counts 16-byte units, so a stage
       // is + s * kStageBytes / 16 and a 16-wide K step inside the 128-byte row is + 2
       const uint64_t a_desc0 = smem_desc_sw128(smem_u32(stage_base));
@@ -402,8 +410,9 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
       int s = 0;
       uint32_t ph = 0, xa_par = 0;  // xa_par: bit s = parity of stage s's next xa_full phase
       bool ok = true;
-      // the 16-wide K chunks of `chunks` (bit kk) of a stage; `first` starts the accumulator
-      auto mma4 = [&](uint32_t d_tmem, int stage, bool first, unsigned chunks) {
+      // the 16-wide K chunks of `chunks` (bit kk) of a stage; `first` starts the accumulator;
+      // `expand`: a low-rank expand block (bf16 operands whatever the base's)
+      auto mma4 = [&](uint32_t d_tmem, int stage, bool first, unsigned chunks, bool expand) {
         const uint64_t stage_off = (uint64_t)(stage * (kStageBytes >> 4));
         const uint64_t a_desc = a_desc0 + stage_off, b_desc = b_desc0 + stage_off;
 #pragma unroll
@@ -411,18 +420,18 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
           if (!((chunks >> kk) & 1u)) continue;
           const uint32_t acc = (first && kk == 0) ? 0u : 1u;
           // (a 32-byte step of the row either way: 16 bf16 or 32 e4m3 elements of K)
-          if (FP8 && PAIR)
+          if (FP8 && !expand && PAIR)
             tc_mma_f8_pair(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
                            idesc, acc);
-          else if (FP8)
+          else if (FP8 && !expand)
             tc_mma_f8(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2), idesc,
                       acc);
           else if (PAIR)
             tc_mma_bf16_pair(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
-                             idesc, acc);
+                             FP8 ? idesc_x : idesc, acc);
           else
-            tc_mma_bf16(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2), idesc,
-                        acc);
+            tc_mma_bf16(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2),
+                        FP8 ? idesc_x : idesc, acc);
         }
         if (PAIR)
           tc_commit_pair_mc(&empty[stage], pair_mask);  // frees the stage in both CTAs
@@ -434,7 +443,7 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
         int u, k0, k1;
         if (!seg_at(k, g0, G, U, nkb, full_rounds, sk_slots, u, k0, k1)) break;
         const int b = k & 1;
-        const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(b * kAccCols);
         // the epilogue has drained this buffer's previous tile (tile k - 2); pairs: both
         // CTAs' epilogues, the peer's across the cluster
         if (!(PAIR ? mbar_wait_cluster(&tmem_empty[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, a.err)
@@ -447,7 +456,7 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
             break;
           }
           tc_fence_after();
-          mma4(d_tmem, s, it == 0, 0xFu);
+          mma4(d_tmem, s, it == 0, 0xFu, false);
           if (++s == stages) {
             s = 0;
             ph ^= 1u;
@@ -474,7 +483,11 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
               break;
             }
             tc_fence_after();
-            mma4(d_tmem, s, false, expand_chunks(xl, a.ex.R, e % xl.nbs));
+            // (e4m3 base: the second accumulator, started by the tile's first expand block)
+            if (FP8)
+              mma4(d_tmem + BN, s, e == 0, expand_chunks(xl, a.ex.R, e % xl.nbs), true);
+            else
+              mma4(d_tmem, s, false, expand_chunks(xl, a.ex.R, e % xl.nbs), true);
             if (++s == stages) {
               s = 0;
               ph ^= 1u;
@@ -514,8 +527,18 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
       const int row = m0 + rt;
       const int b = k & 1;
       const uint32_t tmem_row =
-          tmem_base + (uint32_t)(b * BN) + (static_cast<uint32_t>(quad * 32) << 16);
+          tmem_base + (uint32_t)(b * kAccCols) + (static_cast<uint32_t>(quad * 32) << 16);
       bool ok = true;
+      int tile_nx = 0;  // v mode: the tile's expand blocks (e4m3: its second accumulator is
+                        // written only when there are some)
+      // e4m3 base, v mode: the row's scale and the tile's column scales, requested while the
+      // tile's main loop runs (the previous tile's epilogue is past its last barrier)
+      float sxr_v = 0.f;
+      if (FP8 && VMODE) {
+        sxr_v = row < a.M ? __ldcg(a.sx + row) : 0.f;
+        for (int i = et; i < BN; i += 128) sw_tile[i] = __ldg(a.sw + n0 + i);
+        named_barrier(1, 128);
+      }
       if (vmode && head) {
         // ---- v mode: write the low-rank expand as extra K blocks of the ring ----
         // y_tile += sum over the tile's distinct slots u of [v_u^hi | v_u^lo] [B_u^T ; B_u^T],
@@ -554,6 +577,7 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
         }
         named_barrier(1, 128);
         const int nx = m * xl.nbs;
+        tile_nx = nx;
         if (et == 0) {
           *x_blocks = nx;
           mbar_arrive(xinfo_bar);
@@ -708,10 +732,9 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
           }
         }
         // e4m3 base: the row's scale (written by the row quantiser this kernel's producer
-        // waited for: read through L2) and this CTA's column scales, staged in the v-mode
-        // slot tables (idle here)
+        // waited for: read through L2) and this CTA's column scales, staged in shared memory
         float sxr = 0.f;
-        float* sw_s = reinterpret_cast<float*>(slot_bits);  // [bnc <= 2 * kBM]
+        float* sw_s = sw_tile;
         if (FP8) {
           sxr = row < a.M ? __ldcg(a.sx + row) : 0.f;
           for (int i = et; i < bnc; i += 128) sw_s[i] = __ldg(a.sw + n0 + cbase + i);
@@ -790,6 +813,7 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
         }
       } else {
         // ---- v mode: a stream-K head adds its tail's partial (one block) ----
+        // (e4m3 base: y = sx sw (base accumulator + the tail's partial) + expand accumulator)
         if (sk_src >= 0) {
           named_barrier(1, 128);  // the flag was seen by thread 0 of the epilogue
           const float4* src = reinterpret_cast<const float4*>(a.sk_part) +
@@ -804,6 +828,15 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
           float acc[32];
           tmem_acc32(tmem_row + cbase + c, acc);
           for (int j = 0; j < n_extra; ++j) add_block32(acc, xin + (size_t)j * nq * kBM + rt, c);
+          if (FP8) {
+            scale32(acc, sxr_v, sw_tile + c);
+            if (tile_nx > 0) {
+              float ex[32];
+              tmem_acc32(tmem_row + BN + c, ex);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i] += ex[i];
+            }
+          }
           store_y32(acc, a, row, n0 + cbase + c, yrow);
         }
       }
@@ -841,9 +874,9 @@ __global__ void __maxnreg__(VMODE ? 168 : 136)
   if (warp == 1) {
     tc_fence_after();
     if (PAIR)
-      tmem_dealloc_pair(tmem_base, 2 * BN);
+      tmem_dealloc_pair(tmem_base, 2 * kAccCols);
     else
-      tmem_dealloc(tmem_base, 2 * BN);
+      tmem_dealloc(tmem_base, 2 * kAccCols);
   }
 }
 
@@ -1049,9 +1082,10 @@ size_t gemm_tc_plan_exchange_floats(const GemmPlan& p, int M, int N) {
 
 int gemm_tc_tile_index(int BN) { return BN == 256 ? 0 : (BN == 128 ? 1 : 2); }
 
-static size_t tc_smem_bytes(int BN, bool pair, int stages, int xscr_bytes) {
+static size_t tc_smem_bytes(int BN, bool pair, bool fp8, int stages, int xscr_bytes) {
   const size_t stage = (size_t)kABytes + (size_t)(pair ? BN / 2 : BN) * kBK * 2;
-  return 1024 + stages * stage + xscr_bytes + (2 * kBM + 6) * 4 + (4 * stages + 6) * 8;
+  return 1024 + stages * stage + xscr_bytes + (2 * kBM + 8) * 4 + (fp8 ? BN * 4 : 0) +
+         (4 * stages + 6) * 8;
 }
 
 template <int BN, bool PAIR, bool VMODE, bool FP8 = false>
@@ -1069,8 +1103,8 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   if (cs > 1 && (!a.xk || a.xk_floats < exchange_floats(plan, a.M, a.n_end - a.n_begin)))
     return cudaErrorInvalidValue;
   int stages = 8;
-  while (stages > 2 && tc_smem_bytes(BN, PAIR, stages, xscr) > budget) --stages;
-  const size_t smem = tc_smem_bytes(BN, PAIR, stages, xscr);
+  while (stages > 2 && tc_smem_bytes(BN, PAIR, FP8, stages, xscr) > budget) --stages;
+  const size_t smem = tc_smem_bytes(BN, PAIR, FP8, stages, xscr);
   if (smem > budget) return cudaErrorInvalidConfiguration;
   // the epilogue lands its split-K partials and delta rows (128 x BN fp32) in the ring, and
   // counts each 32-column delta box on one of the 2 * stages v-mode stage barriers
@@ -1129,7 +1163,17 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
 
 static cudaError_t launch_variant_fp8(const GemmArgs& a, const GemmPlan& plan,
                                       const CUtensorMap& tmap_x, const CUtensorMap& tw,
-                                      cudaStream_t stream) {
+                                      const CUtensorMap& tb, cudaStream_t stream) {
+  if (a.ex.mode == kExpandV) {  // (tiles of at most 128 columns: see gemm_tc_kernel)
+    if (plan.pair)
+      return plan.block_n == 128 ? launch_tc<128, true, true, true>(a, plan, tmap_x, tw, tb, stream)
+                                 : cudaErrorInvalidConfiguration;
+    switch (plan.block_n) {
+      case 128: return launch_tc<128, false, true, true>(a, plan, tmap_x, tw, tb, stream);
+      case 64: return launch_tc<64, false, true, true>(a, plan, tmap_x, tw, tb, stream);
+      default: return cudaErrorInvalidConfiguration;
+    }
+  }
   if (plan.pair) {
     if (plan.block_n == 256) return launch_tc<256, true, false, true>(a, plan, tmap_x, tw, tw, stream);
     if (plan.block_n == 128) return launch_tc<128, true, false, true>(a, plan, tmap_x, tw, tw, stream);
@@ -1165,8 +1209,7 @@ static cudaError_t launch_one(const GemmArgs& a, const GemmPlan& plan,
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
                            const CUtensorMap* tmap_bx3, cudaStream_t stream) {
   if (a.ex.mode == kExpandV && !tmap_bx3) return cudaErrorInvalidValue;
-  if (a.fp8 && (a.ex.mode != kExpandDelta || !a.tmap_xq || !a.sx || !a.sw || a.K % 16 != 0))
-    return cudaErrorInvalidValue;
+  if (a.fp8 && (!a.tmap_xq || !a.sx || !a.sw || a.K % 16 != 0)) return cudaErrorInvalidValue;
   // the plan counts K blocks of 128 bytes: an e4m3 row of K elements is K / 2 bf16 wide
   const int k_bytes2 = a.fp8 ? (a.K + 1) / 2 : a.K;
   GemmPlan plan = gemm_tc_plan(a.M, a.N, k_bytes2, a.num_sms, a.ex.mode != kExpandV,
@@ -1176,6 +1219,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
     plan = GemmPlan{a.force_bn, a.ex.mode == kExpandV ? 1 : a.force_cs, a.force_pair};
     const int nkb = (k_bytes2 + kBK - 1) / kBK, c = plan.ksplit;
     if (c > 1 && (c - 1) * ((nkb + c - 1) / c) >= nkb) return cudaErrorInvalidConfiguration;
+  } else if (a.fp8 && a.ex.mode == kExpandV && plan.block_n > 128) {
+    plan.block_n = 128;  // the e4m3 base in v mode keeps two accumulators per tile
   }
   GemmArgs whole = a;
   whole.n_begin = 0;
@@ -1205,7 +1250,8 @@ static cudaError_t launch_one(const GemmArgs& a, const GemmPlan& plan, const CUt
                               const CUtensorMap* tmap_bx3, cudaStream_t stream) {
   if (a.fp8) {
     const int ti = gemm_tc_tile_index(plan.pair ? plan.block_n / 2 : plan.block_n);
-    return launch_variant_fp8(a, plan, *a.tmap_xq, tmap_w3[ti], stream);
+    return launch_variant_fp8(a, plan, *a.tmap_xq, tmap_w3[ti],
+                              tmap_bx3 ? tmap_bx3[ti] : tmap_w3[ti], stream);
   }
   CUtensorMap tmap_x;
   cudaError_t e = encode_tmap_bf16(&tmap_x, a.x, a.M, a.K, kBM);

@@ -142,7 +142,7 @@ static int create_layer(lora_layer_t** out, int K, int N, int num_slots, int max
   if (dtype != LORA_F32 && dtype != LORA_BF16) return LORA_EINVAL;
   if (dtype == LORA_BF16 && (K % 8 != 0 || N % 8 != 0)) return LORA_EINVAL;
   // an e4m3 base: bf16 activations, K a multiple of 16 (16-byte rows), decode batches only
-  if (fp8 && (dtype != LORA_BF16 || K % 16 != 0 || max_tokens > kDeltaMaxT)) return LORA_EINVAL;
+  if (fp8 && (dtype != LORA_BF16 || K % 16 != 0)) return LORA_EINVAL;
   const int R8 = (max_rank + 7) / 8 * 8;
   if (pool_rows < 0 || (pool_rows > 0 && ((pool_rows + 7) / 8 * 8 < R8 ||
                                            (long long)pool_rows > (long long)num_slots * R8)))
@@ -270,6 +270,11 @@ static int create_layer(lora_layer_t** out, int K, int N, int num_slots, int max
     if (encode_tmap_bf16(&L->tmap_a, L->A_pool, (int)P, K, (L->R + 15) / 16 * 16) !=
         cudaSuccess)
       return bail(LORA_ECUDA);
+    if (L->Bx_pool)  // batches beyond 512 rows: the expand blocks stay bf16
+      for (int i = 0; i < 3; ++i)
+        if (encode_tmap_bf16(&L->tmap_bx[i], L->Bx_pool, (int)(S * N),
+                             expand_layout((int)R).wx, kTcTileN[i]) != cudaSuccess)
+          return bail(LORA_ECUDA);
   } else if (dtype == LORA_BF16) {
     if (launch_pack_w_bf16(W_dev, L->Wp, K, N, stream) != cudaSuccess) return bail(LORA_ECUDA);
     for (int i = 0; i < 3; ++i)
@@ -615,6 +620,14 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     }
     LORA_CUDA(L, launch_bgmv_delta(ba, stream));
   } else if (bf16) {
+    if (L->fp8) {
+      // e4m3 base: the rows quantised first (a programmatic launch; the shrink below waits
+      // for it, and the GEMM's loads of xq wait for its row count)
+      if (L->q_dirty) LORA_CUDA(L, cudaMemsetAsync(L->q_ready, 0, 2 * sizeof(int32_t), stream));
+      L->q_dirty = true;
+      LORA_CUDA(L, launch_quant_rows_e4m3(x_dev, T, L->K, L->xq, L->sx, L->q_ready, L->num_sms,
+                                          stream));
+    }
     ShrinkTcArgs sa;
     sa.x = x_dev;
     sa.T = T;

@@ -106,9 +106,91 @@ def test_fp8_limits():
     W = torch.zeros(72, 64, dtype=BF16, device="cuda")  # K = 72: not a multiple of 16
     with pytest.raises(LoraError):
         LoraLayer(W, 2, 8, 16, fp8_base=True)
-    W = torch.zeros(64, 64, dtype=BF16, device="cuda")
-    with pytest.raises(LoraError):
-        LoraLayer(W, 2, 8, 513, fp8_base=True)  # prefill batches: not served
+    # batches beyond 512 rows run on tiles of at most 128 columns: a forced 256-column plan
+    # fails at forward time, the automatic one does not
+    wl = workloads.synthetic(790, 600, 128, 256, S=2, ranks=[8, 4], R=8, base_frac=0.1)
+    layer = _layer(wl)
+    try:
+        layer.set_gemm_plan(256, 1, 0)
+        with pytest.raises(LoraError):
+            layer(wl.x.cuda(), wl.token_slot.cuda())
+        layer.set_gemm_plan(0)
+        y = layer(wl.x.cuda(), wl.token_slot.cuda())
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        assert_parity(y, _ref(wl), BF16, what="fp8 prefill after a refused plan")
+    finally:
+        layer.close()
+
+
+# ---- batches of more than 512 rows: the SGMV path, with the expand blocks' bf16 MMAs in an
+# accumulator of their own beside the e4m3 base's ----
+
+@pytest.mark.parametrize("T,K,N,layout", [(700, 1024, 1040, "runs"), (1300, 512, 264, "random"),
+                                          (513, 2048, 4096, "runs")])
+def test_fp8_prefill_parity(T, K, N, layout):
+    wl = workloads.synthetic(800 + T, T, K, N, S=9, ranks=[16, 1, 8, 16, 3, 12, 16, 5, 2], R=16,
+                             base_frac=0.1, layout=layout, empty_slots=(6,))
+    layer = _layer(wl)
+    try:
+        for rep in range(2):
+            y = layer(wl.x.cuda(), wl.token_slot.cuda())
+            torch.cuda.synchronize()
+            assert layer.status() == (-4 if (wl.token_slot == 6).any() else 0)
+            assert_parity(y, _ref(wl), BF16, what="fp8 prefill T=%d K=%d N=%d (%d)" % (T, K, N, rep))
+    finally:
+        layer.close()
+
+
+def test_fp8_prefill_every_plan():
+    # 700 rows (5.5 row tiles; pairs: the last CTA partial), 8 e4m3 K blocks, N = 1000
+    wl = workloads.synthetic(830, 700, 1024, 1000, S=24, ranks=16, R=16, base_frac=0.1,
+                             layout="runs")
+    ref = _ref(wl)
+    layer = _layer(wl)
+    try:
+        for bn, pair in ((64, 0), (128, 0), (128, 1)):
+            layer.set_gemm_plan(bn, 1, pair)
+            y = layer(wl.x.cuda(), wl.token_slot.cuda())
+            torch.cuda.synchronize()
+            assert layer.status() == 0
+            assert_parity(y, ref, BF16, what="fp8 prefill plan (%d, 1, %d)" % (bn, pair))
+    finally:
+        layer.close()
+
+
+def test_fp8_prefill_stream_k_tail_and_wide_rank():
+    # more tiles than resident CTAs with a short last round (its tiles cut in two, the
+    # tail's partial added to the head's base accumulator before the scales), and rank 64
+    # (two expand blocks per slot and half)
+    for wl in (workloads.synthetic(840, 2600, 1024, 2048, S=24, ranks=16, R=16, base_frac=0.1,
+                                   layout="runs"),
+               workloads.synthetic(841, 900, 512, 512, S=10,
+                                   ranks=[64, 40, 8, 64, 17, 64, 1, 33, 64, 2], R=64,
+                                   base_frac=0.05, layout="random")):
+        layer = _layer(wl)
+        try:
+            y = layer(wl.x.cuda(), wl.token_slot.cuda())
+            torch.cuda.synchronize()
+            assert layer.status() == 0
+            assert_parity(y, _ref(wl), BF16, what="fp8 prefill " + wl.name)
+        finally:
+            layer.close()
+
+
+def test_fp8_prefill_workload_full_shape():
+    wl = workloads.prefill_sgmv(seed=1003, device="cpu")
+    layer = _layer(wl)
+    try:
+        y = layer(wl.x.cuda(), wl.token_slot.cuda())
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        # segment edges and a spread of rows (the oracle's e4m3 product over all 8192 rows
+        # of the 4096 x 14336 weight would take minutes)
+        rows = np.unique(np.concatenate([np.arange(0, wl.T, 61), np.arange(wl.T - 8, wl.T)]))
+        assert_parity(y[rows], _ref(wl, rows), BF16, what="fp8 base, prefill workload")
+    finally:
+        layer.close()
 
 
 def test_fp8_back_to_back_forwards_and_split_batches():
