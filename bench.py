@@ -454,8 +454,10 @@ def run_stack(args):
         "step_hbm": {"algorithmic_bytes": base_bytes + ad_bytes + act_bytes,
                      "achieved_gbs": (base_bytes + ad_bytes + act_bytes) / step_s / 1e9},
         "per_projection": per_shape,
-        # per projection: BGMV + GEMM (decode batch: no segment builder)
-        "gpu_launches": 2 * n_proj * st.n_layers * args.steps,
+        # per projection: BGMV + GEMM (two launches for a split batch), + the e4m3 row
+        # quantiser; counted by the layers themselves (no segment builder at 512 rows)
+        "gpu_launches": sum(layer.launch_count() for row in st.layers for layer in row) *
+                        args.steps,
         "clocks": clocks,
         "e2e": e2e,
         "setup_s": setup_s,
@@ -716,9 +718,9 @@ def run_ours(args):
         "lowrank_kernel": {"algorithmic_bytes": work["lowrank_bytes"],
                            "achieved_gbs": work["lowrank_bytes"] / (kern_us["shrink"] * 1e-6) / 1e9,
                            "mode": work["mode"]},
-        # decode batches (bf16, <= 512 rows): BGMV (which also quantises x for an e4m3
-        # base) + GEMM; larger: builder + shrink + GEMM
-        "gpu_launches": (2 if work["mode"] == "delta" else 3) * args.steps,
+        # decode batches (bf16, <= 512 rows): BGMV + GEMM; larger: builder + shrink + GEMM;
+        # + the e4m3 row quantiser, + a split GEMM's second launch (counted by the layer)
+        "gpu_launches": layers[0].launch_count() * args.steps,
         "clocks": clocks,
         "e2e": e2e,
         "wall_s_timed": t_wall1 - t_wall0,

@@ -312,6 +312,14 @@ int lora_wait_selftest(int which, void* stream);
 /* Text of the last error raised on this layer ("" if none).  Owned by the layer. */
 const char* lora_last_error(const lora_layer_t* layer);
 
+/*
+ * Kernels this layer has launched since its last set_batch_segments (that call's segment
+ * builder, if it ran, then every lora_forward and lora_get_segments on the batch), e.g.
+ * 2 for a bf16 decode forward (BGMV, base GEMM), 3 when the GEMM runs as two launches or
+ * the base is e4m3 (its row quantiser).  -1 for NULL.
+ */
+int lora_get_launch_count(const lora_layer_t* layer);
+
 /* Synchronise the layer's device, then free everything the layer owns.  NULL is a no-op. */
 void lora_layer_destroy(lora_layer_t* layer);
 

@@ -1207,7 +1207,7 @@ static cudaError_t launch_one(const GemmArgs& a, const GemmPlan& plan,
                               cudaStream_t stream);
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
-                           const CUtensorMap* tmap_bx3, cudaStream_t stream) {
+                           const CUtensorMap* tmap_bx3, cudaStream_t stream, int* launches) {
   if (a.ex.mode == kExpandV && !tmap_bx3) return cudaErrorInvalidValue;
   if (a.fp8 && (!a.tmap_xq || !a.sx || !a.sw || a.K % 16 != 0)) return cudaErrorInvalidValue;
   // the plan counts K blocks of 128 bytes: an e4m3 row of K elements is K / 2 bf16 wide
@@ -1240,9 +1240,14 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
     const GemmPlan plan2{plan.block_n, 2, plan.pair};
     cudaError_t e = launch_one(first, plan, tmap_w3, tmap_bx3, stream);
     if (e != cudaSuccess) return e;
-    return launch_one(second, plan2, tmap_w3, tmap_bx3, stream);
+    if (launches) ++*launches;
+    e = launch_one(second, plan2, tmap_w3, tmap_bx3, stream);
+    if (e == cudaSuccess && launches) ++*launches;
+    return e;
   }
-  return launch_one(whole, plan, tmap_w3, tmap_bx3, stream);
+  const cudaError_t e = launch_one(whole, plan, tmap_w3, tmap_bx3, stream);
+  if (e == cudaSuccess && launches) ++*launches;
+  return e;
 }
 
 // One launch of the tcgen05 GEMM with the given plan (columns a.n_begin .. a.n_end).

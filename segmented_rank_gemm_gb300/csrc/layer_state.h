@@ -25,6 +25,7 @@ struct lora_layer {
   CUtensorMap tmap_xq;     // fp8: xq with (128 x 128) boxes
   int32_t* q_ready = nullptr;  // fp8: {rows of xq written, GEMM CTAs that saw them} (zeroed)
   bool q_dirty = false;    // fp8: a forward stopped between the BGMV and the GEMM launches
+  int launches = 0;        // kernels of the last set_batch_segments + lora_forward
   void* A_pool = nullptr;  // [P][K] rank rows: slot s from row row_base[s]
   void* B_pool = nullptr;  // [P][N] rank rows
   int P = 0;               // pool rows: S * R, or the row budget of a pooled layer

@@ -151,7 +151,8 @@ struct BgmvArgs {
   int32_t* q_ready = nullptr;
 };
 // Launched with programmatic stream serialization; it does not wait for the builder.
-cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream);
+// launches (may be null): incremented per kernel launched (the e4m3 quantiser, the BGMV).
+cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream, int* launches = nullptr);
 
 // ---- the tensor-core expand's layout of a slot's rank columns ----
 // v of a row is split as v = hi + lo (two bf16) and multiplied by the slot's B^T on the
@@ -240,8 +241,10 @@ struct GemmArgs {
 // packed weight for N tiles of 256, 128 and 64 rows (in that order); tmap_bx3 the maps of
 // the B expand pool [S*N rows][wx] with (64 x 256/128/64) boxes (v mode; may be null in
 // delta mode).
+// launches (may be null): incremented per kernel launched (1, or 2 for a split batch).
 cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
-                           const CUtensorMap* tmap_bx3, cudaStream_t stream);
+                           const CUtensorMap* tmap_bx3, cudaStream_t stream,
+                           int* launches = nullptr);
 constexpr int kTcTileN[3] = {256, 128, 64};
 
 // ---- e4m3 base (fp8.cu) ----

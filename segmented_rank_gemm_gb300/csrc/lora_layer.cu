@@ -522,6 +522,7 @@ int set_batch_segments(lora_layer_t* L, const int32_t* token_slot_dev, int T, vo
 
   L->T_batch = T;
   L->token_slot = token_slot_dev;
+  L->launches = 0;
   // A bf16 batch of at most kDeltaMaxT rows is computed without its segments (the BGMV
   // kernel and the base GEMM read the ids directly, and the GEMM reports bad ids), so the
   // builder runs only if lora_get_segments asks for them.
@@ -555,6 +556,7 @@ static int run_builder(lora_layer_t* L, cudaStream_t stream) {
   a.err = L->err;
   LORA_CUDA(L, trace_mark(L, 0, stream));
   LORA_CUDA(L, launch_segment_builder(a, stream));
+  ++L->launches;
   LORA_CUDA(L, trace_mark(L, 1, stream));
   L->segments_pending = false;
   return LORA_OK;
@@ -618,7 +620,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
       ba.sx = L->sx;
       ba.q_ready = L->q_ready;
     }
-    LORA_CUDA(L, launch_bgmv_delta(ba, stream));
+    LORA_CUDA(L, launch_bgmv_delta(ba, stream, &L->launches));
   } else if (bf16) {
     if (L->fp8) {
       // e4m3 base: the rows quantised first (a programmatic launch; the shrink below waits
@@ -627,6 +629,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
       L->q_dirty = true;
       LORA_CUDA(L, launch_quant_rows_e4m3(x_dev, T, L->K, L->xq, L->sx, L->q_ready, L->num_sms,
                                           stream));
+      ++L->launches;
     }
     ShrinkTcArgs sa;
     sa.x = x_dev;
@@ -651,6 +654,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     sa.err = L->err;
     sa.num_sms = L->num_sms;
     LORA_CUDA(L, launch_sgmv_shrink_tc(sa, L->tmap_a, stream));
+    ++L->launches;
   } else {
     TileArgs ta;
     ta.x = x_dev;
@@ -675,6 +679,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     ta.max_tiles = (T + kTileRows - 1) / kTileRows + std::min(T, L->S);
     ta.num_sms = L->num_sms;
     LORA_CUDA(L, launch_lora_tile(ta, bf16, false, stream));
+    ++L->launches;
   }
   LORA_CUDA(L, trace_mark(L, 3, stream));
 
@@ -718,9 +723,11 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.tmap_delta = L->delta ? &L->tmap_delta : nullptr;
   LORA_CUDA(L, trace_mark(L, 4, stream));
   if (bf16)
-    LORA_CUDA(L, launch_gemm_tc(ga, L->tmap_w, L->Bx_pool ? L->tmap_bx : nullptr, stream));
+    LORA_CUDA(L, launch_gemm_tc(ga, L->tmap_w, L->Bx_pool ? L->tmap_bx : nullptr, stream,
+                                &L->launches));
   else
     LORA_CUDA(L, launch_gemm_simt_f32(ga, stream));
+    ++L->launches;
   L->q_dirty = false;
   LORA_CUDA(L, trace_mark(L, 5, stream));
 
@@ -843,6 +850,8 @@ int lora_set_gemm_plan(lora_layer_t* L, int block_n, int k_split, int cta_pair) 
 }
 
 const char* lora_last_error(const lora_layer_t* L) { return L ? L->last_error : "null layer"; }
+
+int lora_get_launch_count(const lora_layer_t* L) { return L ? L->launches : -1; }
 
 void lora_layer_destroy(lora_layer_t* L) {
   if (!L) return;

@@ -673,12 +673,14 @@ static cudaError_t launch_bgmv_stream(const BgmvArgs& a, cudaStream_t stream) {
                    : launch_bgmv_stream_r<32, 1>(a, stream);
 }
 
-cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream) {
+cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream, int* launches) {
   if (a.xq) {  // e4m3 base: the row quantiser first (it lets this kernel launch at once)
     const cudaError_t e =
         launch_quant_rows_e4m3(a.x, a.T, a.K, a.xq, a.sx, a.q_ready, a.num_sms, stream);
     if (e != cudaSuccess) return e;
+    if (launches && a.T > 0) ++*launches;
   }
+  if (launches) ++*launches;  // (counted before the launch: an error fails the forward)
   if (a.R <= 32 && a.T <= kSlotMaxT && a.K % 8 == 0 && a.N % 8 == 0)
     return launch_bgmv_stream(a, stream);  // slot-major, registers only
   // row-major: cluster of cs CTAs per row: 4 normally, fewer when K or N is small

@@ -36,7 +36,7 @@ ABI_FUNCTIONS = ("lora_layer_create", "lora_layer_create_pooled", "lora_layer_cr
                  "set_batch_segments", "lora_forward", "lora_forward_host", "lora_get_status",
                  "lora_get_segments", "lora_set_trace_events", "lora_set_gemm_plan",
                  "lora_last_error", "lora_layer_destroy", "lora_build_segments_static",
-                 "lora_wait_selftest")
+                 "lora_wait_selftest", "lora_get_launch_count")
 # every entry point declared in include/lora_residency.h
 CACHE_FUNCTIONS = ("lora_cache_create", "lora_cache_add", "lora_cache_add_composed",
                    "lora_cache_remove",
@@ -86,6 +86,7 @@ def _load() -> ctypes.CDLL:
     L.lora_set_gemm_plan.argtypes = [vp, i32, i32, i32]
     L.lora_build_segments_static.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp]
     L.lora_wait_selftest.argtypes = [i32, vp]
+    L.lora_get_launch_count.argtypes = [vp]
     L.lora_last_error.argtypes = [vp]
     L.lora_last_error.restype = ctypes.c_char_p
     L.lora_layer_destroy.argtypes = [vp]
@@ -299,6 +300,11 @@ def lora_wait_selftest(which: int, stream=None) -> int:
     return _lib.lora_wait_selftest(int(which), _stream(stream))
 
 
+def lora_get_launch_count(layer) -> int:
+    """Kernels the layer launched since its last set_batch_segments."""
+    return int(_lib.lora_get_launch_count(layer))
+
+
 def lora_last_error(layer) -> str:
     return _lib.lora_last_error(layer).decode()
 
@@ -385,6 +391,9 @@ class LoraLayer:
     def forward_host(self, x_host, ids_host, y_host, stream=None):
         lora_forward_host(self.handle, x_host, ids_host, y_host, int(x_host.shape[0]), stream)
         return y_host
+
+    def launch_count(self) -> int:
+        return lora_get_launch_count(self.handle)
 
     def status(self, stream=None) -> int:
         return lora_get_status(self.handle, stream)

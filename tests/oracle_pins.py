@@ -119,6 +119,21 @@ def pin_handbook_toy(L):
     rows, grouped, merged = all_evaluators(L, wl.x, wl.W, table, wl.token_slot)
     close(grouped, rows)
     close(merged, rows)
+    # the page's own check, restated: a library evaluation in fp32, one request at a time
+    # (its rows times W, plus the scale times (rows A) B of its adapter), agrees with the
+    # oracle at the printed tolerance (allclose, atol 1e-5)
+    import torch
+    parts, s0 = [], 0
+    for a, n in zip(g["owners"], g["lengths"]):
+        xr = wl.x[s0:s0 + n].float()
+        A, B, alpha = wl.adapters[a]
+        scale = alpha / A.shape[1]
+        parts.append(torch.matmul(xr, wl.W.float()) +
+                     scale * torch.matmul(torch.matmul(xr, A.float()), B.float()))
+        s0 += n
+    per_request = torch.cat(parts)
+    assert torch.allclose(torch.from_numpy(np.asarray(rows)).float(), per_request,
+                          atol=g["allclose_atol"])
 
 
 # --------------------------------------------------------------------------------

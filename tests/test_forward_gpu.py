@@ -206,3 +206,29 @@ def test_argument_errors():
         layer.forward(x)
     assert e.value.code == -1  # misaligned x
     layer.close()
+
+
+def test_launch_count():
+    # the kernels a batch launches, as the layer counts them (the bench's gpu_launches):
+    # decode bf16: BGMV + GEMM; prefill: builder + shrink + GEMM; fp32: builder + tile + GEMM;
+    # e4m3 decode: + the row quantiser
+    from segmented_rank_gemm_gb300.lora import LoraLayer
+    cases = [(workloads.synthetic(5101, 64, 256, 256, S=3, ranks=8, R=8), False, 2),
+             (workloads.synthetic(5102, 600, 256, 256, S=3, ranks=8, R=8), False, 3),
+             (workloads.synthetic(5103, 40, 64, 48, S=3, ranks=4, R=8, dtype=torch.float32),
+              False, 3),
+             (workloads.synthetic(5104, 64, 256, 256, S=3, ranks=8, R=8), True, 3)]
+    for wl, fp8, want in cases:
+        if fp8:
+            layer = LoraLayer(wl.W.cuda(), wl.S, wl.R, wl.T, fp8_base=True)
+            for s, ad in enumerate(wl.adapters):
+                layer.load(s, ad[0].cuda(), ad[1].cuda(), ad[2])
+        else:
+            layer = build_layer(wl)
+        try:
+            run_layer(layer, wl)
+            torch.cuda.synchronize()
+            assert layer.status() == 0
+            assert layer.launch_count() == want, (wl.name, fp8, layer.launch_count())
+        finally:
+            layer.close()
