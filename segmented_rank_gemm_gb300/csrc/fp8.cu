@@ -17,45 +17,59 @@
 
 namespace lora {
 
-static constexpr int kQThreads = 256;
 static constexpr int kQHold = 8;  // 16-byte chunks a thread holds between the max and the conversion
 
 // The decode step's row quantiser (see launch_quant_rows_e4m3 and quantize_rows_e4m3_cta).
-__global__ void __launch_bounds__(kQThreads)
+// NT = 128 (4 warps of at most 112 registers) for batches of more than two rows a CTA: with
+// the decode BGMV (2 warps of 120 per scheduler) and an e4m3 GEMM CTA (at most 2 warps of 80
+// per scheduler), one warp of this kernel per scheduler fills an SM's 16K-register files
+// exactly, so the three kernels share the SM and the GEMM's CTAs start while it runs.
+// NT = 256 for at most two rows a CTA: each row then has 4 warps (a decode batch's rows are
+// ready sooner), and the GEMM's CTAs start once it leaves.
+template <int NT>
+__global__ void __maxnreg__(112)
     quant_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ x, int T, int K,
                            uint8_t* __restrict__ xq, float* __restrict__ sx,
                            int32_t* __restrict__ q_ready) {
-  __shared__ float wmax[kQThreads / 32];
+  __shared__ float wmax[NT / 32];
   // the previous forward's base GEMM may still read xq, and the previous kernel may have
   // written x: wait for it; the low-rank kernel may then start at once (it relies on this
   // wait for the previous GEMM, and the base GEMM waits for the rows counted on q_ready)
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows = quantize_rows_e4m3_cta<kQThreads, kQHold>(x, T, K, xq, sx, wmax, warp, lane);
+  const int rows = quantize_rows_e4m3_cta<NT, kQHold>(x, T, K, xq, sx, wmax, warp, lane);
   if (q_ready) publish_rows(q_ready, rows);
 }
 
-cudaError_t launch_quant_rows_e4m3(const void* x, int T, int K, uint8_t* xq, float* sx,
-                                   int32_t* q_ready, int num_sms, cudaStream_t stream) {
-  if (T < 1) return cudaSuccess;
-  if (K % 16 != 0) return cudaErrorInvalidValue;
+template <int NT>
+static cudaError_t launch_quant_rows_t(const void* x, int T, int K, uint8_t* xq, float* sx,
+                                       int32_t* q_ready, int num_sms, cudaStream_t stream) {
   // it shares SMs with the low-rank kernel and the base GEMM launched behind it: the SMs
   // must keep the shared-memory split a GEMM CTA needs, or that CTA waits for them to drain
   static bool carveout[kAttrDevices] = {};
-  cudaError_t e = prefer_max_smem_carveout(quant_rows_e4m3_kernel, carveout);
+  cudaError_t e = prefer_max_smem_carveout(quant_rows_e4m3_kernel<NT>, carveout);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(std::max(1, std::min(T, num_sms)));
-  cfg.blockDim = dim3(kQThreads);
+  cfg.blockDim = dim3(NT);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, quant_rows_e4m3_kernel, static_cast<const __nv_bfloat16*>(x), T,
-                            K, xq, sx, q_ready);
+  return cudaLaunchKernelEx(&cfg, quant_rows_e4m3_kernel<NT>, static_cast<const __nv_bfloat16*>(x),
+                            T, K, xq, sx, q_ready);
+}
+
+cudaError_t launch_quant_rows_e4m3(const void* x, int T, int K, uint8_t* xq, float* sx,
+                                   int32_t* q_ready, int num_sms, cudaStream_t stream) {
+  if (T < 1) return cudaSuccess;
+  if (K % 16 != 0) return cudaErrorInvalidValue;
+  return T <= 2 * std::max(1, num_sms)
+             ? launch_quant_rows_t<256>(x, T, K, xq, sx, q_ready, num_sms, stream)
+             : launch_quant_rows_t<128>(x, T, K, xq, sx, q_ready, num_sms, stream);
 }
 
 // max |W[k][n]| over the rows [k0, k1) of each column, into amax[n] (float bits as int:

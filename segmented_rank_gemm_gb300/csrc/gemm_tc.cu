@@ -190,14 +190,15 @@ __device__ __forceinline__ bool seg_at(int k, int g, int G, int U, int nkb, int 
 
 // Delta mode (decode) caps registers at 136: two warps of this kernel and two of the
 // decode BGMV kernel (120 registers) share each of an SM's four 16K-register files, so the
-// two kernels run side by side.  VMODE is a template parameter so that the delta-mode
+// two kernels run side by side.  The e4m3 variants take 80, so that one warp of the row
+// quantiser (112) fits beside the two as well and this kernel's CTAs start while it runs.  VMODE is a template parameter so that the delta-mode
 // variants carry none of the expand-block and stream-K code; the v-mode variants share
 // their SMs with no other kernel and get more registers.
 // FP8: the base operands are e4m3 (x quantised per row, W per column; delta mode only): a
 // 128-byte K block then holds 128 elements instead of 64, the MMAs are kind::f8f6f4, and
 // the epilogue scales the accumulator by sx[row] sw[col] before it adds the delta.
 template <int BN, bool PAIR, bool VMODE, bool FP8 = false>
-__global__ void __maxnreg__(VMODE ? 168 : 136)
+__global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_bx,
