@@ -93,9 +93,7 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
  *   - the base runs as e4m3 x e4m3 tcgen05 MMAs (kind::f8f6f4) with fp32 accumulation;
  *     batches of more than 512 rows keep the low-rank expand's bf16 MMAs in an accumulator
  *     of their own beside the base's, added after the base product is scaled.
- * Limits: K a multiple of 16.  The packed weight takes K x N bytes.  Batches of more than
- * 512 rows run on GEMM tiles of at most 128 columns (lora_set_gemm_plan with block_n 256
- * makes such a forward fail).
+ * Limits: K a multiple of 16.  The packed weight takes K x N bytes.
  * Errors: as lora_layer_create.
  */
 int lora_layer_create_fp8(lora_layer_t** out, int K, int N, int num_slots, int max_rank,

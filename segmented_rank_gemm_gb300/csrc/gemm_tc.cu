@@ -207,9 +207,11 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
                    int sk_slots) {
   // e4m3 base in v mode: the low-rank expand blocks (bf16) accumulate apart from the base
   // (e4m3) blocks, in a second accumulator of BN columns beside each buffer's, so that the
-  // epilogue scales the base product alone: TMEM holds 2 x 2 x BN columns, BN <= 128
-  static_assert(!(FP8 && VMODE) || BN <= 128, "e4m3 v mode: tiles of at most 128 columns");
+  // epilogue scales the base product alone.  TMEM holds 512 columns: two buffers of two
+  // accumulators up to 128-column tiles; one buffer at 256 columns (the MMAs of a tile then
+  // wait for the previous tile's epilogue to drain it).
   constexpr int kAccCols = FP8 && VMODE ? 2 * BN : BN;  // TMEM columns of one buffer
+  constexpr int kBufs = kAccCols > 256 ? 1 : 2;         // accumulator buffers
   constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of the W (or B expand) tile this CTA loads
   constexpr int kBBytes = kBRows * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
@@ -305,9 +307,9 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
   // other with the next tile
   if (warp == 1) {
     if (PAIR)
-      tmem_alloc_pair(tmem_holder, 2 * kAccCols);
+      tmem_alloc_pair(tmem_holder, kBufs * kAccCols);
     else
-      tmem_alloc(tmem_holder, 2 * kAccCols);
+      tmem_alloc(tmem_holder, kBufs * kAccCols);
   }
   tc_fence_before();
   __syncthreads();
@@ -443,12 +445,13 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
       for (int k = 0; ok; ++k) {
         int u, k0, k1;
         if (!seg_at(k, g0, G, U, nkb, full_rounds, sk_slots, u, k0, k1)) break;
-        const int b = k & 1;
+        // buffer b of the tile; kph: the tile's use of that buffer (its barriers' phase)
+        const int b = kBufs == 2 ? (k & 1) : 0, kph = kBufs == 2 ? (k >> 1) : k;
         const uint32_t d_tmem = tmem_base + (uint32_t)(b * kAccCols);
         // the epilogue has drained this buffer's previous tile (tile k - 2); pairs: both
         // CTAs' epilogues, the peer's across the cluster
-        if (!(PAIR ? mbar_wait_cluster(&tmem_empty[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, a.err)
-                   : mbar_wait(&tmem_empty[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, a.err)))
+        if (!(PAIR ? mbar_wait_cluster(&tmem_empty[b], ((uint32_t)kph & 1u) ^ 1u, a.err)
+                   : mbar_wait(&tmem_empty[b], ((uint32_t)kph & 1u) ^ 1u, a.err)))
           break;
         tc_fence_after();
         for (int it = 0; it < k1 - k0; ++it) {
@@ -526,7 +529,7 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
       const int mt_i = PAIR ? 2 * pm_i + pr : pm_i;
       const int m0 = mt_i * kBM, n0 = a.n_begin + nt_i * BN;
       const int row = m0 + rt;
-      const int b = k & 1;
+      const int b = kBufs == 2 ? (k & 1) : 0, kph = kBufs == 2 ? (k >> 1) : k;
       const uint32_t tmem_row =
           tmem_base + (uint32_t)(b * kAccCols) + (static_cast<uint32_t>(quad * 32) << 16);
       bool ok = true;
@@ -630,7 +633,7 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
         ring += nx;
       }
       ring += nk;
-      const bool full_ok = ok && mbar_wait(&tmem_full[b], (uint32_t)(k >> 1) & 1u, a.err);
+      const bool full_ok = ok && mbar_wait(&tmem_full[b], (uint32_t)kph & 1u, a.err);
       // a split K (one tile per CTA) must still meet its cluster barrier below, whatever
       // the error (the flag is set); otherwise stop here
       if (!full_ok && cs == 1) break;
@@ -875,9 +878,9 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
   if (warp == 1) {
     tc_fence_after();
     if (PAIR)
-      tmem_dealloc_pair(tmem_base, 2 * kAccCols);
+      tmem_dealloc_pair(tmem_base, kBufs * kAccCols);
     else
-      tmem_dealloc(tmem_base, 2 * kAccCols);
+      tmem_dealloc(tmem_base, kBufs * kAccCols);
   }
 }
 
@@ -1165,14 +1168,16 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
 static cudaError_t launch_variant_fp8(const GemmArgs& a, const GemmPlan& plan,
                                       const CUtensorMap& tmap_x, const CUtensorMap& tw,
                                       const CUtensorMap& tb, cudaStream_t stream) {
-  if (a.ex.mode == kExpandV) {  // (tiles of at most 128 columns: see gemm_tc_kernel)
-    if (plan.pair)
-      return plan.block_n == 128 ? launch_tc<128, true, true, true>(a, plan, tmap_x, tw, tb, stream)
-                                 : cudaErrorInvalidConfiguration;
+  if (a.ex.mode == kExpandV) {
+    if (plan.pair) {
+      if (plan.block_n == 256) return launch_tc<256, true, true, true>(a, plan, tmap_x, tw, tb, stream);
+      if (plan.block_n == 128) return launch_tc<128, true, true, true>(a, plan, tmap_x, tw, tb, stream);
+      return cudaErrorInvalidConfiguration;
+    }
     switch (plan.block_n) {
+      case 256: return launch_tc<256, false, true, true>(a, plan, tmap_x, tw, tb, stream);
       case 128: return launch_tc<128, false, true, true>(a, plan, tmap_x, tw, tb, stream);
-      case 64: return launch_tc<64, false, true, true>(a, plan, tmap_x, tw, tb, stream);
-      default: return cudaErrorInvalidConfiguration;
+      default: return launch_tc<64, false, true, true>(a, plan, tmap_x, tw, tb, stream);
     }
   }
   if (plan.pair) {
@@ -1220,8 +1225,6 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
     plan = GemmPlan{a.force_bn, a.ex.mode == kExpandV ? 1 : a.force_cs, a.force_pair};
     const int nkb = (k_bytes2 + kBK - 1) / kBK, c = plan.ksplit;
     if (c > 1 && (c - 1) * ((nkb + c - 1) / c) >= nkb) return cudaErrorInvalidConfiguration;
-  } else if (a.fp8 && a.ex.mode == kExpandV && plan.block_n > 128) {
-    plan.block_n = 128;  // the e4m3 base in v mode keeps two accumulators per tile
   }
   GemmArgs whole = a;
   whole.n_begin = 0;

@@ -611,9 +611,9 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
     ba.num_sms = L->num_sms;
     ba.per_column = L->percol_slots > 0;
     if (L->fp8) {
-      // e4m3 base: the BGMV kernel quantises x's rows as it starts and counts them on
+      // e4m3 base: the row quantiser, launched ahead of the BGMV kernel, counts x's rows on
       // q_ready, which the GEMM's loads wait for and its last CTA resets.  A forward that
-      // stopped between the two launches left the count set: clear it first.
+      // stopped between those launches left the count set: clear it first.
       if (L->q_dirty) LORA_CUDA(L, cudaMemsetAsync(L->q_ready, 0, 2 * sizeof(int32_t), stream));
       L->q_dirty = true;
       ba.xq = L->xq;
@@ -722,12 +722,13 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
   ga.q_ready = L->fp8 ? L->q_ready : nullptr;
   ga.tmap_delta = L->delta ? &L->tmap_delta : nullptr;
   LORA_CUDA(L, trace_mark(L, 4, stream));
-  if (bf16)
+  if (bf16) {
     LORA_CUDA(L, launch_gemm_tc(ga, L->tmap_w, L->Bx_pool ? L->tmap_bx : nullptr, stream,
                                 &L->launches));
-  else
+  } else {
     LORA_CUDA(L, launch_gemm_simt_f32(ga, stream));
     ++L->launches;
+  }
   L->q_dirty = false;
   LORA_CUDA(L, trace_mark(L, 5, stream));
 
