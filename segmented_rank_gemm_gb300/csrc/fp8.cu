@@ -25,7 +25,8 @@ static constexpr int kQHold = 8;  // 16-byte chunks a thread holds between the m
 // per scheduler), one warp of this kernel per scheduler fills an SM's 16K-register files
 // exactly, so the three kernels share the SM and the GEMM's CTAs start while it runs.
 // NT = 256 for at most two rows a CTA: each row then has 4 warps (a decode batch's rows are
-// ready sooner), and the GEMM's CTAs start once it leaves.
+// ready sooner), and the GEMM's CTAs start once it leaves; and ahead of the SGMV shrink
+// (larger batches), where it shares its SMs with nothing.
 template <int NT>
 __global__ void __maxnreg__(112)
     quant_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ x, int T, int K,
@@ -44,7 +45,7 @@ __global__ void __maxnreg__(112)
 
 template <int NT>
 static cudaError_t launch_quant_rows_t(const void* x, int T, int K, uint8_t* xq, float* sx,
-                                       int32_t* q_ready, int num_sms, cudaStream_t stream) {
+                                       int32_t* q_ready, int ctas, cudaStream_t stream) {
   // it shares SMs with the low-rank kernel and the base GEMM launched behind it: the SMs
   // must keep the shared-memory split a GEMM CTA needs, or that CTA waits for them to drain
   static bool carveout[kAttrDevices] = {};
@@ -54,7 +55,7 @@ static cudaError_t launch_quant_rows_t(const void* x, int T, int K, uint8_t* xq,
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(std::max(1, std::min(T, num_sms)));
+  cfg.gridDim = dim3(std::max(1, std::min(T, ctas)));
   cfg.blockDim = dim3(NT);
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -64,12 +65,15 @@ static cudaError_t launch_quant_rows_t(const void* x, int T, int K, uint8_t* xq,
 }
 
 cudaError_t launch_quant_rows_e4m3(const void* x, int T, int K, uint8_t* xq, float* sx,
-                                   int32_t* q_ready, int num_sms, cudaStream_t stream) {
+                                   int32_t* q_ready, int num_sms, bool beside_bgmv,
+                                   cudaStream_t stream) {
   if (T < 1) return cudaSuccess;
   if (K % 16 != 0) return cudaErrorInvalidValue;
-  return T <= 2 * std::max(1, num_sms)
-             ? launch_quant_rows_t<256>(x, T, K, xq, sx, q_ready, num_sms, stream)
-             : launch_quant_rows_t<128>(x, T, K, xq, sx, q_ready, num_sms, stream);
+  const int sms = std::max(1, num_sms);
+  // ahead of the SGMV shrink, which waits for it: two CTAs of 8 warps per SM
+  if (!beside_bgmv) return launch_quant_rows_t<256>(x, T, K, xq, sx, q_ready, 2 * sms, stream);
+  return T <= 2 * sms ? launch_quant_rows_t<256>(x, T, K, xq, sx, q_ready, sms, stream)
+                      : launch_quant_rows_t<128>(x, T, K, xq, sx, q_ready, sms, stream);
 }
 
 // max |W[k][n]| over the rows [k0, k1) of each column, into amax[n] (float bits as int:

@@ -252,12 +252,14 @@ constexpr int kTcTileN[3] = {256, 128, 64};
 // box and the 128-byte swizzle.
 cudaError_t encode_tmap_u8(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
 // x [T][K] bf16 -> xq [T][K] e4m3 and sx [T]: sx = max |x[row]| / 448 (1 for a zero row),
-// xq = e4m3(x / sx), round to nearest even, saturating.  min(T, num_sms) CTAs, CTA b the
-// rows b, b + gridDim.x, ...; each CTA counts its rows on q_ready once their stores are
-// visible.  Programmatic dependent launch: it waits for the previous kernel on the stream
-// (which may read xq or write x) and then at once lets the next one launch.
+// xq = e4m3(x / sx), round to nearest even, saturating.  CTA b takes rows b, b + gridDim.x,
+// ... (beside_bgmv: one CTA per SM, sized to share the SM with the decode BGMV and GEMM;
+// else two per SM); each CTA counts its rows on q_ready once their stores are visible.
+// Programmatic dependent launch: it waits for the previous kernel on the stream (which may
+// read xq or write x) and then at once lets the next one launch.
 cudaError_t launch_quant_rows_e4m3(const void* x, int T, int K, uint8_t* xq, float* sx,
-                                   int32_t* q_ready, int num_sms, cudaStream_t stream);
+                                   int32_t* q_ready, int num_sms, bool beside_bgmv,
+                                   cudaStream_t stream);
 // W [K][N] bf16 -> Wq [N][K] e4m3 (transposed, K-major) and sw [N]: per column as above.
 cudaError_t launch_quant_cols_e4m3(const void* W, int K, int N, uint8_t* Wq, float* sw,
                                    cudaStream_t stream);

@@ -628,7 +628,7 @@ int lora_forward(lora_layer_t* L, const void* x_dev, void* y_dev, int T, void* s
       if (L->q_dirty) LORA_CUDA(L, cudaMemsetAsync(L->q_ready, 0, 2 * sizeof(int32_t), stream));
       L->q_dirty = true;
       LORA_CUDA(L, launch_quant_rows_e4m3(x_dev, T, L->K, L->xq, L->sx, L->q_ready, L->num_sms,
-                                          stream));
+                                          false, stream));
       ++L->launches;
     }
     ShrinkTcArgs sa;

@@ -676,7 +676,7 @@ static cudaError_t launch_bgmv_stream(const BgmvArgs& a, cudaStream_t stream) {
 cudaError_t launch_bgmv_delta(const BgmvArgs& a, cudaStream_t stream, int* launches) {
   if (a.xq) {  // e4m3 base: the row quantiser first (it lets this kernel launch at once)
     const cudaError_t e =
-        launch_quant_rows_e4m3(a.x, a.T, a.K, a.xq, a.sx, a.q_ready, a.num_sms, stream);
+        launch_quant_rows_e4m3(a.x, a.T, a.K, a.xq, a.sx, a.q_ready, a.num_sms, true, stream);
     if (e != cudaSuccess) return e;
     if (launches && a.T > 0) ++*launches;
   }
