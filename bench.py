@@ -703,8 +703,10 @@ def run_ours(args):
                    "T": T, "K": K, "N": N, "slots": wl0.S,
                    "slot_rank_width": wl0.R, "distinct_slots": work["distinct_slots"],
                    "adapted_rows": work["adapted_rows"], "parallelism": "replicas x%d" % world,
-                   "l2": "rotating %d independent layer instances (~%d MB of weights and slots)"
-                         " > 129 MB L2" % (len(layers), len(layers) * work["step_bytes"] // 10**6),
+                   "l2": "rotating %d independent layer instances (~%d MB of weights and slots)%s"
+                         % (len(layers), len(layers) * work["step_bytes"] // 10**6,
+                            " > 129 MB L2" if len(layers) * work["step_bytes"] > 129 * 10**6
+                            else ": fits the 129 MB L2, steps may hit it (not a bench number)"),
                    "graphs": ("one graph per rotation of %d steps (one per instance)" % len(layers))
                              if not args.no_graph else False},
         "roofline": roofline,
