@@ -228,7 +228,8 @@ def aggregate(units_per_rank: int, steps: int, world: int, max_seconds: float) -
 
 def traffic_from_profile(kernel_src: str, config: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if it
-    was taken on the current kernel source (else None)."""
+    was taken on the current kernel source (else None); e4m3-base runs look up
+    ``<config>_fp8``."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -444,7 +445,7 @@ def run_stack(args):
                                "of a pass" % n_gemm,
                      "bound": "tensor", "achieved": gemm_tf, "peak": peak, "unit": "TFLOP/s",
                      "frac": gemm_tf / peak,
-                     "traffic": None if args.fp8 else traffic_from_profile(kernel_src, "stack_8b"),
+                     "traffic": traffic_from_profile(kernel_src, "stack_8b" + ("_fp8" if args.fp8 else "")),
                      "peak_source": peak_note,
                      "frac_of_burst_peak": gemm_tf / (pk["bf16_tflops"] * (2 if args.fp8 else 1)),
                      "algorithmic_flops_per_launch": flops / n_gemm,
@@ -673,7 +674,7 @@ def run_ours(args):
                           % (", e4m3" if args.fp8 else ""), "bound": "hbm",
                 "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"],
-                "traffic": None if args.fp8 else traffic_from_profile(kernel_src, args.config),
+                "traffic": traffic_from_profile(kernel_src, args.config + ("_fp8" if args.fp8 else "")),
                 "peak_source": pk["source"], "algorithmic_bytes_per_launch": work["gemm_bytes"],
                 "avg_launch_us": kern_us["gemm"]}
     if args.config != "decode_bgmv":

@@ -194,9 +194,10 @@ __device__ __forceinline__ bool seg_at(int k, int g, int G, int U, int nkb, int 
 // quantiser (112) fits beside the two as well and this kernel's CTAs start while it runs.  VMODE is a template parameter so that the delta-mode
 // variants carry none of the expand-block and stream-K code; the v-mode variants share
 // their SMs with no other kernel and get more registers.
-// FP8: the base operands are e4m3 (x quantised per row, W per column; delta mode only): a
-// 128-byte K block then holds 128 elements instead of 64, the MMAs are kind::f8f6f4, and
-// the epilogue scales the accumulator by sx[row] sw[col] before it adds the delta.
+// FP8: the base operands are e4m3 (x quantised per row, W per column): a 128-byte K block
+// then holds 128 elements instead of 64, the MMAs are kind::f8f6f4, and the accumulator is
+// scaled by sx[row] sw[col] before the low-rank term is added (delta mode: in the
+// epilogue; v mode: in TMEM, between the base and the expand blocks).
 template <int BN, bool PAIR, bool VMODE, bool FP8 = false>
 __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
@@ -205,13 +206,6 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
                    const __grid_constant__ CUtensorMap tmap_delta, GemmArgs a, int stages,
                    int xscr_bytes, int group_m, int mtp, int nt, int full_rounds,
                    int sk_slots) {
-  // e4m3 base in v mode: the low-rank expand blocks (bf16) accumulate apart from the base
-  // (e4m3) blocks, in a second accumulator of BN columns beside each buffer's, so that the
-  // epilogue scales the base product alone.  TMEM holds 512 columns: two buffers of two
-  // accumulators up to 128-column tiles; one buffer at 256 columns (the MMAs of a tile then
-  // wait for the previous tile's epilogue to drain it).
-  constexpr int kAccCols = FP8 && VMODE ? 2 * BN : BN;  // TMEM columns of one buffer
-  constexpr int kBufs = kAccCols > 256 ? 1 : 2;         // accumulator buffers
   constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of the W (or B expand) tile this CTA loads
   constexpr int kBBytes = kBRows * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
@@ -239,7 +233,8 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
   uint64_t* xinfo_bar = bars + 2 * stages + 4;   // v mode: the tile's x_blocks written
   uint64_t* xgrant = bars + 2 * stages + 5;      // [stages] v mode: stage handed to the epilogue
   uint64_t* xa_full = bars + 3 * stages + 5;     // [stages] v mode: its A half written
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * stages + 5);
+  uint64_t* base_full = bars + 4 * stages + 5;   // [2] e4m3 v mode: the base blocks complete
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 4 * stages + 7);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the first launch of a split batch lets the second one start while it runs (it waits for
@@ -276,6 +271,7 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
       mbar_init(&tmem_empty[b], PAIR ? 2 : 1);  // pairs: one arrival from each CTA's epilogue
+      mbar_init(&base_full[b], 1);
     }
     mbar_init(xinfo_bar, 1);
     for (int s = 0; s < stages; ++s) {
@@ -307,9 +303,9 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
   // other with the next tile
   if (warp == 1) {
     if (PAIR)
-      tmem_alloc_pair(tmem_holder, kBufs * kAccCols);
+      tmem_alloc_pair(tmem_holder, 2 * BN);
     else
-      tmem_alloc(tmem_holder, kBufs * kAccCols);
+      tmem_alloc(tmem_holder, 2 * BN);
   }
   tc_fence_before();
   __syncthreads();
@@ -446,8 +442,8 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
         int u, k0, k1;
         if (!seg_at(k, g0, G, U, nkb, full_rounds, sk_slots, u, k0, k1)) break;
         // buffer b of the tile; kph: the tile's use of that buffer (its barriers' phase)
-        const int b = kBufs == 2 ? (k & 1) : 0, kph = kBufs == 2 ? (k >> 1) : k;
-        const uint32_t d_tmem = tmem_base + (uint32_t)(b * kAccCols);
+        const int b = k & 1, kph = k >> 1;
+        const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
         // the epilogue has drained this buffer's previous tile (tile k - 2); pairs: both
         // CTAs' epilogues, the peer's across the cluster
         if (!(PAIR ? mbar_wait_cluster(&tmem_empty[b], ((uint32_t)kph & 1u) ^ 1u, a.err)
@@ -465,6 +461,14 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
             s = 0;
             ph ^= 1u;
           }
+        }
+        // e4m3 base, v mode: the epilogue scales the base product in TMEM once it is
+        // complete, before it releases the first expand block
+        if (FP8 && VMODE && ok) {
+          if (PAIR)
+            tc_commit_pair_mc(&base_full[b], pair_mask);
+          else
+            tc_commit(&base_full[b]);
         }
         const bool head = k0 == 0;
         if (ok && vmode && head && !mbar_wait(xinfo_bar, (uint32_t)hk & 1u, a.err)) ok = false;
@@ -487,11 +491,7 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
               break;
             }
             tc_fence_after();
-            // (e4m3 base: the second accumulator, started by the tile's first expand block)
-            if (FP8)
-              mma4(d_tmem + BN, s, e == 0, expand_chunks(xl, a.ex.R, e % xl.nbs), true);
-            else
-              mma4(d_tmem, s, false, expand_chunks(xl, a.ex.R, e % xl.nbs), true);
+            mma4(d_tmem, s, false, expand_chunks(xl, a.ex.R, e % xl.nbs), true);
             if (++s == stages) {
               s = 0;
               ph ^= 1u;
@@ -529,12 +529,12 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
       const int mt_i = PAIR ? 2 * pm_i + pr : pm_i;
       const int m0 = mt_i * kBM, n0 = a.n_begin + nt_i * BN;
       const int row = m0 + rt;
-      const int b = kBufs == 2 ? (k & 1) : 0, kph = kBufs == 2 ? (k >> 1) : k;
+      const int b = k & 1, kph = k >> 1;
       const uint32_t tmem_row =
-          tmem_base + (uint32_t)(b * kAccCols) + (static_cast<uint32_t>(quad * 32) << 16);
+          tmem_base + (uint32_t)(b * BN) + (static_cast<uint32_t>(quad * 32) << 16);
       bool ok = true;
-      int tile_nx = 0;  // v mode: the tile's expand blocks (e4m3: its second accumulator is
-                        // written only when there are some)
+      int tile_nx = 0;  // v mode: the tile's expand blocks (e4m3: the accumulator is scaled
+                        // in TMEM only when there are some)
       // e4m3 base, v mode: the row's scale and the tile's column scales, requested while the
       // tile's main loop runs (the previous tile's epilogue is past its last barrier)
       float sxr_v = 0.f;
@@ -602,6 +602,26 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
             *reinterpret_cast<uint4*>(mine + hb * 128 + ((hc ^ sw) << 4)) = hi;
             *reinterpret_cast<uint4*>(mine + lb * 128 + ((lc ^ sw) << 4)) = lo;
           }
+        }
+        if (FP8 && nx > 0) {
+          // e4m3 base: y = sx sw (xq Wq) + the expand, in one accumulator.  Once the base
+          // blocks are complete their product is scaled in TMEM; the expand blocks, the
+          // first released only after this, then add the low-rank term unscaled.  (base_full
+          // of this buffer is at most one phase ahead: its next tile waits for this drain.)
+          if (!mbar_wait(&base_full[b], (uint32_t)kph & 1u, a.err)) ok = false;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 32) {  // (warp-uniform: tcgen05.ld / st are aligned)
+            float acc[32];
+            tmem_acc32(tmem_row + c, acc);
+            scale32(acc, sxr_v, sw_tile + c);
+            uint32_t raw[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(acc[i]);
+            tmem_st_32x32b_x32(tmem_row + c, raw);
+          }
+          tmem_st_wait();
+          tc_fence_before();  // ordered before the MMA lane's expand blocks (xa_full below)
         }
         for (int e = 0; e < nx; ++e) {
           const int st = (ring + nk + e) % stages;  // after the tile's base blocks
@@ -817,7 +837,8 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
         }
       } else {
         // ---- v mode: a stream-K head adds its tail's partial (one block) ----
-        // (e4m3 base: y = sx sw (base accumulator + the tail's partial) + expand accumulator)
+        // (e4m3 base: the accumulator holds sx sw base + expand when the tile has expand
+        // blocks, so the partial is scaled alone; else the sum is scaled here)
         if (sk_src >= 0) {
           named_barrier(1, 128);  // the flag was seen by thread 0 of the epilogue
           const float4* src = reinterpret_cast<const float4*>(a.sk_part) +
@@ -831,15 +852,19 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
         for (int c = 0; c < bnc; c += 32) {
           float acc[32];
           tmem_acc32(tmem_row + cbase + c, acc);
-          for (int j = 0; j < n_extra; ++j) add_block32(acc, xin + (size_t)j * nq * kBM + rt, c);
-          if (FP8) {
-            scale32(acc, sxr_v, sw_tile + c);
-            if (tile_nx > 0) {
-              float ex[32];
-              tmem_acc32(tmem_row + BN + c, ex);
+          if (FP8 && tile_nx > 0) {
+            if (n_extra > 0) {
+              float p[32];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) acc[i] += ex[i];
+              for (int i = 0; i < 32; ++i) p[i] = 0.f;
+              for (int j = 0; j < n_extra; ++j) add_block32(p, xin + (size_t)j * nq * kBM + rt, c);
+              scale32(p, sxr_v, sw_tile + c);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i] += p[i];
             }
+          } else {
+            for (int j = 0; j < n_extra; ++j) add_block32(acc, xin + (size_t)j * nq * kBM + rt, c);
+            if (FP8) scale32(acc, sxr_v, sw_tile + c);
           }
           store_y32(acc, a, row, n0 + cbase + c, yrow);
         }
@@ -878,9 +903,9 @@ __global__ void __maxnreg__(VMODE ? 168 : (FP8 ? 80 : 136))
   if (warp == 1) {
     tc_fence_after();
     if (PAIR)
-      tmem_dealloc_pair(tmem_base, kBufs * kAccCols);
+      tmem_dealloc_pair(tmem_base, 2 * BN);
     else
-      tmem_dealloc(tmem_base, kBufs * kAccCols);
+      tmem_dealloc(tmem_base, 2 * BN);
   }
 }
 
@@ -1003,7 +1028,11 @@ static int resident_ctas(int csize, int num_sms) {
 // the estimate, but a pair runs the expand blocks of all its 256 rows on both CTAs, which
 // doubles them where slots change every few rows: pairs are taken there only when the
 // batch averages at least 128 rows per slot (`slots` = the layer's slot count, 0 = none).
-GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split, int slots) {
+// With the e4m3 base in v mode single CTAs at N = 256 measured faster than pairs on every
+// shape tried but one (8-18% at K = 4096; pairs 4% ahead at K = 14336, N = 4096), so the
+// caller turns pairs off there.
+GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split, int slots,
+                      bool allow_pair) {
   const int mt = (M + kBM - 1) / kBM;
   const int nkb = (K + kBK - 1) / kBK;
   // every one of the cs K ranges of ceil(nkb / cs) blocks must be non-empty
@@ -1013,7 +1042,7 @@ GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split, int sl
   const int cand[3] = {256, 128, 64};
   // single CTAs first: a pair is taken only where it is estimated faster
   for (int pair = 0; pair <= 1; ++pair) {
-    if (pair && mt < 2) continue;  // a pair over one row tile would leave a CTA idle
+    if (pair && (mt < 2 || !allow_pair)) continue;  // (one row tile: a pair leaves a CTA idle)
     if (pair && !allow_split && slots > 0 && (long long)M < 128LL * slots) continue;
     for (int i = 0; i < 3; ++i) {
       const int bn = cand[i];
@@ -1089,7 +1118,7 @@ int gemm_tc_tile_index(int BN) { return BN == 256 ? 0 : (BN == 128 ? 1 : 2); }
 static size_t tc_smem_bytes(int BN, bool pair, bool fp8, int stages, int xscr_bytes) {
   const size_t stage = (size_t)kABytes + (size_t)(pair ? BN / 2 : BN) * kBK * 2;
   return 1024 + stages * stage + xscr_bytes + (2 * kBM + 8) * 4 + (fp8 ? BN * 4 : 0) +
-         (4 * stages + 6) * 8;
+         (4 * stages + 8) * 8;
 }
 
 template <int BN, bool PAIR, bool VMODE, bool FP8 = false>
@@ -1219,7 +1248,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const CUtensorMap* tmap_w3,
   // the plan counts K blocks of 128 bytes: an e4m3 row of K elements is K / 2 bf16 wide
   const int k_bytes2 = a.fp8 ? (a.K + 1) / 2 : a.K;
   GemmPlan plan = gemm_tc_plan(a.M, a.N, k_bytes2, a.num_sms, a.ex.mode != kExpandV,
-                               a.ex.mode == kExpandV ? a.ex.S : 0);
+                               a.ex.mode == kExpandV ? a.ex.S : 0,
+                               !(a.fp8 && a.ex.mode == kExpandV));
   if (a.force_bn != 0) {
     // v mode never splits K: its expand blocks run after the base ones in one accumulator
     plan = GemmPlan{a.force_bn, a.ex.mode == kExpandV ? 1 : a.force_cs, a.force_pair};

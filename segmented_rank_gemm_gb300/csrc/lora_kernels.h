@@ -274,7 +274,10 @@ struct GemmPlan {
   int ksplit;   // K ranges per output tile, 1..4
   int pair;     // 1: CTA pairs (cta_group::2 MMAs, 256-row tiles, N tile 256 or 128)
 };
-GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split, int slots);
+// allow_pair = false keeps every tile on one CTA (the e4m3 base in v mode, where pairs
+// measured slower).
+GemmPlan gemm_tc_plan(int M, int N, int K, int num_sms, bool allow_split, int slots,
+                      bool allow_pair = true);
 // Floats of split-K exchange scratch the tcgen05 GEMM needs for an M-row batch with the
 // K split allowed (0 when its plan does not split K).
 size_t gemm_tc_exchange_floats(int M, int N, int K, int num_sms);
