@@ -1168,9 +1168,12 @@ static cudaError_t launch_tc(const GemmArgs& a, const GemmPlan& plan, const CUte
   int G = units;
   if (a.ex.mode == kExpandV) G = std::max(1, std::min(units, resident_ctas(csize, a.num_sms) / csize));
   // stream-K: when the units leave a last round of at most half the slots busy, those
-  // tiles are cut in two (head and tail on two slots) instead
+  // tiles are cut in two (head and tail on two slots) instead; only a K range of at least
+  // two of the kernel's K blocks (128 elements each with the e4m3 base) is cut, so that
+  // the head starts its accumulator with a block of its own
+  constexpr int kKE = FP8 ? 2 * kBK : kBK;
   int full_rounds = (units + G - 1) / G, sk_slots = 0;
-  if (a.ex.mode == kExpandV && a.sk_part && a.sk_sync && units > G && (a.K + kBK - 1) / kBK >= 2) {
+  if (a.ex.mode == kExpandV && a.sk_part && a.sk_sync && units > G && (a.K + kKE - 1) / kKE >= 2) {
     const int rem = units % G;
     if (rem > 0 && 2 * rem <= G) {
       full_rounds = units / G;

@@ -176,6 +176,45 @@ def test_fp8_prefill_stream_k_tail_and_wide_rank():
             layer.close()
 
 
+def test_fp8_prefill_base_only_tiles_and_stream_k_heads():
+    # The base product is scaled in TMEM before a tile's expand blocks add to it; a tile
+    # with no adapted row has no expand block and is scaled as it drains.  Rows 0-255 and
+    # 1024-1535 are base-only, so whole row tiles of each kind run in the full rounds and
+    # among the stream-K heads of the short last round (whose tails' partials are added
+    # before or after the scales), on the automatic plan, 128-wide tiles and CTA pairs.
+    wl = workloads.synthetic(850, 2600, 1024, 2048, S=24, ranks=16, R=16, base_frac=0.1,
+                             layout="runs")
+    wl.token_slot[0:256] = -1
+    wl.token_slot[1024:1536] = -1
+    ref = _ref(wl)
+    layer = _layer(wl)
+    try:
+        for plan in ((0, 1, 0), (128, 1, 0), (256, 1, 1)):
+            layer.set_gemm_plan(*plan)
+            y = layer(wl.x.cuda(), wl.token_slot.cuda())
+            torch.cuda.synchronize()
+            assert layer.status() == 0
+            assert_parity(y, ref, BF16, what="fp8 prefill, base-only tiles, plan %s" % (plan,))
+    finally:
+        layer.close()
+
+
+@pytest.mark.parametrize("K", [128, 192])
+def test_fp8_prefill_short_k_range(K):
+    # one e4m3 K block (K = 128) is never cut between a stream-K head and tail; two (the
+    # second ragged, K = 192) are cut one and one
+    wl = workloads.synthetic(860 + K, 2600, K, 2048, S=24, ranks=16, R=16, base_frac=0.1,
+                             layout="runs")
+    layer = _layer(wl)
+    try:
+        y = layer(wl.x.cuda(), wl.token_slot.cuda())
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        assert_parity(y, _ref(wl), BF16, what="fp8 prefill, K = %d" % K)
+    finally:
+        layer.close()
+
+
 def test_fp8_prefill_workload_full_shape():
     wl = workloads.prefill_sgmv(seed=1003, device="cpu")
     layer = _layer(wl)
