@@ -91,8 +91,8 @@ int lora_layer_create(lora_layer_t** out, int K, int N, int num_slots, int max_r
  *     kernel of its own before the low-rank kernel; scales and divisions are fp32;
  *   - the low-rank term is computed from the bf16 x as in a plain layer;
  *   - the base runs as e4m3 x e4m3 tcgen05 MMAs (kind::f8f6f4) with fp32 accumulation;
- *     batches of more than 512 rows keep the low-rank expand's bf16 MMAs in an accumulator
- *     of their own beside the base's, added after the base product is scaled.
+ *     in batches of more than 512 rows the low-rank expand's bf16 MMAs add to the base's
+ *     accumulator after the base product is scaled there.
  * Limits: K a multiple of 16.  The packed weight takes K x N bytes.
  * Errors: as lora_layer_create.
  */

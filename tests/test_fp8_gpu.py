@@ -120,9 +120,8 @@ def test_fp8_limits():
         layer.close()
 
 
-# ---- batches of more than 512 rows: the SGMV path, with the expand blocks' bf16 MMAs in an
-# accumulator of their own beside the e4m3 base's (two buffers of two accumulators up to
-# 128-column tiles, one buffer at 256) ----
+# ---- batches of more than 512 rows: the SGMV path; the e4m3 base product is scaled in TMEM
+# before the expand blocks' bf16 MMAs add to the same accumulator ----
 
 @pytest.mark.parametrize("T,K,N,layout", [(700, 1024, 1040, "runs"), (1300, 512, 264, "random"),
                                           (513, 2048, 4096, "runs")])
