@@ -970,7 +970,7 @@ def main(argv=None):
     ap.add_argument("--pooled", action="store_true",
                     help="adapters at their true rank in a row pool (lora_layer_create_pooled)")
     ap.add_argument("--fp8", action="store_true",
-                    help="decode workload with the base in e4m3 (lora_layer_create_fp8)")
+                    help="the base in e4m3 (lora_layer_create_fp8), for any --config")
     ap.add_argument("--swap-in", action="store_true",
                     help="measure adapter swap-ins through the adapter cache instead")
     args = ap.parse_args(argv)
