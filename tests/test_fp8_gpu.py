@@ -96,8 +96,7 @@ def test_fp8_decode_workload_full_shape():
     y = layer(wl.x.cuda(), wl.token_slot.cuda())
     torch.cuda.synchronize()
     assert layer.status() == 0
-    rows = np.arange(0, wl.T, 5)
-    assert_parity(y[rows], _ref(wl, rows), BF16, what="fp8 base, decode workload")
+    assert_parity(y, _ref(wl), BF16, what="fp8 base, decode workload, every row")
     layer.close()
 
 
@@ -221,10 +220,9 @@ def test_fp8_prefill_workload_full_shape():
         y = layer(wl.x.cuda(), wl.token_slot.cuda())
         torch.cuda.synchronize()
         assert layer.status() == 0
-        # segment edges and a spread of rows (the oracle's e4m3 product over all 8192 rows
-        # of the 4096 x 14336 weight would take minutes)
-        rows = np.unique(np.concatenate([np.arange(0, wl.T, 61), np.arange(wl.T - 8, wl.T)]))
-        assert_parity(y[rows], _ref(wl, rows), BF16, what="fp8 base, prefill workload")
+        # every row (the e4m3 base product is one fp64 matrix product on the host; the
+        # low-rank term comes from the C oracle)
+        assert_parity(y, _ref(wl), BF16, what="fp8 base, prefill workload, every row")
     finally:
         layer.close()
 
