@@ -227,6 +227,20 @@ def test_fp8_prefill_workload_full_shape():
         layer.close()
 
 
+def test_fp8_mixed_workload_full_shape():
+    # the continuous batch: 8 prefill requests of 448 rows and 512 one-row decode requests
+    # over 100 slots (K = 14336, N = 4096), so most row tiles carry many expand blocks
+    wl = workloads.mixed_continuous(seed=1004, device="cpu")
+    layer = _layer(wl)
+    try:
+        y = layer(wl.x.cuda(), wl.token_slot.cuda())
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        assert_parity(y, _ref(wl), BF16, what="fp8 base, mixed workload, every row")
+    finally:
+        layer.close()
+
+
 def test_fp8_back_to_back_forwards_and_split_batches():
     # The BGMV kernel quantises x's rows as it starts and counts them; the GEMM's loads wait
     # for the count, and the last CTA of the batch's last GEMM launch resets it.  Several
